@@ -1,0 +1,189 @@
+/*
+ * cconv_oracle.c -- plain fp64 CPU statement of the depthwise causal short convolution
+ * with fused SiLU: forward, backward and the single-token decode update.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle the CUDA path is checked against.
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline / reference arm
+ * may load it.  It shares no code, header, table or helper with the CUDA library, and the
+ * library never calls it.
+ *
+ * Every function is written for a reader checking it against the definitions by eye:
+ * straight loops in the order of the definition, fp64 arithmetic, libm exp(), no
+ * blocking, no fusion, no reordering.  Sources (page title, file / section):
+ *
+ *   forward   y[b,t,d] = silu(bias[d] + sum_{k<W} w[d,W-1-k] * x[b,t-k,d]),
+ *             x = 0 left of the sequence.
+ *             kernel-fun 0.2.0.dev1 wheel, kernel_fun/cconv/_kernels/strip.py:
+ *             `_tap` (w[:, W-1-k] multiplies x[t-k]), `_ld_ring` (zero left of the
+ *             sequence), `_silu`.  The bias sits inside the activation (problem
+ *             statement of the forward; the strip kernel itself carries no bias).
+ *   backward  g = dy * s * (1 + z (1 - s)), s = sigmoid(z)    (strip.py `_dsilu`)
+ *             dx[t] = sum_k w[d,W-1-k] * g[t+k], g = 0 past the end (strip.py `_bwd4`)
+ *             dw[d,W-1-k] = sum_{b,t} g[t] * x[t-k]  (strip.py `_bwd4`, partial store
+ *             at the end of `cconv_bwd_strip`), dbias[d] = sum_{b,t} g[b,t,d].
+ *   decode    "Add experimental causal conv1d decode update - #797" (NVIDIA/cudnn-frontend),
+ *             PR summary: per row i the state slot s = state_indices[i] is read, the new
+ *             token emits y, then the state shifts by one and takes the token.  Negative,
+ *             out-of-range and duplicate indices fail closed (nothing is mutated).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - state[s,d,0] is the oldest entry; the window for the new token is
+ *     (state[s,d,0..W-2], x[i,d]) and tap j multiplies window[j], which is the
+ *     forward's orientation (window[W-1-k] = x[t-k]).
+ *   - a repeated index is a "duplicate" only when it is in range; an out-of-range value
+ *     is reported as out-of-range however often it occurs.
+ *   - state_indices == NULL means row i uses slot i.
+ *
+ * Number formats: the forward and backward take real values as double (the exact bf16
+ * or fp32 values the GPU receives, widened by the caller), so they are plain functions of
+ * real inputs.  The decode update moves state bits, so it takes the bf16 state and token
+ * as their raw 16-bit patterns (uint16); a bf16 is the upper half of an IEEE-754
+ * binary32, which is how it is widened for the arithmetic.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_IDX_NEGATIVE 1
+#define ORACLE_IDX_OUT_OF_RANGE 2
+#define ORACLE_IDX_DUPLICATE 4
+
+/* bf16 bit pattern -> double: the pattern is the top 16 bits of a binary32. */
+static double bf16_to_double(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+static double silu(double z) { return z * sigmoid(z); }
+
+/* z[b,t,d] = bias[d] + sum_{k<W} w[d, W-1-k] * x[b, t-k, d], x[t-k] = 0 for t-k < 0 */
+static double preactivation(int64_t T, int64_t D, int W, const double* x,
+                            const double* w, const double* bias,
+                            int64_t b, int64_t t, int64_t d) {
+  double z = bias ? bias[d] : 0.0;
+  for (int k = 0; k < W; ++k) {
+    if (t - k < 0) continue;
+    z += w[d * W + (W - 1 - k)] * x[(b * T + (t - k)) * D + d];
+  }
+  return z;
+}
+
+/* Forward. x: [B,T,D] contiguous.  w: [D,W].  bias: [D] or NULL.
+ * y: [B,T,D] (fp64, unrounded).  z (optional, may be NULL): the pre-activation. */
+int oracle_fwd(int64_t B, int64_t T, int64_t D, int W, const double* x,
+               const double* w, const double* bias, double* y, double* z) {
+  if (B < 0 || T < 0 || D < 0 || W < 1) return -1;
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t t = 0; t < T; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        double zz = preactivation(T, D, W, x, w, bias, b, t, d);
+        if (z) z[(b * T + t) * D + d] = zz;
+        y[(b * T + t) * D + d] = silu(zz);
+      }
+  return 0;
+}
+
+/* Backward. x, dy: [B,T,D] contiguous.  Outputs: dx [B,T,D], dw [D,W], dbias [D]
+ * (dbias may be NULL).  z is recomputed from x, as the definition gives it. */
+int oracle_bwd(int64_t B, int64_t T, int64_t D, int W, const double* x,
+               const double* dy, const double* w, const double* bias,
+               double* dx, double* dw, double* dbias) {
+  if (B < 0 || T < 0 || D < 0 || W < 1) return -1;
+  const int64_t n = B * T * D;
+  double* g = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+  if (!g) return -2;
+
+  /* g = dy * silu'(z),  silu'(z) = s (1 + z (1 - s)) */
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t t = 0; t < T; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        const int64_t i = (b * T + t) * D + d;
+        const double zz = preactivation(T, D, W, x, w, bias, b, t, d);
+        const double s = sigmoid(zz);
+        g[i] = dy[i] * s * (1.0 + zz * (1.0 - s));
+      }
+
+  /* dx[b,t,d] = sum_{k<W} w[d, W-1-k] * g[b, t+k, d],  g = 0 for t+k >= T */
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t t = 0; t < T; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int k = 0; k < W; ++k) {
+          if (t + k >= T) continue;
+          acc += w[d * W + (W - 1 - k)] * g[(b * T + (t + k)) * D + d];
+        }
+        dx[(b * T + t) * D + d] = acc;
+      }
+
+  /* dw[d, W-1-k] = sum_{b,t} g[b,t,d] * x[b,t-k,d] (x = 0 left of the sequence);
+   * dbias[d] = sum_{b,t} g[b,t,d] */
+  for (int64_t d = 0; d < D; ++d) {
+    for (int j = 0; j < W; ++j) dw[d * W + j] = 0.0;
+    if (dbias) dbias[d] = 0.0;
+  }
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t t = 0; t < T; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        const double gg = g[(b * T + t) * D + d];
+        for (int k = 0; k < W; ++k) {
+          if (t - k < 0) continue;
+          dw[d * W + (W - 1 - k)] += gg * x[(b * T + (t - k)) * D + d];
+        }
+        if (dbias) dbias[d] += gg;
+      }
+
+  free(g);
+  return 0;
+}
+
+/* Index validation for the decode update: bit mask of offences, 0 when every index is
+ * in [0, S) and no in-range slot is named twice. */
+int oracle_validate(int64_t N, int64_t S, const int32_t* idx) {
+  int mask = 0;
+  for (int64_t i = 0; i < N; ++i) {
+    if (idx[i] < 0) mask |= ORACLE_IDX_NEGATIVE;
+    else if (idx[i] >= S) mask |= ORACLE_IDX_OUT_OF_RANGE;
+  }
+  for (int64_t i = 0; i < N; ++i) {
+    if (idx[i] < 0 || idx[i] >= S) continue;
+    for (int64_t j = i + 1; j < N; ++j)
+      if (idx[j] == idx[i]) mask |= ORACLE_IDX_DUPLICATE;
+  }
+  return mask;
+}
+
+/* Decode update.  x: [N,D] bf16 bits (contiguous).  state: [S,D,W-1] bf16 bits,
+ * updated in place.  idx: [N] or NULL (row i -> slot i, needs S >= N).
+ * w: [D,W], bias: [D] or NULL.  y: [N,D] fp64.
+ * Returns 0, or the offence mask (> 0) with nothing written, or -1 on a bad shape. */
+int oracle_update(int64_t N, int64_t D, int W, const uint16_t* x, uint16_t* state,
+                  int64_t S, const int32_t* idx, const double* w, const double* bias,
+                  double* y) {
+  if (N < 0 || D < 0 || W < 1 || W > 8 || S < 0) return -1;
+  if (idx) {
+    const int mask = oracle_validate(N, S, idx);
+    if (mask) return mask;
+  } else if (S < N) {
+    return -1;
+  }
+  const int L = W - 1; /* state length */
+  uint16_t window[8];
+  for (int64_t i = 0; i < N; ++i) {
+    const int64_t s = idx ? (int64_t)idx[i] : i;
+    for (int64_t d = 0; d < D; ++d) {
+      uint16_t* st = state + (s * D + d) * L;
+      for (int j = 0; j < L; ++j) window[j] = st[j];
+      window[L] = x[i * D + d];
+      double z = bias ? bias[d] : 0.0;
+      for (int j = 0; j < W; ++j) z += w[d * W + j] * bf16_to_double(window[j]);
+      y[i * D + d] = silu(z);
+      for (int j = 0; j < L; ++j) st[j] = window[j + 1];
+    }
+  }
+  return 0;
+}

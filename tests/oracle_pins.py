@@ -1,0 +1,316 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics.
+
+Each pin takes an ``oracle.Oracle`` handle and raises AssertionError on a mismatch, so the
+same pins run against the real oracle (where all must pass) and against deliberately
+broken copies of it (where at least one must fail; see test_oracle_mutants.py).
+
+What pins what:
+  fwd  - scipy.signal.lfilter (a library FIR filter with zero initial conditions) per
+         channel; torch float64 grouped conv1d; W=1 elementwise; impulse and constant
+         closed forms; silu(0) = 0.
+  bwd  - torch float64 autograd through grouped conv1d + SiLU; central finite differences
+         of L = sum(y * dy) in fp64; closed form at z = 0 (g = dy / 2).
+  taps - zero-weighted padded taps reproduce the narrower width (kernel-fun 0.2.0.dev1
+         wheel, cconv/_kernels/strip.py module docstring: narrow W is zero-weighted taps).
+  decode - T single-token updates from a zero state reproduce every row of the full
+         forward, and the final state is the last W-1 rows of x, bit for bit;
+         index validation against a set-based definition, exhaustively on tiny pools;
+         invalid indices leave the pool untouched ("fail closed", cuDNN decode-update PR).
+"""
+from __future__ import annotations
+
+import itertools
+
+import numpy as np
+import scipy.signal
+import scipy.special
+import torch
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_values(rng, shape):
+    """Random values exactly representable in bf16 (as float64)."""
+    t = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16)
+    return t.double().numpy()
+
+
+def _bf16_bits(a64):
+    return torch.from_numpy(np.ascontiguousarray(a64, dtype=np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _silu(z):
+    return z * scipy.special.expit(z)
+
+
+def _close(a, b, rtol, what):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    scale = max(1.0, float(np.max(np.abs(b))) if b.size else 1.0)
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    assert err <= rtol * scale, f"{what}: max err {err:.3e} > {rtol:.1e} * {scale:.3e}"
+
+
+def _torch_ref(x, dy, w, bias):
+    """float64 torch: grouped conv1d (cross-correlation) with W-1 left zeros + SiLU, and
+    its autograd gradients."""
+    B, T, D = x.shape
+    W = w.shape[1]
+    xt = torch.tensor(x, dtype=torch.float64).permute(0, 2, 1).contiguous().requires_grad_(True)
+    wt = torch.tensor(w, dtype=torch.float64).reshape(D, 1, W).requires_grad_(True)
+    bt = torch.tensor(bias, dtype=torch.float64).requires_grad_(True) if bias is not None else None
+    z = torch.nn.functional.conv1d(torch.nn.functional.pad(xt, (W - 1, 0)), wt, bt, groups=D)
+    y = torch.nn.functional.silu(z)
+    dyt = torch.tensor(dy, dtype=torch.float64).permute(0, 2, 1)
+    (y * dyt).sum().backward()
+    return (y.detach().permute(0, 2, 1).numpy(), xt.grad.permute(0, 2, 1).numpy(),
+            wt.grad.reshape(D, W).numpy(),
+            None if bt is None else bt.grad.numpy())
+
+
+# ---------------------------------------------------------------------------------------
+# forward
+# ---------------------------------------------------------------------------------------
+
+def pin_fwd_lfilter(o):
+    rng = _rng(1)
+    for W in (1, 2, 3, 4):
+        B, T, D = 2, 11, 3
+        x = _bf16_values(rng, (B, T, D))
+        w = rng.uniform(-0.5, 0.5, (D, W))
+        bias = rng.uniform(-0.1, 0.1, D)
+        y = o.fwd(x, w, bias)
+        ref = np.empty_like(y)
+        for b in range(B):
+            for d in range(D):
+                # lfilter coefficient k multiplies x[n-k]: that is w[d, W-1-k]
+                z = scipy.signal.lfilter(w[d, ::-1], [1.0], x[b, :, d]) + bias[d]
+                ref[b, :, d] = _silu(z)
+        _close(y, ref, 1e-13, f"fwd vs lfilter W={W}")
+
+
+def pin_fwd_bwd_torch(o):
+    rng = _rng(2)
+    for W, with_bias in ((4, True), (4, False), (3, True), (2, True), (1, True)):
+        B, T, D = 3, 17, 5
+        x = _bf16_values(rng, (B, T, D))
+        dy = _bf16_values(rng, (B, T, D))
+        w = rng.uniform(-0.5, 0.5, (D, W))
+        bias = rng.uniform(-0.1, 0.1, D) if with_bias else None
+        y_ref, dx_ref, dw_ref, db_ref = _torch_ref(x, dy, w, bias)
+        y = o.fwd(x, w, bias)
+        dx, dw, db = o.bwd(x, dy, w, bias)
+        _close(y, y_ref, 1e-13, f"fwd vs torch W={W}")
+        _close(dx, dx_ref, 1e-12, f"dx vs torch W={W}")
+        _close(dw, dw_ref, 1e-12, f"dw vs torch W={W}")
+        if with_bias:
+            _close(db, db_ref, 1e-12, f"dbias vs torch W={W}")
+        else:
+            # dbias is sum(g) whether or not a bias was added
+            y2, dx2, dw2, db2 = _torch_ref(x, dy, w, np.zeros(D))
+            _close(db, db2, 1e-12, f"dbias (no bias) W={W}")
+
+
+def pin_w1_elementwise(o):
+    rng = _rng(3)
+    B, T, D = 2, 7, 4
+    x = _bf16_values(rng, (B, T, D))
+    w = rng.uniform(-0.5, 0.5, (D, 1))
+    bias = rng.uniform(-0.1, 0.1, D)
+    y = o.fwd(x, w, bias)
+    _close(y, _silu(w[:, 0] * x + bias), 1e-15, "W=1 silu(w x + b)")
+
+
+def pin_impulse(o):
+    # x = unit impulse at t0, bias 0  =>  z[t0 + k] = w[d, W-1-k] for k < W, else 0
+    W, T, D, t0 = 4, 12, 3, 5
+    w = np.array([[0.25, -0.5, 0.75, 1.0], [0.1, 0.2, 0.3, 0.4], [-1.0, 0.5, -0.25, 0.125]])
+    x = np.zeros((1, T, D))
+    x[0, t0, :] = 1.0
+    _, z = o.fwd(x, w, None, return_z=True)
+    expect = np.zeros((T, D))
+    for k in range(W):
+        expect[t0 + k, :] = w[:, W - 1 - k]
+    _close(z[0], expect, 0.0, "impulse response")
+
+
+def pin_constant(o):
+    # x = c everywhere => z[t] = b + c * sum_{j >= W-1-t} w[d, j]  (fewer taps at the start)
+    W, T, D, c = 4, 6, 2, 0.5
+    w = np.array([[0.25, -0.5, 0.75, 1.0], [1.0, 2.0, 3.0, 4.0]])
+    bias = np.array([0.125, -0.0625])
+    x = np.full((1, T, D), c)
+    _, z = o.fwd(x, w, bias, return_z=True)
+    expect = np.empty((T, D))
+    for t in range(T):
+        lo = max(0, W - 1 - t)
+        expect[t] = bias + c * w[:, lo:].sum(axis=1)
+    _close(z[0], expect, 1e-15, "constant input")
+
+
+def pin_zero_point(o):
+    # x = 0, bias = 0 => z = 0 => y = silu(0) = 0 and g = dy * silu'(0) = dy / 2, so
+    # dx[t] = sum_k w[d, W-1-k] dy[t+k] / 2, dw = 0, dbias = sum dy / 2.
+    rng = _rng(4)
+    B, T, D, W = 2, 9, 3, 4
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    x = np.zeros((B, T, D))
+    dy = _bf16_values(rng, (B, T, D))
+    assert np.all(o.fwd(x, w, None) == 0.0), "silu(0) must be 0"
+    dx, dw, db = o.bwd(x, dy, w, None)
+    expect_dx = np.zeros_like(dx)
+    for t in range(T):
+        for k in range(W):
+            if t + k < T:
+                expect_dx[:, t, :] += w[:, W - 1 - k] * dy[:, t + k, :] / 2
+    _close(dx, expect_dx, 1e-15, "dx at z=0")
+    _close(dw, np.zeros_like(dw), 0.0, "dw at x=0")
+    _close(db, dy.sum(axis=(0, 1)) / 2, 1e-15, "dbias at z=0")
+
+
+# ---------------------------------------------------------------------------------------
+# backward: finite differences
+# ---------------------------------------------------------------------------------------
+
+def pin_finite_differences(o):
+    rng = _rng(5)
+    B, T, D, W = 2, 6, 2, 4
+    x = rng.standard_normal((B, T, D))
+    dy = rng.standard_normal((B, T, D))
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    bias = rng.uniform(-0.1, 0.1, D)
+    h = 1e-6
+
+    def loss(x_, w_, b_):
+        return float(np.sum(o.fwd(x_, w_, b_) * dy))
+
+    dx, dw, db = o.bwd(x, dy, w, bias)
+    fd_dx = np.empty_like(x)
+    for i in np.ndindex(x.shape):
+        xp = x.copy(); xp[i] += h
+        xm = x.copy(); xm[i] -= h
+        fd_dx[i] = (loss(xp, w, bias) - loss(xm, w, bias)) / (2 * h)
+    fd_dw = np.empty_like(w)
+    for i in np.ndindex(w.shape):
+        wp = w.copy(); wp[i] += h
+        wm = w.copy(); wm[i] -= h
+        fd_dw[i] = (loss(x, wp, bias) - loss(x, wm, bias)) / (2 * h)
+    fd_db = np.empty_like(bias)
+    for i in range(D):
+        bp = bias.copy(); bp[i] += h
+        bm = bias.copy(); bm[i] -= h
+        fd_db[i] = (loss(x, w, bp) - loss(x, w, bm)) / (2 * h)
+    _close(dx, fd_dx, 1e-7, "dx vs finite differences")
+    _close(dw, fd_dw, 1e-7, "dw vs finite differences")
+    _close(db, fd_db, 1e-7, "dbias vs finite differences")
+
+
+def pin_padded_taps(o):
+    rng = _rng(6)
+    B, T, D = 2, 10, 3
+    x = _bf16_values(rng, (B, T, D))
+    dy = _bf16_values(rng, (B, T, D))
+    bias = rng.uniform(-0.1, 0.1, D)
+    for W in (1, 2, 3):
+        w = rng.uniform(-0.5, 0.5, (D, W))
+        w4 = np.concatenate([np.zeros((D, 4 - W)), w], axis=1)  # zero taps on the old side
+        _close(o.fwd(x, w4, bias), o.fwd(x, w, bias), 0.0, f"padded taps fwd W={W}")
+        dx4, dw4, db4 = o.bwd(x, dy, w4, bias)
+        dx, dw, db = o.bwd(x, dy, w, bias)
+        _close(dx4, dx, 0.0, f"padded taps dx W={W}")
+        _close(dw4[:, 4 - W:], dw, 0.0, f"padded taps dw W={W}")
+        _close(db4, db, 0.0, f"padded taps dbias W={W}")
+
+
+# ---------------------------------------------------------------------------------------
+# decode update
+# ---------------------------------------------------------------------------------------
+
+def pin_decode_matches_forward(o):
+    rng = _rng(7)
+    for W, T in ((4, 9), (3, 5), (2, 4), (4, 2), (1, 3)):
+        B, D, S = 3, 4, 5
+        x = _bf16_values(rng, (B, T, D))
+        w = rng.uniform(-0.5, 0.5, (D, W))
+        bias = rng.uniform(-0.1, 0.1, D)
+        y_full = o.fwd(x, w, bias)
+        idx = np.array([4, 0, 2], np.int32)       # sequence b lives in slot idx[b]
+        state = np.zeros((S, D, W - 1), np.uint16)  # bf16 +0.0
+        xb = _bf16_bits(x)
+        for t in range(T):
+            status, y, state = o.update(xb[:, t, :], state, idx, w, bias)
+            assert status == 0
+            _close(y, y_full[:, t, :], 1e-15, f"decode step {t} vs forward row W={W}")
+        for b in range(B):
+            expect = np.zeros((D, W - 1), np.uint16)
+            for j in range(W - 1):
+                t = T - (W - 1) + j          # state[..., 0] is the oldest
+                if t >= 0:
+                    expect[:, j] = xb[b, t, :]
+            assert np.array_equal(state[idx[b]], expect), f"final state of seq {b} W={W}"
+        untouched = [s for s in range(S) if s not in idx]
+        assert np.all(state[untouched] == 0), "slots not named by state_indices changed"
+
+
+def _validate_by_sets(idx, S):
+    mask = 0
+    if any(v < 0 for v in idx):
+        mask |= 1
+    if any(v >= S for v in idx):
+        mask |= 2
+    valid = [v for v in idx if 0 <= v < S]
+    if len(set(valid)) != len(valid):
+        mask |= 4
+    return mask
+
+
+def pin_validate_exhaustive(o):
+    for S in range(0, 5):
+        for N in range(0, 4):
+            for idx in itertools.product(range(-1, S + 2), repeat=N):
+                got = o.validate(np.array(idx, np.int32), S)
+                assert got == _validate_by_sets(idx, S), f"validate {idx} S={S}: {got}"
+
+
+def pin_update_fail_closed(o):
+    rng = _rng(8)
+    S, N, D, W = 6, 3, 4, 4
+    state = _bf16_bits(_bf16_values(rng, (S, D, W - 1)))
+    x = _bf16_bits(_bf16_values(rng, (N, D)))
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    for idx, mask in (([0, -1, 2], 1), ([0, 6, 2], 2), ([3, 1, 3], 4), ([-5, 9, 1], 3),
+                      ([7, 7, 0], 2), ([2, 2, -1], 5)):
+        status, y, new_state = o.update(x, state, np.array(idx, np.int32), w, None)
+        assert status == mask, f"{idx}: status {status} != {mask}"
+        assert y is None
+        assert np.array_equal(new_state, state), f"{idx}: pool changed on a rejected call"
+    # a valid call changes exactly the named slots
+    status, y, new_state = o.update(x, state, np.array([5, 0, 3], np.int32), w, None)
+    assert status == 0
+    changed = sorted({int(s) for s in np.nonzero(np.any(new_state != state, axis=(1, 2)))[0]})
+    assert set(changed) <= {0, 3, 5}
+    # NULL indices: row i -> slot i
+    status, y2, st2 = o.update(x, state, None, w, None)
+    assert status == 0
+    for i in range(N):
+        assert np.array_equal(st2[i, :, :W - 2], state[i, :, 1:]) and np.array_equal(
+            st2[i, :, W - 2], x[i]), "NULL indices must update slot i"
+
+
+ALL_PINS = [
+    pin_fwd_lfilter,
+    pin_fwd_bwd_torch,
+    pin_w1_elementwise,
+    pin_impulse,
+    pin_constant,
+    pin_zero_point,
+    pin_finite_differences,
+    pin_padded_taps,
+    pin_decode_matches_forward,
+    pin_validate_exhaustive,
+    pin_update_fail_closed,
+]

@@ -1,0 +1,62 @@
+"""Plant single mistakes in copies of the oracle (on the CPU) and check the pins notice.
+
+Each mutant is a one-token change of the kind a careless restatement makes: a reversed
+tap, a dropped term, a wrong sign, a wrong shift.  A pin set that passes a mutant would
+not have caught that mistake in the real oracle.  Mutants that would read out of bounds
+are not planted.
+"""
+import shutil
+
+import pytest
+
+import oracle
+from oracle import build as oracle_build
+from tests import oracle_pins
+
+SRC = oracle_build.SOURCE.read_text()
+
+MUTANTS = {
+    "tap_reversed_fwd": ("z += w[d * W + (W - 1 - k)] * x[", "z += w[d * W + k] * x["),
+    "bias_dropped": ("double z = bias ? bias[d] : 0.0;\n  for (int k = 0; k < W; ++k) {\n    if (t - k < 0)",
+                     "double z = 0.0;\n  for (int k = 0; k < W; ++k) {\n    if (t - k < 0)"),
+    "sigmoid_sign": ("return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
+    "dsilu_term_dropped": ("s * (1.0 + zz * (1.0 - s))", "s * (1.0 + (1.0 - s))"),
+    "dsilu_sign": ("(1.0 - s))", "(1.0 + s))"),
+    "dx_tap_reversed": ("acc += w[d * W + (W - 1 - k)] * g[", "acc += w[d * W + k] * g["),
+    "dw_index_reversed": ("dw[d * W + (W - 1 - k)] += gg", "dw[d * W + k] += gg"),
+    "dbias_dropped": ("if (dbias) dbias[d] += gg;", "if (dbias) dbias[d] += 0.0 * gg;"),
+    "decode_no_shift": ("st[j] = window[j + 1];", "st[j] = window[j];"),
+    "decode_tap_reversed": ("z += w[d * W + j] * bf16_to_double(window[j]);",
+                            "z += w[d * W + (W - 1 - j)] * bf16_to_double(window[j]);"),
+    "validate_no_duplicates": ("mask |= ORACLE_IDX_DUPLICATE;", "mask |= 0;"),
+    "validate_range_off_by_one": ("else if (idx[i] >= S) mask |= ORACLE_IDX_OUT_OF_RANGE;",
+                                  "else if (idx[i] > S) mask |= ORACLE_IDX_OUT_OF_RANGE;"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    d = tmp_path_factory.mktemp("oracle_mutants")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+def _run_pins(o):
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError as e:
+            failed.append(f"{pin.__name__}: {str(e)[:80]}")
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, mutant_dir):
+    old, new = MUTANTS[name]
+    assert SRC.count(old) == 1, f"mutation site for {name} not unique in the oracle source"
+    src = mutant_dir / f"{name}.c"
+    src.write_text(SRC.replace(old, new))
+    lib = oracle_build.build(source=src, out=mutant_dir / f"lib{name}.so", force=True)
+    failed = _run_pins(oracle.Oracle(lib))
+    assert failed, f"no pin catches the planted mistake {name}"
