@@ -1,0 +1,535 @@
+"""Benchmark of the causal short convolution hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+  * cconv_fwd  on the production-length workload  B=2 T=8192 D=4096 W=4, no bias,
+    bf16 activations, fp32 weights;
+  * cconv_bwd  (dx, dw; stream kernel + deterministic reduction) on the same workload;
+  * cconv_update, one decode step of the decode workload: pool [512, 4096, 3] bf16,
+    256 active rows, W=4, bias.
+The reported value is achieved HBM throughput, algorithmic bytes over device time, in
+TB/s (fwd: 4 B/element, bwd: 6 B/element, decode: x + state read/write + y per step);
+per-part TB/s, fractions of the measured copy peak and decode microseconds per step are
+reported beside it.  Inputs are rotated so that no kernel reads data the previous kernel
+touched, and every per-launch working set (>= 268 MB) is larger than the 129 MB L2.
+
+Under torchrun (N > 1) every rank runs the same step on its own data (weak scaling, no
+collective on the data path); the timed region is bracketed by a barrier and
+synchronisation, the max over ranks is taken, and rank 0 prints the JSON line.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this path has) on the
+host cores, on a bounded sample of the same workload per step, and prints the same line
+with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+from depthwise_causal_short_gb300 import inputs  # noqa: E402
+
+METRIC = "achieved HBM TB/s (fwd, bwd) and % of GB300 peak; decode update µs/step"
+UNIT = "TB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+FWD = inputs.PROD
+DEC = inputs.DECODE_SHAPE
+N_ELEM = FWD.B * FWD.T * FWD.D
+FWD_BYTES = 4 * N_ELEM                       # x read + y written, bf16
+BWD_BYTES = 6 * N_ELEM                       # x, dy read + dx written, bf16
+DEC_BYTES = (2 * DEC.N * DEC.D                # x read
+             + 2 * 2 * DEC.N * DEC.D * (DEC.W - 1)  # named state rows read + written
+             + 2 * DEC.N * DEC.D)             # y written
+STEP_BYTES = FWD_BYTES + BWD_BYTES + DEC_BYTES
+LAUNCHES_PER_STEP = 4                        # fwd, bwd stream, bwd reduce, update
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel (the
+# backward stream kernel) from the ncu capture summarised under profiles/; None when the
+# kernel has changed since the counters were taken.
+BWD_TRAFFIC_BYTES = None
+
+WORKLOAD = ("fwd+bwd B=2 T=8192 D=4096 W=4 no bias (bf16 x/dy, f32 w) + 1 decode update "
+            "S=512 N=256 D=4096 W=4 bias per step")
+
+
+def measured_peak():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (identity on one rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(per_rank_units: float, elapsed_max_s: float, world: int) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return per_rank_units * world / elapsed_max_s
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: str):
+        self.dev = device
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm, smax, names = [], [], set()
+        labels = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for lab, val in zip(labels, parts[5:9]):
+                if val.lower().startswith("active"):
+                    names.add(lab)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no parsable samples"],
+                    "samples": 0}
+        loaded = [v for v in sm if v > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(names), "samples": len(sm)}
+
+
+def gpu_id(dev) -> str:
+    """nvidia-smi's name for a torch device (its UUID), independent of CUDA_VISIBLE_DEVICES."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import depthwise_causal_short_gb300 as cc
+    from depthwise_causal_short_gb300 import _build
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    barrier(world)
+    cc.load()
+
+    # ---- inputs (seeded, synthetic), resident in HBM before the timed region ----------
+    x, dy, w, _ = inputs.fwd_bwd_inputs(FWD.B, FWD.T, FWD.D, FWD.W, FWD.bias, seed=rank)
+    NSET = 2
+    xf = [x.to(dev) for _ in range(NSET)]            # forward inputs
+    xb = [x.to(dev) for _ in range(NSET)]            # backward inputs (distinct buffers)
+    dyb = [dy.to(dev) for _ in range(NSET)]
+    ys = [torch.empty_like(xf[0]) for _ in range(NSET)]
+    dxs = [torch.empty_like(xf[0]) for _ in range(NSET)]
+    wg = w.to(dev)
+    dw = torch.empty_like(wg)
+    ws = torch.empty(cc.cconv_bwd_workspace_bytes(FWD.B, FWD.T, FWD.D, FWD.W), dtype=torch.uint8,
+                     device=dev)
+    st, xr, idx, wd, bd = inputs.decode_inputs(DEC.S, DEC.N, DEC.D, DEC.W, DEC.bias, n_x=8,
+                                               seed=rank)
+    st, xr, idx, wd, bd = (t.to(dev) for t in (st, xr, idx, wd, bd))
+    yd = torch.empty(DEC.N, DEC.D, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(2, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        k = i % NSET
+        if ev is not None:
+            ev[0].record(stream)
+        cc.cconv_fwd(xf[k], wg, None, y=ys[k], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        cc.cconv_bwd(xb[k], dyb[k], wg, None, want_dbias=False, dx=dxs[k], dw=dw, workspace=ws,
+                     stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        cc.cconv_update(xr[i % xr.shape[0]], st, wd, bd, idx, y=yd, status=status, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps ----------------------------------------------------
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(dev)) as clk:
+        t0 = time.perf_counter()
+        start.record(stream)
+        for i in range(K):
+            step(i, evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    elapsed = start.elapsed_time(end) / 1e3
+    elapsed_max = max_over_ranks(elapsed, world, dev)
+    fwd_us = [e[0].elapsed_time(e[1]) * 1e3 for e in evs]
+    bwd_us = [e[1].elapsed_time(e[2]) * 1e3 for e in evs]
+    upd_us = [e[2].elapsed_time(e[3]) * 1e3 for e in evs]
+    assert status.tolist() == [0, 0]
+
+    # ---- decode: 1000 steps replayed from one CUDA graph --------------------------------
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream(device=dev)
+    s2.wait_stream(stream)
+    with torch.cuda.stream(s2):
+        cc.cconv_update(xr[0], st, wd, bd, idx, y=yd, status=status, stream=s2)
+        with torch.cuda.graph(g, stream=s2):
+            for j in range(DEC.steps):
+                cc.cconv_update(xr[j % xr.shape[0]], st, wd, bd, idx, y=yd, status=status,
+                                stream=s2)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    ga.record(stream)
+    for _ in range(reps):
+        g.replay()
+    gb.record(stream)
+    torch.cuda.synchronize()
+    dec_graph_us = ga.elapsed_time(gb) * 1e3 / (reps * DEC.steps)
+
+    # ---- end to end through the public API with host buffers ------------------------------
+    e2e = run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank != 0:
+        return None
+    peak_gbs, peak_kind = measured_peak()
+    f_us, b_us, u_us = (statistics.mean(v) for v in (fwd_us, bwd_us, upd_us))
+    fwd_tbps = FWD_BYTES / (f_us * 1e-6) / 1e12
+    bwd_tbps = BWD_BYTES / (b_us * 1e-6) / 1e12
+    value = aggregate(STEP_BYTES * K, elapsed_max, world) / 1e12
+    out = {
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_max * 1e3 / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "storage": "bf16 activations and state, f32 weights",
+            "l2": "inputs larger than L2 and rotated: each launch reads buffers the previous "
+                  "launch did not touch (per-launch working set >= 268 MB > 129 MB L2)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "parts": {
+            "fwd": {"us": round(f_us, 3), "tbps": round(fwd_tbps, 4),
+                    "frac_of_peak": round(fwd_tbps * 1e3 / peak_gbs, 4)},
+            "bwd": {"us": round(b_us, 3), "tbps": round(bwd_tbps, 4),
+                    "frac_of_peak": round(bwd_tbps * 1e3 / peak_gbs, 4),
+                    "note": "stream kernel + deterministic reduction kernel"},
+            "decode_update": {"us_per_step_eager": round(u_us, 3),
+                              "us_per_step_graph": round(dec_graph_us, 3),
+                              "bytes_per_step": DEC_BYTES},
+        },
+        "roofline": {
+            "kernel": "cconv_bwd (stream + reduction)",
+            "bound": "hbm",
+            "achieved": round(bwd_tbps * 1e3, 1),
+            "peak": peak_gbs,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(bwd_tbps * 1e3 / peak_gbs, 4),
+            "traffic": BWD_TRAFFIC_BYTES,
+            "algorithmic_bytes_per_launch": BWD_BYTES,
+        },
+        "e2e": e2e,
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 4),
+    }
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out
+
+
+def run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world):
+    """The same step through the public API, inputs copied in from pinned host memory and
+    results copied back, copies inside the timed region."""
+    hx = x.pin_memory()
+    hdy = dy.pin_memory()
+    hxd = xr[0].cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    hdw = torch.empty(wg.shape, dtype=wg.dtype).pin_memory()
+    hyd = torch.empty(DEC.N, DEC.D, dtype=torch.bfloat16).pin_memory()
+    dx_ = torch.empty(x.shape, dtype=torch.bfloat16, device=dev)
+    x_ = torch.empty_like(dx_)
+    dy_ = torch.empty_like(dx_)
+    y_ = torch.empty_like(dx_)
+    dw_ = torch.empty_like(wg)
+    xd_ = torch.empty(DEC.N, DEC.D, dtype=torch.bfloat16, device=dev)
+    yd_ = torch.empty_like(xd_)
+    status = torch.zeros(2, dtype=torch.int32, device=dev)
+
+    def e2e_step():
+        x_.copy_(hx, non_blocking=True)
+        dy_.copy_(hdy, non_blocking=True)
+        xd_.copy_(hxd, non_blocking=True)
+        cc.cconv_fwd(x_, wg, None, y=y_, stream=stream)
+        cc.cconv_bwd(x_, dy_, wg, None, want_dbias=False, dx=dx_, dw=dw_, workspace=ws,
+                     stream=stream)
+        cc.cconv_update(xd_, st, wd, bd, idx, y=yd_, status=status, stream=stream)
+        hy.copy_(y_, non_blocking=True)
+        hdx.copy_(dx_, non_blocking=True)
+        hdw.copy_(dw_, non_blocking=True)
+        hyd.copy_(yd_, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    n = args.e2e_steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record(stream)
+    for _ in range(n):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    el = max_over_ranks(a.elapsed_time(b) / 1e3, world, dev)
+    h2d = (hx.numel() + hdy.numel() + hxd.numel()) * 2
+    d2h = (hy.numel() + hdx.numel() + hyd.numel()) * 2 + hdw.numel() * hdw.element_size()
+    return {"value": round(aggregate(STEP_BYTES * n, el, world) / 1e12, 4), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(el * 1e3 / n, 4), "steps": n}
+
+
+# ---------------------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------------------
+
+def _oracle_sample(B: int, rows: int):
+    """Inputs for a bounded sample of the workload: B sequences' first `rows` rows at the
+    production width, plus the decode workload's pool and two token rows."""
+    import oracle
+    x, dy, w, _ = inputs.fwd_bwd_inputs(B, rows, FWD.D, FWD.W, False)
+    xd, dyd, wdd = (t.double().numpy() for t in (x, dy, w))
+    st, xr, idx, wdec, bdec = inputs.decode_inputs(DEC.S, DEC.N, DEC.D, DEC.W, DEC.bias, n_x=2)
+    stb = st.view(torch.int16).numpy().view(np.uint16).copy()
+    xrb = xr.view(torch.int16).numpy().view(np.uint16)
+    return oracle, (xd, dyd, wdd), (stb, xrb, idx.numpy(), wdec.double().numpy(),
+                                    bdec.double().numpy())
+
+
+def _oracle_step(o, fb, dec):
+    """One step of the workload's composition on the oracle: fwd + bwd of the sample, then
+    one decode update.  Returns the algorithmic bytes it stands for."""
+    xd, dyd, wdd = fb
+    o.fwd(xd, wdd, None)
+    o.bwd(xd, dyd, wdd, None, want_dbias=False)
+    stb, xrb, idx, wdec, bdec = dec
+    rc, _, new = o.update(xrb[0], stb, idx, wdec, bdec)
+    assert rc == 0
+    dec[0][...] = new
+    return xd.size * (FWD_BYTES + BWD_BYTES) / N_ELEM + DEC_BYTES
+
+
+def cpu_baseline(seconds: float):
+    """The oracle, as it stands, on whole steps of the workload (B=2 T=8192 D=4096 fwd+bwd
+    + one decode update each), repeated while the total stays near `seconds`."""
+    o, fb, dec = _oracle_sample(FWD.B, FWD.T)
+    t0 = time.perf_counter()
+    nbytes = _oracle_step(o, fb, dec)
+    steps = 1
+    while True:
+        dt = time.perf_counter() - t0
+        if dt * (steps + 1) / steps > seconds:
+            break
+        nbytes += _oracle_step(o, fb, dec)
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e12, 8), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 C oracle, one thread: {steps} whole workload step(s) (fwd+bwd "
+                      f"B={FWD.B} T={FWD.T} D={FWD.D} W={FWD.W} + 1 decode update), "
+                      f"{dt:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle timed as the reference arm: each step is a bounded sample of the workload
+    (the first `rows` rows of one sequence, fwd + bwd, plus one decode update), sized so the
+    whole run takes about `--reference-seconds`."""
+    if rank != 0:
+        return None
+    o, fb, dec = _oracle_sample(1, 64)
+    t0 = time.perf_counter()
+    _oracle_step(o, fb, dec)
+    t_small = time.perf_counter() - t0
+    o, fb, dec = _oracle_sample(1, 128)
+    t0 = time.perf_counter()
+    _oracle_step(o, fb, dec)
+    per_row = max(1e-7, (time.perf_counter() - t0 - t_small) / 64)
+    fixed = max(0.0, t_small - 64 * per_row)
+    total = max(1, args.steps + args.warmup)
+    rows = int((args.reference_seconds / total - fixed) / per_row)
+    rows = max(8, min(FWD.T, rows))
+    o, fb, dec = _oracle_sample(1, rows)
+    for _ in range(args.warmup):
+        _oracle_step(o, fb, dec)
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for _ in range(args.steps):
+        nbytes += _oracle_step(o, fb, dec)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e12
+    sample = (f"fp64 C oracle, one thread; per step: fwd+bwd of one sequence's first {rows} "
+              f"rows at D={FWD.D} W={FWD.W} + 1 decode update (S={DEC.S} N={DEC.N} D={DEC.D})")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 8),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_per_step": sample},
+        "cpu_baseline": {"value": round(value, 8), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 8), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the (untimed) oracle baseline leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" and torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+    else:
+        out = run_ours(args, world, rank, local)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,24 @@
+"""GB300 (sm_103a) depthwise causal short convolution with fused SiLU.
+
+The computation lives in ``libcconv.so`` (C ABI: ``include/cconv.h``); this package is its
+thin Python binding with the same names, plus the build step and the seeded synthetic
+input generators.  Importing the package does not load the library; the first call does,
+and raises if it has not been built.
+"""
+from .binding import (  # noqa: F401
+    CCONV_BF16,
+    CCONV_F32,
+    IDX_DUPLICATE,
+    IDX_NEGATIVE,
+    IDX_OUT_OF_RANGE,
+    CConvError,
+    cconv_bwd,
+    cconv_bwd_workspace_bytes,
+    cconv_device_fault,
+    cconv_fwd,
+    cconv_status_str,
+    cconv_update,
+    header_functions,
+    lib_path,
+    load,
+)

@@ -1,0 +1,206 @@
+"""ctypes binding of libcconv.so, with the C ABI's names (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module only turns
+torch tensors into pointers, sizes and strides, allocates outputs with torch when the
+caller does not pass them, and raises on a nonzero status.  There is no fallback: if the
+library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import torch
+
+from . import _build
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+
+CCONV_BF16 = 0
+CCONV_F32 = 1
+STATUS = {
+    0: "CCONV_OK", -1: "CCONV_ERR_NULL", -2: "CCONV_ERR_SHAPE", -3: "CCONV_ERR_WIDTH",
+    -4: "CCONV_ERR_ALIGN", -5: "CCONV_ERR_STRIDE", -6: "CCONV_ERR_DTYPE",
+    -7: "CCONV_ERR_WORKSPACE", -8: "CCONV_ERR_INDEX", -9: "CCONV_ERR_CUDA",
+    -10: "CCONV_ERR_DEVICE",
+}
+IDX_NEGATIVE = 1
+IDX_OUT_OF_RANGE = 2
+IDX_DUPLICATE = 4
+
+
+class CConvError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {STATUS.get(status, status)} ({status})")
+
+
+_lib = None
+
+
+def lib_path() -> Path:
+    return _build.LIB
+
+
+def load(path: str | Path | None = None):
+    """Load libcconv.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path else _build.LIB
+    if not p.exists():
+        raise RuntimeError(
+            f"{p} is missing: build the CUDA library first "
+            "(python -m depthwise_causal_short_gb300._build, or __graft_entry__.build())")
+    lib = ctypes.CDLL(str(p))
+    lib.cconv_fwd.argtypes = [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _INT, _INT, _P, _P]
+    lib.cconv_fwd.restype = _INT
+    lib.cconv_bwd_workspace_bytes.argtypes = [_I64, _I64, _I64, _INT, ctypes.POINTER(ctypes.c_size_t)]
+    lib.cconv_bwd_workspace_bytes.restype = _INT
+    lib.cconv_bwd.argtypes = [_P, _I64, _I64, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _INT,
+                              _INT, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.cconv_bwd.restype = _INT
+    lib.cconv_update.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _INT, _INT, _P, _P, _P]
+    lib.cconv_update.restype = _INT
+    lib.cconv_status_str.argtypes = [_INT]
+    lib.cconv_status_str.restype = ctypes.c_char_p
+    lib.cconv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+    lib.cconv_device_fault.restype = _INT
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/cconv.h declares (CCONV_API ... name(...))."""
+    text = (_build.INCLUDE / "cconv.h").read_text()
+    return re.findall(r"CCONV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+# ---------------------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------------------
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _wdt(w: torch.Tensor) -> int:
+    if w.dtype == torch.float32:
+        return CCONV_F32
+    if w.dtype == torch.bfloat16:
+        return CCONV_BF16
+    raise TypeError(f"weight dtype must be float32 or bfloat16, got {w.dtype}")
+
+
+def _check(rc: int, call: str):
+    if rc != 0:
+        raise CConvError(rc, call)
+
+
+def _bf16_rows(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 3 or t.stride(2) != 1:
+        raise ValueError(f"{name} must be [B,T,D] with channel stride 1")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+# ---------------------------------------------------------------------------------------
+# the three calls
+# ---------------------------------------------------------------------------------------
+
+def cconv_fwd(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None = None, *,
+              y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = silu(bias + causal depthwise conv(x, w)); x [B,T,D] bf16, w [D,W]."""
+    _bf16_rows(x, "x")
+    B, T, D = x.shape
+    W = w.shape[1]
+    if y is None:
+        y = torch.empty((B, T, D), dtype=torch.bfloat16, device=x.device)
+    rc = load().cconv_fwd(_ptr(x), B, T, D, x.stride(0), x.stride(1), _ptr(w), _ptr(bias),
+                          _wdt(w), W, _ptr(y), _stream(stream))
+    _check(rc, "cconv_fwd")
+    return y
+
+
+def cconv_bwd_workspace_bytes(B: int, T: int, D: int, W: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().cconv_bwd_workspace_bytes(B, T, D, W, ctypes.byref(n)), "cconv_bwd_workspace_bytes")
+    return int(n.value)
+
+
+def cconv_bwd(x: torch.Tensor, dy: torch.Tensor, w: torch.Tensor,
+              bias: torch.Tensor | None = None, *, want_dbias: bool | None = None,
+              dx: torch.Tensor | None = None, dw: torch.Tensor | None = None,
+              dbias: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+              stream=None):
+    """(dx, dw, dbias) for upstream gradient dy; dbias is None unless wanted (default:
+    when a bias is given)."""
+    _bf16_rows(x, "x")
+    _bf16_rows(dy, "dy")
+    B, T, D = x.shape
+    W = w.shape[1]
+    if want_dbias is None:
+        want_dbias = bias is not None or dbias is not None
+    if dx is None:
+        dx = torch.empty((B, T, D), dtype=torch.bfloat16, device=x.device)
+    if dw is None:
+        dw = torch.empty((D, W), dtype=w.dtype, device=x.device)
+    if want_dbias and dbias is None:
+        dbias = torch.empty((D,), dtype=w.dtype, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(cconv_bwd_workspace_bytes(B, T, D, W), dtype=torch.uint8,
+                                device=x.device)
+    rc = load().cconv_bwd(_ptr(x), x.stride(0), x.stride(1), _ptr(dy), dy.stride(0), dy.stride(1),
+                          B, T, D, _ptr(w), _ptr(bias), _wdt(w), W, _ptr(dx), _ptr(dw),
+                          _ptr(dbias if want_dbias else None), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "cconv_bwd")
+    return dx, dw, (dbias if want_dbias else None)
+
+
+def cconv_update(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
+                 bias: torch.Tensor | None = None, state_indices: torch.Tensor | None = None,
+                 *, y: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                 stream=None):
+    """One decode step: (y [N,D], status int32[2] on the device).  state [S,D,W-1] is
+    updated in place unless status[0] reports CCONV_ERR_INDEX."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [N,D] bfloat16 with channel stride 1")
+    N, D = x.shape
+    W = w.shape[1]
+    if state.dtype != torch.bfloat16 or not state.is_contiguous():
+        raise ValueError("state must be a contiguous [S,D,W-1] bfloat16 tensor")
+    S = state.shape[0]
+    if y is None:
+        y = torch.empty((N, D), dtype=torch.bfloat16, device=x.device)
+    if status is None:
+        status = torch.empty(2, dtype=torch.int32, device=x.device)
+    if state_indices is not None and state_indices.dtype != torch.int32:
+        raise TypeError("state_indices must be int32")
+    rc = load().cconv_update(_ptr(x), N, D, x.stride(0), _ptr(state), S, _ptr(state_indices),
+                             _ptr(w), _ptr(bias), _wdt(w), W, _ptr(y), _ptr(status),
+                             _stream(stream))
+    _check(rc, "cconv_update")
+    return y, status
+
+
+def cconv_status_str(status: int) -> str:
+    return load().cconv_status_str(status).decode()
+
+
+def cconv_device_fault() -> int:
+    v = ctypes.c_int32(0)
+    _check(load().cconv_device_fault(ctypes.byref(v)), "cconv_device_fault")
+    return int(v.value)

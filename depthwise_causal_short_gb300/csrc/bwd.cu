@@ -1,0 +1,410 @@
+// bwd.cu -- cconv_bwd: the backward stream plus a deterministic reduction (two kernels).
+//
+// With z recomputed from x and g = dy * sigmoid(z) * (1 + z * (1 - sigmoid(z))):
+//   dx[b,t,d]    = sum_{k<W} w[d,W-1-k] * g[b,t+k,d]     (g = 0 for t+k >= T)
+//   dw[d,W-1-k]  = sum_{b,t} g[b,t,d] * x[b,t-k,d]
+//   dbias[d]     = sum_{b,t} g[b,t,d]
+// Definition: kernel-fun 0.2.0.dev1 wheel, kernel_fun/cconv/_kernels/strip.py (`_dsilu`,
+// `_bwd4`, `cconv_bwd_strip`, `cconv_bwd`).  Kept from that design: one pass over x and dy,
+// z recomputed in registers from the same x ring the dw sums need, dx for row t-3 finished
+// from a g ring three rows later, a 3-row halo after each range, and a fixed-shape
+// reduction of fp32 partials instead of atomics.
+//
+// GB300 layout: the same per-warp TMA pipeline as the forward (x and dy tiles of a stage
+// complete on one mbarrier), packed f32x2 arithmetic, and one fp32 partial record per warp
+// ([5][32*VEC]: four lags of dw, then dbias).  Because each lane owns its channels for the
+// whole range, the time sum needs no shuffles; the cross-warp sum is a second small kernel
+// that adds each strip's records in a fixed order, launched as a programmatic dependent of
+// the first so its launch overlaps the stream's tail.
+#include "strip.cuh"
+
+namespace cconv {
+
+static __device__ unsigned g_fault_bwd = 0;
+
+int read_clear_fault_bwd(unsigned* out) {
+  unsigned zero = 0;
+  if (cudaMemcpyFromSymbol(out, g_fault_bwd, sizeof(unsigned)) != cudaSuccess) return CCONV_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_fault_bwd, &zero, sizeof(unsigned)) != cudaSuccess) return CCONV_ERR_CUDA;
+  return CCONV_OK;
+}
+
+constexpr int kRec = 5;  // partial record rows: dw lags 0..3, dbias
+
+struct BwdArgs {
+  const void* w;
+  const void* bias;
+  uint16_t* dx;   // [B,T,D] contiguous bf16
+  float* ws;      // [total_warps][kRec][32*VEC] fp32 partials
+  int64_t T, D, BT;
+  int wpc, total_warps;
+  int W, wdt;
+};
+
+// FULL: every row of the tile computes g, accumulates dw / dbias and stores dx[t-3].
+template <int VEC, int R, bool FULL>
+__device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, int lane,
+                                         const TileCursor& c, bool active, const BwdArgs& p,
+                                         int64_t d0, const f2 (&tap)[4][VEC / 2],
+                                         const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
+                                         f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
+  constexpr int P = VEC / 2;
+  constexpr int ROWB = 32 * VEC * 2;
+  const f2 half = f2_splat(0.5f);
+  const f2 nhalf = f2_splat(-0.5f);
+  const f2 one = f2_splat(1.0f);
+  uint16_t* dxbase = p.dx + (static_cast<int64_t>(c.b) * p.T) * p.D + d0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int64_t t = c.tt + i;
+    f2 x[P], g[P];
+    smem_row<VEC>(xt + i * ROWB, lane, x);
+    const bool live = FULL || t >= c.a;  // rows before the range only fill the x ring
+    if (live) {
+      f2 dy[P];
+      smem_row<VEC>(dyt + i * ROWB, lane, dy);
+      const bool sum = FULL || t < c.e;  // halo rows after the range: g only
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
+        z = f2_fma(tap[1][q], h[0][q], z);
+        z = f2_fma(tap[2][q], h[1][q], z);
+        z = f2_fma(tap[3][q], h[2][q], z);
+        const f2 th = f2_tanh(f2_mul(z, half));
+        const f2 sg = f2_fma(th, half, half);       // sigmoid(z)
+        const f2 om = f2_fma(th, nhalf, half);      // 1 - sigmoid(z)
+        const f2 d1 = f2_fma(z, om, one);           // 1 + z (1 - sigmoid(z))
+        g[q] = f2_mul(f2_mul(dy[q], sg), d1);
+        if (sum) {
+          acc[0][q] = f2_fma(g[q], x[q], acc[0][q]);
+          acc[1][q] = f2_fma(g[q], h[0][q], acc[1][q]);
+          acc[2][q] = f2_fma(g[q], h[1][q], acc[2][q]);
+          acc[3][q] = f2_fma(g[q], h[2][q], acc[3][q]);
+          acc[4][q] = f2_add(g[q], acc[4][q]);
+        }
+      }
+      // dx[t-3] = sum_k tap[k] g[t-3+k]; final once g[t] is known
+      const bool store = FULL || (t - kRing >= c.a && t - kRing < c.e);
+      if (store) {
+        f2 dxv[P];
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          f2 v = f2_mul(tap[3][q], g[q]);
+          v = f2_fma(tap[2][q], gr[0][q], v);
+          v = f2_fma(tap[1][q], gr[1][q], v);
+          v = f2_fma(tap[0][q], gr[2][q], v);
+          dxv[q] = v;
+        }
+        if (active) store_row<VEC>(dxbase + (t - kRing) * p.D, dxv);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < P; ++q) g[q] = 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      h[2][q] = h[1][q];
+      h[1][q] = h[0][q];
+      h[0][q] = x[q];
+      gr[2][q] = gr[1][q];
+      gr[1][q] = gr[0][q];
+      gr[0][q] = g[q];
+    }
+  }
+}
+
+template <int VEC, int R, int S, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
+    cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
+                     const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
+  constexpr int CB = 32 * VEC;
+  constexpr int P = VEC / 2;
+  constexpr int TILE = R * CB * 2;
+  constexpr int STAGE = 2 * TILE;  // x tile, then dy tile
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * NW + warp;
+  if (gw >= p.total_warps) return;  // no CTA-wide barrier follows
+
+  uint8_t* stages = smem + warp * (S * STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
+
+  const int cb = gw / p.wpc;
+  const int k = gw - cb * p.wpc;
+  const int64_t r0 = static_cast<int64_t>(k) * p.BT / p.wpc;
+  const int64_t r1 = static_cast<int64_t>(k + 1) * p.BT / p.wpc;
+  const int c0 = cb * CB;
+  const int64_t d0 = c0 + lane * VEC;
+  const bool active = d0 < p.D;
+
+  f2 tap[4][P], bias2[P];
+  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
+
+  if (lane == 0) {
+    prefetch_tensormap(&tmx);
+    prefetch_tensormap(&tmdy);
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  TileCursor pc, cc;
+  pc.init(r0, r1, p.T, kRing);
+  cc = pc;
+  const uint64_t pol = policy_evict_first();
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      if (!pc.done) {
+        mbar_arrive_expect_tx(&bars[s], STAGE);
+        tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
+        tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, static_cast<int>(pc.tt),
+                    pc.b, pol);
+        pc.advance(R);
+      }
+    }
+  }
+
+  f2 h[3][P], gr[3][P], acc[kRec][P];
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      h[j][q] = 0ull;
+      gr[j][q] = 0ull;
+    }
+#pragma unroll
+    for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
+  }
+
+  uint32_t parity = 0;
+  int s = 0;
+  while (!cc.done) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
+                                                             kWaitLimitNs));
+    if (!ok) {
+      if (lane == 0) atomicOr(&g_fault_bwd, kFaultBwdWait);
+      for (int j = 0; j < S; ++j) (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
+      return;
+    }
+    parity ^= 1u << s;
+    const uint8_t* xt = stages + s * STAGE;
+    const bool full = cc.tt >= cc.a + kRing && cc.tt + R <= cc.e;
+    if (full)
+      bwd_tile<VEC, R, true>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+    else
+      bwd_tile<VEC, R, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+    __syncwarp();
+    if (lane == 0 && !pc.done) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bars[s], STAGE);
+      tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
+      tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, static_cast<int>(pc.tt), pc.b,
+                  pol);
+      pc.advance(R);
+    }
+    cc.advance(R);
+    s = (s + 1 == S) ? 0 : s + 1;
+  }
+
+  grid_launch_dependents();
+
+  // This warp's partial record: ws[gw][j][lane*VEC + v]
+  float* rec = p.ws + static_cast<int64_t>(gw) * kRec * CB + lane * VEC;
+#pragma unroll
+  for (int j = 0; j < kRec; ++j) {
+    float v[VEC];
+#pragma unroll
+    for (int q = 0; q < P; ++q) f2_unpack(acc[j][q], v[2 * q], v[2 * q + 1]);
+#pragma unroll
+    for (int q = 0; q < VEC; q += 4)
+      *reinterpret_cast<float4*>(rec + j * CB + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+  }
+}
+
+// dw[d, W-1-lag] and dbias[d] from the wpc partial records of d's strip, summed in a fixed
+// order: thread group j of 8 adds records j, j+8, j+16, ... and the 8 group sums are then
+// added in group order.  Deterministic; no atomics.
+constexpr int kRedGroups = 8;
+
+__global__ void __launch_bounds__(32 * kRedGroups)
+    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int wpc, int64_t D, int W,
+                            int wdt, void* dw, void* dbias) {
+  __shared__ float part[kRec][kRedGroups][33];
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int grp = threadIdx.x >> 5;
+  const int64_t d = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  if (d < D) {
+    const int64_t cb = d / cb_width;
+    const int c = static_cast<int>(d - cb * cb_width);
+    const float* base = ws + (cb * wpc) * kRec * cb_width + c;
+#pragma unroll
+    for (int j = 0; j < kRec; ++j) {
+      float a = 0.f;
+      for (int r = grp; r < wpc; r += kRedGroups) a += base[(static_cast<int64_t>(r) * kRec + j) * cb_width];
+      part[j][grp][lane] = a;
+    }
+  }
+  __syncthreads();
+  if (grp < kRec && d < D) {
+    float a = 0.f;
+#pragma unroll
+    for (int g = 0; g < kRedGroups; ++g) a += part[grp][g][lane];
+    if (grp < 4) {
+      const int lag = grp;
+      if (lag < W) {
+        const int64_t o = d * W + (W - 1 - lag);
+        if (wdt == CCONV_F32)
+          static_cast<float*>(dw)[o] = a;
+        else
+          static_cast<uint16_t*>(dw)[o] = f32_to_bf16(a);
+      }
+    } else if (dbias) {
+      if (wdt == CCONV_F32)
+        static_cast<float*>(dbias)[d] = a;
+      else
+        static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(a);
+    }
+  }
+}
+
+struct BwdConfig {
+  int vec, rows, stages, warps;
+  void (*kernel)(const CUtensorMap, const CUtensorMap, const BwdArgs);
+};
+
+#define CCONV_BWD_CFG(V, R, S, NW) \
+  BwdConfig { V, R, S, NW, cconv_bwd_kernel<V, R, S, NW> }
+
+static const BwdConfig kBwdConfigs[] = {
+    CCONV_BWD_CFG(4, 16, 3, 8),
+    CCONV_BWD_CFG(8, 8, 3, 8),
+    CCONV_BWD_CFG(4, 8, 4, 8),
+    CCONV_BWD_CFG(4, 16, 2, 12),
+};
+static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
+
+static int bwd_config_index() {
+  static int idx = -1;
+  if (idx < 0) {
+    const char* e = getenv("CCONV_BWD_CONFIG");
+    int v = e ? atoi(e) : 0;
+    idx = (v >= 0 && v < kNumBwdConfigs) ? v : 0;
+  }
+  return idx;
+}
+
+static int bwd_plan(int64_t B, int64_t T, int64_t D, const BwdConfig& cfg, StripPlan* plan,
+                    size_t* ws_bytes) {
+  int sms = 0;
+  const int rc = sm_count_current_device(&sms, nullptr);
+  if (rc != CCONV_OK) return rc;
+  *plan = make_strip_plan(B, T, D, cfg.vec, cfg.warps, 1, sms, 32);
+  *ws_bytes = static_cast<size_t>(plan->total_warps) * kRec * (32 * cfg.vec) * sizeof(float);
+  return CCONV_OK;
+}
+
+static int check_sizes(int64_t B, int64_t T, int64_t D, int W) {
+  if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
+  if (B < 1 || T < 1 || D < 1 || T > (int64_t(1) << 31) - 8 || D > (int64_t(1) << 31) - 8 ||
+      B > (int64_t(1) << 31) - 8)
+    return CCONV_ERR_SHAPE;
+  if (D % 8 != 0) return CCONV_ERR_ALIGN;
+  return CCONV_OK;
+}
+
+}  // namespace cconv
+
+extern "C" {
+
+CCONV_API int cconv_bwd_workspace_bytes(int64_t B, int64_t T, int64_t D, int W, size_t* bytes) {
+  using namespace cconv;
+  if (!bytes) return CCONV_ERR_NULL;
+  int rc = check_sizes(B, T, D, W);
+  if (rc != CCONV_OK) return rc;
+  StripPlan plan;
+  return bwd_plan(B, T, D, kBwdConfigs[bwd_config_index()], &plan, bytes);
+}
+
+CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy, int64_t sdb,
+                        int64_t sdt, int64_t B, int64_t T, int64_t D, const void* w,
+                        const void* bias, cconv_dtype wdt, int W, void* dx, void* dw,
+                        void* dbias, void* workspace, size_t workspace_bytes,
+                        cconv_stream_t stream) {
+  using namespace cconv;
+  if (!x || !dy || !w || !dx || !dw) return CCONV_ERR_NULL;
+  if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
+  int rc = check_sizes(B, T, D, W);
+  if (rc != CCONV_OK) return rc;
+  rc = check_rows_tensor(x, B, T, D, sxb, sxt);
+  if (rc != CCONV_OK) return rc;
+  rc = check_rows_tensor(dy, B, T, D, sdb, sdt);
+  if (rc != CCONV_OK) return rc;
+  const int ew = wdt == CCONV_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(dx) % 16 != 0) return CCONV_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(w) % ew != 0 || reinterpret_cast<uintptr_t>(dw) % ew != 0)
+    return CCONV_ERR_ALIGN;
+  if ((bias && reinterpret_cast<uintptr_t>(bias) % ew != 0) ||
+      (dbias && reinterpret_cast<uintptr_t>(dbias) % ew != 0))
+    return CCONV_ERR_ALIGN;
+
+  const BwdConfig& cfg = kBwdConfigs[bwd_config_index()];
+  StripPlan plan;
+  size_t need = 0;
+  rc = bwd_plan(B, T, D, cfg, &plan, &need);
+  if (rc != CCONV_OK) return rc;
+  if (!workspace || workspace_bytes < need) return CCONV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return CCONV_ERR_ALIGN;
+
+  normalise_strides(B, T, D, sxb, sxt);
+  normalise_strides(B, T, D, sdb, sdt);
+  CUtensorMap tmx, tmdy;
+  rc = encode_rows_map(&tmx, x, B, T, D, sxb, sxt, 32 * cfg.vec, cfg.rows);
+  if (rc != CCONV_OK) return rc;
+  rc = encode_rows_map(&tmdy, dy, B, T, D, sdb, sdt, 32 * cfg.vec, cfg.rows);
+  if (rc != CCONV_OK) return rc;
+
+  BwdArgs a;
+  a.w = w;
+  a.bias = bias;
+  a.dx = static_cast<uint16_t*>(dx);
+  a.ws = static_cast<float*>(workspace);
+  a.T = T;
+  a.D = D;
+  a.BT = B * T;
+  a.wpc = plan.wpc;
+  a.total_warps = plan.total_warps;
+  a.W = W;
+  a.wdt = wdt;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
+  if (rc != CCONV_OK) return rc;
+  cfg.kernel<<<plan.grid, cfg.warps * 32, smem, st>>>(tmx, tmdy, a);
+  if (cudaGetLastError() != cudaSuccess) return CCONV_ERR_CUDA;
+
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>((D + 31) / 32));
+  lc.blockDim = dim3(32 * kRedGroups);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  const float* wsp = a.ws;
+  const int cbw = 32 * cfg.vec;
+  const int wpc = plan.wpc;
+  const int wdt_i = static_cast<int>(wdt);
+  if (cudaLaunchKernelEx(&lc, cconv_bwd_reduce_kernel, wsp, cbw, wpc, D, W, wdt_i, dw, dbias) !=
+      cudaSuccess)
+    return CCONV_ERR_CUDA;
+  return CCONV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// host.cu -- host-side pieces shared by the cconv entry points: status names, device SM
+// count, TMA descriptor encoding, the fault-word reader.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace cconv {
+
+// Per-TU fault readers (each kernel file owns its own device fault word).
+int read_clear_fault_fwd(unsigned* out);
+int read_clear_fault_bwd(unsigned* out);
+
+int sm_count_current_device(int* sms, int* device) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CCONV_ERR_CUDA;
+  if (device) *device = dev;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *sms = c;
+      return CCONV_OK;
+    }
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return CCONV_ERR_CUDA;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  *sms = n;
+  return CCONV_OK;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a [B, T, D] bf16 tensor (channel stride 1) read in boxes of
+// box_c channels x box_r rows x 1 batch.  Zero fill outside the tensor.
+int encode_rows_map(CUtensorMap* map, const void* base, int64_t B, int64_t T, int64_t D,
+                    int64_t sb, int64_t st, int box_c, int box_r) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return CCONV_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)st * 2u, (cuuint64_t)sb * 2u};
+  cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)box_r, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CCONV_OK : CCONV_ERR_CUDA;
+}
+
+int set_max_dynamic_smem(const void* func, int bytes) {
+  // Per device and cheap; repeated on every launch rather than cached.
+  return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+                 cudaSuccess
+             ? CCONV_OK
+             : CCONV_ERR_CUDA;
+}
+
+}  // namespace cconv
+
+extern "C" {
+
+CCONV_API const char* cconv_status_str(int status) {
+  switch (status) {
+    case CCONV_OK: return "CCONV_OK";
+    case CCONV_ERR_NULL: return "CCONV_ERR_NULL: a required pointer is NULL";
+    case CCONV_ERR_SHAPE: return "CCONV_ERR_SHAPE: a size is out of range";
+    case CCONV_ERR_WIDTH: return "CCONV_ERR_WIDTH: W must be in [1, 4]";
+    case CCONV_ERR_ALIGN: return "CCONV_ERR_ALIGN: pointer, row stride or D breaks the 16-byte rule";
+    case CCONV_ERR_STRIDE: return "CCONV_ERR_STRIDE: a stride is not positive (or ldx < D)";
+    case CCONV_ERR_DTYPE: return "CCONV_ERR_DTYPE: unknown weight dtype";
+    case CCONV_ERR_WORKSPACE: return "CCONV_ERR_WORKSPACE: workspace missing or too small";
+    case CCONV_ERR_INDEX: return "CCONV_ERR_INDEX: state_indices invalid";
+    case CCONV_ERR_CUDA: return "CCONV_ERR_CUDA: a CUDA call failed";
+    case CCONV_ERR_DEVICE: return "CCONV_ERR_DEVICE: a kernel gave up a bounded wait";
+    default: return "unknown cconv status";
+  }
+}
+
+CCONV_API int cconv_device_fault(int32_t* fault) {
+  if (!fault) return CCONV_ERR_NULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CCONV_ERR_CUDA;
+  unsigned a = 0, b = 0;
+  int rc = cconv::read_clear_fault_fwd(&a);
+  if (rc != CCONV_OK) return rc;
+  rc = cconv::read_clear_fault_bwd(&b);
+  if (rc != CCONV_OK) return rc;
+  *fault = static_cast<int32_t>(a | b);
+  return CCONV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// strip.cuh -- how the forward and backward split a [B, T, D] tensor among warps.
+//
+// A channel strip is 32*VEC consecutive channels: one warp, VEC channels per lane, reads a
+// row of the strip as one coalesced 16-byte (VEC=8) or 8-byte (VEC=4) access per lane.
+// Each strip's rows, flattened over (b, t), are cut into `wpc` equal contiguous ranges, one
+// per warp, so every warp of the grid gets the same number of rows (to within one) and the
+// grid is one wave of resident CTAs.  A warp walks its range in time order, tile by tile,
+// keeping the W-1 previous rows in registers (the ring).  Where a range starts inside a
+// sequence, its first tile starts 3 rows early to fill the ring; where it starts a sequence,
+// those 3 rows lie at t < 0 and the copy engine fills them with zeros, which is exactly the
+// causal zero padding.
+#pragma once
+
+#include "common.cuh"
+
+namespace cconv {
+
+constexpr int kRing = 3;  // previous rows kept: W-1 for the widest supported W (4)
+
+struct StripPlan {
+  int n_cb;          // channel strips: ceil(D / (32*VEC))
+  int wpc;           // warps (row ranges) per strip
+  int total_warps;   // n_cb * wpc
+  int grid;          // CTAs of `warps_per_cta` warps
+};
+
+// rows_min: shortest range worth a warp (the ring refill is 3 rows per range).
+inline StripPlan make_strip_plan(int64_t B, int64_t T, int64_t D, int vec, int warps_per_cta,
+                                 int ctas_per_sm, int sms, int64_t rows_min) {
+  StripPlan p;
+  const int64_t cb_width = 32 * vec;
+  p.n_cb = static_cast<int>((D + cb_width - 1) / cb_width);
+  const int64_t target = static_cast<int64_t>(sms) * ctas_per_sm * warps_per_cta;
+  int64_t wpc = target / p.n_cb;
+  if (wpc < 1) wpc = 1;
+  int64_t by_rows = (B * T) / rows_min;
+  if (by_rows < 1) by_rows = 1;
+  if (wpc > by_rows) wpc = by_rows;
+  p.wpc = static_cast<int>(wpc);
+  p.total_warps = p.n_cb * p.wpc;
+  p.grid = (p.total_warps + warps_per_cta - 1) / warps_per_cta;
+  return p;
+}
+
+// Walks the tiles of one warp's row range [r0, r1) of the flattened (b, t) space.
+// A segment is the part of the range inside one sequence: rows [a, e) of batch b.  Its
+// tiles start at a - kRing and step by R until they cover e + tail - 1 (tail = 0 for the
+// forward; 3 for the backward, whose last dx rows need g of the next 3 rows).
+struct TileCursor {
+  int64_t T, r1;
+  int64_t a, e, tt;
+  int b;
+  int tail;
+  bool done;
+
+  __device__ __forceinline__ void init(int64_t r0, int64_t r1_, int64_t T_, int tail_) {
+    T = T_;
+    r1 = r1_;
+    tail = tail_;
+    done = r0 >= r1_;
+    b = static_cast<int>(r0 / T_);
+    a = r0 - static_cast<int64_t>(b) * T_;
+    const int64_t rest = r1_ - r0;
+    e = (a + rest < T_) ? a + rest : T_;
+    tt = a - kRing;
+  }
+
+  __device__ __forceinline__ void advance(int R) {
+    tt += R;
+    if (tt >= e + tail) {
+      const int64_t r = static_cast<int64_t>(b) * T + e;  // next flattened row
+      if (r >= r1) {
+        done = true;
+        return;
+      }
+      b += 1;
+      a = 0;
+      const int64_t rest = r1 - static_cast<int64_t>(b) * T;
+      e = rest < T ? rest : T;
+      tt = -kRing;
+    }
+  }
+};
+
+// Taps of one lane, as fp32 pairs: tap[k][p] multiplies x[t-k] for channels
+// (d0 + 2p, d0 + 2p + 1); it is w[d, W-1-k], zero for k >= W (a narrow W is the width-4
+// case with zero taps on the old side).  bias2[p] likewise (zero without a bias).
+template <int VEC>
+__device__ __forceinline__ void load_taps(const void* w, const void* bias, int wdt, int W,
+                                          int64_t d0, bool active, f2 (&tap)[4][VEC / 2],
+                                          f2 (&bias2)[VEC / 2]) {
+#pragma unroll
+  for (int p = 0; p < VEC / 2; ++p) {
+    float lo[4], hi[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      lo[k] = 0.f;
+      hi[k] = 0.f;
+      if (active && k < W) {
+        const int64_t i0 = (d0 + 2 * p) * W + (W - 1 - k);
+        const int64_t i1 = (d0 + 2 * p + 1) * W + (W - 1 - k);
+        if (wdt == CCONV_F32) {
+          lo[k] = static_cast<const float*>(w)[i0];
+          hi[k] = static_cast<const float*>(w)[i1];
+        } else {
+          lo[k] = bf16_to_f32(static_cast<const uint16_t*>(w)[i0]);
+          hi[k] = bf16_to_f32(static_cast<const uint16_t*>(w)[i1]);
+        }
+      }
+      tap[k][p] = f2_pack(lo[k], hi[k]);
+    }
+    float b0 = 0.f, b1 = 0.f;
+    if (active && bias) {
+      if (wdt == CCONV_F32) {
+        b0 = static_cast<const float*>(bias)[d0 + 2 * p];
+        b1 = static_cast<const float*>(bias)[d0 + 2 * p + 1];
+      } else {
+        b0 = bf16_to_f32(static_cast<const uint16_t*>(bias)[d0 + 2 * p]);
+        b1 = bf16_to_f32(static_cast<const uint16_t*>(bias)[d0 + 2 * p + 1]);
+      }
+    }
+    bias2[p] = f2_pack(b0, b1);
+  }
+}
+
+// One row of this lane's VEC channels from a shared-memory tile row, as fp32 pairs.
+template <int VEC>
+__device__ __forceinline__ void smem_row(const uint8_t* row, int lane, f2 (&x)[VEC / 2]) {
+  if constexpr (VEC == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + lane * 16);
+    x[0] = bf16x2_to_f2(v.x);
+    x[1] = bf16x2_to_f2(v.y);
+    x[2] = bf16x2_to_f2(v.z);
+    x[3] = bf16x2_to_f2(v.w);
+  } else {
+    static_assert(VEC == 4, "VEC is 4 or 8");
+    const uint2 v = *reinterpret_cast<const uint2*>(row + lane * 8);
+    x[0] = bf16x2_to_f2(v.x);
+    x[1] = bf16x2_to_f2(v.y);
+  }
+}
+
+// Stores one row of this lane's VEC channels (fp32 pairs -> bf16, nearest even).
+template <int VEC>
+__device__ __forceinline__ void store_row(uint16_t* dst, const f2 (&v)[VEC / 2]) {
+  if constexpr (VEC == 8) {
+    uint4 o;
+    o.x = f2_to_bf16x2(v[0]);
+    o.y = f2_to_bf16x2(v[1]);
+    o.z = f2_to_bf16x2(v[2]);
+    o.w = f2_to_bf16x2(v[3]);
+    *reinterpret_cast<uint4*>(dst) = o;
+  } else {
+    uint2 o;
+    o.x = f2_to_bf16x2(v[0]);
+    o.y = f2_to_bf16x2(v[1]);
+    *reinterpret_cast<uint2*>(dst) = o;
+  }
+}
+
+// Host: the strided-[B,T,D] argument rules shared by the forward and the backward.  Inputs
+// are only read, so overlapping rows (any positive stride) are allowed; the copy engine
+// needs 16-byte aligned bases and row / batch strides that are multiples of 8 elements.
+inline int check_rows_tensor(const void* p, int64_t B, int64_t T, int64_t D, int64_t sb,
+                             int64_t st) {
+  (void)D;
+  if (!p) return CCONV_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return CCONV_ERR_ALIGN;
+  if (T > 1) {
+    if (st <= 0) return CCONV_ERR_STRIDE;
+    if (st % 8 != 0) return CCONV_ERR_ALIGN;
+  }
+  if (B > 1) {
+    if (sb <= 0) return CCONV_ERR_STRIDE;
+    if (sb % 8 != 0) return CCONV_ERR_ALIGN;
+  }
+  return CCONV_OK;
+}
+
+// Host: strides as the tensor map needs them (a dimension of extent 1 has a free stride).
+inline void normalise_strides(int64_t B, int64_t T, int64_t D, int64_t& sb, int64_t& st) {
+  (void)B;
+  const int64_t d8 = (D + 7) / 8 * 8;
+  if (T == 1) st = d8;
+  if (B == 1) sb = st * T;
+}
+
+}  // namespace cconv

@@ -1,0 +1,224 @@
+// update.cu -- cconv_update: single-token decode update of a pooled conv state (one kernel).
+//
+// Per row i with slot s = state_indices[i] (or i):
+//   window     = (state[s,d,0..W-2], x[i,d])          state[...,0] is the oldest
+//   y[i,d]     = silu(bias[d] + sum_{j<W} w[d,j] * window[j])
+//   state[s,d] = window[1..W-1]                        (bf16 bits copied exactly)
+// Source: "Add experimental causal conv1d decode update - #797" (NVIDIA/cudnn-frontend),
+// PR summary; the forward's tap orientation (kernel-fun 0.2.0.dev1 wheel,
+// cconv/_kernels/strip.py `_tap`) fixes which tap meets which window entry.
+//
+// Index validation is fused and fails closed without a trap: every CTA loads all N
+// indices, range-checks them and finds repeats with a one-bit-per-slot bitmap in shared
+// memory, so all CTAs reach the same verdict with no inter-CTA communication.  On a bad
+// vector no CTA writes anything but CTA 0's status words.  This replaces the pages'
+// per-CTA O(N^2) scan and device trap with an O(N + S/32) check and a status word.
+#include "common.cuh"
+
+namespace cconv {
+
+struct UpdArgs {
+  const uint16_t* x;  // [N, ldx]
+  uint16_t* state;    // [S, D, L]
+  const int32_t* idx; // [N] or null
+  const void* w;      // [D, W]
+  const void* bias;   // [D] or null
+  uint16_t* y;        // [N, D]
+  int32_t* status;    // [2]
+  int64_t N, D, ldx, S;
+  int wdt;
+  int rows_per_cta;
+};
+
+constexpr int kUpdThreads = 256;
+
+__device__ __forceinline__ float load_w(const void* p, int64_t i, int wdt) {
+  return wdt == CCONV_F32 ? static_cast<const float*>(p)[i]
+                          : bf16_to_f32(static_cast<const uint16_t*>(p)[i]);
+}
+
+__device__ __forceinline__ float silu_f(float z) {
+  return z * fmaf(tanh_approx(0.5f * z), 0.5f, 0.5f);
+}
+
+// VEC = channels per thread (8: 16-byte vectors; 1: scalar path).  L = W - 1.
+template <int VEC, int L>
+__global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs p) {
+  constexpr int W = L + 1;
+  extern __shared__ uint32_t bitmap[];
+  __shared__ int s_bad;
+
+  // ---- validation: identical verdict in every CTA --------------------------------------
+  int bad = 0;
+  if (p.idx) {
+    const int nwords = static_cast<int>((p.S + 31) / 32);
+    if (threadIdx.x == 0) s_bad = 0;
+    for (int i = threadIdx.x; i < nwords; i += kUpdThreads) bitmap[i] = 0u;
+    __syncthreads();
+    int mine = 0;
+    for (int64_t i = threadIdx.x; i < p.N; i += kUpdThreads) {
+      const int32_t v = p.idx[i];
+      if (v < 0) {
+        mine |= CCONV_IDX_NEGATIVE;
+      } else if (v >= p.S) {
+        mine |= CCONV_IDX_OUT_OF_RANGE;
+      } else {
+        const uint32_t m = 1u << (v & 31);
+        if (atomicOr(&bitmap[v >> 5], m) & m) mine |= CCONV_IDX_DUPLICATE;
+      }
+    }
+    if (mine) atomicOr(&s_bad, mine);
+    __syncthreads();
+    bad = s_bad;
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    p.status[0] = bad ? CCONV_ERR_INDEX : CCONV_OK;
+    p.status[1] = bad;
+  }
+  if (bad) return;
+
+  // ---- update: thread -> VEC channels, CTA -> rows_per_cta rows ------------------------
+  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kUpdThreads + threadIdx.x) * VEC;
+  if (d0 >= p.D) return;
+  float tw[VEC][W], tb[VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) tw[v][j] = load_w(p.w, (d0 + v) * W + j, p.wdt);
+    tb[v] = p.bias ? load_w(p.bias, d0 + v, p.wdt) : 0.f;
+  }
+
+  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * p.rows_per_cta;
+  const int64_t i1 = min(p.N, i0 + p.rows_per_cta);
+  for (int64_t i = i0; i < i1; ++i) {
+    const int64_t s = p.idx ? static_cast<int64_t>(p.idx[i]) : i;
+    uint16_t win[VEC][W];
+    uint16_t* st = p.state + (s * p.D + d0) * L;
+    const uint16_t* xr = p.x + i * p.ldx + d0;
+    if constexpr (VEC == 8) {
+      // 8 channels x L state entries are 16*L contiguous bytes; x is one 16-byte vector.
+      uint4 sv[L > 0 ? L : 1];
+#pragma unroll
+      for (int u = 0; u < L; ++u) sv[u] = reinterpret_cast<const uint4*>(st)[u];
+      const uint4 xv = *reinterpret_cast<const uint4*>(xr);
+      const uint16_t* sh = reinterpret_cast<const uint16_t*>(sv);
+      const uint16_t* xh = reinterpret_cast<const uint16_t*>(&xv);
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) {
+#pragma unroll
+        for (int j = 0; j < L; ++j) win[v][j] = sh[v * L + j];
+        win[v][L] = xh[v];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < L; ++j) win[0][j] = st[j];
+      win[0][L] = xr[0];
+    }
+    uint16_t yo[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      float z = tb[v];
+#pragma unroll
+      for (int j = 0; j < W; ++j) z = fmaf(tw[v][j], bf16_to_f32(win[v][j]), z);
+      yo[v] = f32_to_bf16(silu_f(z));
+    }
+    uint16_t* yr = p.y + i * p.D + d0;
+    if constexpr (VEC == 8) {
+      *reinterpret_cast<uint4*>(yr) = *reinterpret_cast<const uint4*>(yo);
+      if constexpr (L > 0) {
+        uint4 nv[L];
+        uint16_t* nh = reinterpret_cast<uint16_t*>(nv);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v)
+#pragma unroll
+          for (int j = 0; j < L; ++j) nh[v * L + j] = win[v][j + 1];
+#pragma unroll
+        for (int u = 0; u < L; ++u) reinterpret_cast<uint4*>(st)[u] = nv[u];
+      }
+    } else {
+      yr[0] = yo[0];
+#pragma unroll
+      for (int j = 0; j < L; ++j) st[j] = win[0][j + 1];
+    }
+  }
+}
+
+typedef void (*UpdKernel)(const UpdArgs);
+
+template <int VEC>
+static UpdKernel pick_update_kernel(int W) {
+  switch (W) {
+    case 1: return cconv_update_kernel<VEC, 0>;
+    case 2: return cconv_update_kernel<VEC, 1>;
+    case 3: return cconv_update_kernel<VEC, 2>;
+    default: return cconv_update_kernel<VEC, 3>;
+  }
+}
+
+}  // namespace cconv
+
+extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx,
+                                      void* state, int64_t S, const int32_t* state_indices,
+                                      const void* w, const void* bias, cconv_dtype wdt, int W,
+                                      void* y, int32_t* status_dev, cconv_stream_t stream) {
+  using namespace cconv;
+  if (!x || !w || !y || !status_dev) return CCONV_ERR_NULL;
+  if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
+  if (W > 1 && !state) return CCONV_ERR_NULL;
+  if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
+  if (N < 1 || D < 1 || S < 0 || N > (int64_t(1) << 31) - 1 || D > (int64_t(1) << 31) - 8)
+    return CCONV_ERR_SHAPE;
+  if (ldx < D) return CCONV_ERR_STRIDE;
+  if (state_indices) {
+    if (S > CCONV_UPDATE_MAX_SLOTS) return CCONV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(state_indices) % 4 != 0) return CCONV_ERR_ALIGN;
+  } else if (S < N) {
+    return CCONV_ERR_SHAPE;
+  }
+  const int ew = wdt == CCONV_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(w) % ew != 0 ||
+      (bias && reinterpret_cast<uintptr_t>(bias) % ew != 0))
+    return CCONV_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(x) % 2 != 0 || reinterpret_cast<uintptr_t>(y) % 2 != 0 ||
+      (state && reinterpret_cast<uintptr_t>(state) % 2 != 0) ||
+      reinterpret_cast<uintptr_t>(status_dev) % 4 != 0)
+    return CCONV_ERR_ALIGN;
+
+  const bool vec8 = D % 8 == 0 && ldx % 8 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
+                    (!state || reinterpret_cast<uintptr_t>(state) % 16 == 0);
+  const int vec = vec8 ? 8 : 1;
+  UpdKernel kern = vec8 ? pick_update_kernel<8>(W) : pick_update_kernel<1>(W);
+
+  UpdArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.state = static_cast<uint16_t*>(state);
+  a.idx = state_indices;
+  a.w = w;
+  a.bias = bias;
+  a.y = static_cast<uint16_t*>(y);
+  a.status = status_dev;
+  a.N = N;
+  a.D = D;
+  a.ldx = ldx;
+  a.S = S;
+  a.wdt = wdt;
+  a.rows_per_cta = 4;
+
+  const int64_t nvec = (D + vec - 1) / vec;
+  const int64_t gx = (nvec + kUpdThreads - 1) / kUpdThreads;
+  const int64_t gy = (N + a.rows_per_cta - 1) / a.rows_per_cta;
+  if (gx > 2147483647 || gy > 65535) {
+    // too many row groups for grid.y: give each CTA more rows
+    a.rows_per_cta = static_cast<int>((N + 65534) / 65535);
+  }
+  const int64_t gy2 = (N + a.rows_per_cta - 1) / a.rows_per_cta;
+  const size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
+  if (smem > 48 * 1024) {
+    if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) != CCONV_OK)
+      return CCONV_ERR_CUDA;
+  }
+  kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy2)), kUpdThreads, smem,
+         reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? CCONV_OK : CCONV_ERR_CUDA;
+}

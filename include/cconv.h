@@ -1,0 +1,171 @@
+/*
+ * cconv.h -- C ABI of the GB300 (sm_103a) depthwise causal short convolution with fused
+ * SiLU: forward, backward and the single-token decode update.
+ *
+ * What the calls compute (sources: the kernel-fun 0.2.0.dev1 wheel, files
+ * kernel_fun/cconv/__init__.py and kernel_fun/cconv/_kernels/strip.py; and the pull
+ * request "Add experimental causal conv1d decode update - #797" on NVIDIA/cudnn-frontend,
+ * PR summary):
+ *
+ *   forward   z[b,t,d] = bias[d] + sum_{k<W} w[d, W-1-k] * x[b, t-k, d]   (x = 0 for t-k < 0)
+ *             y[b,t,d] = silu(z) = z * sigmoid(z)
+ *   backward  g = dy * sigmoid(z) * (1 + z * (1 - sigmoid(z)))            (z recomputed)
+ *             dx[b,t,d]     = sum_{k<W} w[d, W-1-k] * g[b, t+k, d]      (g = 0 for t+k >= T)
+ *             dw[d, W-1-k]  = sum_{b,t} g[b,t,d] * x[b, t-k, d]
+ *             dbias[d]      = sum_{b,t} g[b,t,d]
+ *   decode    per row i, slot s = state_indices[i] (or i): window = (state[s,d,0..W-2], x[i,d]),
+ *             y[i,d] = silu(bias[d] + sum_{j<W} w[d,j] * window[j]),
+ *             state[s,d,:] <- window[1..W-1]  (state[...,0] is the oldest; bits copied exactly)
+ *
+ * Conventions shared by every call:
+ *   - 1 <= W <= 4.  Narrower widths are the width-4 case with zero taps on the old side.
+ *   - Activations (x, dy, y, dx, decode state) are bf16; the weight, bias, dw and dbias
+ *     share one dtype, `wdt` (bf16 or fp32).  Arithmetic is fp32; y, dx, dw and dbias are
+ *     rounded to nearest-even on store.  The sigmoid uses the hardware tanh approximation
+ *     (sigmoid(z) = 0.5 * tanh(z / 2) + 0.5), whose relative error is about 2^-11.
+ *   - All pointers are DEVICE pointers owned by the caller; the library allocates nothing,
+ *     keeps no tensor cache and never aliases one call's buffers into another.
+ *   - All work is enqueued on `stream` (NULL = the legacy default stream) with no host
+ *     synchronisation, so every call may be captured in a CUDA graph.
+ *   - Argument errors are found on the host, before anything is enqueued: the call returns
+ *     a negative cconv_status and launches nothing.  CCONV_OK means "enqueued".
+ *   - Strides are in elements.  The channel stride is 1 for every [.., D] tensor.
+ *   - Fast-path alignment: bf16 row strides must be multiples of 8 elements (16 bytes) and
+ *     every base pointer 16-byte aligned; D must be a multiple of 8 for the forward and
+ *     backward.  Anything else returns CCONV_ERR_ALIGN (no slow path is taken silently).
+ *     The decode update also accepts unaligned rows (ldx == D with any D) on a scalar path.
+ */
+#ifndef CCONV_H
+#define CCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CCONV_API __attribute__((visibility("default")))
+#else
+#define CCONV_API
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* cconv_stream_t;
+
+typedef enum {
+  CCONV_BF16 = 0,
+  CCONV_F32 = 1
+} cconv_dtype;
+
+typedef enum {
+  CCONV_OK = 0,
+  CCONV_ERR_NULL = -1,      /* a required pointer is NULL */
+  CCONV_ERR_SHAPE = -2,     /* a size is out of range (B, T, D, N < 1; S < N without indices; ...) */
+  CCONV_ERR_WIDTH = -3,     /* W outside [1, 4] */
+  CCONV_ERR_ALIGN = -4,     /* a base pointer, row stride or D breaks the 16-byte rule */
+  CCONV_ERR_STRIDE = -5,    /* a stride is not positive (or ldx < D) */
+  CCONV_ERR_DTYPE = -6,     /* unknown cconv_dtype */
+  CCONV_ERR_WORKSPACE = -7, /* workspace NULL or smaller than cconv_bwd_workspace_bytes() */
+  CCONV_ERR_INDEX = -8,     /* decode: state_indices invalid (written to status_dev only) */
+  CCONV_ERR_CUDA = -9,      /* a CUDA runtime / driver call failed */
+  CCONV_ERR_DEVICE = -10    /* a kernel gave up a bounded wait (see cconv_device_fault) */
+} cconv_status;
+
+/* Offence bits of an invalid state_indices vector (status_dev[1] of cconv_update). */
+#define CCONV_IDX_NEGATIVE 1
+#define CCONV_IDX_OUT_OF_RANGE 2
+#define CCONV_IDX_DUPLICATE 4
+
+/* Largest slot pool cconv_update validates in one pass (one bit per slot in shared memory). */
+#define CCONV_UPDATE_MAX_SLOTS 393216
+
+/*
+ * cconv_fwd -- forward of the causal depthwise convolution + SiLU.
+ * Source: kernel-fun 0.2.0.dev1 wheel, cconv/_kernels/strip.py (`_tap`, `_ld_ring`,
+ * `_silu`, `cconv_fwd_strip`); bias added inside the activation.
+ *
+ *   x     [B,T,D] bf16, element (b,t,d) at x[b*sxb + t*sxt + d]; sxt, sxb positive
+ *         multiples of 8 (ignored where the dimension they step over has extent 1); rows
+ *         may overlap (x is only read); base 16-byte aligned.
+ *   w     [D,W] contiguous, dtype wdt.
+ *   bias  [D] dtype wdt, or NULL for no bias.
+ *   y     [B,T,D] bf16 contiguous output, 16-byte aligned.  Must not overlap x.
+ *   B, T, D >= 1, D % 8 == 0, T < 2^31 - 8.
+ */
+CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t D, int64_t sxb,
+                        int64_t sxt, const void* w, const void* bias, cconv_dtype wdt, int W,
+                        void* y, cconv_stream_t stream);
+
+/*
+ * cconv_bwd_workspace_bytes -- scratch that cconv_bwd needs for its per-warp fp32 partial
+ * sums of dw and dbias, for the CURRENT device (the split of work follows its SM count).
+ * Returns CCONV_OK and writes *bytes, or an error for invalid sizes / no device.
+ */
+CCONV_API int cconv_bwd_workspace_bytes(int64_t B, int64_t T, int64_t D, int W,
+                                        size_t* bytes);
+
+/*
+ * cconv_bwd -- backward: dx, dw and (optionally) dbias, with z recomputed from x.
+ * Source: kernel-fun 0.2.0.dev1 wheel, cconv/_kernels/strip.py (`_dsilu`, `_bwd4`,
+ * `cconv_bwd_strip`, `cconv_bwd`): one streaming pass, then a fixed-order (deterministic,
+ * atomic-free) reduction of per-warp partial sums.  Two kernels on `stream`.
+ *
+ *   x, dy   [B,T,D] bf16 with strides (sxb, sxt) and (sdb, sdt); same rules as cconv_fwd.
+ *   w, bias as cconv_fwd (bias may be NULL).
+ *   dx      [B,T,D] bf16 contiguous output, 16-byte aligned, overlapping neither x nor dy.
+ *   dw      [D,W] output in wdt.
+ *   dbias   [D] output in wdt, or NULL to skip it (sum of g; written whether or not a bias
+ *           was passed).
+ *   workspace, workspace_bytes: device scratch of at least cconv_bwd_workspace_bytes(),
+ *           16-byte aligned; contents on entry do not matter.  It must not be shared with
+ *           a concurrently running cconv_bwd.
+ * Results are bit-identical from run to run for the same inputs and device.
+ */
+CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy, int64_t sdb,
+                        int64_t sdt, int64_t B, int64_t T, int64_t D, const void* w,
+                        const void* bias, cconv_dtype wdt, int W, void* dx, void* dw,
+                        void* dbias, void* workspace, size_t workspace_bytes,
+                        cconv_stream_t stream);
+
+/*
+ * cconv_update -- single-token decode update of a pooled bf16 convolution state.
+ * Source: "Add experimental causal conv1d decode update - #797" (NVIDIA/cudnn-frontend),
+ * PR summary: the state rows named by state_indices are read, y is emitted for the new
+ * token, the state shifts by one; invalid indices fail closed.
+ *
+ *   x       [N,D] bf16, row i at x + i*ldx, ldx >= D.
+ *   state   [S,D,W-1] bf16 contiguous pool, read and written in place.
+ *   state_indices [N] int32 slot per row, or NULL (row i uses slot i; needs S >= N).
+ *   w, bias as cconv_fwd.
+ *   y       [N,D] bf16 contiguous output.
+ *   status_dev  int32[2] in device memory, written by the kernel on every call:
+ *           [0] = CCONV_OK or CCONV_ERR_INDEX, [1] = OR of CCONV_IDX_* offence bits.
+ *           An index is invalid when negative, >= S, or (in range and) named twice.  On an
+ *           invalid vector NOTHING is written: neither the state pool nor y.
+ *   S <= CCONV_UPDATE_MAX_SLOTS when state_indices is given.
+ * The vector path needs ldx % 8 == 0, D % 8 == 0 and 16-byte aligned x, state and y;
+ * otherwise a scalar path of the same kernel runs.  Rows must name distinct slots for the
+ * update to be well defined, which the validation enforces.
+ */
+CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx, void* state,
+                           int64_t S, const int32_t* state_indices, const void* w,
+                           const void* bias, cconv_dtype wdt, int W, void* y,
+                           int32_t* status_dev, cconv_stream_t stream);
+
+/* Human-readable name of a cconv_status value (static storage). */
+CCONV_API const char* cconv_status_str(int status);
+
+/*
+ * cconv_device_fault -- reads (and clears) the library's device fault word on the current
+ * device after synchronising it.  *fault = 0 when no kernel has given up a bounded wait;
+ * otherwise a nonzero code naming the kernel.  Returns CCONV_OK or CCONV_ERR_CUDA.
+ */
+CCONV_API int cconv_device_fault(int32_t* fault);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCONV_H */

@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library builds, loads, exports exactly the functions
+include/cconv.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+
+import pytest
+
+import depthwise_causal_short_gb300 as cc
+from depthwise_causal_short_gb300 import _build
+
+BF16, F32 = 0, 1
+OK, ENULL, ESHAPE, EWIDTH, EALIGN, ESTRIDE, EDTYPE = 0, -1, -2, -3, -4, -5, -6
+
+P = 0x100000  # a fake, 16-byte aligned device address; never dereferenced by these tests
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return cc.load()
+
+
+def test_exports_match_header(lib):
+    declared = cc.header_functions()
+    assert set(declared) == {"cconv_fwd", "cconv_bwd_workspace_bytes", "cconv_bwd",
+                             "cconv_update", "cconv_status_str", "cconv_device_fault"}
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in cconv.h but not exported"
+
+
+def test_only_header_symbols_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", str(cc.lib_path())],
+                         capture_output=True, text=True, check=True).stdout
+    names = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert names == set(cc.header_functions())
+
+
+def test_status_strings(lib):
+    for code in range(-10, 1):
+        s = cc.cconv_status_str(code)
+        assert s.startswith(cc.binding.STATUS[code])
+    assert "unknown" in cc.cconv_status_str(-99)
+
+
+def _fwd(lib, x=P, B=2, T=16, D=64, sxb=16 * 64, sxt=64, w=P, bias=None, wdt=F32, W=4, y=P):
+    return lib.cconv_fwd(x, B, T, D, sxb, sxt, w, bias, wdt, W, y, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), ENULL), (dict(w=None), ENULL), (dict(y=None), ENULL),
+    (dict(W=0), EWIDTH), (dict(W=5), EWIDTH), (dict(wdt=7), EDTYPE),
+    (dict(B=0), ESHAPE), (dict(T=0), ESHAPE), (dict(D=0), ESHAPE), (dict(T=1 << 31), ESHAPE),
+    (dict(D=60, sxt=64), EALIGN), (dict(x=P + 2), EALIGN), (dict(y=P + 8), EALIGN),
+    (dict(sxt=68), EALIGN), (dict(sxb=16 * 64 + 4), EALIGN),
+    (dict(sxt=0), ESTRIDE), (dict(sxt=-64), ESTRIDE), (dict(sxb=0), ESTRIDE),
+    (dict(w=P + 2, wdt=F32), EALIGN), (dict(bias=P + 1, wdt=BF16), EALIGN),
+])
+def test_fwd_rejects(lib, kw, expect):
+    assert _fwd(lib, **kw) == expect
+
+
+def _bwd(lib, x=P, dy=P, B=2, T=16, D=64, w=P, bias=None, wdt=F32, W=4, dx=P, dw=P,
+         dbias=None, ws=P, wsb=1 << 30, sxb=16 * 64, sxt=64, sdb=16 * 64, sdt=64):
+    return lib.cconv_bwd(x, sxb, sxt, dy, sdb, sdt, B, T, D, w, bias, wdt, W, dx, dw, dbias, ws,
+                         wsb, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), ENULL), (dict(dy=None), ENULL), (dict(dx=None), ENULL), (dict(dw=None), ENULL),
+    (dict(W=9), EWIDTH), (dict(wdt=2), EDTYPE), (dict(T=0), ESHAPE), (dict(D=12), EALIGN),
+    (dict(dy=P + 4), EALIGN), (dict(dx=P + 2), EALIGN), (dict(sdt=-8), ESTRIDE),
+    (dict(sdb=12), EALIGN), (dict(dbias=P + 2, wdt=F32), EALIGN),
+])
+def test_bwd_rejects(lib, kw, expect):
+    assert _bwd(lib, **kw) == expect
+
+
+def test_workspace_query_rejects(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.cconv_bwd_workspace_bytes(1, 1, 8, 4, None) == ENULL
+    assert lib.cconv_bwd_workspace_bytes(1, 0, 8, 4, ctypes.byref(n)) == ESHAPE
+    assert lib.cconv_bwd_workspace_bytes(1, 1, 8, 0, ctypes.byref(n)) == EWIDTH
+
+
+def _upd(lib, x=P, N=4, D=64, ldx=64, state=P, S=8, idx=P, w=P, bias=None, wdt=F32, W=4, y=P,
+         status=P):
+    return lib.cconv_update(x, N, D, ldx, state, S, idx, w, bias, wdt, W, y, status, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), ENULL), (dict(w=None), ENULL), (dict(y=None), ENULL),
+    (dict(status=None), ENULL), (dict(state=None), ENULL), (dict(W=5), EWIDTH),
+    (dict(wdt=3), EDTYPE), (dict(N=0), ESHAPE), (dict(D=0), ESHAPE), (dict(S=-1), ESHAPE),
+    (dict(ldx=63), ESTRIDE), (dict(idx=None, S=3), ESHAPE),
+    (dict(S=393217), ESHAPE), (dict(idx=P + 2), EALIGN), (dict(status=P + 2), EALIGN),
+    (dict(x=P + 1), EALIGN), (dict(w=P + 2), EALIGN),
+])
+def test_update_rejects(lib, kw, expect):
+    assert _upd(lib, **kw) == expect
