@@ -214,7 +214,8 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
   }
   const int64_t gy2 = (N + a.rows_per_cta - 1) / a.rows_per_cta;
   const size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
-  if (smem > 48 * 1024) {
+  // Dynamic plus static shared memory above 48 KB needs the per-function opt-in.
+  if (smem > 32 * 1024) {
     if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) != CCONV_OK)
       return CCONV_ERR_CUDA;
   }
