@@ -125,7 +125,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * NW + warp;
-  if (gw >= p.total_warps) return;  // no CTA-wide barrier follows
+  if (gw >= p.total_warps) {  // no CTA-wide barrier follows
+    grid_launch_dependents();
+    return;
+  }
 
   uint8_t* stages = smem + warp * (S * STAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
@@ -138,9 +141,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int64_t d0 = c0 + lane * VEC;
   const bool active = d0 < p.D;
 
-  f2 tap[4][P], bias2[P];
-  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
-
   if (lane == 0) {
     prefetch_tensormap(&tmx);
     prefetch_tensormap(&tmdy);
@@ -149,6 +149,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     fence_mbar_init();
   }
   __syncwarp();
+
+  // Everything above touches no global memory; from here on the previous kernel on the
+  // stream has completed.
+  grid_dependency_wait();
 
   TileCursor pc, cc;
   pc.init(r0, r1, p.T, kRing);
@@ -166,6 +170,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
     }
   }
+
+  // Taps load while the first tiles are in flight.
+  f2 tap[4][P], bias2[P];
+  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
 
   f2 h[3][P], gr[3][P], acc[kRec][P];
 #pragma unroll
@@ -225,48 +233,57 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 // dw[d, W-1-lag] and dbias[d] from the wpc partial records of d's strip, summed in a fixed
-// order: thread group j of 8 adds records j, j+8, j+16, ... and the 8 group sums are then
-// added in group order.  Deterministic; no atomics.
-constexpr int kRedGroups = 8;
+// order.  CTA = 32 channels x kRedGroups groups for one record row j (blockIdx.y): group g
+// adds records g, g + G, g + 2G, ... with four interleaved accumulators combined in a fixed
+// order, then the G group sums are added in group order.  Deterministic; no atomics.
+constexpr int kRedGroups = 16;
 
 __global__ void __launch_bounds__(32 * kRedGroups)
     cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int wpc, int64_t D, int W,
                             int wdt, void* dw, void* dbias) {
-  __shared__ float part[kRec][kRedGroups][33];
+  __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x >> 5;
+  const int j = blockIdx.y;
   const int64_t d = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  float a = 0.f;
   if (d < D) {
     const int64_t cb = d / cb_width;
     const int c = static_cast<int>(d - cb * cb_width);
-    const float* base = ws + (cb * wpc) * kRec * cb_width + c;
-#pragma unroll
-    for (int j = 0; j < kRec; ++j) {
-      float a = 0.f;
-      for (int r = grp; r < wpc; r += kRedGroups) a += base[(static_cast<int64_t>(r) * kRec + j) * cb_width];
-      part[j][grp][lane] = a;
+    const int64_t step = static_cast<int64_t>(kRec) * cb_width;
+    const float* base = ws + (cb * wpc) * step + static_cast<int64_t>(j) * cb_width + c;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int r = grp;
+    for (; r + 3 * kRedGroups < wpc; r += 4 * kRedGroups) {
+      a0 += base[r * step];
+      a1 += base[(r + kRedGroups) * step];
+      a2 += base[(r + 2 * kRedGroups) * step];
+      a3 += base[(r + 3 * kRedGroups) * step];
     }
+    for (; r < wpc; r += kRedGroups) a0 += base[r * step];
+    a = (a0 + a1) + (a2 + a3);
   }
+  part[grp][lane] = a;
   __syncthreads();
-  if (grp < kRec && d < D) {
-    float a = 0.f;
+  if (grp == 0 && d < D) {
+    float s = 0.f;
 #pragma unroll
-    for (int g = 0; g < kRedGroups; ++g) a += part[grp][g][lane];
-    if (grp < 4) {
-      const int lag = grp;
+    for (int g = 0; g < kRedGroups; ++g) s += part[g][lane];
+    if (j < 4) {
+      const int lag = j;
       if (lag < W) {
         const int64_t o = d * W + (W - 1 - lag);
         if (wdt == CCONV_F32)
-          static_cast<float*>(dw)[o] = a;
+          static_cast<float*>(dw)[o] = s;
         else
-          static_cast<uint16_t*>(dw)[o] = f32_to_bf16(a);
+          static_cast<uint16_t*>(dw)[o] = f32_to_bf16(s);
       }
     } else if (dbias) {
       if (wdt == CCONV_F32)
-        static_cast<float*>(dbias)[d] = a;
+        static_cast<float*>(dbias)[d] = s;
       else
-        static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(a);
+        static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(s);
     }
   }
 }
@@ -284,6 +301,10 @@ static const BwdConfig kBwdConfigs[] = {
     CCONV_BWD_CFG(8, 8, 3, 8),
     CCONV_BWD_CFG(4, 8, 4, 8),
     CCONV_BWD_CFG(4, 16, 2, 12),
+    CCONV_BWD_CFG(4, 8, 3, 16),
+    CCONV_BWD_CFG(4, 8, 4, 12),
+    CCONV_BWD_CFG(4, 8, 2, 16),
+    CCONV_BWD_CFG(4, 4, 4, 16),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
@@ -384,24 +405,16 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   const int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  cfg.kernel<<<plan.grid, cfg.warps * 32, smem, st>>>(tmx, tmdy, a);
-  if (cudaGetLastError() != cudaSuccess) return CCONV_ERR_CUDA;
-
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(static_cast<unsigned>((D + 31) / 32));
-  lc.blockDim = dim3(32 * kRedGroups);
-  lc.dynamicSmemBytes = 0;
-  lc.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
+  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
+      cudaSuccess)
+    return CCONV_ERR_CUDA;
   const float* wsp = a.ws;
   const int cbw = 32 * cfg.vec;
   const int wpc = plan.wpc;
   const int wdt_i = static_cast<int>(wdt);
-  if (cudaLaunchKernelEx(&lc, cconv_bwd_reduce_kernel, wsp, cbw, wpc, D, W, wdt_i, dw, dbias) !=
+  if (launch_pdl(cconv_bwd_reduce_kernel,
+                 dim3(static_cast<unsigned>((D + 31) / 32), dbias ? kRec : W),
+                 dim3(32 * kRedGroups), 0, st, wsp, cbw, wpc, D, W, wdt_i, dw, dbias) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;

@@ -203,6 +203,30 @@ __device__ __forceinline__ f2 f2_silu(f2 z) {
 }
 
 // ------------------------------------------------------------------------------------
+// host: launch with programmatic stream serialisation.  The kernel may be scheduled
+// before the previous kernel on the stream has finished (once that kernel's CTAs have all
+// triggered or exited); every cconv kernel executes griddepcontrol.wait before its first
+// global-memory access, so it still reads and writes only after the previous kernel has
+// completed and flushed.  Without a trigger in the previous kernel this is an ordinary
+// stream-ordered launch.
+// ------------------------------------------------------------------------------------
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, args...);
+}
+
+// ------------------------------------------------------------------------------------
 // host side helpers (defined in host.cu)
 // ------------------------------------------------------------------------------------
 int sm_count_current_device(int* sms, int* device);

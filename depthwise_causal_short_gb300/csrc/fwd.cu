@@ -72,14 +72,17 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
 
 template <int VEC, int R, int S, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
-    cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
+cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * NW + warp;
-  if (gw >= p.total_warps) return;  // no CTA-wide barrier follows
+  if (gw >= p.total_warps) {  // no CTA-wide barrier follows
+    grid_launch_dependents();
+    return;
+  }
 
   uint8_t* tiles = smem + warp * (S * TILE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * TILE) + warp * S;
@@ -92,9 +95,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int64_t d0 = c0 + lane * VEC;
   const bool active = d0 < p.D;
 
-  f2 tap[4][VEC / 2], bias2[VEC / 2];
-  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
-
   if (lane == 0) {
     prefetch_tensormap(&tmx);
 #pragma unroll
@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     fence_mbar_init();
   }
   __syncwarp();
+
+  // Everything above touches no global memory; from here on the previous kernel on the
+  // stream has completed.
+  grid_dependency_wait();
 
   TileCursor pc, cc;
   pc.init(r0, r1, p.T, 0);
@@ -117,6 +121,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
     }
   }
+
+  // Taps load while the first tiles are in flight.
+  f2 tap[4][VEC / 2], bias2[VEC / 2];
+  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
 
   f2 h[3][VEC / 2];
 #pragma unroll
@@ -152,6 +160,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     cc.advance(R);
     s = (s + 1 == S) ? 0 : s + 1;
   }
+  grid_launch_dependents();
 }
 
 // ------------------------------------------------------------------------------------
@@ -170,6 +179,10 @@ static const FwdConfig kFwdConfigs[] = {
     CCONV_FWD_CFG(8, 8, 4, 8),
     CCONV_FWD_CFG(4, 16, 4, 8),
     CCONV_FWD_CFG(8, 16, 4, 4),
+    CCONV_FWD_CFG(8, 8, 3, 16),
+    CCONV_FWD_CFG(4, 16, 3, 16),
+    CCONV_FWD_CFG(4, 8, 4, 16),
+    CCONV_FWD_CFG(8, 8, 2, 16),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 
@@ -229,6 +242,8 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   const int smem = cfg.warps * cfg.stages * (cfg.rows * 32 * cfg.vec * 2 + 8);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  cfg.kernel<<<plan.grid, cfg.warps * 32, smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmx, a);
-  return cudaGetLastError() == cudaSuccess ? CCONV_OK : CCONV_ERR_CUDA;
+  return launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem,
+                    reinterpret_cast<cudaStream_t>(stream), tmx, a) == cudaSuccess
+             ? CCONV_OK
+             : CCONV_ERR_CUDA;
 }

@@ -27,7 +27,6 @@ struct UpdArgs {
   int32_t* status;    // [2]
   int64_t N, D, ldx, S;
   int wdt;
-  int rows_per_cta;
 };
 
 constexpr int kUpdThreads = 256;
@@ -41,12 +40,67 @@ __device__ __forceinline__ float silu_f(float z) {
   return z * fmaf(tanh_approx(0.5f * z), 0.5f, 0.5f);
 }
 
-// VEC = channels per thread (8: 16-byte vectors; 1: scalar path).  L = W - 1.
-template <int VEC, int L>
+// Taps w[d0..d0+VEC-1][0..W-1] and bias of VEC consecutive channels.  The vector path
+// (VEC = 8) reads them as 16-byte runs: 8 channels x W taps are 32*W contiguous bytes in
+// fp32 (16*W in bf16), and the host only picks it when w and bias are 16-byte aligned.
+template <int VEC, int W>
+__device__ __forceinline__ void load_update_taps(const UpdArgs& p, int64_t d0,
+                                                 float (&tw)[VEC][W], float (&tb)[VEC]) {
+  if constexpr (VEC == 8) {
+    if (p.wdt == CCONV_F32) {
+      float4 v[2 * W];
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.w) + d0 * W);
+#pragma unroll
+      for (int u = 0; u < 2 * W; ++u) v[u] = src[u];
+      const float* f = reinterpret_cast<const float*>(v);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c)
+#pragma unroll
+        for (int j = 0; j < W; ++j) tw[c][j] = f[c * W + j];
+    } else {
+      uint4 v[W];
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.w) + d0 * W);
+#pragma unroll
+      for (int u = 0; u < W; ++u) v[u] = src[u];
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c)
+#pragma unroll
+        for (int j = 0; j < W; ++j) tw[c][j] = bf16_to_f32(h[c * W + j]);
+    }
+    if (!p.bias) {
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) tb[c] = 0.f;
+    } else if (p.wdt == CCONV_F32) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + d0);
+      const float4 b0 = src[0], b1 = src[1];
+      tb[0] = b0.x; tb[1] = b0.y; tb[2] = b0.z; tb[3] = b0.w;
+      tb[4] = b1.x; tb[5] = b1.y; tb[6] = b1.z; tb[7] = b1.w;
+    } else {
+      const uint4 b = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + d0);
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(&b);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) tb[c] = bf16_to_f32(h[c]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) tw[c][j] = load_w(p.w, (d0 + c) * W + j, p.wdt);
+      tb[c] = p.bias ? load_w(p.bias, d0 + c, p.wdt) : 0.f;
+    }
+  }
+}
+
+// VEC = channels per thread (8: 16-byte vectors; 1: scalar path), L = W - 1, ROWS = rows
+// per thread.  Grid: x over channel vectors, y over groups of ROWS rows.
+template <int VEC, int L, int ROWS>
 __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs p) {
   constexpr int W = L + 1;
   extern __shared__ uint32_t bitmap[];
   __shared__ int s_bad;
+
+  grid_dependency_wait();
 
   // ---- validation: identical verdict in every CTA --------------------------------------
   int bad = 0;
@@ -75,26 +129,26 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
     p.status[0] = bad ? CCONV_ERR_INDEX : CCONV_OK;
     p.status[1] = bad;
   }
-  if (bad) return;
-
-  // ---- update: thread -> VEC channels, CTA -> rows_per_cta rows ------------------------
   const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kUpdThreads + threadIdx.x) * VEC;
-  if (d0 >= p.D) return;
-  float tw[VEC][W], tb[VEC];
-#pragma unroll
-  for (int v = 0; v < VEC; ++v) {
-#pragma unroll
-    for (int j = 0; j < W; ++j) tw[v][j] = load_w(p.w, (d0 + v) * W + j, p.wdt);
-    tb[v] = p.bias ? load_w(p.bias, d0 + v, p.wdt) : 0.f;
+  if (bad || d0 >= p.D) {
+    grid_launch_dependents();
+    return;
   }
 
-  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * p.rows_per_cta;
-  const int64_t i1 = min(p.N, i0 + p.rows_per_cta);
-  for (int64_t i = i0; i < i1; ++i) {
-    const int64_t s = p.idx ? static_cast<int64_t>(p.idx[i]) : i;
-    uint16_t win[VEC][W];
-    uint16_t* st = p.state + (s * p.D + d0) * L;
-    const uint16_t* xr = p.x + i * p.ldx + d0;
+  // ---- update: all of this thread's rows are loaded before any is computed -------------
+  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * ROWS;
+  int64_t slot[ROWS];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    const int64_t i = i0 + r;
+    slot[r] = (i < p.N) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
+  }
+  uint16_t win[ROWS][VEC][W];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    if (slot[r] < 0) continue;
+    const uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
+    const uint16_t* xr = p.x + (i0 + r) * p.ldx + d0;
     if constexpr (VEC == 8) {
       // 8 channels x L state entries are 16*L contiguous bytes; x is one 16-byte vector.
       uint4 sv[L > 0 ? L : 1];
@@ -104,54 +158,72 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
       const uint16_t* sh = reinterpret_cast<const uint16_t*>(sv);
       const uint16_t* xh = reinterpret_cast<const uint16_t*>(&xv);
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) {
+      for (int c = 0; c < VEC; ++c) {
 #pragma unroll
-        for (int j = 0; j < L; ++j) win[v][j] = sh[v * L + j];
-        win[v][L] = xh[v];
+        for (int j = 0; j < L; ++j) win[r][c][j] = sh[c * L + j];
+        win[r][c][L] = xh[c];
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < L; ++j) win[0][j] = st[j];
-      win[0][L] = xr[0];
+      for (int j = 0; j < L; ++j) win[r][0][j] = st[j];
+      win[r][0][L] = xr[0];
     }
+  }
+  float tw[VEC][W], tb[VEC];
+  load_update_taps<VEC, W>(p, d0, tw, tb);
+  grid_launch_dependents();
+
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    if (slot[r] < 0) continue;
     uint16_t yo[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-      float z = tb[v];
+    for (int c = 0; c < VEC; ++c) {
+      float z = tb[c];
 #pragma unroll
-      for (int j = 0; j < W; ++j) z = fmaf(tw[v][j], bf16_to_f32(win[v][j]), z);
-      yo[v] = f32_to_bf16(silu_f(z));
+      for (int j = 0; j < W; ++j) z = fmaf(tw[c][j], bf16_to_f32(win[r][c][j]), z);
+      yo[c] = f32_to_bf16(silu_f(z));
     }
-    uint16_t* yr = p.y + i * p.D + d0;
+    uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
+    uint16_t* yr = p.y + (i0 + r) * p.D + d0;
     if constexpr (VEC == 8) {
       *reinterpret_cast<uint4*>(yr) = *reinterpret_cast<const uint4*>(yo);
       if constexpr (L > 0) {
         uint4 nv[L];
         uint16_t* nh = reinterpret_cast<uint16_t*>(nv);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v)
+        for (int c = 0; c < VEC; ++c)
 #pragma unroll
-          for (int j = 0; j < L; ++j) nh[v * L + j] = win[v][j + 1];
+          for (int j = 0; j < L; ++j) nh[c * L + j] = win[r][c][j + 1];
 #pragma unroll
         for (int u = 0; u < L; ++u) reinterpret_cast<uint4*>(st)[u] = nv[u];
       }
     } else {
       yr[0] = yo[0];
 #pragma unroll
-      for (int j = 0; j < L; ++j) st[j] = win[0][j + 1];
+      for (int j = 0; j < L; ++j) st[j] = win[r][0][j + 1];
     }
   }
 }
 
 typedef void (*UpdKernel)(const UpdArgs);
 
-template <int VEC>
-static UpdKernel pick_update_kernel(int W) {
+template <int VEC, int ROWS>
+static UpdKernel pick_update_kernel_w(int W) {
   switch (W) {
-    case 1: return cconv_update_kernel<VEC, 0>;
-    case 2: return cconv_update_kernel<VEC, 1>;
-    case 3: return cconv_update_kernel<VEC, 2>;
-    default: return cconv_update_kernel<VEC, 3>;
+    case 1: return cconv_update_kernel<VEC, 0, ROWS>;
+    case 2: return cconv_update_kernel<VEC, 1, ROWS>;
+    case 3: return cconv_update_kernel<VEC, 2, ROWS>;
+    default: return cconv_update_kernel<VEC, 3, ROWS>;
+  }
+}
+
+template <int VEC>
+static UpdKernel pick_update_kernel(int W, int rows) {
+  switch (rows) {
+    case 1: return pick_update_kernel_w<VEC, 1>(W);
+    case 2: return pick_update_kernel_w<VEC, 2>(W);
+    default: return pick_update_kernel_w<VEC, 4>(W);
   }
 }
 
@@ -184,11 +256,26 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
       reinterpret_cast<uintptr_t>(status_dev) % 4 != 0)
     return CCONV_ERR_ALIGN;
 
+  const int ew16 = 16;
   const bool vec8 = D % 8 == 0 && ldx % 8 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
                     reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
-                    (!state || reinterpret_cast<uintptr_t>(state) % 16 == 0);
+                    (!state || reinterpret_cast<uintptr_t>(state) % 16 == 0) &&
+                    reinterpret_cast<uintptr_t>(w) % ew16 == 0 &&
+                    (!bias || reinterpret_cast<uintptr_t>(bias) % ew16 == 0);
   const int vec = vec8 ? 8 : 1;
-  UpdKernel kern = vec8 ? pick_update_kernel<8>(W) : pick_update_kernel<1>(W);
+
+  int sms = 0;
+  int rc = sm_count_current_device(&sms, nullptr);
+  if (rc != CCONV_OK) return rc;
+  // Rows per thread: the fewest that keep the grid within about four CTAs per SM (every
+  // CTA repeats the O(N) index check, so more rows per CTA also means fewer repeats).
+  const int64_t nvec = (D + vec - 1) / vec;
+  const int64_t gx = (nvec + kUpdThreads - 1) / kUpdThreads;
+  int rows = 1;
+  while (rows < 4 && gx * ((N + rows - 1) / rows) > 4 * static_cast<int64_t>(sms)) rows *= 2;
+  const int64_t gy = (N + rows - 1) / rows;
+  if (gx > 2147483647 || gy > 65535) return CCONV_ERR_SHAPE;
+  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows) : pick_update_kernel<1>(W, rows);
 
   UpdArgs a;
   a.x = static_cast<const uint16_t*>(x);
@@ -203,23 +290,17 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
   a.ldx = ldx;
   a.S = S;
   a.wdt = wdt;
-  a.rows_per_cta = 4;
 
-  const int64_t nvec = (D + vec - 1) / vec;
-  const int64_t gx = (nvec + kUpdThreads - 1) / kUpdThreads;
-  const int64_t gy = (N + a.rows_per_cta - 1) / a.rows_per_cta;
-  if (gx > 2147483647 || gy > 65535) {
-    // too many row groups for grid.y: give each CTA more rows
-    a.rows_per_cta = static_cast<int>((N + 65534) / 65535);
-  }
-  const int64_t gy2 = (N + a.rows_per_cta - 1) / a.rows_per_cta;
   const size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
   // Dynamic plus static shared memory above 48 KB needs the per-function opt-in.
   if (smem > 32 * 1024) {
     if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) != CCONV_OK)
       return CCONV_ERR_CUDA;
   }
-  kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy2)), kUpdThreads, smem,
-         reinterpret_cast<cudaStream_t>(stream)>>>(a);
-  return cudaGetLastError() == cudaSuccess ? CCONV_OK : CCONV_ERR_CUDA;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
+                    dim3(kUpdThreads), smem, reinterpret_cast<cudaStream_t>(stream), a) ==
+                 cudaSuccess
+             ? CCONV_OK
+             : CCONV_ERR_CUDA;
 }
+
