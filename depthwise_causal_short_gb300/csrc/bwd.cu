@@ -57,6 +57,7 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int64_t t = c.tt + i;
+    if (!FULL && t < c.from) continue;  // processed with the previous tile
     f2 x[P], g[P];
     smem_row<VEC>(xt + i * ROWB, lane, x);
     const bool live = FULL || t >= c.a;  // rows before the range only fill the x ring
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   grid_dependency_wait();
 
   TileCursor pc, cc;
-  pc.init(r0, r1, p.T, kRing);
+  pc.init(r0, r1, p.T, kRing, R);
   cc = pc;
   const uint64_t pol = policy_evict_first();
   if (lane == 0) {
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
         tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, static_cast<int>(pc.tt),
                     pc.b, pol);
-        pc.advance(R);
+        pc.advance();
       }
     }
   }
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     parity ^= 1u << s;
     const uint8_t* xt = stages + s * STAGE;
-    const bool full = cc.tt >= cc.a + kRing && cc.tt + R <= cc.e;
+    const bool full = cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e;
     if (full)
       bwd_tile<VEC, R, true>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
     else
@@ -211,9 +212,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
       tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
       tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, static_cast<int>(pc.tt), pc.b,
                   pol);
-      pc.advance(R);
+      pc.advance();
     }
-    cc.advance(R);
+    cc.advance();
     s = (s + 1 == S) ? 0 : s + 1;
   }
 

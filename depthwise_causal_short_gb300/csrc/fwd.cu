@@ -46,6 +46,7 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int64_t t = c.tt + i;
+    if (!full && t < c.from) continue;  // processed with the previous tile
     f2 x[P];
     smem_row<VEC>(tile + i * ROWB, lane, x);
     const bool emit = full || (t >= c.a && t < c.e);
@@ -108,7 +109,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   grid_dependency_wait();
 
   TileCursor pc, cc;
-  pc.init(r0, r1, p.T, 0);
+  pc.init(r0, r1, p.T, 0, R);
   cc = pc;
   const uint64_t pol = policy_evict_first();
   if (lane == 0) {
@@ -117,7 +118,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
       if (!pc.done) {
         mbar_arrive_expect_tx(&bars[s], TILE);
         tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
-        pc.advance(R);
+        pc.advance();
       }
     }
   }
@@ -145,7 +146,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     }
     parity ^= 1u << s;
     const uint8_t* tile = tiles + s * TILE;
-    const bool full = cc.tt >= cc.a && cc.tt + R <= cc.e;
+    const bool full = cc.from == cc.tt && cc.tt >= cc.a && cc.tt + R <= cc.e;
     if (full)
       fwd_tile<VEC, R>(tile, lane, cc, true, active, p, d0, tap, bias2, h);
     else
@@ -155,9 +156,9 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&bars[s], TILE);
       tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
-      pc.advance(R);
+      pc.advance();
     }
-    cc.advance(R);
+    cc.advance();
     s = (s + 1 == S) ? 0 : s + 1;
   }
   grid_launch_dependents();

@@ -44,30 +44,47 @@ inline StripPlan make_strip_plan(int64_t B, int64_t T, int64_t D, int vec, int w
 
 // Walks the tiles of one warp's row range [r0, r1) of the flattened (b, t) space.
 // A segment is the part of the range inside one sequence: rows [a, e) of batch b.  Its
-// tiles start at a - kRing and step by R until they cover e + tail - 1 (tail = 0 for the
-// forward; 3 for the backward, whose last dx rows need g of the next 3 rows).
+// rows a - kRing .. e + tail - 1 are needed (tail = 0 for the forward; 3 for the backward,
+// whose last dx rows need g of the next 3 rows).  Tiles start at a - kRing and step by R;
+// the last one is pulled back so that it ends at e + tail instead of reading rows of the
+// next warp's range (those would be read from DRAM twice).  `from` is the first row of the
+// current tile that has not been processed yet: rows before it, shared with the previous
+// tile, are skipped.
 struct TileCursor {
   int64_t T, r1;
-  int64_t a, e, tt;
+  int64_t a, e, tt, from;
   int b;
   int tail;
+  int R;
   bool done;
 
-  __device__ __forceinline__ void init(int64_t r0, int64_t r1_, int64_t T_, int tail_) {
+  __device__ __forceinline__ void place(int64_t start) {
+    from = start;
+    tt = start;
+    const int64_t lim = e + tail;
+    if (tt + R > lim) {
+      const int64_t back = lim - R;
+      tt = back > a - kRing ? back : a - kRing;
+      if (tt > from) tt = from;
+    }
+  }
+
+  __device__ __forceinline__ void init(int64_t r0, int64_t r1_, int64_t T_, int tail_, int R_) {
     T = T_;
     r1 = r1_;
     tail = tail_;
+    R = R_;
     done = r0 >= r1_;
     b = static_cast<int>(r0 / T_);
     a = r0 - static_cast<int64_t>(b) * T_;
     const int64_t rest = r1_ - r0;
     e = (a + rest < T_) ? a + rest : T_;
-    tt = a - kRing;
+    place(a - kRing);
   }
 
-  __device__ __forceinline__ void advance(int R) {
-    tt += R;
-    if (tt >= e + tail) {
+  __device__ __forceinline__ void advance() {
+    const int64_t next = tt + R;
+    if (next >= e + tail) {
       const int64_t r = static_cast<int64_t>(b) * T + e;  // next flattened row
       if (r >= r1) {
         done = true;
@@ -77,8 +94,10 @@ struct TileCursor {
       a = 0;
       const int64_t rest = r1 - static_cast<int64_t>(b) * T;
       e = rest < T ? rest : T;
-      tt = -kRing;
+      place(-kRing);
+      return;
     }
+    place(next);
   }
 };
 
