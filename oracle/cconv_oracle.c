@@ -175,6 +175,7 @@ int oracle_update(int64_t N, int64_t D, int W, const uint16_t* x, uint16_t* stat
   uint16_t window[8];
   for (int64_t i = 0; i < N; ++i) {
     const int64_t s = idx ? (int64_t)idx[i] : i;
+    if (s < 0 || s >= S) return -1; /* unreachable after a correct validation */
     for (int64_t d = 0; d < D; ++d) {
       uint16_t* st = state + (s * D + d) * L;
       for (int j = 0; j < L; ++j) window[j] = st[j];

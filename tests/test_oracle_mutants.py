@@ -46,8 +46,8 @@ def _run_pins(o):
     for pin in oracle_pins.ALL_PINS:
         try:
             pin(o)
-        except AssertionError as e:
-            failed.append(f"{pin.__name__}: {str(e)[:80]}")
+        except Exception as e:  # an assertion, or the oracle refusing its own result
+            failed.append(f"{pin.__name__}: {type(e).__name__}: {str(e)[:80]}")
     return failed
 
 
