@@ -37,7 +37,7 @@ struct BwdArgs {
   uint16_t* dx;   // [B,T,D] contiguous bf16
   float* ws;      // [total_warps][kRec][32*VEC] fp32 partials
   int64_t T, D, BT;
-  int wpc, total_warps;
+  int n_cb, wpc, total_warps;
   int W, wdt;
 };
 
@@ -134,8 +134,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
   uint8_t* stages = smem + warp * (S * STAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
 
-  const int cb = gw / p.wpc;
-  const int k = gw - cb * p.wpc;
+  // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
+  // strips of the same rows at about the same time (contiguous row segments in DRAM).
+  const int k = gw / p.n_cb;
+  const int cb = gw - k * p.n_cb;
   const int64_t r0 = static_cast<int64_t>(k) * p.BT / p.wpc;
   const int64_t r1 = static_cast<int64_t>(k + 1) * p.BT / p.wpc;
   const int c0 = cb * CB;
@@ -240,8 +242,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
 constexpr int kRedGroups = 16;
 
 __global__ void __launch_bounds__(32 * kRedGroups)
-    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int wpc, int64_t D, int W,
-                            int wdt, void* dw, void* dbias) {
+    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int n_cb, int wpc,
+                            int64_t D, int W, int wdt, void* dw, void* dbias) {
   __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
@@ -252,8 +254,9 @@ __global__ void __launch_bounds__(32 * kRedGroups)
   if (d < D) {
     const int64_t cb = d / cb_width;
     const int c = static_cast<int>(d - cb * cb_width);
-    const int64_t step = static_cast<int64_t>(kRec) * cb_width;
-    const float* base = ws + (cb * wpc) * step + static_cast<int64_t>(j) * cb_width + c;
+    // strip cb's records are those of warps k * n_cb + cb, k = 0 .. wpc-1
+    const int64_t step = static_cast<int64_t>(kRec) * cb_width * n_cb;
+    const float* base = ws + cb * kRec * cb_width + static_cast<int64_t>(j) * cb_width + c;
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     int r = grp;
     for (; r + 3 * kRedGroups < wpc; r += 4 * kRedGroups) {
@@ -397,6 +400,7 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   a.T = T;
   a.D = D;
   a.BT = B * T;
+  a.n_cb = plan.n_cb;
   a.wpc = plan.wpc;
   a.total_warps = plan.total_warps;
   a.W = W;
@@ -415,7 +419,7 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   const int wdt_i = static_cast<int>(wdt);
   if (launch_pdl(cconv_bwd_reduce_kernel,
                  dim3(static_cast<unsigned>((D + 31) / 32), dbias ? kRec : W),
-                 dim3(32 * kRedGroups), 0, st, wsp, cbw, wpc, D, W, wdt_i, dw, dbias) !=
+                 dim3(32 * kRedGroups), 0, st, wsp, cbw, plan.n_cb, wpc, D, W, wdt_i, dw, dbias) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;

@@ -31,7 +31,7 @@ struct FwdArgs {
   const void* bias;
   uint16_t* y;  // [B,T,D] contiguous bf16
   int64_t T, D, BT;
-  int wpc, total_warps;
+  int n_cb, wpc, total_warps;
   int W, wdt;
 };
 
@@ -88,8 +88,10 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   uint8_t* tiles = smem + warp * (S * TILE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * TILE) + warp * S;
 
-  const int cb = gw / p.wpc;
-  const int k = gw - cb * p.wpc;
+  // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
+  // strips of the same rows at about the same time (contiguous row segments in DRAM).
+  const int k = gw / p.n_cb;
+  const int cb = gw - k * p.n_cb;
   const int64_t r0 = static_cast<int64_t>(k) * p.BT / p.wpc;
   const int64_t r1 = static_cast<int64_t>(k + 1) * p.BT / p.wpc;
   const int c0 = cb * CB;
@@ -235,6 +237,7 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   a.T = T;
   a.D = D;
   a.BT = B * T;
+  a.n_cb = plan.n_cb;
   a.wpc = plan.wpc;
   a.total_warps = plan.total_warps;
   a.W = W;

@@ -4,7 +4,8 @@
 // row of the strip as one coalesced 16-byte (VEC=8) or 8-byte (VEC=4) access per lane.
 // Each strip's rows, flattened over (b, t), are cut into `wpc` equal contiguous ranges, one
 // per warp, so every warp of the grid gets the same number of rows (to within one) and the
-// grid is one wave of resident CTAs.  A warp walks its range in time order, tile by tile,
+// grid is one wave of resident CTAs.  Warp gw takes strip gw % n_cb of range gw / n_cb:
+// the warps of one CTA cover neighbouring strips of the same rows.  A warp walks its range in time order, tile by tile,
 // keeping the W-1 previous rows in registers (the ring).  Where a range starts inside a
 // sequence, its first tile starts 3 rows early to fill the ring; where it starts a sequence,
 // those 3 rows lie at t < 0 and the copy engine fills them with zeros, which is exactly the
