@@ -301,13 +301,13 @@ struct BwdConfig {
   BwdConfig { V, R, S, NW, cconv_bwd_kernel<V, R, S, NW> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 16, 3, 8),
+    CCONV_BWD_CFG(4, 8, 2, 16),  // measured fastest at B=2 T=8192 D=4096
     CCONV_BWD_CFG(8, 8, 3, 8),
     CCONV_BWD_CFG(4, 8, 4, 8),
     CCONV_BWD_CFG(4, 16, 2, 12),
     CCONV_BWD_CFG(4, 8, 3, 16),
     CCONV_BWD_CFG(4, 8, 4, 12),
-    CCONV_BWD_CFG(4, 8, 2, 16),
+    CCONV_BWD_CFG(4, 16, 3, 8),
     CCONV_BWD_CFG(4, 4, 4, 16),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
