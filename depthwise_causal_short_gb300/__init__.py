@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     IDX_OUT_OF_RANGE,
     CConvError,
     cconv_bwd,
+    cconv_bwd_noalloc,
     cconv_bwd_workspace_bytes,
     cconv_device_fault,
     cconv_fwd,

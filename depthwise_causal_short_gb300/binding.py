@@ -63,6 +63,9 @@ def load(path: str | Path | None = None):
     lib.cconv_bwd.argtypes = [_P, _I64, _I64, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _INT,
                               _INT, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.cconv_bwd.restype = _INT
+    lib.cconv_bwd_noalloc.argtypes = [_P, _I64, _I64, _P, _I64, _I64, _I64, _I64, _I64, _P, _P,
+                                      _INT, _INT, _P, _P, _P, _P]
+    lib.cconv_bwd_noalloc.restype = _INT
     lib.cconv_update.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _INT, _INT, _P, _P, _P]
     lib.cconv_update.restype = _INT
     lib.cconv_status_str.argtypes = [_INT]
@@ -168,6 +171,22 @@ def cconv_bwd(x: torch.Tensor, dy: torch.Tensor, w: torch.Tensor,
                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "cconv_bwd")
     return dx, dw, (dbias if want_dbias else None)
+
+
+def cconv_bwd_noalloc(x: torch.Tensor, dy: torch.Tensor, w: torch.Tensor,
+                      bias: torch.Tensor | None = None, *, dx: torch.Tensor,
+                      dw: torch.Tensor, dbias: torch.Tensor | None = None, stream=None):
+    """cconv_bwd for callers that cannot allocate device memory at this point: every output
+    must be passed in, and the partial sums use the library's fixed 8 MiB device scratch
+    array instead of a workspace.  Calls that overlap on the GPU race on that array."""
+    _bf16_rows(x, "x")
+    _bf16_rows(dy, "dy")
+    B, T, D = x.shape
+    rc = load().cconv_bwd_noalloc(_ptr(x), x.stride(0), x.stride(1), _ptr(dy), dy.stride(0),
+                                  dy.stride(1), B, T, D, _ptr(w), _ptr(bias), _wdt(w), w.shape[1],
+                                  _ptr(dx), _ptr(dw), _ptr(dbias), _stream(stream))
+    _check(rc, "cconv_bwd_noalloc")
+    return dx, dw, dbias
 
 
 def cconv_update(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,

@@ -16,6 +16,8 @@
 // whole range, the time sum needs no shuffles; the cross-warp sum is a second small kernel
 // that adds each strip's records in a fixed order, launched as a programmatic dependent of
 // the first so its launch overlaps the stream's tail.
+#include <mutex>
+
 #include "strip.cuh"
 
 namespace cconv {
@@ -426,3 +428,68 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
 }
 
 }  // extern "C"
+
+namespace cconv {
+
+// ------------------------------------------------------------------------------------
+// cconv_bwd_noalloc: the backward with its scratch in a fixed device array.
+//
+// Some callers cannot allocate device memory at the point where they run the backward:
+// an inference or training runtime that hands out memory only from an arena it sized up
+// front, a plugin inside another framework that owns every allocation, or a host thread
+// that must not call cudaMalloc because cudaMalloc can synchronise the device and stall
+// other streams.  For them this entry point takes its per-warp partial sums from
+// g_bwd_noalloc_scratch, a file-scope __device__ array of kBwdNoallocScratchBytes that every
+// GPU loading this library holds until the process exits.  The caller still passes all
+// inputs and outputs; nothing here calls cudaMalloc, cudaFree or any allocating routine.
+//
+// Host code cannot use the array's name as a device address (it names a host-side
+// stand-in), so the first call on each device, with that device current, looks the
+// address up with cudaGetSymbolAddress and keeps it.  That first call should therefore
+// happen before any stream capture.  All calls on a device share the array, which keeps
+// whatever the last call left in it; nothing in it needs to start at zero, because every
+// record is fully written before it is read.  Calls whose work overlaps on the GPU (for
+// example on two streams) race on the array and must be serialised by the caller.
+// ------------------------------------------------------------------------------------
+constexpr size_t kBwdNoallocScratchBytes = size_t(8) << 20;  // 8 MiB
+
+static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[kBwdNoallocScratchBytes];
+
+static void* bwd_noalloc_scratch_address(int* status) {
+  static void* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *status = CCONV_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || !p) {
+      *status = CCONV_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *status = CCONV_OK;
+  return addr[dev];
+}
+
+}  // namespace cconv
+
+extern "C" CCONV_API int cconv_bwd_noalloc(const void* x, int64_t sxb, int64_t sxt,
+                                           const void* dy, int64_t sdb, int64_t sdt, int64_t B,
+                                           int64_t T, int64_t D, const void* w,
+                                           const void* bias, cconv_dtype wdt, int W, void* dx,
+                                           void* dw, void* dbias, cconv_stream_t stream) {
+  using namespace cconv;
+  size_t need = 0;
+  int rc = cconv_bwd_workspace_bytes(B, T, D, W, &need);
+  if (rc != CCONV_OK) return rc;
+  if (need > kBwdNoallocScratchBytes) return CCONV_ERR_WORKSPACE;  // too large for the array
+  void* scratch = bwd_noalloc_scratch_address(&rc);
+  if (rc != CCONV_OK) return rc;
+  return cconv_bwd(x, sxb, sxt, dy, sdb, sdt, B, T, D, w, bias, wdt, W, dx, dw, dbias, scratch,
+                   kBwdNoallocScratchBytes, stream);
+}

@@ -154,6 +154,26 @@ CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx, voi
                            const void* bias, cconv_dtype wdt, int W, void* y,
                            int32_t* status_dev, cconv_stream_t stream);
 
+/*
+ * cconv_bwd_noalloc -- cconv_bwd without a workspace argument, for callers that cannot
+ * allocate device memory where they run the backward (a runtime that hands out memory only
+ * from a pre-sized arena, a plugin inside a framework that owns every allocation, a thread
+ * that must not call cudaMalloc because it can synchronise the device).  The pages have no
+ * counterpart to this call; it exists for those callers.
+ *
+ * Arguments and results are those of cconv_bwd minus (workspace, workspace_bytes).  The
+ * partial sums live in a fixed 8 MiB device array inside the library (held by every GPU
+ * that loads it until the process exits); a problem whose cconv_bwd_workspace_bytes()
+ * exceeds 8 MiB returns CCONV_ERR_WORKSPACE.  The call allocates nothing.  Its first call on
+ * a device (with that device current) looks up the array's device address, so make that
+ * first call before any stream capture.  All calls on a device share the array: calls whose
+ * work overlaps on the GPU race and must be serialised by the caller.
+ */
+CCONV_API int cconv_bwd_noalloc(const void* x, int64_t sxb, int64_t sxt, const void* dy,
+                                int64_t sdb, int64_t sdt, int64_t B, int64_t T, int64_t D,
+                                const void* w, const void* bias, cconv_dtype wdt, int W,
+                                void* dx, void* dw, void* dbias, cconv_stream_t stream);
+
 /* Human-readable name of a cconv_status value (static storage). */
 CCONV_API const char* cconv_status_str(int status);
 

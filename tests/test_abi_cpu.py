@@ -22,7 +22,8 @@ def lib():
 def test_exports_match_header(lib):
     declared = cc.header_functions()
     assert set(declared) == {"cconv_fwd", "cconv_bwd_workspace_bytes", "cconv_bwd",
-                             "cconv_update", "cconv_status_str", "cconv_device_fault"}
+                             "cconv_bwd_noalloc", "cconv_update", "cconv_status_str",
+                             "cconv_device_fault"}
     for name in declared:
         assert hasattr(lib, name), f"{name} declared in cconv.h but not exported"
 
