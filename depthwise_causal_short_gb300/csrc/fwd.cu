@@ -30,50 +30,83 @@ struct FwdArgs {
   const void* w;
   const void* bias;
   uint16_t* y;  // [B,T,D] contiguous bf16
-  int64_t T, D, BT;
+  int64_t D;
+  int T, BT;
   int n_cb, wpc, total_warps;
   int W, wdt;
 };
 
+// One output row from the new input row x and the ring h = (x[t-1], x[t-2], x[t-3]).
+template <int P>
+__device__ __forceinline__ void fwd_row(const f2 (&x)[P], const f2 (&h)[3][P],
+                                        const f2 (&tap)[4][P], const f2 (&bias2)[P],
+                                        f2 (&yv)[P]) {
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
+    z = f2_fma(tap[1][q], h[0][q], z);
+    z = f2_fma(tap[2][q], h[1][q], z);
+    z = f2_fma(tap[3][q], h[2][q], z);
+    yv[q] = f2_silu(z);
+  }
+}
+
+template <int P>
+__device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    h[2][q] = h[1][q];
+    h[1][q] = h[0][q];
+    h[0][q] = x[q];
+  }
+}
+
+// A tile whose R rows all lie inside the segment: y overwrites x in the tile, row by row
+// (each lane rewrites exactly the bytes it read), and the tile leaves by one TMA store.
 template <int VEC, int R>
-__device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const TileCursor& c,
-                                         bool full, bool active, const FwdArgs& p, int64_t d0,
-                                         const f2 (&tap)[4][VEC / 2], const f2 (&bias2)[VEC / 2],
-                                         f2 (&h)[3][VEC / 2]) {
+__device__ __forceinline__ void fwd_tile_full(uint8_t* tile, int lane, const f2 (&tap)[4][VEC / 2],
+                                              const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2]) {
   constexpr int P = VEC / 2;
   constexpr int ROWB = 32 * VEC * 2;
-  uint16_t* ybase = p.y + (static_cast<int64_t>(c.b) * p.T) * p.D + d0;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
-    const int64_t t = c.tt + i;
-    if (!full && t < c.from) continue;  // processed with the previous tile
+    f2 x[P], yv[P];
+    smem_row<VEC>(tile + i * ROWB, lane, x);
+    fwd_row<P>(x, h, tap, bias2, yv);
+    smem_store_row<VEC>(tile + i * ROWB, lane, yv);
+    ring_push<P>(h, x);
+  }
+}
+
+// The first tile of a segment (rows before a only fill the ring) or a last tile pulled
+// back over rows already done (skipped): rows are stored one by one.
+template <int VEC, int R>
+__device__ __forceinline__ void fwd_tile_edge(const uint8_t* tile, int lane, const TileCursor& c,
+                                              bool active, const FwdArgs& p, int64_t d0,
+                                              const f2 (&tap)[4][VEC / 2],
+                                              const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2]) {
+  constexpr int P = VEC / 2;
+  constexpr int ROWB = 32 * VEC * 2;
+  uint16_t* ybase = p.y + static_cast<int64_t>(c.b) * p.T * p.D + d0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int t = c.tt + i;
+    if (t < c.from) continue;  // processed with the previous tile
     f2 x[P];
     smem_row<VEC>(tile + i * ROWB, lane, x);
-    const bool emit = full || (t >= c.a && t < c.e);
-    if (emit) {
+    if (t >= c.a && t < c.e) {
       f2 yv[P];
-#pragma unroll
-      for (int q = 0; q < P; ++q) {
-        f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
-        z = f2_fma(tap[1][q], h[0][q], z);
-        z = f2_fma(tap[2][q], h[1][q], z);
-        z = f2_fma(tap[3][q], h[2][q], z);
-        yv[q] = f2_silu(z);
-      }
-      if (active) store_row<VEC>(ybase + t * p.D, yv);
+      fwd_row<P>(x, h, tap, bias2, yv);
+      if (active) store_row<VEC>(ybase + static_cast<int64_t>(t) * p.D, yv);
     }
-#pragma unroll
-    for (int q = 0; q < P; ++q) {
-      h[2][q] = h[1][q];
-      h[1][q] = h[0][q];
-      h[0][q] = x[q];
-    }
+    ring_push<P>(h, x);
   }
 }
 
 template <int VEC, int R, int S, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
-cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
+cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
+                 const FwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -92,14 +125,15 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   // strips of the same rows at about the same time (contiguous row segments in DRAM).
   const int k = gw / p.n_cb;
   const int cb = gw - k * p.n_cb;
-  const int64_t r0 = static_cast<int64_t>(k) * p.BT / p.wpc;
-  const int64_t r1 = static_cast<int64_t>(k + 1) * p.BT / p.wpc;
+  const int r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
+  const int r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
   const int c0 = cb * CB;
   const int64_t d0 = c0 + lane * VEC;
   const bool active = d0 < p.D;
 
   if (lane == 0) {
     prefetch_tensormap(&tmx);
+    prefetch_tensormap(&tmy);
 #pragma unroll
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -119,7 +153,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     for (int s = 0; s < S; ++s) {
       if (!pc.done) {
         mbar_arrive_expect_tx(&bars[s], TILE);
-        tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
+        tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
         pc.advance();
       }
     }
@@ -137,32 +171,51 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
 
   uint32_t parity = 0;  // bit s: phase parity expected next on stage s
   int s = 0;
+  int prev = -1;        // stage of the previous tile, re-armed one tile late
   while (!cc.done) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
                                                              kWaitLimitNs));
     if (!ok) {
-      if (lane == 0) atomicOr(&g_fault_fwd, kFaultFwdWait);
+      if (lane == 0) {
+        atomicOr(&g_fault_fwd, kFaultFwdWait);
+        bulk_wait_group_all();
+      }
       // Let this warp's other copies land (bounded) before the CTA can exit.
       for (int j = 0; j < S; ++j) (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
       return;
     }
     parity ^= 1u << s;
-    const uint8_t* tile = tiles + s * TILE;
+    uint8_t* tile = tiles + s * TILE;
     const bool full = cc.from == cc.tt && cc.tt >= cc.a && cc.tt + R <= cc.e;
-    if (full)
-      fwd_tile<VEC, R>(tile, lane, cc, true, active, p, d0, tap, bias2, h);
-    else
-      fwd_tile<VEC, R>(tile, lane, cc, false, active, p, d0, tap, bias2, h);
-    __syncwarp();
-    if (lane == 0 && !pc.done) {
+    if (full) {
+      fwd_tile_full<VEC, R>(tile, lane, tap, bias2, h);
+      fence_proxy_async_smem();  // this lane's y writes, before the copy engine reads them
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tmy, tile, c0, cc.tt, cc.b);
+        bulk_commit_group();
+      }
+    } else {
+      fwd_tile_edge<VEC, R>(tile, lane, cc, active, p, d0, tap, bias2, h);
+      __syncwarp();
+    }
+    // Re-arm the previous tile's stage: its store (if any) must have finished reading the
+    // tile.  Only this tile's own store (if it made one) may still be pending.
+    if (lane == 0 && prev >= 0 && !pc.done) {
+      if (full)
+        bulk_wait_group_read<1>();
+      else
+        bulk_wait_group_read<0>();
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[s], TILE);
-      tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, static_cast<int>(pc.tt), pc.b, pol);
+      mbar_arrive_expect_tx(&bars[prev], TILE);
+      tma_load_3d(tiles + prev * TILE, &tmx, &bars[prev], c0, pc.tt, pc.b, pol);
       pc.advance();
     }
+    prev = s;
     cc.advance();
     s = (s + 1 == S) ? 0 : s + 1;
   }
+  if (lane == 0) bulk_wait_group_all();  // y stores complete before the warp exits
   grid_launch_dependents();
 }
 
@@ -171,7 +224,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
 // ------------------------------------------------------------------------------------
 struct FwdConfig {
   int vec, rows, stages, warps;
-  void (*kernel)(const CUtensorMap, const FwdArgs);
+  void (*kernel)(const CUtensorMap, const CUtensorMap, const FwdArgs);
 };
 
 #define CCONV_FWD_CFG(V, R, S, NW) \
@@ -208,8 +261,7 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   if (!x || !w || !y) return CCONV_ERR_NULL;
   if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
   if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
-  if (B < 1 || T < 1 || D < 1 || T > (int64_t(1) << 31) - 8 || D > (int64_t(1) << 31) - 8 ||
-      B > (int64_t(1) << 31) - 8)
+  if (B < 1 || T < 1 || D < 1 || B * T > (int64_t(1) << 31) - 16 || D > (int64_t(1) << 31) - 8)
     return CCONV_ERR_SHAPE;
   if (D % 8 != 0) return CCONV_ERR_ALIGN;
   int rc = check_rows_tensor(x, B, T, D, sxb, sxt);
@@ -226,17 +278,19 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   const StripPlan plan = make_strip_plan(B, T, D, cfg.vec, cfg.warps, 1, sms, 32);
 
   normalise_strides(B, T, D, sxb, sxt);
-  CUtensorMap tmx;
+  CUtensorMap tmx, tmy;
   rc = encode_rows_map(&tmx, x, B, T, D, sxb, sxt, 32 * cfg.vec, cfg.rows);
+  if (rc != CCONV_OK) return rc;
+  rc = encode_rows_map(&tmy, y, B, T, D, T * D, D, 32 * cfg.vec, cfg.rows);
   if (rc != CCONV_OK) return rc;
 
   FwdArgs a;
   a.w = w;
   a.bias = bias;
   a.y = static_cast<uint16_t*>(y);
-  a.T = T;
+  a.T = static_cast<int>(T);
   a.D = D;
-  a.BT = B * T;
+  a.BT = static_cast<int>(B * T);
   a.n_cb = plan.n_cb;
   a.wpc = plan.wpc;
   a.total_warps = plan.total_warps;
@@ -247,7 +301,7 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
   return launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem,
-                    reinterpret_cast<cudaStream_t>(stream), tmx, a) == cudaSuccess
+                    reinterpret_cast<cudaStream_t>(stream), tmx, tmy, a) == cudaSuccess
              ? CCONV_OK
              : CCONV_ERR_CUDA;
 }

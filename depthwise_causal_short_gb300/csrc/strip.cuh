@@ -52,48 +52,47 @@ inline StripPlan make_strip_plan(int64_t B, int64_t T, int64_t D, int vec, int w
 // current tile that has not been processed yet: rows before it, shared with the previous
 // tile, are skipped.
 struct TileCursor {
-  int64_t T, r1;
-  int64_t a, e, tt, from;
+  int T, r1;      // sequence length; end of the range (flattened rows, B*T < 2^31)
+  int a, e;       // current segment: rows [a, e) of batch b
+  int tt, from;   // current tile: rows [tt, tt+R), of which [from, tt+R) are new
   int b;
-  int tail;
-  int R;
+  int tail, R;
   bool done;
 
-  __device__ __forceinline__ void place(int64_t start) {
+  __device__ __forceinline__ void place(int start) {
     from = start;
     tt = start;
-    const int64_t lim = e + tail;
+    const int lim = e + tail;
     if (tt + R > lim) {
-      const int64_t back = lim - R;
+      const int back = lim - R;
       tt = back > a - kRing ? back : a - kRing;
-      if (tt > from) tt = from;
     }
   }
 
-  __device__ __forceinline__ void init(int64_t r0, int64_t r1_, int64_t T_, int tail_, int R_) {
+  __device__ __forceinline__ void init(int r0, int r1_, int T_, int tail_, int R_) {
     T = T_;
     r1 = r1_;
     tail = tail_;
     R = R_;
     done = r0 >= r1_;
-    b = static_cast<int>(r0 / T_);
-    a = r0 - static_cast<int64_t>(b) * T_;
-    const int64_t rest = r1_ - r0;
+    b = r0 / T_;
+    a = r0 - b * T_;
+    const int rest = r1_ - r0;
     e = (a + rest < T_) ? a + rest : T_;
     place(a - kRing);
   }
 
   __device__ __forceinline__ void advance() {
-    const int64_t next = tt + R;
+    const int next = tt + R;
     if (next >= e + tail) {
-      const int64_t r = static_cast<int64_t>(b) * T + e;  // next flattened row
+      const int r = b * T + e;  // next flattened row
       if (r >= r1) {
         done = true;
         return;
       }
       b += 1;
       a = 0;
-      const int64_t rest = r1 - static_cast<int64_t>(b) * T;
+      const int rest = r1 - b * T;
       e = rest < T ? rest : T;
       place(-kRing);
       return;
@@ -157,6 +156,24 @@ __device__ __forceinline__ void smem_row(const uint8_t* row, int lane, f2 (&x)[V
     const uint2 v = *reinterpret_cast<const uint2*>(row + lane * 8);
     x[0] = bf16x2_to_f2(v.x);
     x[1] = bf16x2_to_f2(v.y);
+  }
+}
+
+// Writes one row of this lane's VEC channels into a shared-memory tile row (bf16).
+template <int VEC>
+__device__ __forceinline__ void smem_store_row(uint8_t* row, int lane, const f2 (&v)[VEC / 2]) {
+  if constexpr (VEC == 8) {
+    uint4 o;
+    o.x = f2_to_bf16x2(v[0]);
+    o.y = f2_to_bf16x2(v[1]);
+    o.z = f2_to_bf16x2(v[2]);
+    o.w = f2_to_bf16x2(v[3]);
+    *reinterpret_cast<uint4*>(row + lane * 16) = o;
+  } else {
+    uint2 o;
+    o.x = f2_to_bf16x2(v[0]);
+    o.y = f2_to_bf16x2(v[1]);
+    *reinterpret_cast<uint2*>(row + lane * 8) = o;
   }
 }
 

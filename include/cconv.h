@@ -92,7 +92,7 @@ typedef enum {
  *   w     [D,W] contiguous, dtype wdt.
  *   bias  [D] dtype wdt, or NULL for no bias.
  *   y     [B,T,D] bf16 contiguous output, 16-byte aligned.  Must not overlap x.
- *   B, T, D >= 1, D % 8 == 0, T < 2^31 - 8.
+ *   B, T, D >= 1, D % 8 == 0, B*T < 2^31 - 16.
  */
 CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t D, int64_t sxb,
                         int64_t sxt, const void* w, const void* bias, cconv_dtype wdt, int W,
