@@ -108,10 +108,11 @@ __device__ __forceinline__ void rings_push(f2 (&h)[3][P], f2 (&gr)[3][P], const 
 }
 
 // A tile whose rows all compute g, accumulate, and finish dx[t-3] inside the segment:
-// dx[t-3] overwrites x[t] in the tile, and the tile (rows tt-3 .. tt+R-4) leaves by one TMA
-// store.
+// dx[t-3] goes into row i of an output tile in shared memory, which (rows tt-3 .. tt+R-4)
+// leaves by one TMA store.
 template <int VEC, int R>
-__device__ __forceinline__ void bwd_tile_full(uint8_t* xt, const uint8_t* dyt, int lane,
+__device__ __forceinline__ void bwd_tile_full(const uint8_t* xt, const uint8_t* dyt, uint8_t* out,
+                                              int lane,
                                               const f2 (&tap)[4][VEC / 2],
                                               const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
                                               f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
@@ -125,7 +126,7 @@ __device__ __forceinline__ void bwd_tile_full(uint8_t* xt, const uint8_t* dyt, i
     bwd_g<P>(x, dy, h, tap, bias2, g);
     bwd_acc<P>(x, h, g, acc);
     bwd_dx<P>(g, gr, tap, dxv);
-    smem_store_row<VEC>(xt + i * ROWB, lane, dxv);
+    smem_store_row<VEC>(out + i * ROWB, lane, dxv);
     rings_push<P>(h, gr, x, g);
   }
 }
@@ -183,8 +184,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     return;
   }
 
-  uint8_t* stages = smem + warp * (S * STAGE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
+  // per warp: S stages (x tile + dy tile), then 2 dx tiles (used alternately by full tiles)
+  uint8_t* stages = smem + warp * (S * STAGE + 2 * TILE);
+  uint8_t* outs = stages + S * STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * (S * STAGE + 2 * TILE)) + warp * S;
 
   // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
   // strips of the same rows at about the same time (contiguous row segments in DRAM).
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   uint32_t parity = 0;
   int s = 0;
-  int prev = -1;  // stage of the previous tile, re-armed one tile late
+  int nfull = 0;  // full tiles so far: output tile nfull & 1
   while (!cc.done) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
                                                              kWaitLimitNs));
@@ -258,33 +261,30 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     parity ^= 1u << s;
     uint8_t* xt = stages + s * STAGE;
-    const bool full = cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e;
-    if (full) {
-      bwd_tile_full<VEC, R>(xt, xt + TILE, lane, tap, bias2, h, gr, acc);
+    if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
+      uint8_t* out = outs + (nfull & 1) * TILE;
+      // The store that last read this output tile (two full tiles ago) must be done with it.
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+      bwd_tile_full<VEC, R>(xt, xt + TILE, out, lane, tap, bias2, h, gr, acc);
       fence_proxy_async_smem();  // this lane's dx writes, before the copy engine reads them
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(&tmdx, xt, c0, cc.tt - kRing, cc.b);
+        tma_store_3d(&tmdx, out, c0, cc.tt - kRing, cc.b);
         bulk_commit_group();
       }
+      ++nfull;
     } else {
       bwd_tile_edge<VEC, R>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
       __syncwarp();
     }
-    // Re-arm the previous tile's stage: its store (if any) must have finished reading the
-    // tile.  Only this tile's own store (if it made one) may still be pending.
-    if (lane == 0 && prev >= 0 && !pc.done) {
-      if (full)
-        bulk_wait_group_read<1>();
-      else
-        bulk_wait_group_read<0>();
+    if (lane == 0 && !pc.done) {
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[prev], STAGE);
-      tma_load_3d(stages + prev * STAGE, &tmx, &bars[prev], c0, pc.tt, pc.b, pol);
-      tma_load_3d(stages + prev * STAGE + TILE, &tmdy, &bars[prev], c0, pc.tt, pc.b, pol);
+      mbar_arrive_expect_tx(&bars[s], STAGE);
+      tma_load_3d(xt, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
+      tma_load_3d(xt + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b, pol);
       pc.advance();
     }
-    prev = s;
     cc.advance();
     s = (s + 1 == S) ? 0 : s + 1;
   }
@@ -371,14 +371,14 @@ struct BwdConfig {
   BwdConfig { V, R, S, NW, cconv_bwd_kernel<V, R, S, NW> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 8, 2, 16),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_BWD_CFG(8, 8, 3, 8),
-    CCONV_BWD_CFG(4, 8, 4, 8),
-    CCONV_BWD_CFG(4, 16, 2, 12),
-    CCONV_BWD_CFG(4, 8, 3, 16),
-    CCONV_BWD_CFG(4, 8, 4, 12),
-    CCONV_BWD_CFG(4, 16, 3, 8),
+    CCONV_BWD_CFG(4, 8, 2, 16),
+    CCONV_BWD_CFG(4, 8, 3, 12),
+    CCONV_BWD_CFG(4, 16, 2, 8),
     CCONV_BWD_CFG(4, 4, 4, 16),
+    CCONV_BWD_CFG(8, 8, 2, 8),
+    CCONV_BWD_CFG(4, 16, 3, 6),
+    CCONV_BWD_CFG(4, 8, 2, 12),
+    CCONV_BWD_CFG(4, 12, 2, 12),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
@@ -478,7 +478,8 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   a.wdt = wdt;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
+  const int tile = cfg.rows * 32 * cfg.vec * 2;
+  const int smem = cfg.warps * (cfg.stages * (2 * tile + 8) + 2 * tile);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
   if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, tmdx, a) !=

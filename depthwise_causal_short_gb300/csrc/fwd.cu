@@ -61,10 +61,11 @@ __device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
   }
 }
 
-// A tile whose R rows all lie inside the segment: y overwrites x in the tile, row by row
-// (each lane rewrites exactly the bytes it read), and the tile leaves by one TMA store.
+// A tile whose R rows all lie inside the segment: y goes row by row into an output tile in
+// shared memory, which leaves by one TMA store.
 template <int VEC, int R>
-__device__ __forceinline__ void fwd_tile_full(uint8_t* tile, int lane, const f2 (&tap)[4][VEC / 2],
+__device__ __forceinline__ void fwd_tile_full(const uint8_t* tile, uint8_t* out, int lane,
+                                              const f2 (&tap)[4][VEC / 2],
                                               const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2]) {
   constexpr int P = VEC / 2;
   constexpr int ROWB = 32 * VEC * 2;
@@ -73,7 +74,7 @@ __device__ __forceinline__ void fwd_tile_full(uint8_t* tile, int lane, const f2 
     f2 x[P], yv[P];
     smem_row<VEC>(tile + i * ROWB, lane, x);
     fwd_row<P>(x, h, tap, bias2, yv);
-    smem_store_row<VEC>(tile + i * ROWB, lane, yv);
+    smem_store_row<VEC>(out + i * ROWB, lane, yv);
     ring_push<P>(h, x);
   }
 }
@@ -118,8 +119,10 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant_
     return;
   }
 
-  uint8_t* tiles = smem + warp * (S * TILE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * TILE) + warp * S;
+  // per warp: S input tiles, then 2 output tiles (used alternately by the full tiles)
+  uint8_t* tiles = smem + warp * ((S + 2) * TILE);
+  uint8_t* outs = tiles + S * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * (S + 2) * TILE) + warp * S;
 
   // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
   // strips of the same rows at about the same time (contiguous row segments in DRAM).
@@ -171,7 +174,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant_
 
   uint32_t parity = 0;  // bit s: phase parity expected next on stage s
   int s = 0;
-  int prev = -1;        // stage of the previous tile, re-armed one tile late
+  int nfull = 0;        // full tiles so far: output tile nfull & 1
   while (!cc.done) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
                                                              kWaitLimitNs));
@@ -186,32 +189,29 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant_
     }
     parity ^= 1u << s;
     uint8_t* tile = tiles + s * TILE;
-    const bool full = cc.from == cc.tt && cc.tt >= cc.a && cc.tt + R <= cc.e;
-    if (full) {
-      fwd_tile_full<VEC, R>(tile, lane, tap, bias2, h);
+    if (cc.from == cc.tt && cc.tt >= cc.a && cc.tt + R <= cc.e) {
+      uint8_t* out = outs + (nfull & 1) * TILE;
+      // The store that last read this output tile (two full tiles ago) must be done with it.
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+      fwd_tile_full<VEC, R>(tile, out, lane, tap, bias2, h);
       fence_proxy_async_smem();  // this lane's y writes, before the copy engine reads them
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(&tmy, tile, c0, cc.tt, cc.b);
+        tma_store_3d(&tmy, out, c0, cc.tt, cc.b);
         bulk_commit_group();
       }
+      ++nfull;
     } else {
       fwd_tile_edge<VEC, R>(tile, lane, cc, active, p, d0, tap, bias2, h);
       __syncwarp();
     }
-    // Re-arm the previous tile's stage: its store (if any) must have finished reading the
-    // tile.  Only this tile's own store (if it made one) may still be pending.
-    if (lane == 0 && prev >= 0 && !pc.done) {
-      if (full)
-        bulk_wait_group_read<1>();
-      else
-        bulk_wait_group_read<0>();
+    if (lane == 0 && !pc.done) {
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[prev], TILE);
-      tma_load_3d(tiles + prev * TILE, &tmx, &bars[prev], c0, pc.tt, pc.b, pol);
+      mbar_arrive_expect_tx(&bars[s], TILE);
+      tma_load_3d(tile, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
       pc.advance();
     }
-    prev = s;
     cc.advance();
     s = (s + 1 == S) ? 0 : s + 1;
   }
@@ -231,14 +231,14 @@ struct FwdConfig {
   FwdConfig { V, R, S, NW, cconv_fwd_kernel<V, R, S, NW> }
 
 static const FwdConfig kFwdConfigs[] = {
-    CCONV_FWD_CFG(4, 16, 4, 8),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_FWD_CFG(8, 8, 4, 8),
-    CCONV_FWD_CFG(8, 16, 3, 8),
-    CCONV_FWD_CFG(8, 16, 4, 4),
-    CCONV_FWD_CFG(8, 8, 3, 16),
-    CCONV_FWD_CFG(4, 16, 3, 16),
+    CCONV_FWD_CFG(4, 16, 4, 8),
+    CCONV_FWD_CFG(4, 16, 3, 8),
     CCONV_FWD_CFG(4, 8, 4, 16),
-    CCONV_FWD_CFG(8, 8, 2, 16),
+    CCONV_FWD_CFG(4, 8, 3, 16),
+    CCONV_FWD_CFG(8, 8, 4, 8),
+    CCONV_FWD_CFG(4, 24, 2, 8),
+    CCONV_FWD_CFG(8, 16, 2, 6),
+    CCONV_FWD_CFG(4, 16, 2, 12),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 
@@ -297,7 +297,8 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   a.W = W;
   a.wdt = wdt;
 
-  const int smem = cfg.warps * cfg.stages * (cfg.rows * 32 * cfg.vec * 2 + 8);
+  const int tile = cfg.rows * 32 * cfg.vec * 2;
+  const int smem = cfg.warps * ((cfg.stages + 2) * tile + cfg.stages * 8);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
   return launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem,
