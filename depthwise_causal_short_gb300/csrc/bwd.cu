@@ -44,133 +44,83 @@ struct BwdArgs {
   int W, wdt;
 };
 
-// g for one row, from its x and dy and the x ring h = (x[t-1], x[t-2], x[t-3]).
-template <int P>
-__device__ __forceinline__ void bwd_g(const f2 (&x)[P], const f2 (&dy)[P], const f2 (&h)[3][P],
-                                      const f2 (&tap)[4][P], const f2 (&bias2)[P], f2 (&g)[P]) {
+// FULL: every row of the tile computes g, accumulates dw / dbias and stores dx[t-3].
+template <int VEC, int R, bool FULL>
+__device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, int lane,
+                                         const TileCursor& c, bool active, const BwdArgs& p,
+                                         int64_t d0, const f2 (&tap)[4][VEC / 2],
+                                         const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
+                                         f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
+  constexpr int P = VEC / 2;
+  constexpr int ROWB = 32 * VEC * 2;
   const f2 half = f2_splat(0.5f);
   const f2 nhalf = f2_splat(-0.5f);
   const f2 one = f2_splat(1.0f);
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
-    z = f2_fma(tap[1][q], h[0][q], z);
-    z = f2_fma(tap[2][q], h[1][q], z);
-    z = f2_fma(tap[3][q], h[2][q], z);
-    const f2 th = f2_tanh(f2_mul(z, half));
-    const f2 sg = f2_fma(th, half, half);   // sigmoid(z)
-    const f2 om = f2_fma(th, nhalf, half);  // 1 - sigmoid(z)
-    const f2 d1 = f2_fma(z, om, one);       // 1 + z (1 - sigmoid(z))
-    g[q] = f2_mul(f2_mul(dy[q], sg), d1);
-  }
-}
-
-// dw lags and dbias: acc[k] += g[t] x[t-k], acc[4] += g[t]
-template <int P>
-__device__ __forceinline__ void bwd_acc(const f2 (&x)[P], const f2 (&h)[3][P], const f2 (&g)[P],
-                                        f2 (&acc)[kRec][P]) {
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    acc[0][q] = f2_fma(g[q], x[q], acc[0][q]);
-    acc[1][q] = f2_fma(g[q], h[0][q], acc[1][q]);
-    acc[2][q] = f2_fma(g[q], h[1][q], acc[2][q]);
-    acc[3][q] = f2_fma(g[q], h[2][q], acc[3][q]);
-    acc[4][q] = f2_add(g[q], acc[4][q]);
-  }
-}
-
-// dx[t-3] = sum_k tap[k] g[t-3+k], from g[t] and the g ring gr = (g[t-1], g[t-2], g[t-3])
-template <int P>
-__device__ __forceinline__ void bwd_dx(const f2 (&g)[P], const f2 (&gr)[3][P],
-                                       const f2 (&tap)[4][P], f2 (&dxv)[P]) {
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    f2 v = f2_mul(tap[3][q], g[q]);
-    v = f2_fma(tap[2][q], gr[0][q], v);
-    v = f2_fma(tap[1][q], gr[1][q], v);
-    v = f2_fma(tap[0][q], gr[2][q], v);
-    dxv[q] = v;
-  }
-}
-
-template <int P>
-__device__ __forceinline__ void rings_push(f2 (&h)[3][P], f2 (&gr)[3][P], const f2 (&x)[P],
-                                           const f2 (&g)[P]) {
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    h[2][q] = h[1][q];
-    h[1][q] = h[0][q];
-    h[0][q] = x[q];
-    gr[2][q] = gr[1][q];
-    gr[1][q] = gr[0][q];
-    gr[0][q] = g[q];
-  }
-}
-
-// A tile whose rows all compute g, accumulate, and finish dx[t-3] inside the segment:
-// dx[t-3] goes into row i of an output tile in shared memory, which (rows tt-3 .. tt+R-4)
-// leaves by one TMA store.
-template <int VEC, int R>
-__device__ __forceinline__ void bwd_tile_full(const uint8_t* xt, const uint8_t* dyt, uint8_t* out,
-                                              int lane,
-                                              const f2 (&tap)[4][VEC / 2],
-                                              const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
-                                              f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
-  constexpr int P = VEC / 2;
-  constexpr int ROWB = 32 * VEC * 2;
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    f2 x[P], dy[P], g[P], dxv[P];
-    smem_row<VEC>(xt + i * ROWB, lane, x);
-    smem_row<VEC>(dyt + i * ROWB, lane, dy);
-    bwd_g<P>(x, dy, h, tap, bias2, g);
-    bwd_acc<P>(x, h, g, acc);
-    bwd_dx<P>(g, gr, tap, dxv);
-    smem_store_row<VEC>(out + i * ROWB, lane, dxv);
-    rings_push<P>(h, gr, x, g);
-  }
-}
-
-// Segment edges: ring-only rows before a, halo rows after e (g only), rows already done
-// skipped; dx rows are stored one by one.
-template <int VEC, int R>
-__device__ __forceinline__ void bwd_tile_edge(const uint8_t* xt, const uint8_t* dyt, int lane,
-                                              const TileCursor& c, bool active, const BwdArgs& p,
-                                              int64_t d0, const f2 (&tap)[4][VEC / 2],
-                                              const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
-                                              f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
-  constexpr int P = VEC / 2;
-  constexpr int ROWB = 32 * VEC * 2;
   uint16_t* dxbase = p.dx + static_cast<int64_t>(c.b) * p.T * p.D + d0;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int t = c.tt + i;
-    if (t < c.from) continue;  // processed with the previous tile
+    if (!FULL && t < c.from) continue;  // processed with the previous tile
     f2 x[P], g[P];
     smem_row<VEC>(xt + i * ROWB, lane, x);
-    if (t >= c.a) {
+    const bool live = FULL || t >= c.a;  // rows before the range only fill the x ring
+    if (live) {
       f2 dy[P];
       smem_row<VEC>(dyt + i * ROWB, lane, dy);
-      bwd_g<P>(x, dy, h, tap, bias2, g);
-      if (t < c.e) bwd_acc<P>(x, h, g, acc);
-      if (t - kRing >= c.a && t - kRing < c.e) {
+      const bool sum = FULL || t < c.e;  // halo rows after the range: g only
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
+        z = f2_fma(tap[1][q], h[0][q], z);
+        z = f2_fma(tap[2][q], h[1][q], z);
+        z = f2_fma(tap[3][q], h[2][q], z);
+        const f2 th = f2_tanh(f2_mul(z, half));
+        const f2 sg = f2_fma(th, half, half);       // sigmoid(z)
+        const f2 om = f2_fma(th, nhalf, half);      // 1 - sigmoid(z)
+        const f2 d1 = f2_fma(z, om, one);           // 1 + z (1 - sigmoid(z))
+        g[q] = f2_mul(f2_mul(dy[q], sg), d1);
+        if (sum) {
+          acc[0][q] = f2_fma(g[q], x[q], acc[0][q]);
+          acc[1][q] = f2_fma(g[q], h[0][q], acc[1][q]);
+          acc[2][q] = f2_fma(g[q], h[1][q], acc[2][q]);
+          acc[3][q] = f2_fma(g[q], h[2][q], acc[3][q]);
+          acc[4][q] = f2_add(g[q], acc[4][q]);
+        }
+      }
+      // dx[t-3] = sum_k tap[k] g[t-3+k]; final once g[t] is known
+      const bool store = FULL || (t - kRing >= c.a && t - kRing < c.e);
+      if (store) {
         f2 dxv[P];
-        bwd_dx<P>(g, gr, tap, dxv);
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          f2 v = f2_mul(tap[3][q], g[q]);
+          v = f2_fma(tap[2][q], gr[0][q], v);
+          v = f2_fma(tap[1][q], gr[1][q], v);
+          v = f2_fma(tap[0][q], gr[2][q], v);
+          dxv[q] = v;
+        }
         if (active) store_row<VEC>(dxbase + static_cast<int64_t>(t - kRing) * p.D, dxv);
       }
     } else {
 #pragma unroll
-      for (int q = 0; q < P; ++q) g[q] = 0ull;  // rows before the range: only the x ring
+      for (int q = 0; q < P; ++q) g[q] = 0ull;
     }
-    rings_push<P>(h, gr, x, g);
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      h[2][q] = h[1][q];
+      h[1][q] = h[0][q];
+      h[0][q] = x[q];
+      gr[2][q] = gr[1][q];
+      gr[1][q] = gr[0][q];
+      gr[0][q] = g[q];
+    }
   }
 }
 
 template <int VEC, int R, int S, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
     cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
-                     const __grid_constant__ CUtensorMap tmdy,
-                     const __grid_constant__ CUtensorMap tmdx, const BwdArgs p) {
+                     const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int P = VEC / 2;
   constexpr int TILE = R * CB * 2;
@@ -184,10 +134,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     return;
   }
 
-  // per warp: S stages (x tile + dy tile), then 2 dx tiles (used alternately by full tiles)
-  uint8_t* stages = smem + warp * (S * STAGE + 2 * TILE);
-  uint8_t* outs = stages + S * STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * (S * STAGE + 2 * TILE)) + warp * S;
+  uint8_t* stages = smem + warp * (S * STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
 
   // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
   // strips of the same rows at about the same time (contiguous row segments in DRAM).
@@ -202,7 +150,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
   if (lane == 0) {
     prefetch_tensormap(&tmx);
     prefetch_tensormap(&tmdy);
-    prefetch_tensormap(&tmdx);
 #pragma unroll
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -223,7 +170,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       if (!pc.done) {
         mbar_arrive_expect_tx(&bars[s], STAGE);
         tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-        tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+        tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt,
+                    pc.b, pol);
         pc.advance();
       }
     }
@@ -247,48 +195,33 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   uint32_t parity = 0;
   int s = 0;
-  int nfull = 0;  // full tiles so far: output tile nfull & 1
   while (!cc.done) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
                                                              kWaitLimitNs));
     if (!ok) {
-      if (lane == 0) {
-        atomicOr(&g_fault_bwd, kFaultBwdWait);
-        bulk_wait_group_all();
-      }
+      if (lane == 0) atomicOr(&g_fault_bwd, kFaultBwdWait);
       for (int j = 0; j < S; ++j) (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
       return;
     }
     parity ^= 1u << s;
-    uint8_t* xt = stages + s * STAGE;
-    if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
-      uint8_t* out = outs + (nfull & 1) * TILE;
-      // The store that last read this output tile (two full tiles ago) must be done with it.
-      if (lane == 0) bulk_wait_group_read<1>();
-      __syncwarp();
-      bwd_tile_full<VEC, R>(xt, xt + TILE, out, lane, tap, bias2, h, gr, acc);
-      fence_proxy_async_smem();  // this lane's dx writes, before the copy engine reads them
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d(&tmdx, out, c0, cc.tt - kRing, cc.b);
-        bulk_commit_group();
-      }
-      ++nfull;
-    } else {
-      bwd_tile_edge<VEC, R>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
-      __syncwarp();
-    }
+    const uint8_t* xt = stages + s * STAGE;
+    const bool full = cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e;
+    if (full)
+      bwd_tile<VEC, R, true>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+    else
+      bwd_tile<VEC, R, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+    __syncwarp();
     if (lane == 0 && !pc.done) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&bars[s], STAGE);
-      tma_load_3d(xt, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-      tma_load_3d(xt + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+      tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
+      tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b,
+                  pol);
       pc.advance();
     }
     cc.advance();
     s = (s + 1 == S) ? 0 : s + 1;
   }
-  if (lane == 0) bulk_wait_group_all();  // dx stores complete before the warp exits
 
   grid_launch_dependents();
 
@@ -364,21 +297,21 @@ __global__ void __launch_bounds__(32 * kRedGroups)
 
 struct BwdConfig {
   int vec, rows, stages, warps;
-  void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const BwdArgs);
+  void (*kernel)(const CUtensorMap, const CUtensorMap, const BwdArgs);
 };
 
 #define CCONV_BWD_CFG(V, R, S, NW) \
   BwdConfig { V, R, S, NW, cconv_bwd_kernel<V, R, S, NW> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 8, 2, 16),
-    CCONV_BWD_CFG(4, 8, 3, 12),
-    CCONV_BWD_CFG(4, 16, 2, 8),
+    CCONV_BWD_CFG(4, 8, 2, 16),  // measured fastest at B=2 T=8192 D=4096
+    CCONV_BWD_CFG(8, 8, 3, 8),
+    CCONV_BWD_CFG(4, 8, 4, 8),
+    CCONV_BWD_CFG(4, 16, 2, 12),
+    CCONV_BWD_CFG(4, 8, 3, 16),
+    CCONV_BWD_CFG(4, 8, 4, 12),
+    CCONV_BWD_CFG(4, 16, 3, 8),
     CCONV_BWD_CFG(4, 4, 4, 16),
-    CCONV_BWD_CFG(8, 8, 2, 8),
-    CCONV_BWD_CFG(4, 16, 3, 6),
-    CCONV_BWD_CFG(4, 8, 2, 12),
-    CCONV_BWD_CFG(4, 12, 2, 12),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
@@ -455,12 +388,10 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
 
   normalise_strides(B, T, D, sxb, sxt);
   normalise_strides(B, T, D, sdb, sdt);
-  CUtensorMap tmx, tmdy, tmdx;
+  CUtensorMap tmx, tmdy;
   rc = encode_rows_map(&tmx, x, B, T, D, sxb, sxt, 32 * cfg.vec, cfg.rows);
   if (rc != CCONV_OK) return rc;
   rc = encode_rows_map(&tmdy, dy, B, T, D, sdb, sdt, 32 * cfg.vec, cfg.rows);
-  if (rc != CCONV_OK) return rc;
-  rc = encode_rows_map(&tmdx, dx, B, T, D, T * D, D, 32 * cfg.vec, cfg.rows);
   if (rc != CCONV_OK) return rc;
 
   BwdArgs a;
@@ -478,11 +409,10 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   a.wdt = wdt;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int tile = cfg.rows * 32 * cfg.vec * 2;
-  const int smem = cfg.warps * (cfg.stages * (2 * tile + 8) + 2 * tile);
+  const int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, tmdx, a) !=
+  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
   const float* wsp = a.ws;

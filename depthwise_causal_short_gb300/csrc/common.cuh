@@ -236,32 +236,3 @@ int set_max_dynamic_smem(const void* func, int bytes);
 
 }  // namespace cconv
 
-namespace cconv {
-
-// ------------------------------------------------------------------------------------
-// TMA bulk tensor store (shared -> global) and its bulk-group bookkeeping
-// ------------------------------------------------------------------------------------
-// 3-D tiled store of one box from shared memory.  Parts of the box outside the tensor are
-// not written.  The start coordinate must not be negative.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c,
-                                             int r, int b) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_addr(src)), "r"(c), "r"(r), "r"(b)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until at most N committed bulk groups still read their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Waits until every committed bulk group has completed (writes performed).
-__device__ __forceinline__ void bulk_wait_group_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-}  // namespace cconv

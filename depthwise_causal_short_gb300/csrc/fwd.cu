@@ -36,78 +36,45 @@ struct FwdArgs {
   int W, wdt;
 };
 
-// One output row from the new input row x and the ring h = (x[t-1], x[t-2], x[t-3]).
-template <int P>
-__device__ __forceinline__ void fwd_row(const f2 (&x)[P], const f2 (&h)[3][P],
-                                        const f2 (&tap)[4][P], const f2 (&bias2)[P],
-                                        f2 (&yv)[P]) {
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
-    z = f2_fma(tap[1][q], h[0][q], z);
-    z = f2_fma(tap[2][q], h[1][q], z);
-    z = f2_fma(tap[3][q], h[2][q], z);
-    yv[q] = f2_silu(z);
-  }
-}
-
-template <int P>
-__device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-    h[2][q] = h[1][q];
-    h[1][q] = h[0][q];
-    h[0][q] = x[q];
-  }
-}
-
-// A tile whose R rows all lie inside the segment: y goes row by row into an output tile in
-// shared memory, which leaves by one TMA store.
 template <int VEC, int R>
-__device__ __forceinline__ void fwd_tile_full(const uint8_t* tile, uint8_t* out, int lane,
-                                              const f2 (&tap)[4][VEC / 2],
-                                              const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2]) {
-  constexpr int P = VEC / 2;
-  constexpr int ROWB = 32 * VEC * 2;
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    f2 x[P], yv[P];
-    smem_row<VEC>(tile + i * ROWB, lane, x);
-    fwd_row<P>(x, h, tap, bias2, yv);
-    smem_store_row<VEC>(out + i * ROWB, lane, yv);
-    ring_push<P>(h, x);
-  }
-}
-
-// The first tile of a segment (rows before a only fill the ring) or a last tile pulled
-// back over rows already done (skipped): rows are stored one by one.
-template <int VEC, int R>
-__device__ __forceinline__ void fwd_tile_edge(const uint8_t* tile, int lane, const TileCursor& c,
-                                              bool active, const FwdArgs& p, int64_t d0,
-                                              const f2 (&tap)[4][VEC / 2],
-                                              const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2]) {
+__device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const TileCursor& c,
+                                         bool full, bool active, const FwdArgs& p, int64_t d0,
+                                         const f2 (&tap)[4][VEC / 2], const f2 (&bias2)[VEC / 2],
+                                         f2 (&h)[3][VEC / 2]) {
   constexpr int P = VEC / 2;
   constexpr int ROWB = 32 * VEC * 2;
   uint16_t* ybase = p.y + static_cast<int64_t>(c.b) * p.T * p.D + d0;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int t = c.tt + i;
-    if (t < c.from) continue;  // processed with the previous tile
+    if (!full && t < c.from) continue;  // processed with the previous tile
     f2 x[P];
     smem_row<VEC>(tile + i * ROWB, lane, x);
-    if (t >= c.a && t < c.e) {
+    const bool emit = full || (t >= c.a && t < c.e);
+    if (emit) {
       f2 yv[P];
-      fwd_row<P>(x, h, tap, bias2, yv);
+#pragma unroll
+      for (int q = 0; q < P; ++q) {
+        f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
+        z = f2_fma(tap[1][q], h[0][q], z);
+        z = f2_fma(tap[2][q], h[1][q], z);
+        z = f2_fma(tap[3][q], h[2][q], z);
+        yv[q] = f2_silu(z);
+      }
       if (active) store_row<VEC>(ybase + static_cast<int64_t>(t) * p.D, yv);
     }
-    ring_push<P>(h, x);
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      h[2][q] = h[1][q];
+      h[1][q] = h[0][q];
+      h[0][q] = x[q];
+    }
   }
 }
 
 template <int VEC, int R, int S, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
-cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
-                 const FwdArgs p) {
+cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -119,10 +86,8 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant_
     return;
   }
 
-  // per warp: S input tiles, then 2 output tiles (used alternately by the full tiles)
-  uint8_t* tiles = smem + warp * ((S + 2) * TILE);
-  uint8_t* outs = tiles + S * TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * (S + 2) * TILE) + warp * S;
+  uint8_t* tiles = smem + warp * (S * TILE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * TILE) + warp * S;
 
   // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
   // strips of the same rows at about the same time (contiguous row segments in DRAM).
@@ -136,7 +101,6 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant_
 
   if (lane == 0) {
     prefetch_tensormap(&tmx);
-    prefetch_tensormap(&tmy);
 #pragma unroll
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -174,48 +138,32 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant_
 
   uint32_t parity = 0;  // bit s: phase parity expected next on stage s
   int s = 0;
-  int nfull = 0;        // full tiles so far: output tile nfull & 1
   while (!cc.done) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
                                                              kWaitLimitNs));
     if (!ok) {
-      if (lane == 0) {
-        atomicOr(&g_fault_fwd, kFaultFwdWait);
-        bulk_wait_group_all();
-      }
+      if (lane == 0) atomicOr(&g_fault_fwd, kFaultFwdWait);
       // Let this warp's other copies land (bounded) before the CTA can exit.
       for (int j = 0; j < S; ++j) (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
       return;
     }
     parity ^= 1u << s;
-    uint8_t* tile = tiles + s * TILE;
-    if (cc.from == cc.tt && cc.tt >= cc.a && cc.tt + R <= cc.e) {
-      uint8_t* out = outs + (nfull & 1) * TILE;
-      // The store that last read this output tile (two full tiles ago) must be done with it.
-      if (lane == 0) bulk_wait_group_read<1>();
-      __syncwarp();
-      fwd_tile_full<VEC, R>(tile, out, lane, tap, bias2, h);
-      fence_proxy_async_smem();  // this lane's y writes, before the copy engine reads them
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d(&tmy, out, c0, cc.tt, cc.b);
-        bulk_commit_group();
-      }
-      ++nfull;
-    } else {
-      fwd_tile_edge<VEC, R>(tile, lane, cc, active, p, d0, tap, bias2, h);
-      __syncwarp();
-    }
+    const uint8_t* tile = tiles + s * TILE;
+    const bool full = cc.from == cc.tt && cc.tt >= cc.a && cc.tt + R <= cc.e;
+    if (full)
+      fwd_tile<VEC, R>(tile, lane, cc, true, active, p, d0, tap, bias2, h);
+    else
+      fwd_tile<VEC, R>(tile, lane, cc, false, active, p, d0, tap, bias2, h);
+    __syncwarp();
     if (lane == 0 && !pc.done) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&bars[s], TILE);
-      tma_load_3d(tile, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
+      tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
       pc.advance();
     }
     cc.advance();
     s = (s + 1 == S) ? 0 : s + 1;
   }
-  if (lane == 0) bulk_wait_group_all();  // y stores complete before the warp exits
   grid_launch_dependents();
 }
 
@@ -224,21 +172,21 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant_
 // ------------------------------------------------------------------------------------
 struct FwdConfig {
   int vec, rows, stages, warps;
-  void (*kernel)(const CUtensorMap, const CUtensorMap, const FwdArgs);
+  void (*kernel)(const CUtensorMap, const FwdArgs);
 };
 
 #define CCONV_FWD_CFG(V, R, S, NW) \
   FwdConfig { V, R, S, NW, cconv_fwd_kernel<V, R, S, NW> }
 
 static const FwdConfig kFwdConfigs[] = {
-    CCONV_FWD_CFG(4, 16, 4, 8),
-    CCONV_FWD_CFG(4, 16, 3, 8),
-    CCONV_FWD_CFG(4, 8, 4, 16),
-    CCONV_FWD_CFG(4, 8, 3, 16),
+    CCONV_FWD_CFG(4, 16, 4, 8),  // measured fastest at B=2 T=8192 D=4096
     CCONV_FWD_CFG(8, 8, 4, 8),
-    CCONV_FWD_CFG(4, 24, 2, 8),
-    CCONV_FWD_CFG(8, 16, 2, 6),
-    CCONV_FWD_CFG(4, 16, 2, 12),
+    CCONV_FWD_CFG(8, 16, 3, 8),
+    CCONV_FWD_CFG(8, 16, 4, 4),
+    CCONV_FWD_CFG(8, 8, 3, 16),
+    CCONV_FWD_CFG(4, 16, 3, 16),
+    CCONV_FWD_CFG(4, 8, 4, 16),
+    CCONV_FWD_CFG(8, 8, 2, 16),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 
@@ -278,10 +226,8 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   const StripPlan plan = make_strip_plan(B, T, D, cfg.vec, cfg.warps, 1, sms, 32);
 
   normalise_strides(B, T, D, sxb, sxt);
-  CUtensorMap tmx, tmy;
+  CUtensorMap tmx;
   rc = encode_rows_map(&tmx, x, B, T, D, sxb, sxt, 32 * cfg.vec, cfg.rows);
-  if (rc != CCONV_OK) return rc;
-  rc = encode_rows_map(&tmy, y, B, T, D, T * D, D, 32 * cfg.vec, cfg.rows);
   if (rc != CCONV_OK) return rc;
 
   FwdArgs a;
@@ -297,12 +243,11 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   a.W = W;
   a.wdt = wdt;
 
-  const int tile = cfg.rows * 32 * cfg.vec * 2;
-  const int smem = cfg.warps * ((cfg.stages + 2) * tile + cfg.stages * 8);
+  const int smem = cfg.warps * cfg.stages * (cfg.rows * 32 * cfg.vec * 2 + 8);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
   return launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem,
-                    reinterpret_cast<cudaStream_t>(stream), tmx, tmy, a) == cudaSuccess
+                    reinterpret_cast<cudaStream_t>(stream), tmx, a) == cudaSuccess
              ? CCONV_OK
              : CCONV_ERR_CUDA;
 }

@@ -159,24 +159,6 @@ __device__ __forceinline__ void smem_row(const uint8_t* row, int lane, f2 (&x)[V
   }
 }
 
-// Writes one row of this lane's VEC channels into a shared-memory tile row (bf16).
-template <int VEC>
-__device__ __forceinline__ void smem_store_row(uint8_t* row, int lane, const f2 (&v)[VEC / 2]) {
-  if constexpr (VEC == 8) {
-    uint4 o;
-    o.x = f2_to_bf16x2(v[0]);
-    o.y = f2_to_bf16x2(v[1]);
-    o.z = f2_to_bf16x2(v[2]);
-    o.w = f2_to_bf16x2(v[3]);
-    *reinterpret_cast<uint4*>(row + lane * 16) = o;
-  } else {
-    uint2 o;
-    o.x = f2_to_bf16x2(v[0]);
-    o.y = f2_to_bf16x2(v[1]);
-    *reinterpret_cast<uint2*>(row + lane * 8) = o;
-  }
-}
-
 // Stores one row of this lane's VEC channels (fp32 pairs -> bf16, nearest even).
 template <int VEC>
 __device__ __forceinline__ void store_row(uint16_t* dst, const f2 (&v)[VEC / 2]) {
