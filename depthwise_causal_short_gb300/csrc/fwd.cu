@@ -7,12 +7,14 @@
 // in registers.
 //
 // What differs from that Triton design: x does not travel through registers on its way in.
-// Each warp runs its own TMA pipeline: its lane 0 keeps S tiles of R rows x (32*VEC)
-// channels in flight into shared memory, each completing on an mbarrier, so the bytes in
-// flight per SM are set by shared memory (S * tile bytes per warp) rather than by the
-// register budget, which was the limit the pages measured.  The 3 ring rows before a range
-// and the zero padding before t = 0 come from the same tiled copy (out-of-range rows fill
-// with zeros).  Arithmetic is packed f32x2; the sigmoid is 0.5 * tanh.approx(z/2) + 0.5.
+// Each CTA is warp-specialised: a producer warp keeps S stages of R rows x (NC*32*VEC)
+// channels in flight into shared memory with TMA (one box per consumer warp, completing on
+// the stage's "full" mbarrier), and NC consumer warps walk the stages in lockstep, each
+// releasing a stage on its "empty" mbarrier.  Bytes in flight per SM are set by shared
+// memory rather than by the register budget, which was the limit the pages measured, and the
+// lockstep keeps the warps of an SM finishing together.  The 3 ring rows before a range and
+// the zero padding before t = 0 come from the same tiled copy (out-of-range rows fill with
+// zeros).  Arithmetic is packed f32x2; the sigmoid is 0.5 * tanh.approx(z/2) + 0.5.
 #include "strip.cuh"
 
 namespace cconv {
@@ -32,13 +34,41 @@ struct FwdArgs {
   uint16_t* y;  // [B,T,D] contiguous bf16
   int64_t D;
   int T, BT;
-  int n_cb, wpc, total_warps;
+  int cpc;      // CTAs per channel group
   int W, wdt;
 };
 
-template <int VEC, int R>
+// One output row from the new input row x and the ring h = (x[t-1], x[t-2], x[t-3]).
+template <int P>
+__device__ __forceinline__ void fwd_row(const f2 (&x)[P], const f2 (&h)[3][P],
+                                        const f2 (&tap)[4][P], const f2 (&bias2)[P],
+                                        f2 (&yv)[P]) {
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
+    z = f2_fma(tap[1][q], h[0][q], z);
+    z = f2_fma(tap[2][q], h[1][q], z);
+    z = f2_fma(tap[3][q], h[2][q], z);
+    yv[q] = f2_silu(z);
+  }
+}
+
+template <int P>
+__device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    h[2][q] = h[1][q];
+    h[1][q] = h[0][q];
+    h[0][q] = x[q];
+  }
+}
+
+// Rows of one tile for this lane.  FULL: every row lies inside the segment.  Otherwise rows
+// before `from` were done with the previous tile, rows before a only fill the ring, and rows
+// from e on are not needed.
+template <int VEC, int R, bool FULL>
 __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const TileCursor& c,
-                                         bool full, bool active, const FwdArgs& p, int64_t d0,
+                                         bool active, const FwdArgs& p, int64_t d0,
                                          const f2 (&tap)[4][VEC / 2], const f2 (&bias2)[VEC / 2],
                                          f2 (&h)[3][VEC / 2]) {
   constexpr int P = VEC / 2;
@@ -47,122 +77,110 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int t = c.tt + i;
-    if (!full && t < c.from) continue;  // processed with the previous tile
+    if (!FULL && t < c.from) continue;
     f2 x[P];
     smem_row<VEC>(tile + i * ROWB, lane, x);
-    const bool emit = full || (t >= c.a && t < c.e);
-    if (emit) {
+    if (FULL || (t >= c.a && t < c.e)) {
       f2 yv[P];
-#pragma unroll
-      for (int q = 0; q < P; ++q) {
-        f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
-        z = f2_fma(tap[1][q], h[0][q], z);
-        z = f2_fma(tap[2][q], h[1][q], z);
-        z = f2_fma(tap[3][q], h[2][q], z);
-        yv[q] = f2_silu(z);
-      }
+      fwd_row<P>(x, h, tap, bias2, yv);
       if (active) store_row<VEC>(ybase + static_cast<int64_t>(t) * p.D, yv);
     }
-#pragma unroll
-    for (int q = 0; q < P; ++q) {
-      h[2][q] = h[1][q];
-      h[1][q] = h[0][q];
-      h[0][q] = x[q];
-    }
+    ring_push<P>(h, x);
   }
 }
 
-template <int VEC, int R, int S, int NW>
-__global__ void __launch_bounds__(NW * 32, 1)
+// CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile)
+// and one producer warp (index NC).  Stage layout: NC boxes of R rows x CB channels.
+template <int VEC, int R, int S, int NC, int MINB>
+__global__ void __launch_bounds__((NC + 1) * 32, MINB)
 cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
+  constexpr int STAGE = NC * TILE;
   extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+  uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * NW + warp;
-  if (gw >= p.total_warps) {  // no CTA-wide barrier follows
-    grid_launch_dependents();
-    return;
-  }
+  const int cg = blockIdx.x / p.cpc;
+  const int part = blockIdx.x - cg * p.cpc;
+  const int r0 = static_cast<int>(static_cast<int64_t>(part) * p.BT / p.cpc);
+  const int r1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.BT / p.cpc);
+  const int c0 = cg * NC * CB;
+  int nact = static_cast<int>((p.D - c0 + CB - 1) / CB);  // consumer warps with channels
+  if (nact > NC) nact = NC;
 
-  uint8_t* tiles = smem + warp * (S * TILE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * TILE) + warp * S;
-
-  // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
-  // strips of the same rows at about the same time (contiguous row segments in DRAM).
-  const int k = gw / p.n_cb;
-  const int cb = gw - k * p.n_cb;
-  const int r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
-  const int r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
-  const int c0 = cb * CB;
-  const int64_t d0 = c0 + lane * VEC;
-  const bool active = d0 < p.D;
-
-  if (lane == 0) {
+  if (threadIdx.x == 0) {
     prefetch_tensormap(&tmx);
 #pragma unroll
-    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nact);
+    }
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();  // the only CTA-wide barrier
 
-  // Everything above touches no global memory; from here on the previous kernel on the
-  // stream has completed.
+  // Nothing above touches global memory; from here on the previous kernel on the stream has
+  // completed.
   grid_dependency_wait();
 
-  TileCursor pc, cc;
-  pc.init(r0, r1, p.T, 0, R);
-  cc = pc;
-  const uint64_t pol = policy_evict_first();
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-      if (!pc.done) {
-        mbar_arrive_expect_tx(&bars[s], TILE);
-        tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-        pc.advance();
+  TileCursor cur;
+  cur.init(r0, r1, p.T, 0, R);
+  if (warp == NC) {
+    // ---- producer ------------------------------------------------------------------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t eph = 0;
+      int s = 0;
+      for (int i = 0; !cur.done; ++i) {
+        if (i >= S) {  // wait until every consumer has released this stage
+          if (!mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs)) {
+            atomicOr(&g_fault_fwd, kFaultFwdWait);
+            break;
+          }
+          eph ^= 1u << s;
+        }
+        uint8_t* st = smem + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], nact * TILE);
+        for (int w = 0; w < nact; ++w)
+          tma_load_3d(st + w * TILE, &tmx, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
+        cur.advance();
+        s = (s + 1 == S) ? 0 : s + 1;
       }
     }
-  }
-
-  // Taps load while the first tiles are in flight.
-  f2 tap[4][VEC / 2], bias2[VEC / 2];
-  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
-
-  f2 h[3][VEC / 2];
+  } else if (warp < nact) {
+    // ---- consumer ------------------------------------------------------------------------
+    const int64_t d0 = c0 + warp * CB + lane * VEC;
+    const bool active = d0 < p.D;
+    f2 tap[4][VEC / 2], bias2[VEC / 2];
+    load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
+    f2 h[3][VEC / 2];
 #pragma unroll
-  for (int j = 0; j < 3; ++j)
+    for (int j = 0; j < 3; ++j)
 #pragma unroll
-    for (int q = 0; q < VEC / 2; ++q) h[j][q] = 0ull;
+      for (int q = 0; q < VEC / 2; ++q) h[j][q] = 0ull;
 
-  uint32_t parity = 0;  // bit s: phase parity expected next on stage s
-  int s = 0;
-  while (!cc.done) {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
-                                                             kWaitLimitNs));
-    if (!ok) {
-      if (lane == 0) atomicOr(&g_fault_fwd, kFaultFwdWait);
-      // Let this warp's other copies land (bounded) before the CTA can exit.
-      for (int j = 0; j < S; ++j) (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
-      return;
+    uint32_t fph = 0;
+    int s = 0;
+    while (!cur.done) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (fph >> s) & 1u,
+                                                               kWaitLimitNs));
+      if (!ok) {
+        if (lane == 0) atomicOr(&g_fault_fwd, kFaultFwdWait);
+        break;
+      }
+      fph ^= 1u << s;
+      const uint8_t* tile = smem + s * STAGE + warp * TILE;
+      if (cur.from == cur.tt && cur.tt >= cur.a && cur.tt + R <= cur.e)
+        fwd_tile<VEC, R, true>(tile, lane, cur, active, p, d0, tap, bias2, h);
+      else
+        fwd_tile<VEC, R, false>(tile, lane, cur, active, p, d0, tap, bias2, h);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      cur.advance();
+      s = (s + 1 == S) ? 0 : s + 1;
     }
-    parity ^= 1u << s;
-    const uint8_t* tile = tiles + s * TILE;
-    const bool full = cc.from == cc.tt && cc.tt >= cc.a && cc.tt + R <= cc.e;
-    if (full)
-      fwd_tile<VEC, R>(tile, lane, cc, true, active, p, d0, tap, bias2, h);
-    else
-      fwd_tile<VEC, R>(tile, lane, cc, false, active, p, d0, tap, bias2, h);
-    __syncwarp();
-    if (lane == 0 && !pc.done) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[s], TILE);
-      tma_load_3d(tiles + s * TILE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-      pc.advance();
-    }
-    cc.advance();
-    s = (s + 1 == S) ? 0 : s + 1;
   }
   grid_launch_dependents();
 }
@@ -171,22 +189,22 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
 // launch configurations (compile-time tile shapes; the first is the default)
 // ------------------------------------------------------------------------------------
 struct FwdConfig {
-  int vec, rows, stages, warps;
+  int vec, rows, stages, nc, ctas_per_sm;
   void (*kernel)(const CUtensorMap, const FwdArgs);
 };
 
-#define CCONV_FWD_CFG(V, R, S, NW) \
-  FwdConfig { V, R, S, NW, cconv_fwd_kernel<V, R, S, NW> }
+#define CCONV_FWD_CFG(V, R, S, NC, M) \
+  FwdConfig { V, R, S, NC, M, cconv_fwd_kernel<V, R, S, NC, M> }
 
 static const FwdConfig kFwdConfigs[] = {
-    CCONV_FWD_CFG(4, 16, 4, 8),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_FWD_CFG(8, 8, 4, 8),
-    CCONV_FWD_CFG(8, 16, 3, 8),
-    CCONV_FWD_CFG(8, 16, 4, 4),
-    CCONV_FWD_CFG(8, 8, 3, 16),
-    CCONV_FWD_CFG(4, 16, 3, 16),
-    CCONV_FWD_CFG(4, 8, 4, 16),
-    CCONV_FWD_CFG(8, 8, 2, 16),
+    CCONV_FWD_CFG(4, 16, 6, 8, 1),
+    CCONV_FWD_CFG(4, 8, 10, 8, 1),
+    CCONV_FWD_CFG(8, 8, 6, 8, 1),
+    CCONV_FWD_CFG(4, 16, 4, 12, 1),
+    CCONV_FWD_CFG(4, 8, 6, 16, 1),
+    CCONV_FWD_CFG(4, 16, 3, 8, 2),
+    CCONV_FWD_CFG(4, 8, 5, 8, 2),
+    CCONV_FWD_CFG(8, 16, 3, 8, 1),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 
@@ -223,7 +241,7 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   int sms = 0;
   rc = sm_count_current_device(&sms, nullptr);
   if (rc != CCONV_OK) return rc;
-  const StripPlan plan = make_strip_plan(B, T, D, cfg.vec, cfg.warps, 1, sms, 32);
+  const GroupPlan plan = make_group_plan(B, T, D, cfg.vec, cfg.nc, cfg.ctas_per_sm, sms, 32);
 
   normalise_strides(B, T, D, sxb, sxt);
   CUtensorMap tmx;
@@ -234,19 +252,18 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   a.w = w;
   a.bias = bias;
   a.y = static_cast<uint16_t*>(y);
-  a.T = static_cast<int>(T);
   a.D = D;
+  a.T = static_cast<int>(T);
   a.BT = static_cast<int>(B * T);
-  a.n_cb = plan.n_cb;
-  a.wpc = plan.wpc;
-  a.total_warps = plan.total_warps;
+  a.cpc = plan.cpc;
   a.W = W;
   a.wdt = wdt;
 
-  const int smem = cfg.warps * cfg.stages * (cfg.rows * 32 * cfg.vec * 2 + 8);
+  const int stage = cfg.nc * cfg.rows * 32 * cfg.vec * 2;
+  const int smem = cfg.stages * (stage + 16);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  return launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem,
+  return launch_pdl(cfg.kernel, dim3(plan.grid), dim3((cfg.nc + 1) * 32), smem,
                     reinterpret_cast<cudaStream_t>(stream), tmx, a) == cudaSuccess
              ? CCONV_OK
              : CCONV_ERR_CUDA;

@@ -1,15 +1,16 @@
-// strip.cuh -- how the forward and backward split a [B, T, D] tensor among warps.
+// strip.cuh -- how the forward and backward split a [B, T, D] tensor among CTAs and warps.
 //
-// A channel strip is 32*VEC consecutive channels: one warp, VEC channels per lane, reads a
-// row of the strip as one coalesced 16-byte (VEC=8) or 8-byte (VEC=4) access per lane.
-// Each strip's rows, flattened over (b, t), are cut into `wpc` equal contiguous ranges, one
-// per warp, so every warp of the grid gets the same number of rows (to within one) and the
-// grid is one wave of resident CTAs.  Warp gw takes strip gw % n_cb of range gw / n_cb:
-// the warps of one CTA cover neighbouring strips of the same rows.  A warp walks its range in time order, tile by tile,
-// keeping the W-1 previous rows in registers (the ring).  Where a range starts inside a
-// sequence, its first tile starts 3 rows early to fill the ring; where it starts a sequence,
-// those 3 rows lie at t < 0 and the copy engine fills them with zeros, which is exactly the
-// causal zero padding.
+// A channel group is NC * 32 * VEC consecutive channels: one CTA tile row, split among NC
+// consumer warps of 32 lanes with VEC channels each, so each warp reads its part of a row as
+// one coalesced 16-byte (VEC=8) or 8-byte (VEC=4) access per lane.  Each group's rows,
+// flattened over (b, t), are cut into `cpc` equal contiguous ranges, one per CTA, so every
+// CTA gets the same number of rows (to within one) and the grid is one wave of resident
+// CTAs.  Inside a CTA a producer warp streams tiles of R rows x the group's channels into a
+// ring of S shared-memory stages with TMA; the consumer warps walk the same tiles in time
+// order in lockstep, keeping the W-1 previous rows in registers (the ring).  Where a range
+// starts inside a sequence, its first tile starts 3 rows early to fill the ring; where it
+// starts a sequence, those 3 rows lie at t < 0 and the copy engine fills them with zeros,
+// which is exactly the causal zero padding.
 #pragma once
 
 #include "common.cuh"
@@ -18,32 +19,29 @@ namespace cconv {
 
 constexpr int kRing = 3;  // previous rows kept: W-1 for the widest supported W (4)
 
-struct StripPlan {
-  int n_cb;          // channel strips: ceil(D / (32*VEC))
-  int wpc;           // warps (row ranges) per strip
-  int total_warps;   // n_cb * wpc
-  int grid;          // CTAs of `warps_per_cta` warps
+struct GroupPlan {
+  int n_cg;  // channel groups: ceil(D / (NC * 32 * VEC))
+  int cpc;   // CTAs (row ranges) per channel group
+  int grid;  // n_cg * cpc
 };
 
-// rows_min: shortest range worth a warp (the ring refill is 3 rows per range).
-inline StripPlan make_strip_plan(int64_t B, int64_t T, int64_t D, int vec, int warps_per_cta,
+// rows_min: shortest range worth a CTA (the ring refill is 3 rows per range).
+inline GroupPlan make_group_plan(int64_t B, int64_t T, int64_t D, int vec, int nc,
                                  int ctas_per_sm, int sms, int64_t rows_min) {
-  StripPlan p;
-  const int64_t cb_width = 32 * vec;
-  p.n_cb = static_cast<int>((D + cb_width - 1) / cb_width);
-  const int64_t target = static_cast<int64_t>(sms) * ctas_per_sm * warps_per_cta;
-  int64_t wpc = target / p.n_cb;
-  if (wpc < 1) wpc = 1;
+  GroupPlan p;
+  const int64_t width = static_cast<int64_t>(nc) * 32 * vec;
+  p.n_cg = static_cast<int>((D + width - 1) / width);
+  int64_t cpc = static_cast<int64_t>(sms) * ctas_per_sm / p.n_cg;
+  if (cpc < 1) cpc = 1;
   int64_t by_rows = (B * T) / rows_min;
   if (by_rows < 1) by_rows = 1;
-  if (wpc > by_rows) wpc = by_rows;
-  p.wpc = static_cast<int>(wpc);
-  p.total_warps = p.n_cb * p.wpc;
-  p.grid = (p.total_warps + warps_per_cta - 1) / warps_per_cta;
+  if (cpc > by_rows) cpc = by_rows;
+  p.cpc = static_cast<int>(cpc);
+  p.grid = p.n_cg * p.cpc;
   return p;
 }
 
-// Walks the tiles of one warp's row range [r0, r1) of the flattened (b, t) space.
+// Walks the tiles of one CTA's row range [r0, r1) of the flattened (b, t) space.
 // A segment is the part of the range inside one sequence: rows [a, e) of batch b.  Its
 // rows a - kRing .. e + tail - 1 are needed (tail = 0 for the forward; 3 for the backward,
 // whose last dx rows need g of the next 3 rows).  Tiles start at a - kRing and step by R;
