@@ -111,7 +111,9 @@ __device__ __forceinline__ void rings_push(f2 (&h)[3][P], f2 (&gr)[3][P], const 
 // Rows of one tile for this lane.  FULL: every row computes g, accumulates dw / dbias and
 // stores dx[t-3].  Otherwise rows before `from` were done with the previous tile, rows
 // before a only fill the x ring, halo rows after e give g (for the last dx rows) only.
-template <int VEC, int R, bool FULL>
+// STORE: this lane's channels exist, so stores need no per-row test.  The dx row pointer
+// (row t-3) advances by D per row.
+template <int VEC, int R, bool FULL, bool STORE>
 __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, int lane,
                                          const TileCursor& c, bool active, const BwdArgs& p,
                                          int64_t d0, const f2 (&tap)[4][VEC / 2],
@@ -119,28 +121,30 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
                                          f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
   constexpr int P = VEC / 2;
   constexpr int ROWB = 32 * VEC * 2;
-  uint16_t* dxbase = p.dx + static_cast<int64_t>(c.b) * p.T * p.D + d0;
+  uint16_t* dxrow = p.dx + (static_cast<int64_t>(c.b) * p.T + (c.tt - kRing)) * p.D + d0;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int t = c.tt + i;
-    if (!FULL && t < c.from) continue;
-    f2 x[P], g[P];
-    smem_row<VEC>(xt + i * ROWB, lane, x);
-    if (FULL || t >= c.a) {
-      f2 dy[P];
-      smem_row<VEC>(dyt + i * ROWB, lane, dy);
-      bwd_g<P>(x, dy, h, tap, bias2, g);
-      if (FULL || t < c.e) bwd_acc<P>(x, h, g, acc);
-      if (FULL || (t - kRing >= c.a && t - kRing < c.e)) {
-        f2 dxv[P];
-        bwd_dx<P>(g, gr, tap, dxv);
-        if (active) store_row<VEC>(dxbase + static_cast<int64_t>(t - kRing) * p.D, dxv);
-      }
-    } else {
+    if (FULL || t >= c.from) {
+      f2 x[P], g[P];
+      smem_row<VEC>(xt + i * ROWB, lane, x);
+      if (FULL || t >= c.a) {
+        f2 dy[P];
+        smem_row<VEC>(dyt + i * ROWB, lane, dy);
+        bwd_g<P>(x, dy, h, tap, bias2, g);
+        if (FULL || t < c.e) bwd_acc<P>(x, h, g, acc);
+        if (FULL || (t - kRing >= c.a && t - kRing < c.e)) {
+          f2 dxv[P];
+          bwd_dx<P>(g, gr, tap, dxv);
+          if (STORE || active) store_row<VEC>(dxrow, dxv);
+        }
+      } else {
 #pragma unroll
-      for (int q = 0; q < P; ++q) g[q] = 0ull;  // rows before the range: only the x ring
+        for (int q = 0; q < P; ++q) g[q] = 0ull;  // rows before the range: only the x ring
+      }
+      rings_push<P>(h, gr, x, g);
     }
-    rings_push<P>(h, gr, x, g);
+    dxrow += p.D;
   }
 }
 
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
     // ---- consumer ------------------------------------------------------------------------
     const int64_t d0 = c0 + warp * CB + lane * VEC;
     const bool active = d0 < p.D;
+    const bool all_active = c0 + NC * CB <= p.D;  // uniform over the CTA
     f2 tap[4][P], bias2[P];
     load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
     f2 h[3][P], gr[3][P], acc[kRec][P];
@@ -240,10 +245,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MINB)
       fph ^= 1u << s;
       const uint8_t* xt = smem + s * STAGE + warp * TILE;
       const uint8_t* dyt = xt + NC * TILE;
-      if (cur.from == cur.tt && cur.tt >= cur.a + kRing && cur.tt + R <= cur.e)
-        bwd_tile<VEC, R, true>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
-      else
-        bwd_tile<VEC, R, false>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+      if (cur.from == cur.tt && cur.tt >= cur.a + kRing && cur.tt + R <= cur.e) {
+        if (all_active)
+          bwd_tile<VEC, R, true, true>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+        else
+          bwd_tile<VEC, R, true, false>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+      } else {
+        bwd_tile<VEC, R, false, false>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       cur.advance();

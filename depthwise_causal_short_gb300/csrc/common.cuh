@@ -176,9 +176,11 @@ __device__ __forceinline__ f2 f2_tanh(f2 v) {
   return f2_pack(tanh_approx(lo), tanh_approx(hi));
 }
 
-// bf16x2 word -> fp32 pair: a bf16 is the upper half of a binary32.
+// bf16x2 word -> fp32 pair: a bf16 is the upper half of a binary32, so each half is moved
+// into the top 16 bits of a zeroed word (one byte permute each).
 __device__ __forceinline__ f2 bf16x2_to_f2(uint32_t u) {
-  return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  return f2_pack(__uint_as_float(__byte_perm(u, 0u, 0x1044)),
+                 __uint_as_float(__byte_perm(u, 0u, 0x3244)));
 }
 
 // fp32 pair -> bf16x2 word, round to nearest even.

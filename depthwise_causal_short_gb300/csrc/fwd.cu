@@ -65,27 +65,31 @@ __device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
 
 // Rows of one tile for this lane.  FULL: every row lies inside the segment.  Otherwise rows
 // before `from` were done with the previous tile, rows before a only fill the ring, and rows
-// from e on are not needed.
-template <int VEC, int R, bool FULL>
+// from e on are not needed.  STORE: this lane's channels exist (every lane of a CTA whose
+// channel group lies inside D), so stores need no per-row test.  The output row pointer
+// advances by D per row.
+template <int VEC, int R, bool FULL, bool STORE>
 __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const TileCursor& c,
                                          bool active, const FwdArgs& p, int64_t d0,
                                          const f2 (&tap)[4][VEC / 2], const f2 (&bias2)[VEC / 2],
                                          f2 (&h)[3][VEC / 2]) {
   constexpr int P = VEC / 2;
   constexpr int ROWB = 32 * VEC * 2;
-  uint16_t* ybase = p.y + static_cast<int64_t>(c.b) * p.T * p.D + d0;
+  uint16_t* yrow = p.y + (static_cast<int64_t>(c.b) * p.T + c.tt) * p.D + d0;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int t = c.tt + i;
-    if (!FULL && t < c.from) continue;
-    f2 x[P];
-    smem_row<VEC>(tile + i * ROWB, lane, x);
-    if (FULL || (t >= c.a && t < c.e)) {
-      f2 yv[P];
-      fwd_row<P>(x, h, tap, bias2, yv);
-      if (active) store_row<VEC>(ybase + static_cast<int64_t>(t) * p.D, yv);
+    if (FULL || t >= c.from) {
+      f2 x[P];
+      smem_row<VEC>(tile + i * ROWB, lane, x);
+      if (FULL || (t >= c.a && t < c.e)) {
+        f2 yv[P];
+        fwd_row<P>(x, h, tap, bias2, yv);
+        if (STORE || active) store_row<VEC>(yrow, yv);
+      }
+      ring_push<P>(h, x);
     }
-    ring_push<P>(h, x);
+    yrow += p.D;
   }
 }
 
@@ -153,6 +157,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     // ---- consumer ------------------------------------------------------------------------
     const int64_t d0 = c0 + warp * CB + lane * VEC;
     const bool active = d0 < p.D;
+    const bool all_active = c0 + NC * CB <= p.D;  // uniform over the CTA
     f2 tap[4][VEC / 2], bias2[VEC / 2];
     load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
     f2 h[3][VEC / 2];
@@ -172,10 +177,14 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
       }
       fph ^= 1u << s;
       const uint8_t* tile = smem + s * STAGE + warp * TILE;
-      if (cur.from == cur.tt && cur.tt >= cur.a && cur.tt + R <= cur.e)
-        fwd_tile<VEC, R, true>(tile, lane, cur, active, p, d0, tap, bias2, h);
-      else
-        fwd_tile<VEC, R, false>(tile, lane, cur, active, p, d0, tap, bias2, h);
+      if (cur.from == cur.tt && cur.tt >= cur.a && cur.tt + R <= cur.e) {
+        if (all_active)
+          fwd_tile<VEC, R, true, true>(tile, lane, cur, active, p, d0, tap, bias2, h);
+        else
+          fwd_tile<VEC, R, true, false>(tile, lane, cur, active, p, d0, tap, bias2, h);
+      } else {
+        fwd_tile<VEC, R, false, false>(tile, lane, cur, active, p, d0, tap, bias2, h);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       cur.advance();
