@@ -152,7 +152,7 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
 // and one producer warp (index NC).  Stage layout: NC x boxes, then NC dy boxes, each of
 // R rows x CB channels.
 template <int VEC, int R, int S, int NC, int MINB>
-__global__ void __launch_bounds__((NC + 1) * 32, MINB)
+__global__ void __maxnreg__(regs_for(NC, MINB))
     cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
                      const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
   constexpr int CB = 32 * VEC;
@@ -344,14 +344,14 @@ struct BwdConfig {
   BwdConfig { V, R, S, NC, M, cconv_bwd_kernel<V, R, S, NC, M> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 8, 6, 8, 1),
-    CCONV_BWD_CFG(4, 8, 4, 12, 1),
-    CCONV_BWD_CFG(4, 8, 3, 16, 1),
     CCONV_BWD_CFG(4, 16, 3, 8, 1),
+    CCONV_BWD_CFG(4, 8, 3, 16, 1),
     CCONV_BWD_CFG(4, 8, 3, 8, 2),
     CCONV_BWD_CFG(4, 4, 6, 16, 1),
+    CCONV_BWD_CFG(4, 8, 6, 8, 1),
     CCONV_BWD_CFG(4, 4, 5, 8, 2),
-    CCONV_BWD_CFG(8, 8, 3, 8, 1),
+    CCONV_BWD_CFG(4, 12, 4, 8, 1),
+    CCONV_BWD_CFG(4, 4, 4, 16, 1),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 

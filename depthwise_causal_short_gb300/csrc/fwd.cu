@@ -96,7 +96,7 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
 // CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile)
 // and one producer warp (index NC).  Stage layout: NC boxes of R rows x CB channels.
 template <int VEC, int R, int S, int NC, int MINB>
-__global__ void __launch_bounds__((NC + 1) * 32, MINB)
+__global__ void __maxnreg__(regs_for(NC, MINB))
 cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
@@ -206,14 +206,14 @@ struct FwdConfig {
   FwdConfig { V, R, S, NC, M, cconv_fwd_kernel<V, R, S, NC, M> }
 
 static const FwdConfig kFwdConfigs[] = {
+    CCONV_FWD_CFG(4, 8, 10, 8, 1),  // measured fastest at B=2 T=8192 D=4096
     CCONV_FWD_CFG(4, 16, 6, 8, 1),
-    CCONV_FWD_CFG(4, 8, 10, 8, 1),
-    CCONV_FWD_CFG(8, 8, 6, 8, 1),
-    CCONV_FWD_CFG(4, 16, 4, 12, 1),
     CCONV_FWD_CFG(4, 8, 6, 16, 1),
-    CCONV_FWD_CFG(4, 16, 3, 8, 2),
+    CCONV_FWD_CFG(4, 4, 12, 16, 1),
     CCONV_FWD_CFG(4, 8, 5, 8, 2),
-    CCONV_FWD_CFG(8, 16, 3, 8, 1),
+    CCONV_FWD_CFG(4, 4, 20, 8, 1),
+    CCONV_FWD_CFG(8, 8, 6, 8, 1),
+    CCONV_FWD_CFG(4, 8, 4, 16, 1),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 

@@ -19,6 +19,13 @@ namespace cconv {
 
 constexpr int kRing = 3;  // previous rows kept: W-1 for the widest supported W (4)
 
+// Registers per thread that let MINB CTAs of NC consumer warps + 1 producer warp share an
+// SM's 64K registers (multiple of 8, at most 255).
+constexpr int regs_for(int nc, int minb) {
+  return (65536 / ((nc + 1) * 32 * minb)) / 8 * 8 > 255 ? 255
+                                                         : (65536 / ((nc + 1) * 32 * minb)) / 8 * 8;
+}
+
 struct GroupPlan {
   int n_cg;  // channel groups: ceil(D / (NC * 32 * VEC))
   int cpc;   // CTAs (row ranges) per channel group
