@@ -216,6 +216,9 @@ __device__ __forceinline__ f2 f2_silu(f2 z) {
 // completed and flushed.  Without a trigger in the previous kernel this is an ordinary
 // stream-ordered launch.
 // ------------------------------------------------------------------------------------
+// With CCONV_DEBUG set in the environment, failing CUDA calls are reported on stderr.
+cudaError_t report_cuda(const char* what, cudaError_t e);
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args... args) {
@@ -229,7 +232,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kernel, args...);
+  return report_cuda("kernel launch", cudaLaunchKernelEx(&lc, kernel, args...));
 }
 
 // ------------------------------------------------------------------------------------

@@ -3,6 +3,8 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -12,6 +14,13 @@ namespace cconv {
 // Per-TU fault readers (each kernel file owns its own device fault word).
 int read_clear_fault_fwd(unsigned* out);
 int read_clear_fault_bwd(unsigned* out);
+
+cudaError_t report_cuda(const char* what, cudaError_t e) {
+  static const bool debug = getenv("CCONV_DEBUG") != nullptr;
+  if (e != cudaSuccess && debug)
+    fprintf(stderr, "cconv: %s failed: %s (%d)\n", what, cudaGetErrorString(e), static_cast<int>(e));
+  return e;
+}
 
 int sm_count_current_device(int* sms, int* device) {
   static std::atomic<int> cache[64];
@@ -65,8 +74,9 @@ int encode_rows_map(CUtensorMap* map, const void* base, int64_t B, int64_t T, in
 
 int set_max_dynamic_smem(const void* func, int bytes) {
   // Per device and cheap; repeated on every launch rather than cached.
-  return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
-                 cudaSuccess
+  return report_cuda("cudaFuncSetAttribute",
+                     cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          bytes)) == cudaSuccess
              ? CCONV_OK
              : CCONV_ERR_CUDA;
 }
