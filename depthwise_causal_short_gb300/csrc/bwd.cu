@@ -148,11 +148,26 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
   }
 }
 
-// CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile)
-// and one producer warp (index NC).  Stage layout: NC x boxes, then NC dy boxes, each of
-// R rows x CB channels.
-template <int VEC, int R, int S, int NC, int MINB>
-__global__ void __maxnreg__(regs_for(NC, MINB))
+// Loads one tile (rows cur.tt .. cur.tt+R-1: the x and dy box of every consumer warp).
+template <int VEC, int R, int NC>
+__device__ __forceinline__ void bwd_issue(uint8_t* st, uint64_t* full, const CUtensorMap* tmx,
+                                          const CUtensorMap* tmdy, const TileCursor& cur,
+                                          int nact, int c0, uint64_t pol) {
+  constexpr int CB = 32 * VEC;
+  constexpr int TILE = R * CB * 2;
+  mbar_arrive_expect_tx(full, 2 * nact * TILE);
+  for (int w = 0; w < nact; ++w) {
+    tma_load_3d(st + w * TILE, tmx, full, c0 + w * CB, cur.tt, cur.b, pol);
+    tma_load_3d(st + (NC + w) * TILE, tmdy, full, c0 + w * CB, cur.tt, cur.b, pol);
+  }
+}
+
+// CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile).
+// SEP: a separate producer warp (index NC) streams the stages; otherwise lane 0 of consumer
+// warp 0 re-arms each stage once every consumer has released it.  Stage layout: NC x boxes,
+// then NC dy boxes, each of R rows x CB channels.
+template <int VEC, int R, int S, int NC, int MINB, bool SEP>
+__global__ void __maxnreg__(regs_for(NC + SEP, MINB))
     cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
                      const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
   constexpr int CB = 32 * VEC;
@@ -190,10 +205,10 @@ __global__ void __maxnreg__(regs_for(NC, MINB))
 
   TileCursor cur;
   cur.init(r0, r1, p.T, kRing, R);
-  if (warp == NC) {
-    // ---- producer ------------------------------------------------------------------------
+  const uint64_t pol = policy_evict_first();
+  if (SEP && warp == NC) {
+    // ---- producer warp -------------------------------------------------------------------
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
       uint32_t eph = 0;
       int s = 0;
       for (int i = 0; !cur.done; ++i) {
@@ -204,18 +219,21 @@ __global__ void __maxnreg__(regs_for(NC, MINB))
           }
           eph ^= 1u << s;
         }
-        uint8_t* st = smem + s * STAGE;
-        mbar_arrive_expect_tx(&full[s], 2 * nact * TILE);
-        for (int w = 0; w < nact; ++w) {
-          tma_load_3d(st + w * TILE, &tmx, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
-          tma_load_3d(st + (NC + w) * TILE, &tmdy, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
-        }
+        bwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, &tmdy, cur, nact, c0, pol);
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }
     }
   } else if (warp < nact) {
     // ---- consumer ------------------------------------------------------------------------
+    const bool leader = !SEP && warp == 0;
+    TileCursor pc = cur;  // the leader's producer cursor, S tiles ahead
+    if (leader && lane == 0) {
+      for (int s = 0; s < S && !pc.done; ++s) {
+        bwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, &tmdy, pc, nact, c0, pol);
+        pc.advance();
+      }
+    }
     const int64_t d0 = c0 + warp * CB + lane * VEC;
     const bool active = d0 < p.D;
     const bool all_active = c0 + NC * CB <= p.D;  // uniform over the CTA
@@ -233,7 +251,7 @@ __global__ void __maxnreg__(regs_for(NC, MINB))
       for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
     }
 
-    uint32_t fph = 0;
+    uint32_t fph = 0, eph = 0;
     int s = 0;
     while (!cur.done) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (fph >> s) & 1u,
@@ -255,6 +273,21 @@ __global__ void __maxnreg__(regs_for(NC, MINB))
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (leader) {
+        // Re-arm this stage with the tile S ahead once every consumer has released it.
+        bool fine = true;
+        if (lane == 0 && !pc.done) {
+          fine = mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs);
+          if (fine) {
+            bwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, &tmdy, pc, nact, c0, pol);
+            pc.advance();
+          } else {
+            atomicOr(&g_fault_bwd, kFaultBwdWait);
+          }
+        }
+        eph ^= 1u << s;
+        if (!__all_sync(0xffffffffu, fine)) break;
+      }
       cur.advance();
       s = (s + 1 == S) ? 0 : s + 1;
     }
@@ -336,22 +369,22 @@ __global__ void __launch_bounds__(32 * kRedGroups)
 }
 
 struct BwdConfig {
-  int vec, rows, stages, nc, ctas_per_sm;
+  int vec, rows, stages, nc, ctas_per_sm, sep;
   void (*kernel)(const CUtensorMap, const CUtensorMap, const BwdArgs);
 };
 
-#define CCONV_BWD_CFG(V, R, S, NC, M) \
-  BwdConfig { V, R, S, NC, M, cconv_bwd_kernel<V, R, S, NC, M> }
+#define CCONV_BWD_CFG(V, R, S, NC, M, SEP) \
+  BwdConfig { V, R, S, NC, M, SEP, cconv_bwd_kernel<V, R, S, NC, M, SEP> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 16, 3, 8, 1),
-    CCONV_BWD_CFG(4, 8, 3, 16, 1),
-    CCONV_BWD_CFG(4, 8, 3, 8, 2),
-    CCONV_BWD_CFG(4, 4, 6, 16, 1),
-    CCONV_BWD_CFG(4, 8, 6, 8, 1),
-    CCONV_BWD_CFG(4, 4, 5, 8, 2),
-    CCONV_BWD_CFG(4, 12, 4, 8, 1),
-    CCONV_BWD_CFG(4, 4, 4, 16, 1),
+    CCONV_BWD_CFG(4, 16, 3, 8, 1, true),
+    CCONV_BWD_CFG(4, 8, 3, 16, 1, false),
+    CCONV_BWD_CFG(4, 4, 6, 16, 1, false),
+    CCONV_BWD_CFG(4, 8, 3, 8, 2, false),
+    CCONV_BWD_CFG(4, 4, 5, 8, 2, false),
+    CCONV_BWD_CFG(4, 16, 3, 8, 1, false),
+    CCONV_BWD_CFG(4, 8, 6, 8, 1, true),
+    CCONV_BWD_CFG(4, 4, 4, 16, 1, false),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
@@ -451,7 +484,7 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   const int smem = cfg.stages * (stage + 16);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3((cfg.nc + 1) * 32), smem, st, tmx, tmdy, a) !=
+  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3((cfg.nc + cfg.sep) * 32), smem, st, tmx, tmdy, a) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
   const float* wsp = a.ws;

@@ -93,10 +93,23 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
   }
 }
 
-// CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile)
-// and one producer warp (index NC).  Stage layout: NC boxes of R rows x CB channels.
-template <int VEC, int R, int S, int NC, int MINB>
-__global__ void __maxnreg__(regs_for(NC, MINB))
+// Loads one tile (rows cur.tt .. cur.tt+R-1, one box per consumer warp) into a stage.
+template <int VEC, int R, int NC>
+__device__ __forceinline__ void fwd_issue(uint8_t* st, uint64_t* full, const CUtensorMap* tmx,
+                                          const TileCursor& cur, int nact, int c0, uint64_t pol) {
+  constexpr int CB = 32 * VEC;
+  constexpr int TILE = R * CB * 2;
+  mbar_arrive_expect_tx(full, nact * TILE);
+  for (int w = 0; w < nact; ++w)
+    tma_load_3d(st + w * TILE, tmx, full, c0 + w * CB, cur.tt, cur.b, pol);
+}
+
+// CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile).
+// SEP: a separate producer warp (index NC) streams the stages; otherwise lane 0 of consumer
+// warp 0 re-arms each stage once every consumer has released it.  Stage layout: NC boxes of
+// R rows x CB channels.
+template <int VEC, int R, int S, int NC, int MINB, bool SEP>
+__global__ void __maxnreg__(regs_for(NC + SEP, MINB))
 cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
@@ -131,10 +144,10 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
 
   TileCursor cur;
   cur.init(r0, r1, p.T, 0, R);
-  if (warp == NC) {
-    // ---- producer ------------------------------------------------------------------------
+  const uint64_t pol = policy_evict_first();
+  if (SEP && warp == NC) {
+    // ---- producer warp -------------------------------------------------------------------
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
       uint32_t eph = 0;
       int s = 0;
       for (int i = 0; !cur.done; ++i) {
@@ -145,16 +158,21 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
           }
           eph ^= 1u << s;
         }
-        uint8_t* st = smem + s * STAGE;
-        mbar_arrive_expect_tx(&full[s], nact * TILE);
-        for (int w = 0; w < nact; ++w)
-          tma_load_3d(st + w * TILE, &tmx, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
+        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, cur, nact, c0, pol);
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }
     }
   } else if (warp < nact) {
     // ---- consumer ------------------------------------------------------------------------
+    const bool leader = !SEP && warp == 0;
+    TileCursor pc = cur;  // the leader's producer cursor, S tiles ahead
+    if (leader && lane == 0) {
+      for (int s = 0; s < S && !pc.done; ++s) {
+        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, pc, nact, c0, pol);
+        pc.advance();
+      }
+    }
     const int64_t d0 = c0 + warp * CB + lane * VEC;
     const bool active = d0 < p.D;
     const bool all_active = c0 + NC * CB <= p.D;  // uniform over the CTA
@@ -166,7 +184,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
 #pragma unroll
       for (int q = 0; q < VEC / 2; ++q) h[j][q] = 0ull;
 
-    uint32_t fph = 0;
+    uint32_t fph = 0, eph = 0;
     int s = 0;
     while (!cur.done) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (fph >> s) & 1u,
@@ -187,6 +205,21 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (leader) {
+        // Re-arm this stage with the tile S ahead once every consumer has released it.
+        bool fine = true;
+        if (lane == 0 && !pc.done) {
+          fine = mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs);
+          if (fine) {
+            fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, pc, nact, c0, pol);
+            pc.advance();
+          } else {
+            atomicOr(&g_fault_fwd, kFaultFwdWait);
+          }
+        }
+        eph ^= 1u << s;
+        if (!__all_sync(0xffffffffu, fine)) break;
+      }
       cur.advance();
       s = (s + 1 == S) ? 0 : s + 1;
     }
@@ -198,22 +231,22 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
 // launch configurations (compile-time tile shapes; the first is the default)
 // ------------------------------------------------------------------------------------
 struct FwdConfig {
-  int vec, rows, stages, nc, ctas_per_sm;
+  int vec, rows, stages, nc, ctas_per_sm, sep;
   void (*kernel)(const CUtensorMap, const FwdArgs);
 };
 
-#define CCONV_FWD_CFG(V, R, S, NC, M) \
-  FwdConfig { V, R, S, NC, M, cconv_fwd_kernel<V, R, S, NC, M> }
+#define CCONV_FWD_CFG(V, R, S, NC, M, SEP) \
+  FwdConfig { V, R, S, NC, M, SEP, cconv_fwd_kernel<V, R, S, NC, M, SEP> }
 
 static const FwdConfig kFwdConfigs[] = {
-    CCONV_FWD_CFG(4, 8, 10, 8, 1),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_FWD_CFG(4, 16, 6, 8, 1),
-    CCONV_FWD_CFG(4, 8, 6, 16, 1),
-    CCONV_FWD_CFG(4, 4, 12, 16, 1),
-    CCONV_FWD_CFG(4, 8, 5, 8, 2),
-    CCONV_FWD_CFG(4, 4, 20, 8, 1),
-    CCONV_FWD_CFG(8, 8, 6, 8, 1),
-    CCONV_FWD_CFG(4, 8, 4, 16, 1),
+    CCONV_FWD_CFG(4, 8, 10, 8, 1, true),  // measured fastest at B=2 T=8192 D=4096
+    CCONV_FWD_CFG(4, 8, 10, 8, 1, false),
+    CCONV_FWD_CFG(4, 8, 6, 16, 1, false),
+    CCONV_FWD_CFG(4, 4, 12, 16, 1, false),
+    CCONV_FWD_CFG(4, 16, 6, 8, 1, false),
+    CCONV_FWD_CFG(4, 4, 20, 8, 1, true),
+    CCONV_FWD_CFG(4, 8, 5, 8, 2, false),
+    CCONV_FWD_CFG(4, 16, 3, 8, 2, false),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 
@@ -272,7 +305,7 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
   const int smem = cfg.stages * (stage + 16);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  return launch_pdl(cfg.kernel, dim3(plan.grid), dim3((cfg.nc + 1) * 32), smem,
+  return launch_pdl(cfg.kernel, dim3(plan.grid), dim3((cfg.nc + cfg.sep) * 32), smem,
                     reinterpret_cast<cudaStream_t>(stream), tmx, a) == cudaSuccess
              ? CCONV_OK
              : CCONV_ERR_CUDA;

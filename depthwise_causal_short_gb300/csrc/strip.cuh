@@ -19,11 +19,14 @@ namespace cconv {
 
 constexpr int kRing = 3;  // previous rows kept: W-1 for the widest supported W (4)
 
-// Registers per thread that let MINB CTAs of NC consumer warps + 1 producer warp share an
-// SM's 64K registers (multiple of 8, at most 255).
-constexpr int regs_for(int nc, int minb) {
-  return (65536 / ((nc + 1) * 32 * minb)) / 8 * 8 > 255 ? 255
-                                                         : (65536 / ((nc + 1) * 32 * minb)) / 8 * 8;
+// Registers per thread for MINB CTAs of `warps` warps per SM.  The register file is split
+// among the SM's 4 sub-partitions (16K registers each) and a CTA's warps are spread over
+// them, so the bound is set by the sub-partition holding the most warps.  Multiple of 8,
+// at most 255.
+constexpr int regs_for(int warps, int minb) {
+  return (16384 / (((warps * minb + 3) / 4) * 32)) / 8 * 8 > 255
+             ? 255
+             : (16384 / (((warps * minb + 3) / 4) * 32)) / 8 * 8;
 }
 
 struct GroupPlan {
