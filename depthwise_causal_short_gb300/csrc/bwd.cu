@@ -38,10 +38,10 @@ struct BwdArgs {
   const void* w;
   const void* bias;
   uint16_t* dx;   // [B,T,D] contiguous bf16
-  float* ws;      // [grid][NC][kRec][32*VEC] fp32 partial records
+  float* ws;      // [total_warps][kRec][32*VEC] fp32 partials
   int64_t D;
   int T, BT;
-  int cpc;        // CTAs per channel group
+  int n_cb, wpc, total_warps;
   int W, wdt;
 };
 
@@ -148,174 +148,139 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
   }
 }
 
-// Loads one tile (rows cur.tt .. cur.tt+R-1: the x and dy box of every consumer warp).
-template <int VEC, int R, int NC>
-__device__ __forceinline__ void bwd_issue(uint8_t* st, uint64_t* full, const CUtensorMap* tmx,
-                                          const CUtensorMap* tmdy, const TileCursor& cur,
-                                          int nact, int c0, uint64_t pol) {
-  constexpr int CB = 32 * VEC;
-  constexpr int TILE = R * CB * 2;
-  mbar_arrive_expect_tx(full, 2 * nact * TILE);
-  for (int w = 0; w < nact; ++w) {
-    tma_load_3d(st + w * TILE, tmx, full, c0 + w * CB, cur.tt, cur.b, pol);
-    tma_load_3d(st + (NC + w) * TILE, tmdy, full, c0 + w * CB, cur.tt, cur.b, pol);
-  }
-}
-
-// CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile).
-// SEP: a separate producer warp (index NC) streams the stages; otherwise lane 0 of consumer
-// warp 0 re-arms each stage once every consumer has released it.  Stage layout: NC x boxes,
-// then NC dy boxes, each of R rows x CB channels.
-template <int VEC, int R, int S, int NC, int MINB, bool SEP>
-__global__ void __maxnreg__(regs_for(NC + SEP, MINB))
+template <int VEC, int R, int S, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
     cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
                      const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
   constexpr int CB = 32 * VEC;
   constexpr int P = VEC / 2;
   constexpr int TILE = R * CB * 2;
-  constexpr int STAGE = 2 * NC * TILE;
+  constexpr int STAGE = 2 * TILE;  // x tile, then dy tile
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
-  uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int cg = blockIdx.x / p.cpc;
-  const int part = blockIdx.x - cg * p.cpc;
-  const int r0 = static_cast<int>(static_cast<int64_t>(part) * p.BT / p.cpc);
-  const int r1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.BT / p.cpc);
-  const int c0 = cg * NC * CB;
-  int nact = static_cast<int>((p.D - c0 + CB - 1) / CB);  // consumer warps with channels
-  if (nact > NC) nact = NC;
+  const int gw = blockIdx.x * NW + warp;
+  if (gw >= p.total_warps) {  // no CTA-wide barrier follows
+    grid_launch_dependents();
+    return;
+  }
 
-  if (threadIdx.x == 0) {
+  uint8_t* stages = smem + warp * (S * STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
+
+  // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
+  // strips of the same rows at about the same time (contiguous row segments in DRAM).
+  const int k = gw / p.n_cb;
+  const int cb = gw - k * p.n_cb;
+  const int r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
+  const int r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
+  const int c0 = cb * CB;
+  const int64_t d0 = c0 + lane * VEC;
+  const bool active = d0 < p.D;
+  const bool all_active = c0 + CB <= p.D;  // uniform over the warp
+
+  if (lane == 0) {
     prefetch_tensormap(&tmx);
     prefetch_tensormap(&tmdy);
 #pragma unroll
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], nact);
-    }
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
-  __syncthreads();  // the only CTA-wide barrier
+  __syncwarp();
 
-  // Nothing above touches global memory; from here on the previous kernel on the stream has
-  // completed.
+  // Everything above touches no global memory; from here on the previous kernel on the
+  // stream has completed.
   grid_dependency_wait();
 
-  TileCursor cur;
-  cur.init(r0, r1, p.T, kRing, R);
+  TileCursor pc, cc;
+  pc.init(r0, r1, p.T, kRing, R);
+  cc = pc;
   const uint64_t pol = policy_evict_first();
-  if (SEP && warp == NC) {
-    // ---- producer warp -------------------------------------------------------------------
-    if (lane == 0) {
-      uint32_t eph = 0;
-      int s = 0;
-      for (int i = 0; !cur.done; ++i) {
-        if (i >= S) {  // wait until every consumer has released this stage
-          if (!mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs)) {
-            atomicOr(&g_fault_bwd, kFaultBwdWait);
-            break;
-          }
-          eph ^= 1u << s;
-        }
-        bwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, &tmdy, cur, nact, c0, pol);
-        cur.advance();
-        s = (s + 1 == S) ? 0 : s + 1;
-      }
-    }
-  } else if (warp < nact) {
-    // ---- consumer ------------------------------------------------------------------------
-    const bool leader = !SEP && warp == 0;
-    TileCursor pc = cur;  // the leader's producer cursor, S tiles ahead
-    if (leader && lane == 0) {
-      for (int s = 0; s < S && !pc.done; ++s) {
-        bwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, &tmdy, pc, nact, c0, pol);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      if (!pc.done) {
+        mbar_arrive_expect_tx(&bars[s], STAGE);
+        tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
+        tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt,
+                    pc.b, pol);
         pc.advance();
       }
     }
-    const int64_t d0 = c0 + warp * CB + lane * VEC;
-    const bool active = d0 < p.D;
-    const bool all_active = c0 + NC * CB <= p.D;  // uniform over the CTA
-    f2 tap[4][P], bias2[P];
-    load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
-    f2 h[3][P], gr[3][P], acc[kRec][P];
-#pragma unroll
-    for (int q = 0; q < P; ++q) {
-#pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        h[j][q] = 0ull;
-        gr[j][q] = 0ull;
-      }
-#pragma unroll
-      for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
-    }
-
-    uint32_t fph = 0, eph = 0;
-    int s = 0;
-    while (!cur.done) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (fph >> s) & 1u,
-                                                               kWaitLimitNs));
-      if (!ok) {
-        if (lane == 0) atomicOr(&g_fault_bwd, kFaultBwdWait);
-        break;
-      }
-      fph ^= 1u << s;
-      const uint8_t* xt = smem + s * STAGE + warp * TILE;
-      const uint8_t* dyt = xt + NC * TILE;
-      if (cur.from == cur.tt && cur.tt >= cur.a + kRing && cur.tt + R <= cur.e) {
-        if (all_active)
-          bwd_tile<VEC, R, true, true>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
-        else
-          bwd_tile<VEC, R, true, false>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
-      } else {
-        bwd_tile<VEC, R, false, false>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (leader) {
-        // Re-arm this stage with the tile S ahead once every consumer has released it.
-        bool fine = true;
-        if (lane == 0 && !pc.done) {
-          fine = mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs);
-          if (fine) {
-            bwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, &tmdy, pc, nact, c0, pol);
-            pc.advance();
-          } else {
-            atomicOr(&g_fault_bwd, kFaultBwdWait);
-          }
-        }
-        eph ^= 1u << s;
-        if (!__all_sync(0xffffffffu, fine)) break;
-      }
-      cur.advance();
-      s = (s + 1 == S) ? 0 : s + 1;
-    }
-
-    // This warp's partial record: ws[blockIdx.x][warp][j][lane*VEC + v]
-    float* rec = p.ws + (static_cast<int64_t>(blockIdx.x) * NC + warp) * kRec * CB + lane * VEC;
-#pragma unroll
-    for (int j = 0; j < kRec; ++j) {
-      float v[VEC];
-#pragma unroll
-      for (int q = 0; q < P; ++q) f2_unpack(acc[j][q], v[2 * q], v[2 * q + 1]);
-#pragma unroll
-      for (int q = 0; q < VEC; q += 4)
-        *reinterpret_cast<float4*>(rec + j * CB + q) =
-            make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
-    }
   }
+
+  // Taps load while the first tiles are in flight.
+  f2 tap[4][P], bias2[P];
+  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
+
+  f2 h[3][P], gr[3][P], acc[kRec][P];
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      h[j][q] = 0ull;
+      gr[j][q] = 0ull;
+    }
+#pragma unroll
+    for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
+  }
+
+  uint32_t parity = 0;
+  int s = 0;
+  while (!cc.done) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
+                                                             kWaitLimitNs));
+    if (!ok) {
+      if (lane == 0) atomicOr(&g_fault_bwd, kFaultBwdWait);
+      for (int j = 0; j < S; ++j) (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
+      return;
+    }
+    parity ^= 1u << s;
+    const uint8_t* xt = stages + s * STAGE;
+    if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
+      if (all_active)
+        bwd_tile<VEC, R, true, true>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+      else
+        bwd_tile<VEC, R, true, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+    } else {
+      bwd_tile<VEC, R, false, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+    }
+    __syncwarp();
+    if (lane == 0 && !pc.done) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bars[s], STAGE);
+      tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
+      tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b,
+                  pol);
+      pc.advance();
+    }
+    cc.advance();
+    s = (s + 1 == S) ? 0 : s + 1;
+  }
+
   grid_launch_dependents();
+
+  // This warp's partial record: ws[gw][j][lane*VEC + v]
+  float* rec = p.ws + static_cast<int64_t>(gw) * kRec * CB + lane * VEC;
+#pragma unroll
+  for (int j = 0; j < kRec; ++j) {
+    float v[VEC];
+#pragma unroll
+    for (int q = 0; q < P; ++q) f2_unpack(acc[j][q], v[2 * q], v[2 * q + 1]);
+#pragma unroll
+    for (int q = 0; q < VEC; q += 4)
+      *reinterpret_cast<float4*>(rec + j * CB + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+  }
 }
 
-// dw[d, W-1-lag] and dbias[d] from the cpc records of d's channel group, summed in a fixed
+// dw[d, W-1-lag] and dbias[d] from the wpc partial records of d's strip, summed in a fixed
 // order.  CTA = 32 channels x kRedGroups groups for one record row j (blockIdx.y): group g
 // adds records g, g + G, g + 2G, ... with four interleaved accumulators combined in a fixed
 // order, then the G group sums are added in group order.  Deterministic; no atomics.
 constexpr int kRedGroups = 16;
 
 __global__ void __launch_bounds__(32 * kRedGroups)
-    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int nc, int cpc,
+    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int n_cb, int wpc,
                             int64_t D, int W, int wdt, void* dw, void* dbias) {
   __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
@@ -325,23 +290,20 @@ __global__ void __launch_bounds__(32 * kRedGroups)
   const int64_t d = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float a = 0.f;
   if (d < D) {
-    const int64_t group_width = static_cast<int64_t>(nc) * cb_width;
-    const int64_t cg = d / group_width;
-    const int w = static_cast<int>((d - cg * group_width) / cb_width);
-    const int c = static_cast<int>(d % cb_width);
-    // records of channel group cg are those of CTAs cg*cpc .. cg*cpc + cpc - 1
-    const int64_t step = static_cast<int64_t>(nc) * kRec * cb_width;
-    const float* base = ws + (cg * cpc * nc + w) * kRec * cb_width +
-                        static_cast<int64_t>(j) * cb_width + c;
+    const int64_t cb = d / cb_width;
+    const int c = static_cast<int>(d - cb * cb_width);
+    // strip cb's records are those of warps k * n_cb + cb, k = 0 .. wpc-1
+    const int64_t step = static_cast<int64_t>(kRec) * cb_width * n_cb;
+    const float* base = ws + cb * kRec * cb_width + static_cast<int64_t>(j) * cb_width + c;
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     int r = grp;
-    for (; r + 3 * kRedGroups < cpc; r += 4 * kRedGroups) {
+    for (; r + 3 * kRedGroups < wpc; r += 4 * kRedGroups) {
       a0 += base[r * step];
       a1 += base[(r + kRedGroups) * step];
       a2 += base[(r + 2 * kRedGroups) * step];
       a3 += base[(r + 3 * kRedGroups) * step];
     }
-    for (; r < cpc; r += kRedGroups) a0 += base[r * step];
+    for (; r < wpc; r += kRedGroups) a0 += base[r * step];
     a = (a0 + a1) + (a2 + a3);
   }
   part[grp][lane] = a;
@@ -369,22 +331,22 @@ __global__ void __launch_bounds__(32 * kRedGroups)
 }
 
 struct BwdConfig {
-  int vec, rows, stages, nc, ctas_per_sm, sep;
+  int vec, rows, stages, warps;
   void (*kernel)(const CUtensorMap, const CUtensorMap, const BwdArgs);
 };
 
-#define CCONV_BWD_CFG(V, R, S, NC, M, SEP) \
-  BwdConfig { V, R, S, NC, M, SEP, cconv_bwd_kernel<V, R, S, NC, M, SEP> }
+#define CCONV_BWD_CFG(V, R, S, NW) \
+  BwdConfig { V, R, S, NW, cconv_bwd_kernel<V, R, S, NW> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 16, 3, 8, 1, true),
-    CCONV_BWD_CFG(4, 8, 3, 16, 1, false),
-    CCONV_BWD_CFG(4, 4, 6, 16, 1, false),
-    CCONV_BWD_CFG(4, 8, 3, 8, 2, false),
-    CCONV_BWD_CFG(4, 4, 5, 8, 2, false),
-    CCONV_BWD_CFG(4, 16, 3, 8, 1, false),
-    CCONV_BWD_CFG(4, 8, 6, 8, 1, true),
-    CCONV_BWD_CFG(4, 4, 4, 16, 1, false),
+    CCONV_BWD_CFG(4, 8, 2, 16),  // measured fastest at B=2 T=8192 D=4096
+    CCONV_BWD_CFG(8, 8, 3, 8),
+    CCONV_BWD_CFG(4, 8, 4, 8),
+    CCONV_BWD_CFG(4, 16, 2, 12),
+    CCONV_BWD_CFG(4, 8, 3, 16),
+    CCONV_BWD_CFG(4, 8, 4, 12),
+    CCONV_BWD_CFG(4, 16, 3, 8),
+    CCONV_BWD_CFG(4, 4, 4, 16),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
@@ -398,13 +360,13 @@ static int bwd_config_index() {
   return idx;
 }
 
-static int bwd_plan(int64_t B, int64_t T, int64_t D, const BwdConfig& cfg, GroupPlan* plan,
+static int bwd_plan(int64_t B, int64_t T, int64_t D, const BwdConfig& cfg, StripPlan* plan,
                     size_t* ws_bytes) {
   int sms = 0;
   const int rc = sm_count_current_device(&sms, nullptr);
   if (rc != CCONV_OK) return rc;
-  *plan = make_group_plan(B, T, D, cfg.vec, cfg.nc, cfg.ctas_per_sm, sms, 32);
-  *ws_bytes = static_cast<size_t>(plan->grid) * cfg.nc * kRec * (32 * cfg.vec) * sizeof(float);
+  *plan = make_strip_plan(B, T, D, cfg.vec, cfg.warps, 1, sms, 32);
+  *ws_bytes = static_cast<size_t>(plan->total_warps) * kRec * (32 * cfg.vec) * sizeof(float);
   return CCONV_OK;
 }
 
@@ -425,7 +387,7 @@ CCONV_API int cconv_bwd_workspace_bytes(int64_t B, int64_t T, int64_t D, int W, 
   if (!bytes) return CCONV_ERR_NULL;
   int rc = check_sizes(B, T, D, W);
   if (rc != CCONV_OK) return rc;
-  GroupPlan plan;
+  StripPlan plan;
   return bwd_plan(B, T, D, kBwdConfigs[bwd_config_index()], &plan, bytes);
 }
 
@@ -452,7 +414,7 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
     return CCONV_ERR_ALIGN;
 
   const BwdConfig& cfg = kBwdConfigs[bwd_config_index()];
-  GroupPlan plan;
+  StripPlan plan;
   size_t need = 0;
   rc = bwd_plan(B, T, D, cfg, &plan, &need);
   if (rc != CCONV_OK) return rc;
@@ -475,26 +437,26 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   a.D = D;
   a.T = static_cast<int>(T);
   a.BT = static_cast<int>(B * T);
-  a.cpc = plan.cpc;
+  a.n_cb = plan.n_cb;
+  a.wpc = plan.wpc;
+  a.total_warps = plan.total_warps;
   a.W = W;
   a.wdt = wdt;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int stage = 2 * cfg.nc * cfg.rows * 32 * cfg.vec * 2;
-  const int smem = cfg.stages * (stage + 16);
+  const int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3((cfg.nc + cfg.sep) * 32), smem, st, tmx, tmdy, a) !=
+  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
   const float* wsp = a.ws;
   const int cbw = 32 * cfg.vec;
-  const int nc = cfg.nc;
-  const int cpc = plan.cpc;
+  const int wpc = plan.wpc;
   const int wdt_i = static_cast<int>(wdt);
   if (launch_pdl(cconv_bwd_reduce_kernel,
                  dim3(static_cast<unsigned>((D + 31) / 32), dbias ? kRec : W),
-                 dim3(32 * kRedGroups), 0, st, wsp, cbw, nc, cpc, D, W, wdt_i, dw, dbias) !=
+                 dim3(32 * kRedGroups), 0, st, wsp, cbw, plan.n_cb, wpc, D, W, wdt_i, dw, dbias) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;

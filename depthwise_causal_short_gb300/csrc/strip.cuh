@@ -51,7 +51,33 @@ inline GroupPlan make_group_plan(int64_t B, int64_t T, int64_t D, int vec, int n
   return p;
 }
 
-// Walks the tiles of one CTA's row range [r0, r1) of the flattened (b, t) space.
+struct StripPlan {
+  int n_cb;          // channel strips: ceil(D / (32*VEC))
+  int wpc;           // warps (row ranges) per strip
+  int total_warps;   // n_cb * wpc
+  int grid;          // CTAs of `warps_per_cta` warps
+};
+
+// Per-warp split (each warp runs its own pipeline over one channel strip of 32*VEC channels):
+// warp gw takes strip gw % n_cb of range gw / n_cb.  rows_min: shortest range worth a warp.
+inline StripPlan make_strip_plan(int64_t B, int64_t T, int64_t D, int vec, int warps_per_cta,
+                                 int ctas_per_sm, int sms, int64_t rows_min) {
+  StripPlan p;
+  const int64_t cb_width = 32 * vec;
+  p.n_cb = static_cast<int>((D + cb_width - 1) / cb_width);
+  const int64_t target = static_cast<int64_t>(sms) * ctas_per_sm * warps_per_cta;
+  int64_t wpc = target / p.n_cb;
+  if (wpc < 1) wpc = 1;
+  int64_t by_rows = (B * T) / rows_min;
+  if (by_rows < 1) by_rows = 1;
+  if (wpc > by_rows) wpc = by_rows;
+  p.wpc = static_cast<int>(wpc);
+  p.total_warps = p.n_cb * p.wpc;
+  p.grid = (p.total_warps + warps_per_cta - 1) / warps_per_cta;
+  return p;
+}
+
+// Walks the tiles of one CTA's (or warp's) row range [r0, r1) of the flattened (b, t) space.
 // A segment is the part of the range inside one sequence: rows [a, e) of batch b.  Its
 // rows a - kRing .. e + tail - 1 are needed (tail = 0 for the forward; 3 for the backward,
 // whose last dx rows need g of the next 3 rows).  Tiles start at a - kRing and step by R;
