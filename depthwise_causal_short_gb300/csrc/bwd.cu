@@ -45,28 +45,29 @@ struct BwdArgs {
   int W, wdt;
 };
 
-// g for one row, from its x and dy and the x ring h = (x[t-1], x[t-2], x[t-3]).
+// 2g for one row, from its x and dy and the x ring h = (x[t-1], x[t-2], x[t-3]).  With
+// halved taps hz = z / 2 and th = tanh(hz): sigmoid(z) = (1 + th) / 2, 1 - sigmoid(z) =
+// (1 - th) / 2, so g = dy sigmoid(z) (1 + z (1 - sigmoid(z))) = dy (1 + th) (1 + hz (1 - th)) / 2.
+// The kernel carries g2 = 2g: dx = sum_k (w/2) g2 uses the same halved taps, and the dw / dbias
+// sums of g2 are halved once, when the partial record is written.
 template <int P>
 __device__ __forceinline__ void bwd_g(const f2 (&x)[P], const f2 (&dy)[P], const f2 (&h)[3][P],
                                       const f2 (&tap)[4][P], const f2 (&bias2)[P], f2 (&g)[P]) {
-  const f2 half = f2_splat(0.5f);
-  const f2 nhalf = f2_splat(-0.5f);
   const f2 one = f2_splat(1.0f);
+  const f2 mone = f2_splat(-1.0f);
 #pragma unroll
   for (int q = 0; q < P; ++q) {
-    f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
-    z = f2_fma(tap[1][q], h[0][q], z);
-    z = f2_fma(tap[2][q], h[1][q], z);
-    z = f2_fma(tap[3][q], h[2][q], z);
-    const f2 th = f2_tanh(f2_mul(z, half));
-    const f2 sg = f2_fma(th, half, half);   // sigmoid(z)
-    const f2 om = f2_fma(th, nhalf, half);  // 1 - sigmoid(z)
-    const f2 d1 = f2_fma(z, om, one);       // 1 + z (1 - sigmoid(z))
-    g[q] = f2_mul(f2_mul(dy[q], sg), d1);
+    f2 hz = f2_fma(tap[0][q], x[q], bias2[q]);
+    hz = f2_fma(tap[1][q], h[0][q], hz);
+    hz = f2_fma(tap[2][q], h[1][q], hz);
+    hz = f2_fma(tap[3][q], h[2][q], hz);
+    const f2 th = f2_tanh(hz);
+    const f2 d1 = f2_fma(hz, f2_fma(th, mone, one), one);  // 1 + hz (1 - th)
+    g[q] = f2_mul(f2_mul(dy[q], f2_add(th, one)), d1);   // dy (1 + th) (1 + hz (1 - th))
   }
 }
 
-// dw lags and dbias: acc[k] += g[t] x[t-k], acc[4] += g[t]
+// dw lags and dbias (of g2 = 2g): acc[k] += g2[t] x[t-k], acc[4] += g2[t]
 template <int P>
 __device__ __forceinline__ void bwd_acc(const f2 (&x)[P], const f2 (&h)[3][P], const f2 (&g)[P],
                                         f2 (&acc)[kRec][P]) {
@@ -80,7 +81,8 @@ __device__ __forceinline__ void bwd_acc(const f2 (&x)[P], const f2 (&h)[3][P], c
   }
 }
 
-// dx[t-3] = sum_k tap[k] g[t-3+k], from g[t] and the g ring gr = (g[t-1], g[t-2], g[t-3])
+// dx[t-3] = sum_k w[d,W-1-k] g[t-3+k] = sum_k tap[k] g2[t-3+k] (halved taps), from g2[t] and
+// the ring gr = (g2[t-1], g2[t-2], g2[t-3])
 template <int P>
 __device__ __forceinline__ void bwd_dx(const f2 (&g)[P], const f2 (&gr)[3][P],
                                        const f2 (&tap)[4][P], f2 (&dxv)[P]) {
@@ -260,13 +262,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   grid_launch_dependents();
 
-  // This warp's partial record: ws[gw][j][lane*VEC + v]
+  // This warp's partial record: ws[gw][j][lane*VEC + v] (the sums of g2 = 2g, halved here)
   float* rec = p.ws + static_cast<int64_t>(gw) * kRec * CB + lane * VEC;
 #pragma unroll
   for (int j = 0; j < kRec; ++j) {
     float v[VEC];
 #pragma unroll
-    for (int q = 0; q < P; ++q) f2_unpack(acc[j][q], v[2 * q], v[2 * q + 1]);
+    for (int q = 0; q < P; ++q) f2_unpack(f2_mul(acc[j][q], f2_splat(0.5f)), v[2 * q], v[2 * q + 1]);
 #pragma unroll
     for (int q = 0; q < VEC; q += 4)
       *reinterpret_cast<float4*>(rec + j * CB + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
@@ -340,13 +342,13 @@ struct BwdConfig {
 
 static const BwdConfig kBwdConfigs[] = {
     CCONV_BWD_CFG(4, 8, 2, 16),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_BWD_CFG(8, 8, 3, 8),
-    CCONV_BWD_CFG(4, 8, 4, 8),
-    CCONV_BWD_CFG(4, 16, 2, 12),
+    CCONV_BWD_CFG(4, 12, 2, 16),
+    CCONV_BWD_CFG(4, 6, 3, 16),
+    CCONV_BWD_CFG(4, 6, 4, 16),
+    CCONV_BWD_CFG(4, 12, 2, 12),
+    CCONV_BWD_CFG(4, 6, 4, 12),
     CCONV_BWD_CFG(4, 8, 3, 16),
-    CCONV_BWD_CFG(4, 8, 4, 12),
-    CCONV_BWD_CFG(4, 16, 3, 8),
-    CCONV_BWD_CFG(4, 4, 4, 16),
+    CCONV_BWD_CFG(4, 12, 3, 8),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 

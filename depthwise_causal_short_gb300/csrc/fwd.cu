@@ -39,17 +39,18 @@ struct FwdArgs {
 };
 
 // One output row from the new input row x and the ring h = (x[t-1], x[t-2], x[t-3]).
+// With halved taps hz = z / 2, and silu(z) = hz * (1 + tanh(hz)).
 template <int P>
 __device__ __forceinline__ void fwd_row(const f2 (&x)[P], const f2 (&h)[3][P],
                                         const f2 (&tap)[4][P], const f2 (&bias2)[P],
                                         f2 (&yv)[P]) {
 #pragma unroll
   for (int q = 0; q < P; ++q) {
-    f2 z = f2_fma(tap[0][q], x[q], bias2[q]);
-    z = f2_fma(tap[1][q], h[0][q], z);
-    z = f2_fma(tap[2][q], h[1][q], z);
-    z = f2_fma(tap[3][q], h[2][q], z);
-    yv[q] = f2_silu(z);
+    f2 hz = f2_fma(tap[0][q], x[q], bias2[q]);
+    hz = f2_fma(tap[1][q], h[0][q], hz);
+    hz = f2_fma(tap[2][q], h[1][q], hz);
+    hz = f2_fma(tap[3][q], h[2][q], hz);
+    yv[q] = f2_fma(hz, f2_tanh(hz), hz);
   }
 }
 
@@ -240,13 +241,13 @@ struct FwdConfig {
 
 static const FwdConfig kFwdConfigs[] = {
     CCONV_FWD_CFG(4, 8, 10, 8, 1, true),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_FWD_CFG(4, 8, 10, 8, 1, false),
-    CCONV_FWD_CFG(4, 8, 6, 16, 1, false),
-    CCONV_FWD_CFG(4, 4, 12, 16, 1, false),
-    CCONV_FWD_CFG(4, 16, 6, 8, 1, false),
-    CCONV_FWD_CFG(4, 4, 20, 8, 1, true),
-    CCONV_FWD_CFG(4, 8, 5, 8, 2, false),
-    CCONV_FWD_CFG(4, 16, 3, 8, 2, false),
+    CCONV_FWD_CFG(4, 12, 8, 8, 1, true),
+    CCONV_FWD_CFG(4, 6, 16, 8, 1, true),
+    CCONV_FWD_CFG(4, 6, 12, 8, 1, true),
+    CCONV_FWD_CFG(4, 12, 6, 8, 1, true),
+    CCONV_FWD_CFG(4, 16, 6, 8, 1, true),
+    CCONV_FWD_CFG(4, 24, 4, 8, 1, true),
+    CCONV_FWD_CFG(4, 12, 4, 8, 2, true),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 

@@ -135,9 +135,11 @@ struct TileCursor {
   }
 };
 
-// Taps of one lane, as fp32 pairs: tap[k][p] multiplies x[t-k] for channels
-// (d0 + 2p, d0 + 2p + 1); it is w[d, W-1-k], zero for k >= W (a narrow W is the width-4
-// case with zero taps on the old side).  bias2[p] likewise (zero without a bias).
+// Taps of one lane, as fp32 pairs, HALVED: tap[k][p] = w[d, W-1-k] / 2 multiplies x[t-k]
+// for channels (d0 + 2p, d0 + 2p + 1), zero for k >= W (a narrow W is the width-4 case with
+// zero taps on the old side); bias2[p] = bias[d] / 2 (zero without a bias).  With them the
+// kernels form hz = z / 2 directly, the argument of the tanh form of the sigmoid, and
+// silu(z) = z * (1 + tanh(z/2)) / 2 = hz * (1 + tanh(hz)).  Halving is exact.
 template <int VEC>
 __device__ __forceinline__ void load_taps(const void* w, const void* bias, int wdt, int W,
                                           int64_t d0, bool active, f2 (&tap)[4][VEC / 2],
@@ -160,7 +162,7 @@ __device__ __forceinline__ void load_taps(const void* w, const void* bias, int w
           hi[k] = bf16_to_f32(static_cast<const uint16_t*>(w)[i1]);
         }
       }
-      tap[k][p] = f2_pack(lo[k], hi[k]);
+      tap[k][p] = f2_pack(0.5f * lo[k], 0.5f * hi[k]);
     }
     float b0 = 0.f, b1 = 0.f;
     if (active && bias) {
@@ -172,7 +174,7 @@ __device__ __forceinline__ void load_taps(const void* w, const void* bias, int w
         b1 = bf16_to_f32(static_cast<const uint16_t*>(bias)[d0 + 2 * p + 1]);
       }
     }
-    bias2[p] = f2_pack(b0, b1);
+    bias2[p] = f2_pack(0.5f * b0, 0.5f * b1);
   }
 }
 
