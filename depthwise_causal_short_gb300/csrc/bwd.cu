@@ -269,9 +269,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
     float v[VEC];
 #pragma unroll
     for (int q = 0; q < P; ++q) f2_unpack(f2_mul(acc[j][q], f2_splat(0.5f)), v[2 * q], v[2 * q + 1]);
+    if constexpr (VEC == 2) {
+      *reinterpret_cast<float2*>(rec + j * CB) = make_float2(v[0], v[1]);
+    } else {
 #pragma unroll
-    for (int q = 0; q < VEC; q += 4)
-      *reinterpret_cast<float4*>(rec + j * CB + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+      for (int q = 0; q < VEC; q += 4)
+        *reinterpret_cast<float4*>(rec + j * CB + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+    }
   }
 }
 
@@ -341,14 +345,14 @@ struct BwdConfig {
   BwdConfig { V, R, S, NW, cconv_bwd_kernel<V, R, S, NW> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 8, 2, 16),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_BWD_CFG(4, 12, 2, 16),
-    CCONV_BWD_CFG(4, 6, 3, 16),
-    CCONV_BWD_CFG(4, 6, 4, 16),
-    CCONV_BWD_CFG(4, 12, 2, 12),
-    CCONV_BWD_CFG(4, 6, 4, 12),
-    CCONV_BWD_CFG(4, 8, 3, 16),
-    CCONV_BWD_CFG(4, 12, 3, 8),
+    CCONV_BWD_CFG(4, 6, 3, 16),  // measured fastest at B=2 T=8192 D=4096
+    CCONV_BWD_CFG(2, 6, 4, 24),
+    CCONV_BWD_CFG(2, 12, 2, 24),
+    CCONV_BWD_CFG(2, 6, 3, 32),
+    CCONV_BWD_CFG(2, 12, 2, 32),
+    CCONV_BWD_CFG(2, 6, 4, 20),
+    CCONV_BWD_CFG(4, 8, 2, 16),
+    CCONV_BWD_CFG(2, 24, 2, 16),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 

@@ -2,7 +2,7 @@
 //
 // A channel group is NC * 32 * VEC consecutive channels: one CTA tile row, split among NC
 // consumer warps of 32 lanes with VEC channels each, so each warp reads its part of a row as
-// one coalesced 16-byte (VEC=8) or 8-byte (VEC=4) access per lane.  Each group's rows,
+// one coalesced 16-byte (VEC=8), 8-byte (VEC=4) or 4-byte (VEC=2) access per lane.  Each group's rows,
 // flattened over (b, t), are cut into `cpc` equal contiguous ranges, one per CTA, so every
 // CTA gets the same number of rows (to within one) and the grid is one wave of resident
 // CTAs.  Inside a CTA a producer warp streams tiles of R rows x the group's channels into a
@@ -187,11 +187,13 @@ __device__ __forceinline__ void smem_row(const uint8_t* row, int lane, f2 (&x)[V
     x[1] = bf16x2_to_f2(v.y);
     x[2] = bf16x2_to_f2(v.z);
     x[3] = bf16x2_to_f2(v.w);
-  } else {
-    static_assert(VEC == 4, "VEC is 4 or 8");
+  } else if constexpr (VEC == 4) {
     const uint2 v = *reinterpret_cast<const uint2*>(row + lane * 8);
     x[0] = bf16x2_to_f2(v.x);
     x[1] = bf16x2_to_f2(v.y);
+  } else {
+    static_assert(VEC == 2, "VEC is 2, 4 or 8");
+    x[0] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(row + lane * 4));
   }
 }
 
@@ -205,11 +207,13 @@ __device__ __forceinline__ void store_row(uint16_t* dst, const f2 (&v)[VEC / 2])
     o.z = f2_to_bf16x2(v[2]);
     o.w = f2_to_bf16x2(v[3]);
     *reinterpret_cast<uint4*>(dst) = o;
-  } else {
+  } else if constexpr (VEC == 4) {
     uint2 o;
     o.x = f2_to_bf16x2(v[0]);
     o.y = f2_to_bf16x2(v[1]);
     *reinterpret_cast<uint2*>(dst) = o;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = f2_to_bf16x2(v[0]);
   }
 }
 
