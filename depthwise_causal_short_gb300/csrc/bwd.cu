@@ -346,13 +346,13 @@ struct BwdConfig {
 
 static const BwdConfig kBwdConfigs[] = {
     CCONV_BWD_CFG(4, 6, 3, 16),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_BWD_CFG(2, 6, 4, 24),
-    CCONV_BWD_CFG(2, 12, 2, 24),
-    CCONV_BWD_CFG(2, 6, 3, 32),
-    CCONV_BWD_CFG(2, 12, 2, 32),
-    CCONV_BWD_CFG(2, 6, 4, 20),
+    CCONV_BWD_CFG(4, 6, 4, 16),
     CCONV_BWD_CFG(4, 8, 2, 16),
-    CCONV_BWD_CFG(2, 24, 2, 16),
+    CCONV_BWD_CFG(4, 12, 2, 16),
+    CCONV_BWD_CFG(4, 6, 4, 12),
+    CCONV_BWD_CFG(4, 12, 3, 8),
+    CCONV_BWD_CFG(2, 6, 4, 24),
+    CCONV_BWD_CFG(8, 8, 3, 8),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 

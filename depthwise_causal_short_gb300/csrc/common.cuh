@@ -201,12 +201,6 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
   return r;
 }
 
-// silu(z) = z * sigmoid(z), sigmoid(z) = 0.5 * tanh(z / 2) + 0.5
-__device__ __forceinline__ f2 f2_silu(f2 z) {
-  const f2 half = f2_splat(0.5f);
-  const f2 th = f2_tanh(f2_mul(z, half));
-  return f2_mul(z, f2_fma(th, half, half));
-}
 
 // ------------------------------------------------------------------------------------
 // host: launch with programmatic stream serialisation.  The kernel may be scheduled

@@ -241,13 +241,13 @@ struct FwdConfig {
 
 static const FwdConfig kFwdConfigs[] = {
     CCONV_FWD_CFG(4, 8, 10, 8, 1, true),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_FWD_CFG(4, 12, 8, 8, 1, true),
-    CCONV_FWD_CFG(4, 6, 16, 8, 1, true),
-    CCONV_FWD_CFG(4, 6, 12, 8, 1, true),
     CCONV_FWD_CFG(4, 12, 6, 8, 1, true),
     CCONV_FWD_CFG(4, 16, 6, 8, 1, true),
     CCONV_FWD_CFG(4, 24, 4, 8, 1, true),
     CCONV_FWD_CFG(4, 12, 4, 8, 2, true),
+    CCONV_FWD_CFG(8, 8, 6, 8, 1, true),
+    CCONV_FWD_CFG(4, 8, 5, 8, 2, false),
+    CCONV_FWD_CFG(4, 4, 20, 8, 1, true),
 };
 static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 
