@@ -11,8 +11,9 @@
 // Index validation is fused and fails closed without a trap: every CTA loads all N
 // indices, range-checks them and finds repeats with a one-bit-per-slot bitmap in shared
 // memory, so all CTAs reach the same verdict with no inter-CTA communication.  On a bad
-// vector no CTA writes anything but CTA 0's status words.  This replaces the pages'
-// per-CTA O(N^2) scan and device trap with an O(N + S/32) check and a status word.
+// vector no CTA writes anything but CTA 0's status words (state rows are only read, and
+// only for in-range slots).  This replaces the pages' per-CTA O(N^2) scan and device trap
+// with an O(N + S/32) check and a status word.
 #include "common.cuh"
 
 namespace cconv {
@@ -94,85 +95,103 @@ __device__ __forceinline__ void load_update_taps(const UpdArgs& p, int64_t d0,
 
 // VEC = channels per thread (8: 16-byte vectors; 1: scalar path), L = W - 1, ROWS = rows
 // per thread.  Grid: x over channel vectors, y over groups of ROWS rows.
+//
+// Latency is what this kernel is about (a decode step moves ~17 MB, mostly L2-resident), so
+// every independent load is issued before the index check needs to finish: this thread's
+// slot ids, token rows, taps and bias first, then the CTA's pass over all N indices; the
+// state rows of in-range slots are fetched while the check completes.  Only the writes wait
+// for the verdict.
 template <int VEC, int L, int ROWS>
 __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs p) {
   constexpr int W = L + 1;
   extern __shared__ uint32_t bitmap[];
   __shared__ int s_bad;
 
+  if (p.idx) {  // shared-memory set-up only: no global access before the dependency wait
+    if (threadIdx.x == 0) s_bad = 0;
+    const int nwords = static_cast<int>((p.S + 31) / 32);
+    for (int i = threadIdx.x; i < nwords; i += kUpdThreads) bitmap[i] = 0u;
+  }
   grid_dependency_wait();
+
+  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kUpdThreads + threadIdx.x) * VEC;
+  const bool mine = d0 < p.D;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * ROWS;
+
+  // ---- this thread's rows: slot ids, token rows, taps ------------------------------------
+  int64_t slot[ROWS];
+  uint16_t win[ROWS][VEC][W];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    const int64_t i = i0 + r;
+    slot[r] = (mine && i < p.N) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
+    if (mine && i < p.N) {
+      const uint16_t* xr = p.x + i * p.ldx + d0;
+      if constexpr (VEC == 8) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xr);
+        const uint16_t* xh = reinterpret_cast<const uint16_t*>(&xv);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) win[r][c][L] = xh[c];
+      } else {
+        win[r][0][L] = xr[0];
+      }
+    }
+  }
+  float tw[VEC][W], tb[VEC];
+  if (mine) load_update_taps<VEC, W>(p, d0, tw, tb);
 
   // ---- validation: identical verdict in every CTA --------------------------------------
   int bad = 0;
   if (p.idx) {
-    const int nwords = static_cast<int>((p.S + 31) / 32);
-    if (threadIdx.x == 0) s_bad = 0;
-    for (int i = threadIdx.x; i < nwords; i += kUpdThreads) bitmap[i] = 0u;
-    __syncthreads();
-    int mine = 0;
+    __syncthreads();  // the zeroed bitmap is visible
+    int off = 0;
     for (int64_t i = threadIdx.x; i < p.N; i += kUpdThreads) {
       const int32_t v = p.idx[i];
       if (v < 0) {
-        mine |= CCONV_IDX_NEGATIVE;
+        off |= CCONV_IDX_NEGATIVE;
       } else if (v >= p.S) {
-        mine |= CCONV_IDX_OUT_OF_RANGE;
+        off |= CCONV_IDX_OUT_OF_RANGE;
       } else {
         const uint32_t m = 1u << (v & 31);
-        if (atomicOr(&bitmap[v >> 5], m) & m) mine |= CCONV_IDX_DUPLICATE;
+        if (atomicOr(&bitmap[v >> 5], m) & m) off |= CCONV_IDX_DUPLICATE;
       }
     }
-    if (mine) atomicOr(&s_bad, mine);
-    __syncthreads();
+    if (off) atomicOr(&s_bad, off);
+  }
+
+  // ---- state rows of in-range slots, fetched while the check completes ------------------
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    if (slot[r] < 0 || slot[r] >= p.S) continue;
+    const uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
+    if constexpr (VEC == 8) {
+      // 8 channels x L state entries are 16*L contiguous bytes
+      uint4 sv[L > 0 ? L : 1];
+#pragma unroll
+      for (int u = 0; u < L; ++u) sv[u] = reinterpret_cast<const uint4*>(st)[u];
+      const uint16_t* sh = reinterpret_cast<const uint16_t*>(sv);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c)
+#pragma unroll
+        for (int j = 0; j < L; ++j) win[r][c][j] = sh[c * L + j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < L; ++j) win[r][0][j] = st[j];
+    }
+  }
+
+  if (p.idx) {
+    __syncthreads();  // every index of this CTA's pass is checked
     bad = s_bad;
   }
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     p.status[0] = bad ? CCONV_ERR_INDEX : CCONV_OK;
     p.status[1] = bad;
   }
-  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kUpdThreads + threadIdx.x) * VEC;
-  if (bad || d0 >= p.D) {
-    grid_launch_dependents();
-    return;
-  }
-
-  // ---- update: all of this thread's rows are loaded before any is computed -------------
-  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * ROWS;
-  int64_t slot[ROWS];
-#pragma unroll
-  for (int r = 0; r < ROWS; ++r) {
-    const int64_t i = i0 + r;
-    slot[r] = (i < p.N) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
-  }
-  uint16_t win[ROWS][VEC][W];
-#pragma unroll
-  for (int r = 0; r < ROWS; ++r) {
-    if (slot[r] < 0) continue;
-    const uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
-    const uint16_t* xr = p.x + (i0 + r) * p.ldx + d0;
-    if constexpr (VEC == 8) {
-      // 8 channels x L state entries are 16*L contiguous bytes; x is one 16-byte vector.
-      uint4 sv[L > 0 ? L : 1];
-#pragma unroll
-      for (int u = 0; u < L; ++u) sv[u] = reinterpret_cast<const uint4*>(st)[u];
-      const uint4 xv = *reinterpret_cast<const uint4*>(xr);
-      const uint16_t* sh = reinterpret_cast<const uint16_t*>(sv);
-      const uint16_t* xh = reinterpret_cast<const uint16_t*>(&xv);
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) {
-#pragma unroll
-        for (int j = 0; j < L; ++j) win[r][c][j] = sh[c * L + j];
-        win[r][c][L] = xh[c];
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < L; ++j) win[r][0][j] = st[j];
-      win[r][0][L] = xr[0];
-    }
-  }
-  float tw[VEC][W], tb[VEC];
-  load_update_taps<VEC, W>(p, d0, tw, tb);
   grid_launch_dependents();
+  if (bad || !mine) return;
 
+  // ---- y and the shifted state (writes only after a clean verdict) -----------------------
 #pragma unroll
   for (int r = 0; r < ROWS; ++r) {
     if (slot[r] < 0) continue;
