@@ -14,6 +14,8 @@
 // vector no CTA writes anything but CTA 0's status words (state rows are only read, and
 // only for in-range slots).  This replaces the pages' per-CTA O(N^2) scan and device trap
 // with an O(N + S/32) check and a status word.
+#include <cstdlib>
+
 #include "common.cuh"
 
 namespace cconv {
@@ -292,6 +294,12 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
   const int64_t gx = (nvec + kUpdThreads - 1) / kUpdThreads;
   int rows = 1;
   while (rows < 4 && gx * ((N + rows - 1) / rows) > 4 * static_cast<int64_t>(sms)) rows *= 2;
+  static const int rows_override = [] {  // sweeps only: CCONV_UPDATE_ROWS = 1, 2 or 4
+    const char* e = getenv("CCONV_UPDATE_ROWS");
+    const int v = e ? atoi(e) : 0;
+    return (v == 1 || v == 2 || v == 4) ? v : 0;
+  }();
+  if (rows_override) rows = rows_override;
   const int64_t gy = (N + rows - 1) / rows;
   if (gx > 2147483647 || gy > 65535) return CCONV_ERR_SHAPE;
   UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows) : pick_update_kernel<1>(W, rows);
