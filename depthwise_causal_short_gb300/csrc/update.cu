@@ -244,7 +244,9 @@ static UpdKernel pick_update_kernel(int W, int rows) {
   switch (rows) {
     case 1: return pick_update_kernel_w<VEC, 1>(W);
     case 2: return pick_update_kernel_w<VEC, 2>(W);
-    default: return pick_update_kernel_w<VEC, 4>(W);
+    case 4: return pick_update_kernel_w<VEC, 4>(W);
+    case 8: return pick_update_kernel_w<VEC, 8>(W);
+    default: return pick_update_kernel_w<VEC, 16>(W);
   }
 }
 
@@ -294,10 +296,10 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
   const int64_t gx = (nvec + kUpdThreads - 1) / kUpdThreads;
   int rows = 1;
   while (rows < 4 && gx * ((N + rows - 1) / rows) > 4 * static_cast<int64_t>(sms)) rows *= 2;
-  static const int rows_override = [] {  // sweeps only: CCONV_UPDATE_ROWS = 1, 2 or 4
+  static const int rows_override = [] {  // sweeps only: CCONV_UPDATE_ROWS = 1, 2, 4, 8 or 16
     const char* e = getenv("CCONV_UPDATE_ROWS");
     const int v = e ? atoi(e) : 0;
-    return (v == 1 || v == 2 || v == 4) ? v : 0;
+    return (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ? v : 0;
   }();
   if (rows_override) rows = rows_override;
   const int64_t gy = (N + rows - 1) / rows;
