@@ -293,11 +293,11 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
   // Rows per thread: 4 measured fastest for the decode workload (N=256, D=4096: 128 CTAs,
   // 5.1 us per step in a CUDA graph against 8.0 us with one row): every CTA repeats the O(N)
   // index check, so fewer, fuller CTAs cost less, and each thread keeps four rows' loads in
-  // flight.  Fewer rows only when that still leaves under one CTA per SM.
+  // flight.  Fewer rows only when four would leave more than half of the SMs idle.
   const int64_t nvec = (D + vec - 1) / vec;
   const int64_t gx = (nvec + kUpdThreads - 1) / kUpdThreads;
   int rows = 4;
-  while (rows > 1 && gx * ((N + rows - 1) / rows) < static_cast<int64_t>(sms)) rows /= 2;
+  while (rows > 1 && 2 * gx * ((N + rows - 1) / rows) < static_cast<int64_t>(sms)) rows /= 2;
   static const int rows_override = [] {  // sweeps only: CCONV_UPDATE_ROWS = 1, 2, 4, 8 or 16
     const char* e = getenv("CCONV_UPDATE_ROWS");
     const int v = e ? atoi(e) : 0;
