@@ -38,7 +38,7 @@ struct BwdArgs {
   const void* w;
   const void* bias;
   uint16_t* dx;   // [B,T,D] contiguous bf16
-  float* ws;      // [total_warps][kRec][32*VEC] fp32 partials
+  float* ws;      // [grid][NW][kRec][32*VEC] fp32 partial records (slots used per CTA)
   int64_t D;
   int T, BT;
   int n_cb, wpc, total_warps;
@@ -158,30 +158,28 @@ __global__ void __launch_bounds__(NW * 32, 1)
   constexpr int P = VEC / 2;
   constexpr int TILE = R * CB * 2;
   constexpr int STAGE = 2 * TILE;  // x tile, then dy tile
+  constexpr int REC = kRec * CB;   // floats in one partial record
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * NW + warp;
-  if (gw >= p.total_warps) {  // no CTA-wide barrier follows
-    grid_launch_dependents();
-    return;
-  }
+  const bool has_work = gw < p.total_warps;
 
   uint8_t* stages = smem + warp * (S * STAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
 
-  // Strips vary fastest along the warp index, so the warps of a CTA read neighbouring
-  // strips of the same rows at about the same time (contiguous row segments in DRAM).
-  const int k = gw / p.n_cb;
-  const int cb = gw - k * p.n_cb;
+  // Range-major: consecutive warps take consecutive row ranges of one strip, so the warps
+  // of a CTA mostly share a strip and their partial sums can be added inside the CTA.
+  const int cb = gw / p.wpc;
+  const int k = gw - cb * p.wpc;
   const int r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
   const int r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
   const int c0 = cb * CB;
   const int64_t d0 = c0 + lane * VEC;
-  const bool active = d0 < p.D;
+  const bool active = has_work && d0 < p.D;
   const bool all_active = c0 + CB <= p.D;  // uniform over the warp
 
-  if (lane == 0) {
+  if (has_work && lane == 0) {
     prefetch_tensormap(&tmx);
     prefetch_tensormap(&tmdy);
 #pragma unroll
@@ -194,145 +192,144 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // stream has completed.
   grid_dependency_wait();
 
-  TileCursor pc, cc;
-  pc.init(r0, r1, p.T, kRing, R);
-  cc = pc;
-  const uint64_t pol = policy_evict_first();
-  if (lane == 0) {
+  f2 acc[kRec][P];
 #pragma unroll
-    for (int s = 0; s < S; ++s) {
-      if (!pc.done) {
-        mbar_arrive_expect_tx(&bars[s], STAGE);
-        tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-        tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt,
-                    pc.b, pol);
-        pc.advance();
-      }
-    }
-  }
-
-  // Taps load while the first tiles are in flight.
-  f2 tap[4][P], bias2[P];
-  load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
-
-  f2 h[3][P], gr[3][P], acc[kRec][P];
-#pragma unroll
-  for (int q = 0; q < P; ++q) {
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      h[j][q] = 0ull;
-      gr[j][q] = 0ull;
-    }
+  for (int q = 0; q < P; ++q)
 #pragma unroll
     for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
-  }
 
-  uint32_t parity = 0;
-  int s = 0;
-  while (!cc.done) {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
-                                                             kWaitLimitNs));
-    if (!ok) {
-      if (lane == 0) atomicOr(&g_fault_bwd, kFaultBwdWait);
-      for (int j = 0; j < S; ++j) (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
-      return;
+  if (has_work) {
+    TileCursor pc, cc;
+    pc.init(r0, r1, p.T, kRing, R);
+    cc = pc;
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        if (!pc.done) {
+          mbar_arrive_expect_tx(&bars[s], STAGE);
+          tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
+          tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+          pc.advance();
+        }
+      }
     }
-    parity ^= 1u << s;
-    const uint8_t* xt = stages + s * STAGE;
-    if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
-      if (all_active)
-        bwd_tile<VEC, R, true, true>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
-      else
-        bwd_tile<VEC, R, true, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
-    } else {
-      bwd_tile<VEC, R, false, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
-    }
-    __syncwarp();
-    if (lane == 0 && !pc.done) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[s], STAGE);
-      tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-      tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b,
-                  pol);
-      pc.advance();
-    }
-    cc.advance();
-    s = (s + 1 == S) ? 0 : s + 1;
-  }
 
+    // Taps load while the first tiles are in flight.
+    f2 tap[4][P], bias2[P];
+    load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
+
+    f2 h[3][P], gr[3][P];
+#pragma unroll
+    for (int q = 0; q < P; ++q)
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        h[j][q] = 0ull;
+        gr[j][q] = 0ull;
+      }
+
+    uint32_t parity = 0;
+    int s = 0;
+    while (!cc.done) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (parity >> s) & 1u,
+                                                               kWaitLimitNs));
+      if (!ok) {
+        if (lane == 0) atomicOr(&g_fault_bwd, kFaultBwdWait);
+        // Let this warp's other copies land (bounded) before its stages are reused.
+        for (int j = 0; j < S; ++j)
+          (void)mbar_wait_bounded(&bars[j], (parity >> j) & 1u, 100000000ull);
+        break;
+      }
+      parity ^= 1u << s;
+      const uint8_t* xt = stages + s * STAGE;
+      if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
+        if (all_active)
+          bwd_tile<VEC, R, true, true>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+        else
+          bwd_tile<VEC, R, true, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+      } else {
+        bwd_tile<VEC, R, false, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+      }
+      __syncwarp();
+      if (lane == 0 && !pc.done) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[s], STAGE);
+        tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
+        tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+        pc.advance();
+      }
+      cc.advance();
+      s = (s + 1 == S) ? 0 : s + 1;
+    }
+  }
   grid_launch_dependents();
 
-  // This warp's partial record: ws[gw][j][lane*VEC + v] (the sums of g2 = 2g, halved here)
-  float* rec = p.ws + static_cast<int64_t>(gw) * kRec * CB + lane * VEC;
+  // ---- the CTA's partial sums, added in a fixed order ------------------------------------
+  // Every warp has consumed all its tiles, so the stage memory is free for NW records.
+  __syncthreads();
+  float* buf = reinterpret_cast<float*>(smem);  // [NW][kRec][CB], sums of g2 = 2g halved
 #pragma unroll
   for (int j = 0; j < kRec; ++j) {
     float v[VEC];
 #pragma unroll
     for (int q = 0; q < P; ++q) f2_unpack(f2_mul(acc[j][q], f2_splat(0.5f)), v[2 * q], v[2 * q + 1]);
-    if constexpr (VEC == 2) {
-      *reinterpret_cast<float2*>(rec + j * CB) = make_float2(v[0], v[1]);
-    } else {
 #pragma unroll
-      for (int q = 0; q < VEC; q += 4)
-        *reinterpret_cast<float4*>(rec + j * CB + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
-    }
+    for (int q = 0; q < VEC; ++q) buf[warp * REC + j * CB + lane * VEC + q] = v[q];
+  }
+  __syncthreads();
+  // Strips this CTA's working warps touch: slot i holds strip cb_first + i, summed over the
+  // CTA's warps of that strip in warp order.
+  const int g_first = blockIdx.x * NW;
+  const int g_last = min(p.total_warps, g_first + NW) - 1;
+  const int cb_first = g_first / p.wpc;
+  const int nslots = g_last / p.wpc - cb_first + 1;
+  float* rec = p.ws + static_cast<int64_t>(blockIdx.x) * NW * REC;
+  for (int e = threadIdx.x; e < nslots * REC; e += NW * 32) {
+    const int slot = e / REC;
+    const int jc = e - slot * REC;
+    const int cbs = cb_first + slot;
+    const int w_lo = max(cbs * p.wpc - g_first, 0);
+    const int w_hi = min((cbs + 1) * p.wpc - g_first, g_last - g_first + 1);
+    float a = 0.f;
+    for (int w = w_lo; w < w_hi; ++w) a += buf[w * REC + jc];
+    rec[e] = a;
   }
 }
 
-// dw[d, W-1-lag] and dbias[d] from the wpc partial records of d's strip, summed in a fixed
-// order.  CTA = 32 channels x kRedGroups groups for one record row j (blockIdx.y): group g
-// adds records g, g + G, g + 2G, ... with four interleaved accumulators combined in a fixed
-// order, then the G group sums are added in group order.  Deterministic; no atomics.
-constexpr int kRedGroups = 16;
-
-__global__ void __launch_bounds__(32 * kRedGroups)
-    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int n_cb, int wpc,
+// dw[d, W-1-lag] and dbias[d]: the records of d's strip come from CTAs c_lo .. c_hi (the
+// CTAs holding that strip's warps), slot cb - (first strip of the CTA); they are added in
+// CTA order, one thread per output.  Deterministic; no atomics.
+__global__ void __launch_bounds__(256)
+    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int nw, int wpc,
                             int64_t D, int W, int wdt, void* dw, void* dbias) {
-  __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
-  const int lane = threadIdx.x & 31;
-  const int grp = threadIdx.x >> 5;
+  const int64_t d = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   const int j = blockIdx.y;
-  const int64_t d = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  if (d >= D) return;
+  const int64_t cb = d / cb_width;
+  const int c = static_cast<int>(d - cb * cb_width);
+  const int64_t rec = static_cast<int64_t>(kRec) * cb_width;
+  const int64_t c_lo = (cb * wpc) / nw;
+  const int64_t c_hi = ((cb + 1) * wpc - 1) / nw;
   float a = 0.f;
-  if (d < D) {
-    const int64_t cb = d / cb_width;
-    const int c = static_cast<int>(d - cb * cb_width);
-    // strip cb's records are those of warps k * n_cb + cb, k = 0 .. wpc-1
-    const int64_t step = static_cast<int64_t>(kRec) * cb_width * n_cb;
-    const float* base = ws + cb * kRec * cb_width + static_cast<int64_t>(j) * cb_width + c;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int r = grp;
-    for (; r + 3 * kRedGroups < wpc; r += 4 * kRedGroups) {
-      a0 += base[r * step];
-      a1 += base[(r + kRedGroups) * step];
-      a2 += base[(r + 2 * kRedGroups) * step];
-      a3 += base[(r + 3 * kRedGroups) * step];
-    }
-    for (; r < wpc; r += kRedGroups) a0 += base[r * step];
-    a = (a0 + a1) + (a2 + a3);
+  for (int64_t cta = c_lo; cta <= c_hi; ++cta) {
+    const int64_t slot = cb - (cta * nw) / wpc;
+    a += ws[(cta * nw + slot) * rec + static_cast<int64_t>(j) * cb_width + c];
   }
-  part[grp][lane] = a;
-  __syncthreads();
-  if (grp == 0 && d < D) {
-    float s = 0.f;
-#pragma unroll
-    for (int g = 0; g < kRedGroups; ++g) s += part[g][lane];
-    if (j < 4) {
-      const int lag = j;
-      if (lag < W) {
-        const int64_t o = d * W + (W - 1 - lag);
-        if (wdt == CCONV_F32)
-          static_cast<float*>(dw)[o] = s;
-        else
-          static_cast<uint16_t*>(dw)[o] = f32_to_bf16(s);
-      }
-    } else if (dbias) {
+  if (j < 4) {
+    const int lag = j;
+    if (lag < W) {
+      const int64_t o = d * W + (W - 1 - lag);
       if (wdt == CCONV_F32)
-        static_cast<float*>(dbias)[d] = s;
+        static_cast<float*>(dw)[o] = a;
       else
-        static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(s);
+        static_cast<uint16_t*>(dw)[o] = f32_to_bf16(a);
     }
+  } else if (dbias) {
+    if (wdt == CCONV_F32)
+      static_cast<float*>(dbias)[d] = a;
+    else
+      static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(a);
   }
 }
 
@@ -372,7 +369,7 @@ static int bwd_plan(int64_t B, int64_t T, int64_t D, const BwdConfig& cfg, Strip
   const int rc = sm_count_current_device(&sms, nullptr);
   if (rc != CCONV_OK) return rc;
   *plan = make_strip_plan(B, T, D, cfg.vec, cfg.warps, 1, sms, 32);
-  *ws_bytes = static_cast<size_t>(plan->total_warps) * kRec * (32 * cfg.vec) * sizeof(float);
+  *ws_bytes = static_cast<size_t>(plan->grid) * cfg.warps * kRec * (32 * cfg.vec) * sizeof(float);
   return CCONV_OK;
 }
 
@@ -450,7 +447,9 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   a.wdt = wdt;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
+  int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
+  const int red_bytes = cfg.warps * kRec * 32 * cfg.vec * static_cast<int>(sizeof(float));
+  if (smem < red_bytes) smem = red_bytes;  // the stage memory doubles as the reduction buffer
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
   if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
@@ -458,12 +457,12 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
     return CCONV_ERR_CUDA;
   const float* wsp = a.ws;
   const int cbw = 32 * cfg.vec;
+  const int nw = cfg.warps;
   const int wpc = plan.wpc;
   const int wdt_i = static_cast<int>(wdt);
   if (launch_pdl(cconv_bwd_reduce_kernel,
-                 dim3(static_cast<unsigned>((D + 31) / 32), dbias ? kRec : W),
-                 dim3(32 * kRedGroups), 0, st, wsp, cbw, plan.n_cb, wpc, D, W, wdt_i, dw, dbias) !=
-      cudaSuccess)
+                 dim3(static_cast<unsigned>((D + 255) / 256), dbias ? kRec : W), dim3(256), 0,
+                 st, wsp, cbw, nw, wpc, D, W, wdt_i, dw, dbias) != cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;
 }
