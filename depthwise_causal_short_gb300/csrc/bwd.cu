@@ -38,10 +38,10 @@ struct BwdArgs {
   const void* w;
   const void* bias;
   uint16_t* dx;   // [B,T,D] contiguous bf16
-  float* ws;      // [grid][NW][kRec][32*VEC] fp32 partial records (slots used per CTA)
+  float* ws;      // [grid][SW][kRec][32*VEC] fp32 partial records, one per (CTA, strip)
   int64_t D;
   int T, BT;
-  int n_cb, wpc, total_warps;
+  int n_cb, wpc;
   int W, wdt;
 };
 
@@ -150,10 +150,15 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
   }
 }
 
-template <int VEC, int R, int S, int NW>
+// CTA: NW warps = SW neighbouring strips x RW = NW/SW consecutive row ranges (strips fastest,
+// so at any time the CTA reads SW*32*VEC contiguous channels of the same rows); each warp
+// runs its own TMA pipeline; the RW partial sums of each strip are added inside the CTA.
+template <int VEC, int R, int S, int NW, int SW>
 __global__ void __launch_bounds__(NW * 32, 1)
     cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
                      const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
+  static_assert(NW % SW == 0, "SW strips must divide the CTA's warps");
+  constexpr int RW = NW / SW;
   constexpr int CB = 32 * VEC;
   constexpr int P = VEC / 2;
   constexpr int TILE = R * CB * 2;
@@ -162,16 +167,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * NW + warp;
-  const bool has_work = gw < p.total_warps;
+  const int n_sg = (p.n_cb + SW - 1) / SW;  // strip groups
+  const int sg = blockIdx.x % n_sg;
+  const int rg = blockIdx.x / n_sg;          // range group
+  const int si = warp % SW;
+  const int cb = sg * SW + si;
+  const int k = rg * RW + warp / SW;
+  const bool has_work = cb < p.n_cb && k < p.wpc;
 
   uint8_t* stages = smem + warp * (S * STAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
 
-  // Range-major: consecutive warps take consecutive row ranges of one strip, so the warps
-  // of a CTA mostly share a strip and their partial sums can be added inside the CTA.
-  const int cb = gw / p.wpc;
-  const int k = gw - cb * p.wpc;
   const int r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
   const int r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
   const int c0 = cb * CB;
@@ -277,31 +283,24 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int q = 0; q < VEC; ++q) buf[warp * REC + j * CB + lane * VEC + q] = v[q];
   }
   __syncthreads();
-  // Strips this CTA's working warps touch: slot i holds strip cb_first + i, summed over the
-  // CTA's warps of that strip in warp order.
-  const int g_first = blockIdx.x * NW;
-  const int g_last = min(p.total_warps, g_first + NW) - 1;
-  const int cb_first = g_first / p.wpc;
-  const int nslots = g_last / p.wpc - cb_first + 1;
-  float* rec = p.ws + static_cast<int64_t>(blockIdx.x) * NW * REC;
-  for (int e = threadIdx.x; e < nslots * REC; e += NW * 32) {
+  // Record slot si of this CTA: strip sg*SW + si summed over its RW ranges in range order.
+  float* rec = p.ws + static_cast<int64_t>(blockIdx.x) * SW * REC;
+  for (int e = threadIdx.x; e < SW * REC; e += NW * 32) {
     const int slot = e / REC;
     const int jc = e - slot * REC;
-    const int cbs = cb_first + slot;
-    const int w_lo = max(cbs * p.wpc - g_first, 0);
-    const int w_hi = min((cbs + 1) * p.wpc - g_first, g_last - g_first + 1);
     float a = 0.f;
-    for (int w = w_lo; w < w_hi; ++w) a += buf[w * REC + jc];
+#pragma unroll
+    for (int r = 0; r < RW; ++r) a += buf[(r * SW + slot) * REC + jc];
     rec[e] = a;
   }
 }
 
-// dw[d, W-1-lag] and dbias[d]: the records of d's strip come from CTAs c_lo .. c_hi (the
-// CTAs holding that strip's warps), slot cb - (first strip of the CTA); they are added in
-// CTA order, one thread per output.  Deterministic; no atomics.
+// dw[d, W-1-lag] and dbias[d]: strip cb's records are slot cb % SW of the CTAs of strip group
+// cb / SW, one per range group; they are added in range-group order, one thread per output.
+// Deterministic; no atomics.
 __global__ void __launch_bounds__(256)
-    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int nw, int wpc,
-                            int64_t D, int W, int wdt, void* dw, void* dbias) {
+    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int sw, int n_sg,
+                            int n_rg, int64_t D, int W, int wdt, void* dw, void* dbias) {
   grid_dependency_wait();
   const int64_t d = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   const int j = blockIdx.y;
@@ -309,13 +308,12 @@ __global__ void __launch_bounds__(256)
   const int64_t cb = d / cb_width;
   const int c = static_cast<int>(d - cb * cb_width);
   const int64_t rec = static_cast<int64_t>(kRec) * cb_width;
-  const int64_t c_lo = (cb * wpc) / nw;
-  const int64_t c_hi = ((cb + 1) * wpc - 1) / nw;
+  const int64_t sg = cb / sw;
+  const int64_t si = cb - sg * sw;
+  const float* base = ws + (sg * sw + si) * rec + static_cast<int64_t>(j) * cb_width + c;
+  const int64_t step = static_cast<int64_t>(n_sg) * sw * rec;  // next range group's CTA
   float a = 0.f;
-  for (int64_t cta = c_lo; cta <= c_hi; ++cta) {
-    const int64_t slot = cb - (cta * nw) / wpc;
-    a += ws[(cta * nw + slot) * rec + static_cast<int64_t>(j) * cb_width + c];
-  }
+  for (int r = 0; r < n_rg; ++r) a += base[r * step];
   if (j < 4) {
     const int lag = j;
     if (lag < W) {
@@ -334,22 +332,22 @@ __global__ void __launch_bounds__(256)
 }
 
 struct BwdConfig {
-  int vec, rows, stages, warps;
+  int vec, rows, stages, warps, sw;
   void (*kernel)(const CUtensorMap, const CUtensorMap, const BwdArgs);
 };
 
-#define CCONV_BWD_CFG(V, R, S, NW) \
-  BwdConfig { V, R, S, NW, cconv_bwd_kernel<V, R, S, NW> }
+#define CCONV_BWD_CFG(V, R, S, NW, SW) \
+  BwdConfig { V, R, S, NW, SW, cconv_bwd_kernel<V, R, S, NW, SW> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 6, 3, 16),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_BWD_CFG(4, 6, 4, 16),
-    CCONV_BWD_CFG(4, 8, 2, 16),
-    CCONV_BWD_CFG(4, 12, 2, 16),
-    CCONV_BWD_CFG(4, 6, 4, 12),
-    CCONV_BWD_CFG(4, 12, 3, 8),
-    CCONV_BWD_CFG(2, 6, 4, 24),
-    CCONV_BWD_CFG(8, 8, 3, 8),
+    CCONV_BWD_CFG(4, 6, 4, 16, 16),
+    CCONV_BWD_CFG(4, 6, 4, 16, 4),
+    CCONV_BWD_CFG(4, 6, 4, 16, 8),
+    CCONV_BWD_CFG(4, 6, 4, 16, 2),
+    CCONV_BWD_CFG(4, 8, 3, 16, 4),
+    CCONV_BWD_CFG(4, 6, 4, 12, 4),
+    CCONV_BWD_CFG(4, 12, 3, 8, 4),
+    CCONV_BWD_CFG(4, 12, 2, 16, 4),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
@@ -363,13 +361,30 @@ static int bwd_config_index() {
   return idx;
 }
 
-static int bwd_plan(int64_t B, int64_t T, int64_t D, const BwdConfig& cfg, StripPlan* plan,
+// Work split of the backward: strips of 32*VEC channels in groups of SW, each strip's rows in
+// wpc ranges in groups of RW = warps/SW; one CTA per (strip group, range group).  wpc is a
+// multiple of RW chosen so the grid is about one wave of the device's SMs.
+struct BwdPlan {
+  int n_cb, wpc, n_sg, n_rg, grid;
+};
+
+static int bwd_plan(int64_t B, int64_t T, int64_t D, const BwdConfig& cfg, BwdPlan* plan,
                     size_t* ws_bytes) {
   int sms = 0;
   const int rc = sm_count_current_device(&sms, nullptr);
   if (rc != CCONV_OK) return rc;
-  *plan = make_strip_plan(B, T, D, cfg.vec, cfg.warps, 1, sms, 32);
-  *ws_bytes = static_cast<size_t>(plan->grid) * cfg.warps * kRec * (32 * cfg.vec) * sizeof(float);
+  const int rw = cfg.warps / cfg.sw;
+  const int64_t cbw = 32 * cfg.vec;
+  plan->n_cb = static_cast<int>((D + cbw - 1) / cbw);
+  plan->n_sg = (plan->n_cb + cfg.sw - 1) / cfg.sw;
+  int64_t n_rg = sms / plan->n_sg;                       // CTAs per strip group
+  const int64_t by_rows = (B * T) / (32 * rw);           // ranges of at least 32 rows
+  if (n_rg > by_rows) n_rg = by_rows;
+  if (n_rg < 1) n_rg = 1;
+  plan->n_rg = static_cast<int>(n_rg);
+  plan->wpc = plan->n_rg * rw;
+  plan->grid = plan->n_sg * plan->n_rg;
+  *ws_bytes = static_cast<size_t>(plan->grid) * cfg.sw * kRec * cbw * sizeof(float);
   return CCONV_OK;
 }
 
@@ -390,7 +405,7 @@ CCONV_API int cconv_bwd_workspace_bytes(int64_t B, int64_t T, int64_t D, int W, 
   if (!bytes) return CCONV_ERR_NULL;
   int rc = check_sizes(B, T, D, W);
   if (rc != CCONV_OK) return rc;
-  StripPlan plan;
+  BwdPlan plan;
   return bwd_plan(B, T, D, kBwdConfigs[bwd_config_index()], &plan, bytes);
 }
 
@@ -417,7 +432,7 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
     return CCONV_ERR_ALIGN;
 
   const BwdConfig& cfg = kBwdConfigs[bwd_config_index()];
-  StripPlan plan;
+  BwdPlan plan;
   size_t need = 0;
   rc = bwd_plan(B, T, D, cfg, &plan, &need);
   if (rc != CCONV_OK) return rc;
@@ -442,7 +457,6 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   a.BT = static_cast<int>(B * T);
   a.n_cb = plan.n_cb;
   a.wpc = plan.wpc;
-  a.total_warps = plan.total_warps;
   a.W = W;
   a.wdt = wdt;
 
@@ -457,12 +471,13 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
     return CCONV_ERR_CUDA;
   const float* wsp = a.ws;
   const int cbw = 32 * cfg.vec;
-  const int nw = cfg.warps;
-  const int wpc = plan.wpc;
+  const int sw = cfg.sw;
+  const int n_sg = plan.n_sg;
+  const int n_rg = plan.n_rg;
   const int wdt_i = static_cast<int>(wdt);
   if (launch_pdl(cconv_bwd_reduce_kernel,
                  dim3(static_cast<unsigned>((D + 255) / 256), dbias ? kRec : W), dim3(256), 0,
-                 st, wsp, cbw, nw, wpc, D, W, wdt_i, dw, dbias) != cudaSuccess)
+                 st, wsp, cbw, sw, n_sg, n_rg, D, W, wdt_i, dw, dbias) != cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;
 }
