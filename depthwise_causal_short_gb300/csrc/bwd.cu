@@ -340,14 +340,14 @@ struct BwdConfig {
   BwdConfig { V, R, S, NW, SW, cconv_bwd_kernel<V, R, S, NW, SW> }
 
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 6, 4, 16, 16),
-    CCONV_BWD_CFG(4, 6, 4, 16, 4),
-    CCONV_BWD_CFG(4, 6, 4, 16, 8),
-    CCONV_BWD_CFG(4, 6, 4, 16, 2),
-    CCONV_BWD_CFG(4, 8, 3, 16, 4),
-    CCONV_BWD_CFG(4, 6, 4, 12, 4),
-    CCONV_BWD_CFG(4, 12, 3, 8, 4),
-    CCONV_BWD_CFG(4, 12, 2, 16, 4),
+    CCONV_BWD_CFG(4, 12, 3, 8, 4),  // measured fastest at B=2 T=8192 D=4096
+    CCONV_BWD_CFG(4, 12, 3, 8, 8),
+    CCONV_BWD_CFG(4, 12, 3, 8, 2),
+    CCONV_BWD_CFG(4, 16, 3, 8, 4),
+    CCONV_BWD_CFG(4, 12, 4, 8, 4),
+    CCONV_BWD_CFG(4, 18, 2, 8, 4),
+    CCONV_BWD_CFG(4, 24, 2, 8, 4),
+    CCONV_BWD_CFG(4, 12, 2, 12, 4),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
