@@ -296,38 +296,58 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 // dw[d, W-1-lag] and dbias[d]: strip cb's records are slot cb % SW of the CTAs of strip group
-// cb / SW, one per range group; they are added in range-group order, one thread per output.
-// Deterministic; no atomics.
-__global__ void __launch_bounds__(256)
+// cb / SW, one per range group.  CTA = 32 channels x kRedGroups groups for one record row j
+// (blockIdx.y): group g adds range groups g, g + G, g + 2G, ... and the G group sums are then
+// added in group order.  Deterministic; no atomics; a few independent loads per thread.
+constexpr int kRedGroups = 8;
+
+__global__ void __launch_bounds__(32 * kRedGroups)
     cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int sw, int n_sg,
                             int n_rg, int64_t D, int W, int wdt, void* dw, void* dbias) {
+  __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
-  const int64_t d = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int grp = threadIdx.x >> 5;
   const int j = blockIdx.y;
-  if (d >= D) return;
-  const int64_t cb = d / cb_width;
-  const int c = static_cast<int>(d - cb * cb_width);
-  const int64_t rec = static_cast<int64_t>(kRec) * cb_width;
-  const int64_t sg = cb / sw;
-  const int64_t si = cb - sg * sw;
-  const float* base = ws + (sg * sw + si) * rec + static_cast<int64_t>(j) * cb_width + c;
-  const int64_t step = static_cast<int64_t>(n_sg) * sw * rec;  // next range group's CTA
+  const int64_t d = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float a = 0.f;
-  for (int r = 0; r < n_rg; ++r) a += base[r * step];
+  if (d < D) {
+    const int64_t cb = d / cb_width;
+    const int c = static_cast<int>(d - cb * cb_width);
+    const int64_t rec = static_cast<int64_t>(kRec) * cb_width;
+    const int64_t sg = cb / sw;
+    const int64_t si = cb - sg * sw;
+    const float* base = ws + (sg * sw + si) * rec + static_cast<int64_t>(j) * cb_width + c;
+    const int64_t step = static_cast<int64_t>(n_sg) * sw * rec;  // next range group's CTA
+    float a0 = 0.f, a1 = 0.f;
+    int r = grp;
+    for (; r + kRedGroups < n_rg; r += 2 * kRedGroups) {
+      a0 += base[r * step];
+      a1 += base[(r + kRedGroups) * step];
+    }
+    if (r < n_rg) a0 += base[r * step];
+    a = a0 + a1;
+  }
+  part[grp][lane] = a;
+  __syncthreads();
+  if (grp != 0 || d >= D) return;
+  float t = 0.f;
+#pragma unroll
+  for (int g = 0; g < kRedGroups; ++g) t += part[g][lane];
   if (j < 4) {
     const int lag = j;
     if (lag < W) {
       const int64_t o = d * W + (W - 1 - lag);
       if (wdt == CCONV_F32)
-        static_cast<float*>(dw)[o] = a;
+        static_cast<float*>(dw)[o] = t;
       else
-        static_cast<uint16_t*>(dw)[o] = f32_to_bf16(a);
+        static_cast<uint16_t*>(dw)[o] = f32_to_bf16(t);
     }
   } else if (dbias) {
     if (wdt == CCONV_F32)
-      static_cast<float*>(dbias)[d] = a;
+      static_cast<float*>(dbias)[d] = t;
     else
-      static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(a);
+      static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(t);
   }
 }
 
@@ -476,7 +496,8 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   const int n_rg = plan.n_rg;
   const int wdt_i = static_cast<int>(wdt);
   if (launch_pdl(cconv_bwd_reduce_kernel,
-                 dim3(static_cast<unsigned>((D + 255) / 256), dbias ? kRec : W), dim3(256), 0,
+                 dim3(static_cast<unsigned>((D + 31) / 32), dbias ? kRec : W),
+                 dim3(32 * kRedGroups), 0,
                  st, wsp, cbw, sw, n_sg, n_rg, D, W, wdt_i, dw, dbias) != cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;
