@@ -11,7 +11,11 @@ Sources followed (page title, file / section):
     ``_ld_ring``, ``_silu``, ``_dsilu``, ``_bwd4`` and the partial store of
     ``cconv_bwd_strip`` (forward / backward definitions);
   * "Add experimental causal conv1d decode update - #797" (NVIDIA/cudnn-frontend),
-    PR summary (decode update, fail-closed index validation).
+    PR summary (decode update, fail-closed index validation, full-sequence-to-decode
+    state handoff);
+  * kernel-fun 0.2.0.dev1 wheel, kernel_fun/_common/compat.py: the keywords of fla's
+    causal_conv1d (initial_state, output_final_state, activation, cu_seqlens), which the
+    packed-sequence forms ``fwd_seq`` / ``bwd_seq`` follow.
 
 Conventions: the forward and backward take float64 values (the exact bf16 / fp32 values
 the GPU receives, widened); the decode update takes the bf16 token and state as their
@@ -50,6 +54,12 @@ class Oracle:
         lib.oracle_validate.restype = ctypes.c_int
         lib.oracle_update.argtypes = [_I64, _I64, ctypes.c_int, _P, _P, _I64, _P, _P, _P, _P]
         lib.oracle_update.restype = ctypes.c_int
+        lib.oracle_fwd_seq.argtypes = [_I64, _P, _I64, ctypes.c_int, _P, _P, _P, _P, ctypes.c_int,
+                                       _P, _P]
+        lib.oracle_fwd_seq.restype = ctypes.c_int
+        lib.oracle_bwd_seq.argtypes = [_I64, _P, _I64, ctypes.c_int, _P, _P, _P, _P, _P,
+                                       ctypes.c_int, _P, _P, _P, _P]
+        lib.oracle_bwd_seq.restype = ctypes.c_int
         self.lib = lib
 
     # -- marshalling helpers -------------------------------------------------------------
@@ -134,6 +144,62 @@ class Oracle:
         return rc, (y if rc == 0 else None), st
 
 
+    # -- packed sequences, initial / final state, activation ---------------------------------
+    @staticmethod
+    def _cu(cu_seqlens):
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+        assert cu.ndim == 1 and cu.size >= 1 and cu[0] == 0
+        return cu
+
+    def fwd_seq(self, x, cu_seqlens, w, bias=None, initial_state=None, activation="silu",
+                want_final: bool = False):
+        """Packed-sequence forward.  x [total, D]; cu_seqlens [nseq+1]; initial_state
+        [nseq, D, W-1] or None.  Returns y [total, D] (and final_state [nseq, D, W-1])."""
+        x = self._f64(x)
+        total, D = x.shape
+        cu = self._cu(cu_seqlens)
+        assert cu[-1] == total
+        nseq = cu.size - 1
+        w = self._f64(w)
+        W = w.shape[1]
+        b = self._f64(bias)
+        init = self._f64(initial_state)
+        act = {"silu": 0, None: 1, "none": 1}[activation]
+        y = np.empty((total, D), np.float64)
+        fin = np.empty((nseq, D, W - 1), np.float64) if want_final else None
+        rc = self.lib.oracle_fwd_seq(nseq, self._ptr(cu), D, W, self._ptr(x), self._ptr(w),
+                                     self._ptr(b), self._ptr(init), act, self._ptr(y),
+                                     self._ptr(fin))
+        if rc != 0:
+            raise RuntimeError(f"oracle_fwd_seq failed ({rc})")
+        return (y, fin) if want_final else y
+
+    def bwd_seq(self, x, dy, cu_seqlens, w, bias=None, initial_state=None, activation="silu",
+                want_dbias: bool = True, want_dinit: bool = False):
+        """Packed-sequence backward: (dx [total, D], dw [D, W], dbias [D] or None,
+        d_initial_state [nseq, D, W-1] or None)."""
+        x = self._f64(x)
+        dy = self._f64(dy)
+        total, D = x.shape
+        cu = self._cu(cu_seqlens)
+        nseq = cu.size - 1
+        w = self._f64(w)
+        W = w.shape[1]
+        b = self._f64(bias)
+        init = self._f64(initial_state)
+        act = {"silu": 0, None: 1, "none": 1}[activation]
+        dx = np.empty((total, D), np.float64)
+        dw = np.empty((D, W), np.float64)
+        db = np.empty((D,), np.float64) if want_dbias else None
+        di = np.empty((nseq, D, W - 1), np.float64) if want_dinit else None
+        rc = self.lib.oracle_bwd_seq(nseq, self._ptr(cu), D, W, self._ptr(x), self._ptr(dy),
+                                     self._ptr(w), self._ptr(b), self._ptr(init), act,
+                                     self._ptr(dx), self._ptr(dw), self._ptr(db), self._ptr(di))
+        if rc != 0:
+            raise RuntimeError(f"oracle_bwd_seq failed ({rc})")
+        return dx, dw, db, di
+
+
 _default: Oracle | None = None
 
 
@@ -159,3 +225,11 @@ def validate(*a, **k):
 
 def update(*a, **k):
     return get().update(*a, **k)
+
+
+def fwd_seq(*a, **k):
+    return get().fwd_seq(*a, **k)
+
+
+def bwd_seq(*a, **k):
+    return get().bwd_seq(*a, **k)

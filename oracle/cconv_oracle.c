@@ -25,6 +25,13 @@
  *             PR summary: per row i the state slot s = state_indices[i] is read, the new
  *             token emits y, then the state shifts by one and takes the token.  Negative,
  *             out-of-range and duplicate indices fail closed (nothing is mutated).
+ *   packed    oracle_fwd_seq / oracle_bwd_seq: sequences packed along rows by cu_seqlens,
+ *             an optional initial state per sequence, the final state a decode update
+ *             continues from, and activation silu or none.  The keyword list fla's
+ *             causal_conv1d takes (kernel-fun 0.2.0.dev1 wheel,
+ *             kernel_fun/_common/compat.py: initial_state, output_final_state, activation,
+ *             cu_seqlens), the follow-up scope and full-sequence-to-decode handoff of the
+ *             cuDNN decode-update PR, and the decode state layout [.., D, W-1].
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - state[s,d,0] is the oldest entry; the window for the new token is
@@ -33,6 +40,10 @@
  *   - a repeated index is a "duplicate" only when it is in range; an out-of-range value
  *     is reported as out-of-range however often it occurs.
  *   - state_indices == NULL means row i uses slot i.
+ *   - an initial state stands in for the W-1 rows before a sequence's first row, oldest
+ *     first, the decode pool's layout; the final state is the last W-1 rows of the
+ *     sequence extended by its initial state (or by zeros), so a sequence shorter than
+ *     W-1 rows hands on part of its initial state.
  *
  * Number formats: the forward and backward take real values as double (the exact bf16
  * or fp32 values the GPU receives, widened by the caller), so they are plain functions of
@@ -138,6 +149,118 @@ int oracle_bwd(int64_t B, int64_t T, int64_t D, int W, const double* x,
       }
 
   free(g);
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Packed sequences, initial / final state, activation.
+ *
+ * x holds nseq sequences packed along rows: sequence i is rows [cu[i], cu[i+1]) of the
+ * [total, D] array (a batch of equal-length sequences is cu = 0, T, 2T, ...).  Inside each
+ * sequence the convolution is the one above, except that the W-1 rows before its first row
+ * come from init[i] when given (init[i][d][j] is row cu[i] - (W-1) + j, j = 0 the oldest)
+ * and are zero otherwise.  act = 0: y = silu(z); act = 1: y = z (no activation).
+ * final[i][d][j] (optional) is row cu[i+1] - (W-1) + j of that same extended sequence: the
+ * state a decode update continues from.  The backward adds dinit[i][d][j] (optional), the
+ * gradient of init[i][d][j]: sum_k w[d,W-1-k] g[u+k] over rows u+k inside the sequence,
+ * u = cu[i] - (W-1) + j.  Readings: fla's causal_conv1d names initial_state /
+ * output_final_state / cu_seqlens / activation (kernel-fun 0.2.0.dev1 wheel,
+ * _common/compat.py); the decode update's state layout [.., D, W-1] fixes the state's shape.
+ * --------------------------------------------------------------------------------------- */
+
+/* value of sequence i's extended input at packed row u, channel d */
+static double seq_x(int64_t D, int W, const double* x, const int64_t* cu, const double* init,
+                    int64_t i, int64_t u, int64_t d) {
+  if (u >= cu[i]) return x[u * D + d];
+  const int64_t j = u - (cu[i] - (W - 1));
+  if (j < 0 || !init) return 0.0;
+  return init[(i * D + d) * (W - 1) + j];
+}
+
+/* pre-activation of sequence i at packed row t: bias + sum_k w[d, W-1-k] xe[t-k] */
+static double seq_z(int64_t D, int W, const double* x, const int64_t* cu, const double* init,
+                    const double* w, const double* bias, int64_t i, int64_t t, int64_t d) {
+  double zs = bias ? bias[d] : 0.0;
+  for (int k = 0; k < W; ++k) zs += w[d * W + (W - 1 - k)] * seq_x(D, W, x, cu, init, i, t - k, d);
+  return zs;
+}
+
+int oracle_fwd_seq(int64_t nseq, const int64_t* cu, int64_t D, int W, const double* x,
+                   const double* w, const double* bias, const double* init, int act,
+                   double* y, double* final_state) {
+  if (nseq < 0 || D < 0 || W < 1 || (act != 0 && act != 1)) return -1;
+  for (int64_t i = 0; i < nseq; ++i) {
+    if (cu[i + 1] < cu[i]) return -1;
+    for (int64_t t = cu[i]; t < cu[i + 1]; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        const double zs = seq_z(D, W, x, cu, init, w, bias, i, t, d);
+        y[t * D + d] = act == 0 ? silu(zs) : zs;
+      }
+    if (final_state)
+      for (int64_t d = 0; d < D; ++d)
+        for (int j = 0; j < W - 1; ++j)
+          final_state[(i * D + d) * (W - 1) + j] =
+              seq_x(D, W, x, cu, init, i, cu[i + 1] - (W - 1) + j, d);
+  }
+  return 0;
+}
+
+int oracle_bwd_seq(int64_t nseq, const int64_t* cu, int64_t D, int W, const double* x,
+                   const double* dy, const double* w, const double* bias, const double* init,
+                   int act, double* dx, double* dw, double* dbias, double* dinit) {
+  if (nseq < 0 || D < 0 || W < 1 || (act != 0 && act != 1)) return -1;
+  for (int64_t i = 0; i < nseq; ++i)
+    if (cu[i + 1] < cu[i]) return -1;
+  const int64_t total = nseq > 0 ? cu[nseq] : 0;
+  double* gs = (double*)malloc((size_t)(total * D > 0 ? total * D : 1) * sizeof(double));
+  if (!gs) return -2;
+  /* gs = dy * act'(z) on every row of every sequence */
+  for (int64_t i = 0; i < nseq; ++i)
+    for (int64_t t = cu[i]; t < cu[i + 1]; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        double gv = dy[t * D + d];
+        if (act == 0) {
+          const double zv = seq_z(D, W, x, cu, init, w, bias, i, t, d);
+          const double sg = sigmoid(zv);
+          gv *= sg * (1.0 + zv * (1.0 - sg));
+        }
+        gs[t * D + d] = gv;
+      }
+  for (int64_t d = 0; d < D; ++d) {
+    for (int j = 0; j < W; ++j) dw[d * W + j] = 0.0;
+    if (dbias) dbias[d] = 0.0;
+  }
+  for (int64_t i = 0; i < nseq; ++i) {
+    const int64_t s = cu[i], e = cu[i + 1];
+    /* dx[t] = sum_k w[d, W-1-k] gs[t+k], the sum stopping at the sequence's last row */
+    for (int64_t t = s; t < e; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        double ax = 0.0;
+        for (int k = 0; k < W; ++k)
+          if (t + k < e) ax += w[d * W + (W - 1 - k)] * gs[(t + k) * D + d];
+        dx[t * D + d] = ax;
+      }
+    /* dw[d, W-1-k] += gs[t] xe[t-k]; dbias[d] += gs[t] (xe: the extended input) */
+    for (int64_t t = s; t < e; ++t)
+      for (int64_t d = 0; d < D; ++d) {
+        const double gv = gs[t * D + d];
+        for (int k = 0; k < W; ++k)
+          dw[d * W + (W - 1 - k)] += gv * seq_x(D, W, x, cu, init, i, t - k, d);
+        if (dbias) dbias[d] += gv;
+      }
+    /* gradient of the initial-state row u = s-(W-1)+j: the taps that reach into the
+     * sequence from it */
+    if (dinit)
+      for (int64_t d = 0; d < D; ++d)
+        for (int j = 0; j < W - 1; ++j) {
+          const int64_t u = s - (W - 1) + j;
+          double ai = 0.0;
+          for (int k = 0; k < W; ++k)
+            if (u + k >= s && u + k < e) ai += w[d * W + (W - 1 - k)] * gs[(u + k) * D + d];
+          dinit[(i * D + d) * (W - 1) + j] = ai;
+        }
+  }
+  free(gs);
   return 0;
 }
 

@@ -301,6 +301,169 @@ def pin_update_fail_closed(o):
             st2[i, :, W - 2], x[i]), "NULL indices must update slot i"
 
 
+# ---------------------------------------------------------------------------------------
+# packed sequences, initial / final state, activation
+# ---------------------------------------------------------------------------------------
+
+_LENS = (5, 0, 1, 2, 7, 3)   # empty, shorter than W-1, and several-tile-free ragged lengths
+
+
+def _cu_of(lens):
+    return np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+
+
+def _torch_seq_ref(x, dy, cu, w, bias, init, act):
+    """float64 torch, one sequence at a time: concatenate the W-1 initial rows (zeros when
+    no state is given) in front of the sequence, grouped conv1d with no padding, then SiLU
+    or nothing; autograd gives every gradient.  The final state is the last W-1 rows of the
+    concatenation."""
+    D, W = w.shape
+    wt = torch.tensor(w).reshape(D, 1, W).requires_grad_(True)
+    bt = torch.tensor(bias).requires_grad_(True) if bias is not None else None
+    nseq = len(cu) - 1
+    xt = torch.tensor(x).requires_grad_(True)
+    it = torch.tensor(init if init is not None else np.zeros((nseq, D, W - 1))).requires_grad_(True)
+    ys, fins = [], []
+    for i in range(nseq):
+        ext = torch.cat([it[i], xt[cu[i]:cu[i + 1]].t()], dim=1)        # [D, W-1+L]
+        if cu[i + 1] > cu[i]:
+            z = torch.nn.functional.conv1d(ext[None], wt, bt, groups=D)[0]   # [D, L]
+            ys.append((torch.nn.functional.silu(z) if act == "silu" else z).t())
+        fins.append(ext[:, ext.shape[1] - (W - 1):])
+    y = torch.cat(ys, dim=0)
+    (y * torch.tensor(dy)).sum().backward()
+    return (y.detach().numpy(), torch.stack(fins).detach().numpy(), xt.grad.numpy(),
+            wt.grad.reshape(D, W).numpy(), None if bt is None else bt.grad.numpy(),
+            it.grad.numpy())
+
+
+def pin_seq_torch(o):
+    rng = _rng(9)
+    cu = _cu_of(_LENS)
+    total, D = int(cu[-1]), 3
+    for W in (4, 3, 2):
+        for act in ("silu", None):
+            for with_init in (True, False):
+                x = rng.standard_normal((total, D))
+                dy = rng.standard_normal((total, D))
+                w = rng.uniform(-0.7, 0.7, (D, W))
+                bias = rng.uniform(-0.3, 0.3, D)
+                init = rng.standard_normal((len(_LENS), D, W - 1)) if with_init else None
+                ry, rfin, rdx, rdw, rdb, rdi = _torch_seq_ref(x, dy, cu, w, bias, init, act)
+                y, fin = o.fwd_seq(x, cu, w, bias, init, act, want_final=True)
+                dx, dw, db, di = o.bwd_seq(x, dy, cu, w, bias, init, act, want_dinit=True)
+                tag = f"seq W={W} act={act} init={with_init}"
+                _close(y, ry, 1e-13, tag + " y")
+                _close(fin, rfin, 0.0, tag + " final state")
+                _close(dx, rdx, 1e-13, tag + " dx")
+                _close(dw, rdw, 1e-13, tag + " dw")
+                _close(db, rdb, 1e-13, tag + " dbias")
+                _close(di, rdi, 1e-13, tag + " d initial state")
+
+
+def pin_seq_split_handoff(o):
+    """Cutting a sequence anywhere and passing the first part's final state as the second
+    part's initial state changes nothing; the gradients add up the same way."""
+    rng = _rng(10)
+    D, W, L = 2, 4, 11
+    x = rng.standard_normal((L, D))
+    dy = rng.standard_normal((L, D))
+    w = rng.uniform(-0.7, 0.7, (D, W))
+    bias = rng.uniform(-0.3, 0.3, D)
+    init = rng.standard_normal((1, D, W - 1))
+    y_all, fin_all = o.fwd_seq(x, [0, L], w, bias, init, want_final=True)
+    dx_all, dw_all, db_all, di_all = o.bwd_seq(x, dy, [0, L], w, bias, init, want_dinit=True)
+    for cut in (1, 2, 3, 6, 10):
+        y1, f1 = o.fwd_seq(x[:cut], [0, cut], w, bias, init, want_final=True)
+        y2, f2 = o.fwd_seq(x[cut:], [0, L - cut], w, bias, f1, want_final=True)
+        _close(np.concatenate([y1, y2]), y_all, 1e-15, f"split at {cut}: y")
+        _close(f2, fin_all, 0.0, f"split at {cut}: final state")
+        dx2, dw2, db2, di2 = o.bwd_seq(x[cut:], dy[cut:], [0, L - cut], w, bias, f1,
+                                       want_dinit=True)
+        # the second part's initial-state gradient flows back into the first part's rows
+        # (and, for rows the first part took from its own initial state, into that state)
+        ext1 = np.concatenate([init[0].T, x[:cut]])            # [W-1+cut, D]
+        dext = np.zeros_like(ext1)
+        dext[-(W - 1):] += di2[0].T
+        dy1 = dy[:cut]
+        dx1, dw1, db1, di1 = o.bwd_seq(x[:cut], dy1, [0, cut], w, bias, init, want_dinit=True)
+        dx_first = dx1 + dext[W - 1:]
+        di_first = di1[0] + dext[:W - 1].T
+        _close(np.concatenate([dx_first, dx2]), dx_all, 1e-13, f"split at {cut}: dx")
+        _close(dw1 + dw2, dw_all, 1e-13, f"split at {cut}: dw")
+        _close(db1 + db2, db_all, 1e-13, f"split at {cut}: dbias")
+        _close(di_first[None], di_all, 1e-13, f"split at {cut}: d initial state")
+
+
+def pin_seq_decode_handoff(o):
+    """A packed forward's final state, put in the decode pool, continues each sequence: a
+    single-token update then gives the same row as the forward over the lengthened
+    sequence, and leaves the same state."""
+    rng = _rng(11)
+    D, W = 4, 4
+    lens = (6, 1, 0, 3)
+    cu = _cu_of(lens)
+    x = _bf16_values(rng, (int(cu[-1]), D))
+    init = _bf16_values(rng, (len(lens), D, W - 1))
+    xn = _bf16_values(rng, (len(lens), D))               # the next token of each sequence
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    bias = rng.uniform(-0.1, 0.1, D)
+    _, fin = o.fwd_seq(x, cu, w, bias, init, want_final=True)
+    pool = _bf16_bits(fin)                                # exact: rows of x or of init
+    idx = np.arange(len(lens), dtype=np.int32)[::-1].copy()
+    state = np.zeros((len(lens), D, W - 1), np.uint16)
+    state[idx] = pool
+    status, y_dec, state = o.update(_bf16_bits(xn), state, idx, w, bias)
+    assert status == 0
+    # the lengthened sequences, packed
+    lens2 = tuple(n + 1 for n in lens)
+    cu2 = _cu_of(lens2)
+    x2 = np.concatenate([np.concatenate([x[cu[i]:cu[i + 1]], xn[i:i + 1]])
+                         for i in range(len(lens))])
+    y2, fin2 = o.fwd_seq(x2, cu2, w, bias, init, want_final=True)
+    _close(y_dec, y2[cu2[1:] - 1], 1e-15, "decode after packed forward vs lengthened forward")
+    assert np.array_equal(state[idx], _bf16_bits(fin2)), "state after the handoff step"
+
+
+def pin_seq_equal_lengths_batch(o):
+    """Equal lengths with no initial state are the batched [B,T,D] forward / backward."""
+    rng = _rng(12)
+    B, T, D, W = 3, 6, 5, 4
+    x = rng.standard_normal((B, T, D))
+    dy = rng.standard_normal((B, T, D))
+    w = rng.uniform(-0.7, 0.7, (D, W))
+    bias = rng.uniform(-0.3, 0.3, D)
+    cu = np.arange(B + 1, dtype=np.int64) * T
+    y = o.fwd_seq(x.reshape(B * T, D), cu, w, bias)
+    _close(y.reshape(B, T, D), o.fwd(x, w, bias), 0.0, "equal lengths: y")
+    dx, dw, db, _ = o.bwd_seq(x.reshape(B * T, D), dy.reshape(B * T, D), cu, w, bias)
+    rdx, rdw, rdb = o.bwd(x, dy, w, bias)
+    _close(dx.reshape(B, T, D), rdx, 1e-14, "equal lengths: dx")
+    _close(dw, rdw, 1e-14, "equal lengths: dw")
+    _close(db, rdb, 1e-14, "equal lengths: dbias")
+
+
+def pin_act_none_linear(o):
+    """With no activation and no bias, (x, initial state) -> y is linear, and dx does not
+    depend on x."""
+    rng = _rng(13)
+    cu = _cu_of((4, 3))
+    D, W = 3, 4
+    w = rng.uniform(-0.7, 0.7, (D, W))
+    x1 = rng.standard_normal((7, D))
+    x2 = rng.standard_normal((7, D))
+    i1 = rng.standard_normal((2, D, W - 1))
+    i2 = rng.standard_normal((2, D, W - 1))
+    a = 1.75
+    y12 = o.fwd_seq(a * x1 + x2, cu, w, None, a * i1 + i2, None)
+    _close(y12, a * o.fwd_seq(x1, cu, w, None, i1, None) + o.fwd_seq(x2, cu, w, None, i2, None),
+           1e-14, "act=None linearity")
+    dy = rng.standard_normal((7, D))
+    dxa = o.bwd_seq(x1, dy, cu, w, None, i1, None)[0]
+    dxb = o.bwd_seq(x2, dy, cu, w, None, i2, None)[0]
+    _close(dxa, dxb, 0.0, "act=None: dx independent of x")
+
+
 ALL_PINS = [
     pin_fwd_lfilter,
     pin_fwd_bwd_torch,
@@ -313,4 +476,9 @@ ALL_PINS = [
     pin_decode_matches_forward,
     pin_validate_exhaustive,
     pin_update_fail_closed,
+    pin_seq_torch,
+    pin_seq_split_handoff,
+    pin_seq_decode_handoff,
+    pin_seq_equal_lengths_batch,
+    pin_act_none_linear,
 ]

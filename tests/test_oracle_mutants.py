@@ -31,6 +31,20 @@ MUTANTS = {
     "validate_no_duplicates": ("mask |= ORACLE_IDX_DUPLICATE;", "mask |= 0;"),
     "validate_range_off_by_one": ("else if (idx[i] >= S) mask |= ORACLE_IDX_OUT_OF_RANGE;",
                                   "else if (idx[i] > S) mask |= ORACLE_IDX_OUT_OF_RANGE;"),
+    # packed sequences, initial / final state, activation
+    "seq_boundary_leak": ("if (u >= cu[i]) return x[u * D + d];",
+                          "if (u >= 0) return x[u * D + d];"),
+    "seq_init_ignored": ("return init[(i * D + d) * (W - 1) + j];",
+                         "return 0.0 * init[(i * D + d) * (W - 1) + j];"),
+    "seq_init_reversed": ("return init[(i * D + d) * (W - 1) + j];",
+                          "return init[(i * D + d) * (W - 1) + (W - 2 - j)];"),
+    "seq_final_shift": ("seq_x(D, W, x, cu, init, i, cu[i + 1] - (W - 1) + j, d);",
+                        "seq_x(D, W, x, cu, init, i, cu[i + 1] - W + j, d);"),
+    "seq_dx_crosses_end": ("if (t + k < e) ax +=", "if (t + k < total) ax +="),
+    "seq_dinit_tap_reversed": ("ai += w[d * W + (W - 1 - k)] * gs[", "ai += w[d * W + k] * gs["),
+    "seq_dinit_window": ("if (u + k >= s && u + k < e) ai", "if (u + k > s && u + k < e) ai"),
+    "act_none_ignored_fwd": ("y[t * D + d] = act == 0 ? silu(zs) : zs;", "y[t * D + d] = silu(zs);"),
+    "act_none_ignored_bwd": ("if (act == 0) {\n          const double zv", "if (1) {\n          const double zv"),
 }
 
 
