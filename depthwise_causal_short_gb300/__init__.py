@@ -6,6 +6,8 @@ input generators.  Importing the package does not load the library; the first ca
 and raises if it has not been built.
 """
 from .binding import (  # noqa: F401
+    CCONV_ACT_NONE,
+    CCONV_ACT_SILU,
     CCONV_BF16,
     CCONV_F32,
     IDX_DUPLICATE,
@@ -14,9 +16,12 @@ from .binding import (  # noqa: F401
     CConvError,
     cconv_bwd,
     cconv_bwd_noalloc,
+    cconv_bwd_varlen,
+    cconv_bwd_varlen_workspace_bytes,
     cconv_bwd_workspace_bytes,
     cconv_device_fault,
     cconv_fwd,
+    cconv_fwd_varlen,
     cconv_status_str,
     cconv_update,
     header_functions,

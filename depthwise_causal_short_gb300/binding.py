@@ -21,6 +21,8 @@ _INT = ctypes.c_int
 
 CCONV_BF16 = 0
 CCONV_F32 = 1
+CCONV_ACT_SILU = 0
+CCONV_ACT_NONE = 1
 STATUS = {
     0: "CCONV_OK", -1: "CCONV_ERR_NULL", -2: "CCONV_ERR_SHAPE", -3: "CCONV_ERR_WIDTH",
     -4: "CCONV_ERR_ALIGN", -5: "CCONV_ERR_STRIDE", -6: "CCONV_ERR_DTYPE",
@@ -68,6 +70,15 @@ def load(path: str | Path | None = None):
     lib.cconv_bwd_noalloc.restype = _INT
     lib.cconv_update.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _INT, _INT, _P, _P, _P]
     lib.cconv_update.restype = _INT
+    lib.cconv_fwd_varlen.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _INT, _INT, _INT,
+                                     _P, _P, _P, _I64, _P, _P, _P]
+    lib.cconv_fwd_varlen.restype = _INT
+    lib.cconv_bwd_varlen_workspace_bytes.argtypes = [_I64, _I64, _INT,
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.cconv_bwd_varlen_workspace_bytes.restype = _INT
+    lib.cconv_bwd_varlen.argtypes = [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _INT, _INT,
+                                     _INT, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.cconv_bwd_varlen.restype = _INT
     lib.cconv_status_str.argtypes = [_INT]
     lib.cconv_status_str.restype = ctypes.c_char_p
     lib.cconv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -213,6 +224,122 @@ def cconv_update(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
                              _stream(stream))
     _check(rc, "cconv_update")
     return y, status
+
+
+def _act(activation) -> int:
+    if activation in ("silu", "swish"):
+        return CCONV_ACT_SILU
+    if activation is None or activation == "none":
+        return CCONV_ACT_NONE
+    raise ValueError(f"activation must be 'silu' or None, got {activation!r}")
+
+
+def _packed_rows(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be [total, D] with channel stride 1")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _cu(cu_seqlens: torch.Tensor) -> torch.Tensor:
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda:
+        raise TypeError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    if not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be contiguous")
+    return cu_seqlens
+
+
+def _state(t: torch.Tensor | None, name: str):
+    if t is None:
+        return
+    if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [S, D, W-1] bfloat16 tensor")
+
+
+def cconv_fwd_varlen(x: torch.Tensor, cu_seqlens: torch.Tensor, w: torch.Tensor,
+                     bias: torch.Tensor | None = None, *, activation="silu",
+                     initial_state: torch.Tensor | None = None,
+                     final_state: torch.Tensor | bool | None = None,
+                     state_indices: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     y: torch.Tensor | None = None, stream=None):
+    """Packed-sequence forward.  x [total, D] bf16; cu_seqlens int32 [nseq+1] on the device.
+    initial_state / final_state: [S, D, W-1] bf16 state arrays (final_state=True allocates
+    [nseq, D, W-1]); state_indices int32 [nseq] picks each sequence's slot (then a status
+    int32[2] is written on the device).  Returns (y, final_state or None, status or None)."""
+    _packed_rows(x, "x")
+    total, D = x.shape
+    cu = _cu(cu_seqlens)
+    nseq = cu.numel() - 1
+    W = w.shape[1]
+    _state(initial_state, "initial_state")
+    if final_state is True:
+        final_state = torch.empty((nseq, D, W - 1), dtype=torch.bfloat16, device=x.device)
+    elif final_state is False:
+        final_state = None
+    _state(final_state, "final_state")
+    if state_indices is not None:
+        if state_indices.dtype != torch.int32:
+            raise TypeError("state_indices must be int32")
+        if status is None:
+            status = torch.empty(2, dtype=torch.int32, device=x.device)
+    pools = [t for t in (initial_state, final_state) if t is not None]
+    S = pools[0].shape[0] if pools else nseq
+    if y is None:
+        y = torch.empty((total, D), dtype=torch.bfloat16, device=x.device)
+    rc = load().cconv_fwd_varlen(_ptr(x), total, D, x.stride(0), _ptr(cu), nseq, _ptr(w),
+                                 _ptr(bias), _wdt(w), W, _act(activation), _ptr(initial_state),
+                                 _ptr(final_state), _ptr(state_indices), S, _ptr(status), _ptr(y),
+                                 _stream(stream))
+    _check(rc, "cconv_fwd_varlen")
+    return y, final_state, (status if state_indices is not None else None)
+
+
+def cconv_bwd_varlen_workspace_bytes(total: int, D: int, W: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().cconv_bwd_varlen_workspace_bytes(total, D, W, ctypes.byref(n)),
+           "cconv_bwd_varlen_workspace_bytes")
+    return int(n.value)
+
+
+def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor,
+                     w: torch.Tensor, bias: torch.Tensor | None = None, *, activation="silu",
+                     initial_state: torch.Tensor | None = None, want_dbias: bool | None = None,
+                     want_dinit: bool | None = None, dx: torch.Tensor | None = None,
+                     dw: torch.Tensor | None = None, dbias: torch.Tensor | None = None,
+                     d_initial_state: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None):
+    """Packed-sequence backward: (dx, dw, dbias or None, d_initial_state or None)."""
+    _packed_rows(x, "x")
+    _packed_rows(dy, "dy")
+    total, D = x.shape
+    cu = _cu(cu_seqlens)
+    nseq = cu.numel() - 1
+    W = w.shape[1]
+    _state(initial_state, "initial_state")
+    if want_dbias is None:
+        want_dbias = bias is not None or dbias is not None
+    if want_dinit is None:
+        want_dinit = initial_state is not None or d_initial_state is not None
+    if dx is None:
+        dx = torch.empty((total, D), dtype=torch.bfloat16, device=x.device)
+    if dw is None:
+        dw = torch.empty((D, W), dtype=w.dtype, device=x.device)
+    if want_dbias and dbias is None:
+        dbias = torch.empty((D,), dtype=w.dtype, device=x.device)
+    if want_dinit and d_initial_state is None:
+        d_initial_state = torch.empty((nseq, D, W - 1), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(cconv_bwd_varlen_workspace_bytes(total, D, W), 16),
+                                dtype=torch.uint8, device=x.device)
+    rc = load().cconv_bwd_varlen(
+        _ptr(x), x.stride(0), _ptr(dy), dy.stride(0), total, D, _ptr(cu), nseq, _ptr(w),
+        _ptr(bias), _wdt(w), W, _act(activation), _ptr(initial_state), _ptr(dx), _ptr(dw),
+        _ptr(dbias if want_dbias else None), _ptr(d_initial_state if want_dinit else None),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "cconv_bwd_varlen")
+    return dx, dw, (dbias if want_dbias else None), (d_initial_state if want_dinit else None)
 
 
 def cconv_status_str(status: int) -> str:

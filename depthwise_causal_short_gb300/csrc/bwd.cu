@@ -18,6 +18,7 @@
 // a fixed order, launched as a programmatic dependent of the first so its launch overlaps
 // the stream's tail.
 #include <mutex>
+#include <type_traits>
 
 #include "strip.cuh"
 
@@ -37,24 +38,38 @@ constexpr int kRec = 5;  // partial record rows: dw lags 0..3, dbias
 struct BwdArgs {
   const void* w;
   const void* bias;
-  uint16_t* dx;   // [B,T,D] contiguous bf16
+  uint16_t* dx;   // [B,T,D] contiguous bf16 ([total, D] for packed sequences)
   float* ws;      // [grid][SW][kRec][32*VEC] fp32 partial records, one per (CTA, strip)
   int64_t D;
   int T, BT;
   int n_cb, wpc;
   int W, wdt;
+  // packed sequences only
+  const int32_t* cu;        // [nseq + 1] row offsets
+  const uint16_t* init;     // [nseq, D, W-1] initial states, or null (zeros)
+  uint16_t* dinit;          // [nseq, D, W-1] their gradient, or null
+  int nseq;
 };
+
+// Kernel modes: the batched [B,T,D] form with SiLU is mode 0.
+enum : int { kModeVarlen = 1, kModeActNone = 2 };
 
 // 2g for one row, from its x and dy and the x ring h = (x[t-1], x[t-2], x[t-3]).  With
 // halved taps hz = z / 2 and th = tanh(hz): sigmoid(z) = (1 + th) / 2, 1 - sigmoid(z) =
 // (1 - th) / 2, so g = dy sigmoid(z) (1 + z (1 - sigmoid(z))) = dy (1 + th) (1 + hz (1 - th)) / 2.
 // The kernel carries g2 = 2g: dx = sum_k (w/2) g2 uses the same halved taps, and the dw / dbias
 // sums of g2 are halved once, when the partial record is written.
-template <int P>
+// Without the activation g = dy, g2 = 2 dy.
+template <int P, bool ACT>
 __device__ __forceinline__ void bwd_g(const f2 (&x)[P], const f2 (&dy)[P], const f2 (&h)[3][P],
                                       const f2 (&tap)[4][P], const f2 (&bias2)[P], f2 (&g)[P]) {
   const f2 one = f2_splat(1.0f);
   const f2 mone = f2_splat(-1.0f);
+  if constexpr (!ACT) {
+#pragma unroll
+    for (int q = 0; q < P; ++q) g[q] = f2_add(dy[q], dy[q]);
+    return;
+  }
 #pragma unroll
   for (int q = 0; q < P; ++q) {
     f2 hz = f2_fma(tap[0][q], x[q], bias2[q]);
@@ -110,14 +125,32 @@ __device__ __forceinline__ void rings_push(f2 (&h)[3][P], f2 (&gr)[3][P], const 
   }
 }
 
+// Packed sequences: the gradient of initial-state entry j (row ss - (W-1) + j) is the dx
+// formula at that row with g = 0 before the sequence; this lane's VEC channels.
+template <int VEC>
+__device__ __forceinline__ void store_dinit(uint16_t* dinit, int i, int64_t D, int W, int j,
+                                            int64_t d0, const f2 (&v)[VEC / 2]) {
+  const int L = W - 1;
+  uint16_t* o = dinit + (static_cast<int64_t>(i) * D + d0) * L + j;
+#pragma unroll
+  for (int q = 0; q < VEC / 2; ++q) {
+    float lo, hi;
+    f2_unpack(v[q], lo, hi);
+    o[(2 * q) * L] = f32_to_bf16(lo);
+    o[(2 * q + 1) * L] = f32_to_bf16(hi);
+  }
+}
+
 // Rows of one tile for this lane.  FULL: every row computes g, accumulates dw / dbias and
 // stores dx[t-3].  Otherwise rows before `from` were done with the previous tile, rows
 // before a only fill the x ring, halo rows after e give g (for the last dx rows) only.
 // STORE: this lane's channels exist, so stores need no per-row test.  The dx row pointer
-// (row t-3) advances by D per row.
-template <int VEC, int R, bool FULL, bool STORE>
+// (row t-3) advances by D per row.  VL (packed sequences): halo rows past the sequence's
+// end have g = 0, and in a segment that starts its sequence the dx formula for the W-1
+// rows before it gives the initial state's gradient.
+template <int VEC, int R, bool FULL, bool STORE, bool VL, bool ACT, class Cursor>
 __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, int lane,
-                                         const TileCursor& c, bool active, const BwdArgs& p,
+                                         const Cursor& c, bool active, const BwdArgs& p,
                                          int64_t d0, const f2 (&tap)[4][VEC / 2],
                                          const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
                                          f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
@@ -131,14 +164,28 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
       f2 x[P], g[P];
       smem_row<VEC>(xt + i * ROWB, lane, x);
       if (FULL || t >= c.a) {
-        f2 dy[P];
-        smem_row<VEC>(dyt + i * ROWB, lane, dy);
-        bwd_g<P>(x, dy, h, tap, bias2, g);
+        bool live = true;
+        if constexpr (VL) live = FULL || t < c.se;
+        if (live) {
+          f2 dy[P];
+          smem_row<VEC>(dyt + i * ROWB, lane, dy);
+          bwd_g<P, ACT>(x, dy, h, tap, bias2, g);
+        } else {
+#pragma unroll
+          for (int q = 0; q < P; ++q) g[q] = 0ull;
+        }
         if (FULL || t < c.e) bwd_acc<P>(x, h, g, acc);
         if (FULL || (t - kRing >= c.a && t - kRing < c.e)) {
           f2 dxv[P];
           bwd_dx<P>(g, gr, tap, dxv);
           if (STORE || active) store_row<VEC>(dxrow, dxv);
+        } else if constexpr (VL && !FULL) {
+          if (p.dinit && c.a == c.ss && t - kRing < c.a && t - kRing >= c.a - (p.W - 1)) {
+            f2 dxv[P];
+            bwd_dx<P>(g, gr, tap, dxv);
+            if (active)
+              store_dinit<VEC>(p.dinit, c.i, p.D, p.W, t - kRing - (c.a - (p.W - 1)), d0, dxv);
+          }
         }
       } else {
 #pragma unroll
@@ -153,11 +200,16 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
 // CTA: NW warps = SW neighbouring strips x RW = NW/SW consecutive row ranges (strips fastest,
 // so at any time the CTA reads SW*32*VEC contiguous channels of the same rows); each warp
 // runs its own TMA pipeline; the RW partial sums of each strip are added inside the CTA.
-template <int VEC, int R, int S, int NW, int SW>
+// MODE: kModeVarlen walks packed sequences (rows of [total, D], each sequence's ring from
+// its initial state, its gradient written); kModeActNone leaves out the SiLU.
+template <int VEC, int R, int S, int NW, int SW, int MODE>
 __global__ void __launch_bounds__(NW * 32, 1)
     cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
                      const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
   static_assert(NW % SW == 0, "SW strips must divide the CTA's warps");
+  constexpr bool VL = (MODE & kModeVarlen) != 0;
+  constexpr bool ACT = (MODE & kModeActNone) == 0;
+  using Cursor = typename std::conditional<VL, SeqCursor, TileCursor>::type;
   constexpr int RW = NW / SW;
   constexpr int CB = 32 * VEC;
   constexpr int P = VEC / 2;
@@ -205,8 +257,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
 
   if (has_work) {
-    TileCursor pc, cc;
-    pc.init(r0, r1, p.T, kRing, R);
+    Cursor pc, cc;
+    if constexpr (VL)
+      pc.init(r0, r1, p.cu, p.nseq, p.BT, kRing, R, lane);  // all lanes of the warp
+    else
+      pc.init(r0, r1, p.T, kRing, R);
     cc = pc;
     const uint64_t pol = policy_evict_first();
     if (lane == 0) {
@@ -233,6 +288,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
         h[j][q] = 0ull;
         gr[j][q] = 0ull;
       }
+    f2 hin[3][P];  // packed sequences: the x ring the current segment starts from
+    if constexpr (VL) {
+      if (!cc.done && cc.from == cc.ss) init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
+    }
 
     uint32_t parity = 0;
     int s = 0;
@@ -248,13 +307,24 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
       parity ^= 1u << s;
       const uint8_t* xt = stages + s * STAGE;
+      if constexpr (VL) {
+        if (cc.first && cc.from == cc.ss) {  // the segment starts its sequence's rings
+#pragma unroll
+          for (int q = 0; q < P; ++q)
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              h[j][q] = hin[j][q];
+              gr[j][q] = 0ull;
+            }
+        }
+      }
       if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
         if (all_active)
-          bwd_tile<VEC, R, true, true>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+          bwd_tile<VEC, R, true, true, VL, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
         else
-          bwd_tile<VEC, R, true, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+          bwd_tile<VEC, R, true, false, VL, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
       } else {
-        bwd_tile<VEC, R, false, false>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+        bwd_tile<VEC, R, false, false, VL, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
       }
       __syncwarp();
       if (lane == 0 && !pc.done) {
@@ -265,7 +335,33 @@ __global__ void __launch_bounds__(NW * 32, 1)
         pc.advance();
       }
       cc.advance();
+      if constexpr (VL) {
+        if (!cc.done && cc.first && cc.from == cc.ss)
+          init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
+      }
       s = (s + 1 == S) ? 0 : s + 1;
+    }
+  }
+  if constexpr (VL) {
+    // Empty sequences get a zero initial-state gradient (CTA i, i + grid, ...), and warp 0
+    // of CTA 0 checks cu_seqlens.
+    if (p.dinit && p.W > 1) {
+      const int64_t n = p.D * (p.W - 1);
+      for (int i = blockIdx.x; i < p.nseq; i += gridDim.x) {
+        if (clamp_row(p.cu[i + 1], p.BT) > clamp_row(p.cu[i], p.BT)) continue;
+        uint16_t* o = p.dinit + static_cast<int64_t>(i) * n;
+        for (int64_t k = threadIdx.x; k < n; k += NW * 32) o[k] = 0;
+      }
+    }
+    if (blockIdx.x == 0 && warp == 0) {
+      bool bad = false;
+      for (int k = lane; k <= p.nseq; k += 32) {
+        const int v = p.cu[k];
+        if (v < 0 || v > p.BT || (k == 0 && v != 0) || (k == p.nseq && v != p.BT) ||
+            (k > 0 && p.cu[k - 1] > v))
+          bad = true;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_fault_bwd, kFaultSeqlens);
     }
   }
   grid_launch_dependents();
@@ -357,7 +453,7 @@ struct BwdConfig {
 };
 
 #define CCONV_BWD_CFG(V, R, S, NW, SW) \
-  BwdConfig { V, R, S, NW, SW, cconv_bwd_kernel<V, R, S, NW, SW> }
+  BwdConfig { V, R, S, NW, SW, cconv_bwd_kernel<V, R, S, NW, SW, 0> }
 
 static const BwdConfig kBwdConfigs[] = {
     CCONV_BWD_CFG(4, 12, 3, 8, 4),  // measured fastest at B=2 T=8192 D=4096
@@ -569,3 +665,147 @@ extern "C" CCONV_API int cconv_bwd_noalloc(const void* x, int64_t sxb, int64_t s
   return cconv_bwd(x, sxb, sxt, dy, sdb, sdt, B, T, D, w, bias, wdt, W, dx, dw, dbias, scratch,
                    kBwdNoallocScratchBytes, stream);
 }
+
+namespace cconv {
+
+// Packed sequences run the default tile shape (first configuration).
+static void (*const kBwdVarlenKernels[2])(const CUtensorMap, const CUtensorMap, const BwdArgs) = {
+    cconv_bwd_kernel<4, 12, 3, 8, 4, kModeVarlen>,
+    cconv_bwd_kernel<4, 12, 3, 8, 4, kModeVarlen | kModeActNone>,
+};
+static const BwdConfig kBwdVarlenConfig = {4, 12, 3, 8, 4, nullptr};
+
+// Zeroes n bf16 values (the initial-state gradient when there are no rows at all).
+__global__ void cconv_zero_u16_kernel(uint16_t* p, int64_t n) {
+  grid_dependency_wait();
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    p[k] = 0;
+  grid_launch_dependents();
+}
+
+static int check_varlen_sizes(int64_t total, int64_t D, int W, int64_t nseq) {
+  if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
+  if (total < 0 || nseq < 1 || D < 1 || total > (int64_t(1) << 31) - 16 ||
+      nseq > (int64_t(1) << 31) - 2 || D > (int64_t(1) << 31) - 8)
+    return CCONV_ERR_SHAPE;
+  if (D % 8 != 0) return CCONV_ERR_ALIGN;
+  return CCONV_OK;
+}
+
+}  // namespace cconv
+
+extern "C" {
+
+CCONV_API int cconv_bwd_varlen_workspace_bytes(int64_t total, int64_t D, int W, size_t* bytes) {
+  using namespace cconv;
+  if (!bytes) return CCONV_ERR_NULL;
+  int rc = check_varlen_sizes(total, D, W, 1);
+  if (rc != CCONV_OK) return rc;
+  BwdPlan plan;
+  return bwd_plan(1, total, D, kBwdVarlenConfig, &plan, bytes);
+}
+
+CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64_t sdt,
+                               int64_t total, int64_t D, const int32_t* cu_seqlens, int64_t nseq,
+                               const void* w, const void* bias, cconv_dtype wdt, int W,
+                               cconv_activation act, const void* initial_state, void* dx,
+                               void* dw, void* dbias, void* d_initial_state, void* workspace,
+                               size_t workspace_bytes, cconv_stream_t stream) {
+  using namespace cconv;
+  if (!w || !dw || !cu_seqlens) return CCONV_ERR_NULL;
+  if (total > 0 && (!x || !dy || !dx)) return CCONV_ERR_NULL;
+  if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
+  if (act != CCONV_ACT_SILU && act != CCONV_ACT_NONE) return CCONV_ERR_SHAPE;
+  int rc = check_varlen_sizes(total, D, W, nseq);
+  if (rc != CCONV_OK) return rc;
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) % 4 != 0) return CCONV_ERR_ALIGN;
+  if (total > 0) {
+    rc = check_rows_tensor(x, 1, total, D, 0, sxt);
+    if (rc != CCONV_OK) return rc;
+    rc = check_rows_tensor(dy, 1, total, D, 0, sdt);
+    if (rc != CCONV_OK) return rc;
+    if (reinterpret_cast<uintptr_t>(dx) % 16 != 0) return CCONV_ERR_ALIGN;
+  }
+  const int ew = wdt == CCONV_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(w) % ew != 0 || reinterpret_cast<uintptr_t>(dw) % ew != 0)
+    return CCONV_ERR_ALIGN;
+  if ((bias && reinterpret_cast<uintptr_t>(bias) % ew != 0) ||
+      (dbias && reinterpret_cast<uintptr_t>(dbias) % ew != 0))
+    return CCONV_ERR_ALIGN;
+  const int L = W - 1;
+  if (L > 0 && ((initial_state && reinterpret_cast<uintptr_t>(initial_state) % 2 != 0) ||
+                (d_initial_state && reinterpret_cast<uintptr_t>(d_initial_state) % 2 != 0)))
+    return CCONV_ERR_ALIGN;
+
+  const BwdConfig& cfg = kBwdVarlenConfig;
+  BwdPlan plan;
+  size_t need = 0;
+  rc = bwd_plan(1, total, D, cfg, &plan, &need);
+  if (rc != CCONV_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int wdt_i = static_cast<int>(wdt);
+  const dim3 red_grid(static_cast<unsigned>((D + 31) / 32), dbias ? kRec : W);
+
+  if (total == 0) {  // no rows: dw, dbias and the initial-state gradient are all zero
+    if (L > 0 && d_initial_state) {
+      const int64_t n = nseq * D * L;
+      int64_t g = (n + 255) / 256;
+      if (g > 1024) g = 1024;
+      if (launch_pdl(cconv_zero_u16_kernel, dim3(static_cast<unsigned>(g)), dim3(256), 0, st,
+                     static_cast<uint16_t*>(d_initial_state), n) != cudaSuccess)
+        return CCONV_ERR_CUDA;
+    }
+    const float* none = nullptr;
+    if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, none,
+                   32 * cfg.vec, cfg.sw, plan.n_sg, 0, D, W, wdt_i, dw, dbias) != cudaSuccess)
+      return CCONV_ERR_CUDA;
+    return CCONV_OK;
+  }
+
+  if (!workspace || workspace_bytes < need) return CCONV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return CCONV_ERR_ALIGN;
+  int64_t sb = 0, sdb = 0;
+  normalise_strides(1, total, D, sb, sxt);
+  normalise_strides(1, total, D, sdb, sdt);
+  CUtensorMap tmx, tmdy;
+  rc = encode_rows_map(&tmx, x, 1, total, D, sb, sxt, 32 * cfg.vec, cfg.rows);
+  if (rc != CCONV_OK) return rc;
+  rc = encode_rows_map(&tmdy, dy, 1, total, D, sdb, sdt, 32 * cfg.vec, cfg.rows);
+  if (rc != CCONV_OK) return rc;
+
+  BwdArgs a;
+  a.w = w;
+  a.bias = bias;
+  a.dx = static_cast<uint16_t*>(dx);
+  a.ws = static_cast<float*>(workspace);
+  a.D = D;
+  a.T = static_cast<int>(total);
+  a.BT = static_cast<int>(total);
+  a.n_cb = plan.n_cb;
+  a.wpc = plan.wpc;
+  a.W = W;
+  a.wdt = wdt;
+  a.cu = cu_seqlens;
+  a.init = L > 0 ? static_cast<const uint16_t*>(initial_state) : nullptr;
+  a.dinit = L > 0 ? static_cast<uint16_t*>(d_initial_state) : nullptr;
+  a.nseq = static_cast<int>(nseq);
+
+  auto kern = kBwdVarlenKernels[act == CCONV_ACT_NONE ? 1 : 0];
+  int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
+  const int red_bytes = cfg.warps * kRec * 32 * cfg.vec * static_cast<int>(sizeof(float));
+  if (smem < red_bytes) smem = red_bytes;
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+  if (rc != CCONV_OK) return rc;
+  if (launch_pdl(kern, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
+      cudaSuccess)
+    return CCONV_ERR_CUDA;
+  const float* wsp = a.ws;
+  if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, wsp,
+                 32 * cfg.vec, cfg.sw, plan.n_sg, plan.n_rg, D, W, wdt_i, dw, dbias) !=
+      cudaSuccess)
+    return CCONV_ERR_CUDA;
+  return CCONV_OK;
+}
+
+}  // extern "C"

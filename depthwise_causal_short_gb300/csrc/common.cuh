@@ -22,6 +22,7 @@ namespace cconv {
 enum FaultCode : unsigned {
   kFaultFwdWait = 1u,
   kFaultBwdWait = 2u,
+  kFaultSeqlens = 4u,  // an ill-formed cu_seqlens was passed (results unspecified)
 };
 
 // Nanoseconds a kernel waits on one TMA tile before it reports a fault and returns.

@@ -15,6 +15,8 @@
 // lockstep keeps the warps of an SM finishing together.  The 3 ring rows before a range and
 // the zero padding before t = 0 come from the same tiled copy (out-of-range rows fill with
 // zeros).  Arithmetic is packed f32x2; the sigmoid is 0.5 * tanh.approx(z/2) + 0.5.
+#include <type_traits>
+
 #include "strip.cuh"
 
 namespace cconv {
@@ -31,16 +33,26 @@ int read_clear_fault_fwd(unsigned* out) {
 struct FwdArgs {
   const void* w;
   const void* bias;
-  uint16_t* y;  // [B,T,D] contiguous bf16
+  uint16_t* y;  // [B,T,D] contiguous bf16 ([total, D] for packed sequences)
   int64_t D;
   int T, BT;
   int cpc;      // CTAs per channel group
   int W, wdt;
+  // packed sequences only
+  const int32_t* cu;        // [nseq + 1] row offsets
+  const uint16_t* init;     // [S, D, W-1] initial states, or null (zeros)
+  const int32_t* idx;       // [nseq] slot of each sequence, or null (slot i)
+  int64_t S;
+  int nseq;
 };
+
+// Kernel modes: the batched [B,T,D] form with SiLU is mode 0.
+enum : int { kModeVarlen = 1, kModeActNone = 2 };
 
 // One output row from the new input row x and the ring h = (x[t-1], x[t-2], x[t-3]).
 // With halved taps hz = z / 2, and silu(z) = hz * (1 + tanh(hz)).
-template <int P>
+// Without the activation y = z = 2 hz.
+template <int P, bool ACT>
 __device__ __forceinline__ void fwd_row(const f2 (&x)[P], const f2 (&h)[3][P],
                                         const f2 (&tap)[4][P], const f2 (&bias2)[P],
                                         f2 (&yv)[P]) {
@@ -50,7 +62,7 @@ __device__ __forceinline__ void fwd_row(const f2 (&x)[P], const f2 (&h)[3][P],
     hz = f2_fma(tap[1][q], h[0][q], hz);
     hz = f2_fma(tap[2][q], h[1][q], hz);
     hz = f2_fma(tap[3][q], h[2][q], hz);
-    yv[q] = f2_fma(hz, f2_tanh(hz), hz);
+    yv[q] = ACT ? f2_fma(hz, f2_tanh(hz), hz) : f2_add(hz, hz);
   }
 }
 
@@ -69,8 +81,8 @@ __device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
 // from e on are not needed.  STORE: this lane's channels exist (every lane of a CTA whose
 // channel group lies inside D), so stores need no per-row test.  The output row pointer
 // advances by D per row.
-template <int VEC, int R, bool FULL, bool STORE>
-__device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const TileCursor& c,
+template <int VEC, int R, bool FULL, bool STORE, bool ACT, class Cursor>
+__device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Cursor& c,
                                          bool active, const FwdArgs& p, int64_t d0,
                                          const f2 (&tap)[4][VEC / 2], const f2 (&bias2)[VEC / 2],
                                          f2 (&h)[3][VEC / 2]) {
@@ -85,7 +97,7 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
       smem_row<VEC>(tile + i * ROWB, lane, x);
       if (FULL || (t >= c.a && t < c.e)) {
         f2 yv[P];
-        fwd_row<P>(x, h, tap, bias2, yv);
+        fwd_row<P, ACT>(x, h, tap, bias2, yv);
         if (STORE || active) store_row<VEC>(yrow, yv);
       }
       ring_push<P>(h, x);
@@ -95,9 +107,9 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
 }
 
 // Loads one tile (rows cur.tt .. cur.tt+R-1, one box per consumer warp) into a stage.
-template <int VEC, int R, int NC>
+template <int VEC, int R, int NC, class Cursor>
 __device__ __forceinline__ void fwd_issue(uint8_t* st, uint64_t* full, const CUtensorMap* tmx,
-                                          const TileCursor& cur, int nact, int c0, uint64_t pol) {
+                                          const Cursor& cur, int nact, int c0, uint64_t pol) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
   mbar_arrive_expect_tx(full, nact * TILE);
@@ -105,13 +117,39 @@ __device__ __forceinline__ void fwd_issue(uint8_t* st, uint64_t* full, const CUt
     tma_load_3d(st + w * TILE, tmx, full, c0 + w * CB, cur.tt, cur.b, pol);
 }
 
+// Slot of sequence i in the state arrays, or -1 when the index is unusable (the state
+// kernel reports it; here such a sequence just starts from zeros).
+__device__ __forceinline__ int64_t seq_slot(const FwdArgs& p, int i) {
+  const int64_t s = p.idx ? static_cast<int64_t>(p.idx[i]) : i;
+  return (s >= 0 && s < p.S) ? s : -1;
+}
+
+// Packed sequences: checks cu_seqlens (cu[0] = 0, non-decreasing, cu[nseq] = total) with
+// the 32 lanes of one warp, and raises the fault bit if it is ill-formed.
+__device__ __forceinline__ void check_seqlens(const int32_t* cu, int nseq, int total, int lane,
+                                              unsigned* fault) {
+  bool bad = false;
+  for (int k = lane; k <= nseq; k += 32) {
+    const int v = cu[k];
+    if (v < 0 || v > total || (k == 0 && v != 0) || (k == nseq && v != total) ||
+        (k > 0 && cu[k - 1] > v))
+      bad = true;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(fault, kFaultSeqlens);
+}
+
 // CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile).
 // SEP: a separate producer warp (index NC) streams the stages; otherwise lane 0 of consumer
 // warp 0 re-arms each stage once every consumer has released it.  Stage layout: NC boxes of
-// R rows x CB channels.
-template <int VEC, int R, int S, int NC, int MINB, bool SEP>
+// R rows x CB channels.  MODE: kModeVarlen walks packed sequences (rows of [total, D], ring
+// from each sequence's initial state); kModeActNone leaves out the SiLU.
+template <int VEC, int R, int S, int NC, int MINB, bool SEP, int MODE>
 __global__ void __maxnreg__(regs_for(NC + SEP, MINB))
 cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
+  constexpr bool VL = (MODE & kModeVarlen) != 0;
+  constexpr bool ACT = (MODE & kModeActNone) == 0;
+  static_assert(SEP || !VL, "packed sequences use the producer warp to check cu_seqlens");
+  using Cursor = typename std::conditional<VL, SeqCursor, TileCursor>::type;
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
   constexpr int STAGE = NC * TILE;
@@ -143,8 +181,11 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   // completed.
   grid_dependency_wait();
 
-  TileCursor cur;
-  cur.init(r0, r1, p.T, 0, R);
+  Cursor cur;
+  if constexpr (VL)
+    cur.init(r0, r1, p.cu, p.nseq, p.BT, 0, R, lane);  // all lanes of every warp
+  else
+    cur.init(r0, r1, p.T, 0, R);
   const uint64_t pol = policy_evict_first();
   if (SEP && warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
@@ -164,10 +205,14 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
         s = (s + 1 == S) ? 0 : s + 1;
       }
     }
+    if constexpr (VL) {
+      __syncwarp();
+      if (blockIdx.x == 0) check_seqlens(p.cu, p.nseq, p.BT, lane, &g_fault_fwd);
+    }
   } else if (warp < nact) {
     // ---- consumer ------------------------------------------------------------------------
     const bool leader = !SEP && warp == 0;
-    TileCursor pc = cur;  // the leader's producer cursor, S tiles ahead
+    Cursor pc = cur;  // the leader's producer cursor, S tiles ahead
     if (leader && lane == 0) {
       for (int s = 0; s < S && !pc.done; ++s) {
         fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, pc, nact, c0, pol);
@@ -184,6 +229,11 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     for (int j = 0; j < 3; ++j)
 #pragma unroll
       for (int q = 0; q < VEC / 2; ++q) h[j][q] = 0ull;
+    f2 hin[3][VEC / 2];  // packed sequences: the ring the current segment starts from
+    if constexpr (VL) {
+      if (!cur.done && cur.from == cur.ss)
+        init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
+    }
 
     uint32_t fph = 0, eph = 0;
     int s = 0;
@@ -196,13 +246,21 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
       }
       fph ^= 1u << s;
       const uint8_t* tile = smem + s * STAGE + warp * TILE;
+      if constexpr (VL) {
+        if (cur.first && cur.from == cur.ss) {  // the segment starts its sequence's ring
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+#pragma unroll
+            for (int q = 0; q < VEC / 2; ++q) h[j][q] = hin[j][q];
+        }
+      }
       if (cur.from == cur.tt && cur.tt >= cur.a && cur.tt + R <= cur.e) {
         if (all_active)
-          fwd_tile<VEC, R, true, true>(tile, lane, cur, active, p, d0, tap, bias2, h);
+          fwd_tile<VEC, R, true, true, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
         else
-          fwd_tile<VEC, R, true, false>(tile, lane, cur, active, p, d0, tap, bias2, h);
+          fwd_tile<VEC, R, true, false, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
       } else {
-        fwd_tile<VEC, R, false, false>(tile, lane, cur, active, p, d0, tap, bias2, h);
+        fwd_tile<VEC, R, false, false, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -222,10 +280,119 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
         if (!__all_sync(0xffffffffu, fine)) break;
       }
       cur.advance();
+      if constexpr (VL) {
+        // A new segment: fetch its initial ring now, so the loads overlap the next wait.
+        if (!cur.done && cur.first && cur.from == cur.ss)
+          init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
+      }
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }
   grid_launch_dependents();
+}
+
+// ------------------------------------------------------------------------------------
+// packed sequences: final states (second kernel)
+//
+// final[slot(i), d, j] = extended row se - (W-1) + j of sequence i: x where that row lies in
+// the sequence, else its initial state (zero without one).  One thread per 8 channels of a
+// sequence; the 8 channels' W-1 entries are 16*(W-1) contiguous bytes.  It runs after the
+// stream kernel has completed (programmatic dependent launch waits for it), so the final
+// states may overwrite the initial states in place: every read of them is done by then.
+// With state indices it first validates them in every CTA, as the decode update does
+// (negative, >= S, or repeated), and on a bad vector writes nothing but the status words.
+// ------------------------------------------------------------------------------------
+constexpr int kStateThreads = 256;
+
+struct StateArgs {
+  const uint16_t* x;      // [total, D], row stride sxt
+  const int32_t* cu;      // [nseq + 1]
+  const uint16_t* init;   // [S, D, W-1] or null
+  uint16_t* fin;          // [S, D, W-1] or null
+  const int32_t* idx;     // [nseq] or null
+  int32_t* status;        // [2] or null (required with idx)
+  int64_t sxt, D, S;
+  int nseq, total, chunks;
+};
+
+template <int L>
+__global__ void __launch_bounds__(kStateThreads) cconv_fwd_state_kernel(const StateArgs p) {
+  extern __shared__ uint32_t bitmap[];
+  __shared__ int s_bad;
+  if (p.idx) {
+    if (threadIdx.x == 0) s_bad = 0;
+    const int nwords = static_cast<int>((p.S + 31) / 32);
+    for (int k = threadIdx.x; k < nwords; k += kStateThreads) bitmap[k] = 0u;
+  }
+  grid_dependency_wait();
+  int bad = 0;
+  if (p.idx) {
+    __syncthreads();
+    int off = 0;
+    for (int k = threadIdx.x; k < p.nseq; k += kStateThreads) {
+      const int32_t v = p.idx[k];
+      if (v < 0) {
+        off |= CCONV_IDX_NEGATIVE;
+      } else if (v >= p.S) {
+        off |= CCONV_IDX_OUT_OF_RANGE;
+      } else {
+        const uint32_t m = 1u << (v & 31);
+        if (atomicOr(&bitmap[v >> 5], m) & m) off |= CCONV_IDX_DUPLICATE;
+      }
+    }
+    if (off) atomicOr(&s_bad, off);
+    __syncthreads();
+    bad = s_bad;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      p.status[0] = bad ? CCONV_ERR_INDEX : CCONV_OK;
+      p.status[1] = bad;
+    }
+  }
+  grid_launch_dependents();
+  if (bad || !p.fin || L == 0) return;
+
+  const int64_t items = static_cast<int64_t>(p.nseq) * p.chunks;
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * kStateThreads + threadIdx.x; it < items;
+       it += static_cast<int64_t>(gridDim.x) * kStateThreads) {
+    const int i = static_cast<int>(it / p.chunks);
+    const int64_t d0 = (it - static_cast<int64_t>(i) * p.chunks) * 8;
+    const int64_t slot = p.idx ? p.idx[i] : i;
+    const int ss = clamp_row(p.cu[i], p.total);
+    int se = clamp_row(p.cu[i + 1], p.total);
+    if (se < ss) se = ss;
+    uint4 st[L > 0 ? L : 1];  // initial entries of these 8 channels (only if needed)
+    const bool short_seq = se - ss < L;
+    if (short_seq) {
+      if (p.init) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.init + (slot * p.D + d0) * L);
+#pragma unroll
+        for (int u = 0; u < L; ++u) st[u] = src[u];
+      } else {
+#pragma unroll
+        for (int u = 0; u < L; ++u) st[u] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    const uint16_t* sh = reinterpret_cast<const uint16_t*>(st);
+    uint4 out[L > 0 ? L : 1];
+    uint16_t* oh = reinterpret_cast<uint16_t*>(out);
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      const int u = se - L + j;  // extended row
+      if (u >= ss) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(u) * p.sxt + d0);
+        const uint16_t* vh = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) oh[c * L + j] = vh[c];
+      } else {
+        const int jj = u - (ss - L);  // entry of the initial state, 0 <= jj < L
+#pragma unroll
+        for (int c = 0; c < 8; ++c) oh[c * L + j] = sh[c * L + jj];
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.fin + (slot * p.D + d0) * L);
+#pragma unroll
+    for (int u = 0; u < L; ++u) dst[u] = out[u];
+  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -237,7 +404,7 @@ struct FwdConfig {
 };
 
 #define CCONV_FWD_CFG(V, R, S, NC, M, SEP) \
-  FwdConfig { V, R, S, NC, M, SEP, cconv_fwd_kernel<V, R, S, NC, M, SEP> }
+  FwdConfig { V, R, S, NC, M, SEP, cconv_fwd_kernel<V, R, S, NC, M, SEP, 0> }
 
 static const FwdConfig kFwdConfigs[] = {
     CCONV_FWD_CFG(4, 8, 10, 8, 1, true),  // measured fastest at B=2 T=8192 D=4096
@@ -310,4 +477,130 @@ extern "C" CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t 
                     reinterpret_cast<cudaStream_t>(stream), tmx, a) == cudaSuccess
              ? CCONV_OK
              : CCONV_ERR_CUDA;
+}
+
+namespace cconv {
+
+// Packed sequences run the default tile shape (first configuration).
+static void (*const kFwdVarlenKernels[2])(const CUtensorMap, const FwdArgs) = {
+    cconv_fwd_kernel<4, 8, 10, 8, 1, true, kModeVarlen>,
+    cconv_fwd_kernel<4, 8, 10, 8, 1, true, kModeVarlen | kModeActNone>,
+};
+constexpr int kVarlenVec = 4, kVarlenRows = 8, kVarlenStages = 10, kVarlenNc = 8;
+
+static void (*const kStateKernels[4])(const StateArgs) = {
+    cconv_fwd_state_kernel<0>, cconv_fwd_state_kernel<1>, cconv_fwd_state_kernel<2>,
+    cconv_fwd_state_kernel<3>};
+
+}  // namespace cconv
+
+extern "C" CCONV_API int cconv_fwd_varlen(const void* x, int64_t total, int64_t D, int64_t sxt,
+                                          const int32_t* cu_seqlens, int64_t nseq,
+                                          const void* w, const void* bias, cconv_dtype wdt,
+                                          int W, cconv_activation act,
+                                          const void* initial_state, void* final_state,
+                                          const int32_t* state_indices, int64_t S,
+                                          int32_t* status_dev, void* y, cconv_stream_t stream) {
+  using namespace cconv;
+  if (!w || !cu_seqlens) return CCONV_ERR_NULL;
+  if (total > 0 && (!x || !y)) return CCONV_ERR_NULL;
+  if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
+  if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
+  if (act != CCONV_ACT_SILU && act != CCONV_ACT_NONE) return CCONV_ERR_SHAPE;
+  if (total < 0 || nseq < 1 || D < 1 || total > (int64_t(1) << 31) - 16 ||
+      nseq > (int64_t(1) << 31) - 2 || D > (int64_t(1) << 31) - 8)
+    return CCONV_ERR_SHAPE;
+  if (D % 8 != 0) return CCONV_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) % 4 != 0) return CCONV_ERR_ALIGN;
+  int rc;
+  if (total > 0) {
+    rc = check_rows_tensor(x, 1, total, D, 0, sxt);
+    if (rc != CCONV_OK) return rc;
+    if (reinterpret_cast<uintptr_t>(y) % 16 != 0) return CCONV_ERR_ALIGN;
+  }
+  const int ew = wdt == CCONV_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(w) % ew != 0 ||
+      (bias && reinterpret_cast<uintptr_t>(bias) % ew != 0))
+    return CCONV_ERR_ALIGN;
+  const int L = W - 1;
+  const bool states = L > 0 && (initial_state || final_state);
+  if (state_indices) {
+    if (!status_dev) return CCONV_ERR_NULL;
+    if (S < 1 || S > CCONV_UPDATE_MAX_SLOTS) return CCONV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(state_indices) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(status_dev) % 4 != 0)
+      return CCONV_ERR_ALIGN;
+  } else if (states && S < nseq) {
+    return CCONV_ERR_SHAPE;
+  }
+  if (states && ((initial_state && reinterpret_cast<uintptr_t>(initial_state) % 16 != 0) ||
+                 (final_state && reinterpret_cast<uintptr_t>(final_state) % 16 != 0)))
+    return CCONV_ERR_ALIGN;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (total > 0) {
+    int sms = 0;
+    rc = sm_count_current_device(&sms, nullptr);
+    if (rc != CCONV_OK) return rc;
+    const GroupPlan plan =
+        make_group_plan(1, total, D, kVarlenVec, kVarlenNc, 1, sms, 32);
+    int64_t sb = 0;
+    normalise_strides(1, total, D, sb, sxt);
+    CUtensorMap tmx;
+    rc = encode_rows_map(&tmx, x, 1, total, D, sb, sxt, 32 * kVarlenVec, kVarlenRows);
+    if (rc != CCONV_OK) return rc;
+    FwdArgs a;
+    a.w = w;
+    a.bias = bias;
+    a.y = static_cast<uint16_t*>(y);
+    a.D = D;
+    a.T = static_cast<int>(total);
+    a.BT = static_cast<int>(total);
+    a.cpc = plan.cpc;
+    a.W = W;
+    a.wdt = wdt;
+    a.cu = cu_seqlens;
+    a.init = L > 0 ? static_cast<const uint16_t*>(initial_state) : nullptr;
+    a.idx = state_indices;
+    a.S = state_indices ? S : nseq;
+    a.nseq = static_cast<int>(nseq);
+    auto kern = kFwdVarlenKernels[act == CCONV_ACT_NONE ? 1 : 0];
+    const int smem = kVarlenStages * (kVarlenNc * kVarlenRows * 32 * kVarlenVec * 2 + 16);
+    rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (rc != CCONV_OK) return rc;
+    if (launch_pdl(kern, dim3(plan.grid), dim3((kVarlenNc + 1) * 32), smem, st, tmx, a) !=
+        cudaSuccess)
+      return CCONV_ERR_CUDA;
+  }
+  if ((L > 0 && final_state) || state_indices) {
+    int sms = 0;
+    rc = sm_count_current_device(&sms, nullptr);
+    if (rc != CCONV_OK) return rc;
+    StateArgs sa;
+    sa.x = static_cast<const uint16_t*>(x);
+    sa.cu = cu_seqlens;
+    sa.init = L > 0 ? static_cast<const uint16_t*>(initial_state) : nullptr;
+    sa.fin = L > 0 ? static_cast<uint16_t*>(final_state) : nullptr;
+    sa.idx = state_indices;
+    sa.status = status_dev;
+    sa.sxt = sxt;
+    sa.D = D;
+    sa.S = state_indices ? S : nseq;
+    sa.nseq = static_cast<int>(nseq);
+    sa.total = static_cast<int>(total);
+    sa.chunks = static_cast<int>(D / 8);
+    const int64_t items = nseq * (D / 8);
+    int64_t grid = (items + kStateThreads - 1) / kStateThreads;
+    if (grid > 2 * sms) grid = 2 * sms;
+    if (grid < 1) grid = 1;
+    auto kern = kStateKernels[L];
+    const size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
+    if (smem > 32 * 1024 &&
+        set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) != CCONV_OK)
+      return CCONV_ERR_CUDA;
+    if (launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kStateThreads), smem, st, sa) !=
+        cudaSuccess)
+      return CCONV_ERR_CUDA;
+  }
+  return CCONV_OK;
 }

@@ -10,7 +10,8 @@
 // order in lockstep, keeping the W-1 previous rows in registers (the ring).  Where a range
 // starts inside a sequence, its first tile starts 3 rows early to fill the ring; where it
 // starts a sequence, those 3 rows lie at t < 0 and the copy engine fills them with zeros,
-// which is exactly the causal zero padding.
+// which is exactly the causal zero padding.  Packed sequences of any lengths (SeqCursor)
+// take their ring at a sequence start from the sequence's initial state instead.
 #pragma once
 
 #include "common.cuh"
@@ -48,32 +49,6 @@ inline GroupPlan make_group_plan(int64_t B, int64_t T, int64_t D, int vec, int n
   if (cpc > by_rows) cpc = by_rows;
   p.cpc = static_cast<int>(cpc);
   p.grid = p.n_cg * p.cpc;
-  return p;
-}
-
-struct StripPlan {
-  int n_cb;          // channel strips: ceil(D / (32*VEC))
-  int wpc;           // warps (row ranges) per strip
-  int total_warps;   // n_cb * wpc
-  int grid;          // CTAs of `warps_per_cta` warps
-};
-
-// Per-warp split (each warp runs its own pipeline over one channel strip of 32*VEC channels):
-// warp gw takes strip gw % n_cb of range gw / n_cb.  rows_min: shortest range worth a warp.
-inline StripPlan make_strip_plan(int64_t B, int64_t T, int64_t D, int vec, int warps_per_cta,
-                                 int ctas_per_sm, int sms, int64_t rows_min) {
-  StripPlan p;
-  const int64_t cb_width = 32 * vec;
-  p.n_cb = static_cast<int>((D + cb_width - 1) / cb_width);
-  const int64_t target = static_cast<int64_t>(sms) * ctas_per_sm * warps_per_cta;
-  int64_t wpc = target / p.n_cb;
-  if (wpc < 1) wpc = 1;
-  int64_t by_rows = (B * T) / rows_min;
-  if (by_rows < 1) by_rows = 1;
-  if (wpc > by_rows) wpc = by_rows;
-  p.wpc = static_cast<int>(wpc);
-  p.total_warps = p.n_cb * p.wpc;
-  p.grid = (p.total_warps + warps_per_cta - 1) / warps_per_cta;
   return p;
 }
 
@@ -134,6 +109,134 @@ struct TileCursor {
     place(next);
   }
 };
+
+// Packed sequences: sequence i is rows [cu[i], cu[i+1]) of a [total, D] tensor.
+//
+// find_seq: the sequence holding packed row `row` (0 <= row < total), i.e. the largest
+// i < nseq with cu[i] <= row, found by the 32 lanes of a warp together: each round they
+// probe 32 evenly spaced candidates at once and keep the block of the last probe that is
+// still <= row, so nseq <= 32^k entries take k rounds of one load each.  Must be called by
+// all 32 lanes.  Values of cu outside [0, total] are clamped; an ill-formed cu gives some
+// index in [0, nseq) and never an access outside cu[0..nseq].
+__device__ __forceinline__ int clamp_row(int v, int total) {
+  return v < 0 ? 0 : (v > total ? total : v);
+}
+
+__device__ __forceinline__ int find_seq(const int32_t* cu, int nseq, int total, int row, int lane) {
+  int lo = 0, n = nseq;
+  while (n > 1) {
+    const int step = (n + 31) / 32;
+    const int pos = lo + lane * step;
+    const bool le = lane == 0 || (pos < lo + n && clamp_row(cu[pos], total) <= row);
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int last = 31 - __clz(m);
+    lo += last * step;
+    const int left = nseq - lo;
+    n = step < left ? step : left;
+  }
+  return lo;
+}
+
+// The tile walk of TileCursor over a range [r0, r1) of packed rows.  A segment is the part
+// of the range inside one sequence [ss, se): rows [a, e).  Each segment's first tile starts
+// at a - kRing (rows that fill the ring) but rows before the sequence start ss are skipped:
+// `from` starts at max(a - kRing, ss), and when it starts at ss the caller loads the ring
+// from the sequence's initial state instead (`first && from == ss`).  Empty sequences are
+// stepped over.  Every row touched lies in [r0 - kRing, r1 + tail) and every written row in
+// [r0, r1), whatever cu holds.
+struct SeqCursor {
+  const int32_t* cu;
+  int nseq, total, r1;
+  int i;          // current sequence
+  int ss, se;     // its rows, clamped to [0, total]
+  int a, e;       // current segment
+  int tt, from;   // current tile
+  int b;          // always 0: rows are packed
+  int tail, R;
+  bool done, first;
+
+  __device__ __forceinline__ int ld(int k) const { return clamp_row(cu[k], total); }
+
+  __device__ __forceinline__ void place(int start) {
+    from = start;
+    tt = start;
+    const int lim = e + tail;
+    if (tt + R > lim) {
+      const int back = lim - R;
+      tt = back > a - kRing ? back : a - kRing;
+    }
+  }
+
+  __device__ __forceinline__ void begin_segment() {
+    ss = ld(i);
+    se = ld(i + 1);
+    if (se < ss) se = ss;
+    e = se < r1 ? se : r1;
+    if (e < a) e = a;
+    place(a - kRing);
+    if (from < ss) from = ss;
+    first = true;
+  }
+
+  // Warp-collective (all 32 lanes): positions the cursor on the first tile of [r0, r1_).
+  __device__ __forceinline__ void init(int r0, int r1_, const int32_t* cu_, int nseq_,
+                                       int total_, int tail_, int R_, int lane) {
+    cu = cu_;
+    nseq = nseq_;
+    total = total_;
+    r1 = r1_;
+    tail = tail_;
+    R = R_;
+    b = 0;
+    done = r0 >= r1_ || nseq_ < 1;
+    i = done ? 0 : find_seq(cu_, nseq_, total_, r0, lane);
+    a = r0;
+    if (!done) begin_segment();
+  }
+
+  __device__ __forceinline__ void advance() {
+    const int next = tt + R;
+    if (next >= e + tail) {
+      if (e >= r1) {
+        done = true;
+        return;
+      }
+      int j = i + 1;
+      while (j < nseq && ld(j + 1) <= e) ++j;  // step over sequences that end here
+      if (j >= nseq) {
+        done = true;
+        return;
+      }
+      i = j;
+      a = e;
+      begin_segment();
+      return;
+    }
+    first = false;
+    place(next);
+  }
+};
+
+// Ring of the W-1 rows before a sequence, from its initial state (bf16 [.., D, W-1], entry
+// j = row ss - (W-1) + j), as this lane's fp32 pairs: h[k-1] = row ss - k, zero for
+// k > W - 1 or without a state (state == nullptr or slot < 0).
+template <int VEC>
+__device__ __forceinline__ void init_ring(const uint16_t* state, int64_t slot, int64_t D, int W,
+                                          int64_t d0, bool active, f2 (&h)[3][VEC / 2]) {
+  const int L = W - 1;
+#pragma unroll
+  for (int k = 1; k <= 3; ++k)
+#pragma unroll
+    for (int q = 0; q < VEC / 2; ++q) {
+      float lo = 0.f, hi = 0.f;
+      if (state && slot >= 0 && active && k <= L) {
+        const uint16_t* s0 = state + (slot * D + d0 + 2 * q) * L + (L - k);
+        lo = bf16_to_f32(s0[0]);
+        hi = bf16_to_f32(s0[L]);
+      }
+      h[k - 1][q] = f2_pack(lo, hi);
+    }
+}
 
 // Taps of one lane, as fp32 pairs, HALVED: tap[k][p] = w[d, W-1-k] / 2 multiplies x[t-k]
 // for channels (d0 + 2p, d0 + 2p + 1), zero for k >= W (a narrow W is the width-4 case with

@@ -14,6 +14,11 @@ training-shaped workloads; state, x ring, slot permutation, w, bias for the deco
   state  ~ N(0, 1)          decode state pool, [S, D, W-1]
   state_indices              the first N entries of a random permutation of range(S)
 
+Packed sequences (``varlen_inputs``): lengths from ``seqlen_mix`` -- log-uniform weights
+over a 32x range, scaled to the requested total (a ragged mix of long and short sequences;
+the caller may add empty and one-row sequences explicitly), then x, dy ~ N(0,1) [total, D],
+w, bias as above, initial states ~ N(0,1) [nseq, D, W-1], drawn in that order.
+
 The shapes follow the production call of the kernel-fun cconv package (B=16 T=8192 D=2048
 W=4, bf16 x / fp32 weight; kernel-fun 0.2.0.dev1 wheel, kernel_fun/cconv/__init__.py) and
 the decode batch of the cuDNN decode-update PR; there is no dataset behind either.
@@ -82,3 +87,42 @@ def decode_inputs(S: int, N: int, D: int, W: int, bias: bool = True, n_x: int = 
     w = (torch.rand(D, W, generator=g) - 0.5).to(wdtype)
     b = ((torch.rand(D, generator=g) - 0.5) * 0.2).to(wdtype) if bias else None
     return state, x, idx, w, b
+
+
+def seqlen_mix(total: int, nseq: int, seed: int = 0, spread: float = 32.0) -> list[int]:
+    """nseq lengths summing to total, log-uniform over a `spread`-fold range (each >= 1
+    when total >= nseq)."""
+    g = torch.Generator().manual_seed(seed)
+    wts = torch.exp(torch.rand(nseq, generator=g, dtype=torch.float64) * float(torch.log(
+        torch.tensor(spread, dtype=torch.float64))))
+    raw = wts / wts.sum() * total
+    lens = [max(1, int(v)) if total >= nseq else int(v) for v in raw]
+    lens[-1] += total - sum(lens)
+    while lens[-1] < (1 if total >= nseq else 0):   # give rows back from the longest
+        k = max(range(nseq - 1), key=lambda i: lens[i])
+        lens[k] -= 1
+        lens[-1] += 1
+    return lens
+
+
+def cu_of(lengths) -> torch.Tensor:
+    """int32 row offsets [0, l0, l0+l1, ...] (CPU)."""
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def varlen_inputs(lengths, D: int, W: int, bias: bool = True, wdtype: torch.dtype = torch.float32,
+                  seed: int = 0):
+    """(x [total,D], dy [total,D] bf16, cu int32 [nseq+1], w, bias, initial state
+    [nseq,D,W-1] bf16), all on the CPU."""
+    g = torch.Generator().manual_seed(seed)
+    cu = cu_of(lengths)
+    total = int(cu[-1])
+    x = torch.randn(total, D, generator=g).to(torch.bfloat16)
+    dy = torch.randn(total, D, generator=g).to(torch.bfloat16)
+    w = (torch.rand(D, W, generator=g) - 0.5).to(wdtype)
+    b = ((torch.rand(D, generator=g) - 0.5) * 0.2).to(wdtype) if bias else None
+    init = torch.randn(len(lengths), D, W - 1, generator=g).to(torch.bfloat16)
+    return x, dy, cu, w, b, init

@@ -59,6 +59,12 @@ typedef enum {
   CCONV_F32 = 1
 } cconv_dtype;
 
+/* Activation applied to z (packed-sequence calls; the batched calls always apply SiLU). */
+typedef enum {
+  CCONV_ACT_SILU = 0,       /* y = z * sigmoid(z) */
+  CCONV_ACT_NONE = 1        /* y = z */
+} cconv_activation;
+
 typedef enum {
   CCONV_OK = 0,
   CCONV_ERR_NULL = -1,      /* a required pointer is NULL */
@@ -174,13 +180,97 @@ CCONV_API int cconv_bwd_noalloc(const void* x, int64_t sxb, int64_t sxt, const v
                                 const void* w, const void* bias, cconv_dtype wdt, int W,
                                 void* dx, void* dw, void* dbias, cconv_stream_t stream);
 
+/*
+ * Packed variable-length sequences with initial and final states.
+ * Sources: the keyword set of fla's causal_conv1d that the kernel-fun 0.2.0.dev1 wheel
+ * forwards (kernel_fun/_common/compat.py: initial_state, output_final_state, activation,
+ * cu_seqlens), and the full-sequence-to-decode state handoff named in "Add experimental
+ * causal conv1d decode update - #797" (NVIDIA/cudnn-frontend), whose decode state layout
+ * [.., D, W-1] the states here share, so a final state can be the decode pool itself.
+ *
+ * nseq sequences are packed along the rows of a [total, D] tensor: sequence i is rows
+ * [cu_seqlens[i], cu_seqlens[i+1]).  Inside a sequence the computation is the batched one,
+ * except that the W-1 rows before its first row are its initial state (entry j = row
+ * cu[i] - (W-1) + j, oldest first) instead of zeros, and the activation may be left out:
+ *
+ *   z[t,d]   = bias[d] + sum_{k<W} w[d, W-1-k] * xe[t-k, d]     xe: x extended by the state
+ *   y        = silu(z) (CCONV_ACT_SILU) or z (CCONV_ACT_NONE)
+ *   final[i][d][j] = xe[cu[i+1] - (W-1) + j, d]   (the state a decode update continues from)
+ *
+ *   cu_seqlens  int32[nseq+1] in DEVICE memory: cu[0] = 0, non-decreasing, cu[nseq] = total.
+ *           Empty sequences are allowed (their final state is their initial state).  The
+ *           host never reads it.  An ill-formed vector gives unspecified results, every
+ *           access still stays inside the buffers, and cconv_device_fault() then reports
+ *           bit 4.
+ *   x, dy   [total, D] bf16, row t at x + t*sxt (sxt a positive multiple of 8, ignored when
+ *           total == 1), 16-byte aligned.  total may be 0 (x, dy, y, dx may then be NULL).
+ *   states  bf16 arrays of S slots x [D, W-1], contiguous, 16-byte aligned (forward) or
+ *           2-byte aligned (backward).  Ignored when W == 1.
+ *   1 <= nseq < 2^31 - 1, total < 2^31 - 16, D % 8 == 0.
+ */
+
+/*
+ * cconv_fwd_varlen -- forward over packed sequences.  One stream kernel, plus a small state
+ * kernel when final_state or state_indices is given; both on `stream`.
+ *
+ *   initial_state  [S, D, W-1] bf16, or NULL (every sequence starts from zeros).
+ *   final_state    [S, D, W-1] bf16 output, or NULL.  May be the same array as
+ *                  initial_state: the final states are written after every initial state
+ *                  has been read (chunked prefill into a decode pool, in place).
+ *   state_indices  int32[nseq] in device memory, or NULL: sequence i's state lives in slot
+ *                  state_indices[i] (else slot i, and S >= nseq).  With indices,
+ *                  1 <= S <= CCONV_UPDATE_MAX_SLOTS, status_dev is required, and the
+ *                  indices are validated on the device as cconv_update does (negative, >= S,
+ *                  repeated): on an invalid vector no state is written, status_dev gets
+ *                  [CCONV_ERR_INDEX, offence bits], and y is computed with zero initial
+ *                  states for the unusable slots.  Otherwise status_dev gets [CCONV_OK, 0].
+ *   status_dev     int32[2] in device memory (only written when state_indices is given).
+ *   y              [total, D] bf16 contiguous output, 16-byte aligned.
+ * final_state must not overlap x or y; y must not overlap x.
+ */
+CCONV_API int cconv_fwd_varlen(const void* x, int64_t total, int64_t D, int64_t sxt,
+                               const int32_t* cu_seqlens, int64_t nseq, const void* w,
+                               const void* bias, cconv_dtype wdt, int W, cconv_activation act,
+                               const void* initial_state, void* final_state,
+                               const int32_t* state_indices, int64_t S, int32_t* status_dev,
+                               void* y, cconv_stream_t stream);
+
+/* Workspace cconv_bwd_varlen needs on the current device (0 <= total < 2^31 - 16). */
+CCONV_API int cconv_bwd_varlen_workspace_bytes(int64_t total, int64_t D, int W, size_t* bytes);
+
+/*
+ * cconv_bwd_varlen -- backward over packed sequences: dx, dw, dbias and the gradient of
+ * the initial states, with z recomputed (two kernels on `stream`, deterministic).
+ *
+ *   g = dy * silu'(z) (CCONV_ACT_SILU) or dy (CCONV_ACT_NONE)
+ *   dx[t]          = sum_{k<W} w[d, W-1-k] g[t+k]   over t+k inside t's sequence
+ *   dw[d, W-1-k]   = sum over all rows t of g[t] * xe[t-k]
+ *   dbias[d]       = sum of g
+ *   d_initial_state[i][d][j] = sum_{k<W} w[d, W-1-k] g[u+k] over u+k inside sequence i,
+ *                              u = cu[i] - (W-1) + j   (zero for an empty sequence)
+ *
+ *   initial_state    [nseq, D, W-1] bf16 or NULL (zeros); slot i is sequence i.
+ *   dx               [total, D] bf16 contiguous, 16-byte aligned, overlapping neither x nor dy.
+ *   dw, dbias        as cconv_bwd (dbias may be NULL).
+ *   d_initial_state  [nseq, D, W-1] bf16 output, or NULL.
+ *   workspace        at least cconv_bwd_varlen_workspace_bytes(total, D, W), 16-byte
+ *                    aligned (unused when total == 0).
+ */
+CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64_t sdt,
+                               int64_t total, int64_t D, const int32_t* cu_seqlens,
+                               int64_t nseq, const void* w, const void* bias, cconv_dtype wdt,
+                               int W, cconv_activation act, const void* initial_state,
+                               void* dx, void* dw, void* dbias, void* d_initial_state,
+                               void* workspace, size_t workspace_bytes, cconv_stream_t stream);
+
 /* Human-readable name of a cconv_status value (static storage). */
 CCONV_API const char* cconv_status_str(int status);
 
 /*
  * cconv_device_fault -- reads (and clears) the library's device fault word on the current
- * device after synchronising it.  *fault = 0 when no kernel has given up a bounded wait;
- * otherwise a nonzero code naming the kernel.  Returns CCONV_OK or CCONV_ERR_CUDA.
+ * device after synchronising it.  *fault = 0 when nothing went wrong; otherwise an OR of:
+ * 1 = a forward kernel gave up a bounded wait, 2 = a backward kernel did, 4 = an ill-formed
+ * cu_seqlens was passed to a packed-sequence call.  Returns CCONV_OK or CCONV_ERR_CUDA.
  */
 CCONV_API int cconv_device_fault(int32_t* fault);
 

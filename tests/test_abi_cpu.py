@@ -23,7 +23,8 @@ def test_exports_match_header(lib):
     declared = cc.header_functions()
     assert set(declared) == {"cconv_fwd", "cconv_bwd_workspace_bytes", "cconv_bwd",
                              "cconv_bwd_noalloc", "cconv_update", "cconv_status_str",
-                             "cconv_device_fault"}
+                             "cconv_device_fault", "cconv_fwd_varlen",
+                             "cconv_bwd_varlen_workspace_bytes", "cconv_bwd_varlen"}
     for name in declared:
         assert hasattr(lib, name), f"{name} declared in cconv.h but not exported"
 
@@ -98,3 +99,39 @@ def _upd(lib, x=P, N=4, D=64, ldx=64, state=P, S=8, idx=P, w=P, bias=None, wdt=F
 ])
 def test_update_rejects(lib, kw, expect):
     assert _upd(lib, **kw) == expect
+
+
+def _fwdv(lib, x=P, total=64, D=64, sxt=64, cu=P, nseq=2, w=P, bias=None, wdt=F32, W=4, act=0,
+          init=None, fin=None, idx=None, S=2, status=None, y=P):
+    return lib.cconv_fwd_varlen(x, total, D, sxt, cu, nseq, w, bias, wdt, W, act, init, fin, idx,
+                                S, status, y, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(cu=None), ENULL), (dict(w=None), ENULL), (dict(x=None), ENULL), (dict(y=None), ENULL),
+    (dict(W=0), EWIDTH), (dict(wdt=5), EDTYPE), (dict(act=2), ESHAPE), (dict(nseq=0), ESHAPE),
+    (dict(total=-1), ESHAPE), (dict(total=1 << 31), ESHAPE), (dict(D=0), ESHAPE),
+    (dict(D=60, sxt=64), EALIGN), (dict(cu=P + 2), EALIGN), (dict(x=P + 2), EALIGN),
+    (dict(y=P + 4), EALIGN), (dict(sxt=0), ESTRIDE), (dict(sxt=12), EALIGN),
+    (dict(fin=P, S=1), ESHAPE), (dict(init=P + 8), EALIGN), (dict(fin=P + 2), EALIGN),
+    (dict(idx=P), ENULL), (dict(idx=P, status=P, S=0), ESHAPE),
+    (dict(idx=P, status=P, S=393217), ESHAPE), (dict(idx=P + 1, status=P), EALIGN),
+])
+def test_fwd_varlen_rejects(lib, kw, expect):
+    assert _fwdv(lib, **kw) == expect
+
+
+def _bwdv(lib, x=P, sxt=64, dy=P, sdt=64, total=64, D=64, cu=P, nseq=2, w=P, bias=None,
+          wdt=F32, W=4, act=0, init=None, dx=P, dw=P, dbias=None, dinit=None, ws=P, wsb=1 << 30):
+    return lib.cconv_bwd_varlen(x, sxt, dy, sdt, total, D, cu, nseq, w, bias, wdt, W, act, init,
+                                dx, dw, dbias, dinit, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(cu=None), ENULL), (dict(dw=None), ENULL), (dict(dy=None), ENULL),
+    (dict(dx=None), ENULL), (dict(W=5), EWIDTH), (dict(wdt=9), EDTYPE), (dict(act=-1), ESHAPE),
+    (dict(nseq=0), ESHAPE), (dict(D=20), EALIGN), (dict(sdt=-64), ESTRIDE),
+    (dict(dx=P + 8), EALIGN), (dict(dinit=P + 1), EALIGN), (dict(cu=P + 1), EALIGN),
+])
+def test_bwd_varlen_rejects(lib, kw, expect):
+    assert _bwdv(lib, **kw) == expect
