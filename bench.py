@@ -59,6 +59,12 @@ DEC_BYTES = (2 * DEC.N * DEC.D                # x read
              + 2 * 2 * DEC.N * DEC.D * (DEC.W - 1)  # named state rows read + written
              + 2 * DEC.N * DEC.D)             # y written
 STEP_BYTES = FWD_BYTES + BWD_BYTES + DEC_BYTES
+# Packed sequences at the production row count: 16 mixed lengths, initial states in, final
+# states out (forward), initial-state gradient out (backward).
+VL_NSEQ = 16
+VL_STATE_BYTES = 2 * VL_NSEQ * FWD.D * (FWD.W - 1)
+VL_FWD_BYTES = FWD_BYTES + 2 * VL_STATE_BYTES    # + initial states read, final written
+VL_BWD_BYTES = BWD_BYTES + 2 * VL_STATE_BYTES    # + initial states read, gradient written
 LAUNCHES_PER_STEP = 4                        # fwd, bwd stream, bwd reduce, update
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel (the
@@ -301,6 +307,36 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     dec_graph_us = ga.elapsed_time(gb) * 1e3 / (reps * DEC.steps)
 
+    # ---- packed sequences: same rows, 16 mixed lengths, with states ------------------------
+    lens = inputs.seqlen_mix(FWD.B * FWD.T, VL_NSEQ, seed=rank)
+    vx, vdy, vcu, vw, _, vinit = inputs.varlen_inputs(lens, FWD.D, FWD.W, bias=False, seed=rank)
+    vxs = [vx.to(dev) for _ in range(NSET)]
+    vdys = [vdy.to(dev) for _ in range(NSET)]
+    vinits = [vinit.to(dev) for _ in range(NSET)]
+    vcu, vw = vcu.to(dev), vw.to(dev)
+    vfin = torch.empty_like(vinits[0])
+    vdinit = torch.empty_like(vinits[0])
+    vws = torch.empty(cc.cconv_bwd_varlen_workspace_bytes(FWD.B * FWD.T, FWD.D, FWD.W),
+                      dtype=torch.uint8, device=dev)
+
+    def vfwd(i):
+        k = i % NSET
+        cc.cconv_fwd_varlen(vxs[k], vcu, vw, None, initial_state=vinits[k], final_state=vfin,
+                            y=ys[k].view(-1, FWD.D), stream=stream)
+
+    def vbwd(i):
+        k = i % NSET
+        cc.cconv_bwd_varlen(vxs[k], vdys[k], vcu, vw, None, initial_state=vinits[k],
+                            want_dbias=False, dx=dxs[k].view(-1, FWD.D), dw=dw,
+                            d_initial_state=vdinit, workspace=vws, stream=stream)
+
+    for fn in (vfwd, vbwd):
+        for i in range(3):
+            fn(i)
+    vf_us = loop_us(vfwd, K)
+    vb_us = loop_us(vbwd, K)
+    del vxs, vdys
+
     # ---- end to end through the public API with host buffers ------------------------------
     e2e = run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
 
@@ -343,6 +379,16 @@ def run_ours(args, world, rank, local):
             "decode_update": {"us_per_step_stream": round(u_us, 3),
                               "us_per_step_graph": round(dec_graph_us, 3),
                               "bytes_per_step": DEC_BYTES},
+            "fwd_varlen": {"us": round(vf_us, 3),
+                           "tbps": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e12, 4),
+                           "frac_of_peak": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e9 / peak_gbs, 4),
+                           "note": f"{VL_NSEQ} packed sequences of mixed lengths, same rows; "
+                                   "initial states in, final states out (stream + state kernel)"},
+            "bwd_varlen": {"us": round(vb_us, 3),
+                           "tbps": round(VL_BWD_BYTES / (vb_us * 1e-6) / 1e12, 4),
+                           "frac_of_peak": round(VL_BWD_BYTES / (vb_us * 1e-6) / 1e9 / peak_gbs, 4),
+                           "note": "same packing; initial states in, their gradient out "
+                                   "(stream + reduction kernel)"},
         },
         "roofline": {
             "kernel": "cconv_bwd (stream + reduction)",

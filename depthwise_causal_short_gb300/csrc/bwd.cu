@@ -288,9 +288,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
         h[j][q] = 0ull;
         gr[j][q] = 0ull;
       }
-    f2 hin[3][P];  // packed sequences: the x ring the current segment starts from
+    // Packed sequences: hin holds the initial x ring of sequence hin_seq, fetched one
+    // sequence ahead so that its loads overlap the rows before it.
+    f2 hin[3][P];
+    int hin_seq = -1;
     if constexpr (VL) {
-      if (!cc.done && cc.from == cc.ss) init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
+      if (!cc.done && cc.from == cc.ss) {
+        init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
+        hin_seq = cc.i;
+      }
     }
 
     uint32_t parity = 0;
@@ -309,6 +315,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       const uint8_t* xt = stages + s * STAGE;
       if constexpr (VL) {
         if (cc.first && cc.from == cc.ss) {  // the segment starts its sequence's rings
+          if (hin_seq != cc.i) init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
 #pragma unroll
           for (int q = 0; q < P; ++q)
 #pragma unroll
@@ -316,6 +323,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
               h[j][q] = hin[j][q];
               gr[j][q] = 0ull;
             }
+          hin_seq = -1;
+          if (cc.se < cc.r1 && cc.i + 1 < p.nseq) {  // the next sequence starts in range
+            init_ring<VEC>(p.init, cc.i + 1, p.D, p.W, d0, active, hin);
+            hin_seq = cc.i + 1;
+          }
         }
       }
       if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
@@ -335,10 +347,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
         pc.advance();
       }
       cc.advance();
-      if constexpr (VL) {
-        if (!cc.done && cc.first && cc.from == cc.ss)
-          init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
-      }
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }

@@ -42,6 +42,7 @@ struct FwdArgs {
   const int32_t* cu;        // [nseq + 1] row offsets
   const uint16_t* init;     // [S, D, W-1] initial states, or null (zeros)
   const int32_t* idx;       // [nseq] slot of each sequence, or null (slot i)
+  uint16_t* fin;            // [nseq, D, W-1] final states written by this kernel, or null
   int64_t S;
   int nseq;
 };
@@ -78,10 +79,10 @@ __device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
 
 // Rows of one tile for this lane.  FULL: every row lies inside the segment.  Otherwise rows
 // before `from` were done with the previous tile, rows before a only fill the ring, and rows
-// from e on are not needed.  STORE: this lane's channels exist (every lane of a CTA whose
-// channel group lies inside D), so stores need no per-row test.  The output row pointer
-// advances by D per row.
-template <int VEC, int R, bool FULL, bool STORE, bool ACT, class Cursor>
+// from e on are not needed (VL: not even pushed, so the ring ends on the segment's last row).
+// STORE: this lane's channels exist (every lane of a CTA whose channel group lies inside D),
+// so stores need no per-row test.  The output row pointer advances by D per row.
+template <int VEC, int R, bool FULL, bool STORE, bool ACT, bool VL, class Cursor>
 __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Cursor& c,
                                          bool active, const FwdArgs& p, int64_t d0,
                                          const f2 (&tap)[4][VEC / 2], const f2 (&bias2)[VEC / 2],
@@ -100,7 +101,7 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Cu
         fwd_row<P, ACT>(x, h, tap, bias2, yv);
         if (STORE || active) store_row<VEC>(yrow, yv);
       }
-      ring_push<P>(h, x);
+      if (!VL || FULL || t < c.e) ring_push<P>(h, x);
     }
     yrow += p.D;
   }
@@ -136,6 +137,41 @@ __device__ __forceinline__ void check_seqlens(const int32_t* cu, int nseq, int t
       bad = true;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(fault, kFaultSeqlens);
+}
+
+// Final state of sequence i from the ring after its last row: entry j (row se - (W-1) + j)
+// is h[W-2-j].  The ring holds exact bf16 values, so the conversion back is exact.
+template <int VEC>
+__device__ __forceinline__ void store_final(uint16_t* fin, int64_t i, int64_t D, int W,
+                                            int64_t d0, const f2 (&h)[3][VEC / 2]) {
+  const int L = W - 1;
+  uint16_t* o = fin + (i * D + d0) * L;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    if (k >= L) break;
+    const int j = L - 1 - k;
+#pragma unroll
+    for (int q = 0; q < VEC / 2; ++q) {
+      float lo, hi;
+      f2_unpack(h[k][q], lo, hi);
+      o[(2 * q) * L + j] = f32_to_bf16(lo);
+      o[(2 * q + 1) * L + j] = f32_to_bf16(hi);
+    }
+  }
+}
+
+// Final states of empty sequences (their initial state, or zeros) for sequences
+// i = first, first + step, ...: one warp, 16-byte copies.
+__device__ __forceinline__ void final_of_empty(const FwdArgs& p, int first, int step, int lane) {
+  const int64_t n16 = p.D * (p.W - 1) / 8;  // uint4 per sequence
+  for (int i = first; i < p.nseq; i += step) {
+    if (clamp_row(p.cu[i + 1], p.BT) > clamp_row(p.cu[i], p.BT)) continue;
+    uint4* o = reinterpret_cast<uint4*>(p.fin + static_cast<int64_t>(i) * p.D * (p.W - 1));
+    const uint4* src = p.init ? reinterpret_cast<const uint4*>(
+                                    p.init + static_cast<int64_t>(i) * p.D * (p.W - 1))
+                              : nullptr;
+    for (int64_t k = lane; k < n16; k += 32) o[k] = src ? src[k] : make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile).
@@ -208,6 +244,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     if constexpr (VL) {
       __syncwarp();
       if (blockIdx.x == 0) check_seqlens(p.cu, p.nseq, p.BT, lane, &g_fault_fwd);
+      if (p.fin) final_of_empty(p, blockIdx.x, gridDim.x, lane);
     }
   } else if (warp < nact) {
     // ---- consumer ------------------------------------------------------------------------
@@ -229,10 +266,15 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     for (int j = 0; j < 3; ++j)
 #pragma unroll
       for (int q = 0; q < VEC / 2; ++q) h[j][q] = 0ull;
-    f2 hin[3][VEC / 2];  // packed sequences: the ring the current segment starts from
+    // Packed sequences: hin holds the initial ring of sequence hin_seq, fetched one sequence
+    // ahead so that its loads overlap the rows before it.
+    f2 hin[3][VEC / 2];
+    int hin_seq = -1;
     if constexpr (VL) {
-      if (!cur.done && cur.from == cur.ss)
+      if (!cur.done && cur.from == cur.ss) {
         init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
+        hin_seq = cur.i;
+      }
     }
 
     uint32_t fph = 0, eph = 0;
@@ -248,19 +290,30 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
       const uint8_t* tile = smem + s * STAGE + warp * TILE;
       if constexpr (VL) {
         if (cur.first && cur.from == cur.ss) {  // the segment starts its sequence's ring
+          if (hin_seq != cur.i) init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
 #pragma unroll
           for (int j = 0; j < 3; ++j)
 #pragma unroll
             for (int q = 0; q < VEC / 2; ++q) h[j][q] = hin[j][q];
+          hin_seq = -1;
+          if (cur.se < cur.r1 && cur.i + 1 < p.nseq) {  // the next sequence starts in range
+            init_ring<VEC>(p.init, seq_slot(p, cur.i + 1), p.D, p.W, d0, active, hin);
+            hin_seq = cur.i + 1;
+          }
         }
       }
       if (cur.from == cur.tt && cur.tt >= cur.a && cur.tt + R <= cur.e) {
         if (all_active)
-          fwd_tile<VEC, R, true, true, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
+          fwd_tile<VEC, R, true, true, ACT, VL>(tile, lane, cur, active, p, d0, tap, bias2, h);
         else
-          fwd_tile<VEC, R, true, false, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
+          fwd_tile<VEC, R, true, false, ACT, VL>(tile, lane, cur, active, p, d0, tap, bias2, h);
       } else {
-        fwd_tile<VEC, R, false, false, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
+        fwd_tile<VEC, R, false, false, ACT, VL>(tile, lane, cur, active, p, d0, tap, bias2, h);
+      }
+      if constexpr (VL) {
+        // The tile held the last row of a sequence that ends in this range.
+        if (p.fin && cur.e == cur.se && cur.tt + R >= cur.e && active)
+          store_final<VEC>(p.fin, cur.i, p.D, p.W, d0, h);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -280,11 +333,6 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
         if (!__all_sync(0xffffffffu, fine)) break;
       }
       cur.advance();
-      if constexpr (VL) {
-        // A new segment: fetch its initial ring now, so the loads overlap the next wait.
-        if (!cur.done && cur.first && cur.from == cur.ss)
-          init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
-      }
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }
@@ -386,7 +434,13 @@ __global__ void __launch_bounds__(kStateThreads) cconv_fwd_state_kernel(const St
       } else {
         const int jj = u - (ss - L);  // entry of the initial state, 0 <= jj < L
 #pragma unroll
-        for (int c = 0; c < 8; ++c) oh[c * L + j] = sh[c * L + jj];
+        for (int c = 0; c < 8; ++c) {
+          uint16_t v = 0;
+#pragma unroll
+          for (int m = 0; m < L; ++m)  // select in registers (no local-memory indexing)
+            if (m == jj) v = sh[c * L + m];
+          oh[c * L + j] = v;
+        }
       }
     }
     uint4* dst = reinterpret_cast<uint4*>(p.fin + (slot * p.D + d0) * L);
@@ -537,6 +591,15 @@ extern "C" CCONV_API int cconv_fwd_varlen(const void* x, int64_t total, int64_t 
                  (final_state && reinterpret_cast<uintptr_t>(final_state) % 16 != 0)))
     return CCONV_ERR_ALIGN;
 
+  // Dense final states that do not overlap the initial states are written by the stream
+  // kernel itself, from its register ring; slots picked by state_indices (validated first)
+  // or states updated in place need the second kernel, which runs after every read.
+  const size_t state_bytes = static_cast<size_t>(nseq) * D * (L > 0 ? L : 1) * 2;
+  const uintptr_t ib = reinterpret_cast<uintptr_t>(initial_state);
+  const uintptr_t fb = reinterpret_cast<uintptr_t>(final_state);
+  const bool overlap = initial_state && final_state && ib < fb + state_bytes && fb < ib + state_bytes;
+  const bool fused_final = L > 0 && final_state && !state_indices && !overlap && total > 0;
+
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (total > 0) {
     int sms = 0;
@@ -562,6 +625,7 @@ extern "C" CCONV_API int cconv_fwd_varlen(const void* x, int64_t total, int64_t 
     a.cu = cu_seqlens;
     a.init = L > 0 ? static_cast<const uint16_t*>(initial_state) : nullptr;
     a.idx = state_indices;
+    a.fin = fused_final ? static_cast<uint16_t*>(final_state) : nullptr;
     a.S = state_indices ? S : nseq;
     a.nseq = static_cast<int>(nseq);
     auto kern = kFwdVarlenKernels[act == CCONV_ACT_NONE ? 1 : 0];
@@ -572,7 +636,7 @@ extern "C" CCONV_API int cconv_fwd_varlen(const void* x, int64_t total, int64_t 
         cudaSuccess)
       return CCONV_ERR_CUDA;
   }
-  if ((L > 0 && final_state) || state_indices) {
+  if ((L > 0 && final_state && !fused_final) || state_indices) {
     int sms = 0;
     rc = sm_count_current_device(&sms, nullptr);
     if (rc != CCONV_OK) return rc;

@@ -149,6 +149,7 @@ struct SeqCursor {
   int nseq, total, r1;
   int i;          // current sequence
   int ss, se;     // its rows, clamped to [0, total]
+  int nse;        // end of sequence i + 1 (loaded one sequence ahead), or total
   int a, e;       // current segment
   int tt, from;   // current tile
   int b;          // always 0: rows are packed
@@ -167,10 +168,11 @@ struct SeqCursor {
     }
   }
 
+  // Segment of sequence i from row a, given its rows [ss, se).  The next sequence's end is
+  // requested now and only needed at the next boundary, so crossing one waits on no load.
   __device__ __forceinline__ void begin_segment() {
-    ss = ld(i);
-    se = ld(i + 1);
     if (se < ss) se = ss;
+    nse = i + 2 <= nseq ? ld(i + 2) : total;
     e = se < r1 ? se : r1;
     if (e < a) e = a;
     place(a - kRing);
@@ -191,23 +193,34 @@ struct SeqCursor {
     done = r0 >= r1_ || nseq_ < 1;
     i = done ? 0 : find_seq(cu_, nseq_, total_, r0, lane);
     a = r0;
-    if (!done) begin_segment();
+    if (!done) {
+      ss = ld(i);
+      se = ld(i + 1);
+      begin_segment();
+    }
   }
 
   __device__ __forceinline__ void advance() {
     const int next = tt + R;
     if (next >= e + tail) {
-      if (e >= r1) {
+      if (e >= r1 || i + 1 >= nseq) {
         done = true;
         return;
       }
+      // Sequence i + 1 normally starts where this segment ended; step over empty ones.
       int j = i + 1;
-      while (j < nseq && ld(j + 1) <= e) ++j;  // step over sequences that end here
-      if (j >= nseq) {
+      int je = nse;
+      while (je <= e && j + 1 < nseq) {
+        ++j;
+        je = ld(j + 1);
+      }
+      if (je <= e) {
         done = true;
         return;
       }
+      ss = (j == i + 1) ? se : ld(j);
       i = j;
+      se = je;
       a = e;
       begin_segment();
       return;

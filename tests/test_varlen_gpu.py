@@ -179,6 +179,22 @@ def test_pool_in_place_and_decode_handoff():
     assert np.array_equal(bits(pool_g[idx_g.long()]), _bits64(rfin2)), "state after decode"
 
 
+def test_dense_in_place():
+    """initial_state and final_state the same dense array (no indices): the final states are
+    written by the second kernel after every read of the initial ones."""
+    lens = _lengths(2000, 9, seed=11)
+    x, dy, cu, w, b, init = inputs.varlen_inputs(lens, 512, 4, bias=True, seed=11)
+    st = init.cuda()
+    y, fin, _ = cc.cconv_fwd_varlen(x.cuda(), cu.cuda(), w.cuda(), b.cuda(), initial_state=st,
+                                    final_state=st)
+    torch.cuda.synchronize()
+    assert fin is st
+    ry, rfin = oracle.fwd_seq(f64(x), cu.numpy(), f64(w), f64(b), f64(init), "silu",
+                              want_final=True)
+    assert rel_err(f64(y), ry) <= FWD_TOL
+    assert np.array_equal(bits(st), _bits64(rfin))
+
+
 @pytest.mark.parametrize("bad,mask", [([0, -1, 2], 1), ([0, 5, 2], 2), ([3, 1, 3], 4)])
 def test_invalid_state_indices_fail_closed(bad, mask):
     D, W, S = 256, 4, 5
