@@ -54,6 +54,11 @@ class Oracle:
         lib.oracle_validate.restype = ctypes.c_int
         lib.oracle_update.argtypes = [_I64, _I64, ctypes.c_int, _P, _P, _I64, _P, _P, _P, _P]
         lib.oracle_update.restype = ctypes.c_int
+        lib.oracle_validate_pad.argtypes = [_I64, _I64, _P, ctypes.c_int]
+        lib.oracle_validate_pad.restype = ctypes.c_int
+        lib.oracle_update_ex.argtypes = [_I64, _I64, ctypes.c_int, ctypes.c_int, _P, _P, _I64, _P,
+                                         ctypes.c_int, _P, _P, ctypes.c_int, _P]
+        lib.oracle_update_ex.restype = ctypes.c_int
         lib.oracle_fwd_seq.argtypes = [_I64, _P, _I64, ctypes.c_int, _P, _P, _P, _P, ctypes.c_int,
                                        _P, _P]
         lib.oracle_fwd_seq.restype = ctypes.c_int
@@ -143,6 +148,31 @@ class Oracle:
             raise RuntimeError(f"oracle_update failed ({rc})")
         return rc, (y if rc == 0 else None), st
 
+    def validate_pad(self, idx, S: int, pad: bool) -> int:
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        return int(self.lib.oracle_validate_pad(idx.size, S, self._ptr(idx), int(pad)))
+
+    def update_ex(self, x_bits, state_bits, idx, w, bias=None, *, pad: bool = False,
+                  activation="silu"):
+        """General decode update: state [S, D, Ls] with Ls >= W-1 (its newest W-1 entries
+        feed the window); pad: index -1 marks a padding row (no state access, y row NaN);
+        activation 'silu' or None.  Returns (status, y, new_state) like update()."""
+        x = self._bits(x_bits)
+        N, D = x.shape
+        st = np.array(self._bits(state_bits), copy=True)
+        S, _, Ls = st.shape
+        w = self._f64(w)
+        W = w.shape[1]
+        b = self._f64(bias)
+        ix = None if idx is None else np.ascontiguousarray(idx, dtype=np.int32)
+        act = {"silu": 0, None: 1, "none": 1}[activation]
+        y = np.empty((N, D), np.float64)
+        rc = self.lib.oracle_update_ex(N, D, W, Ls, self._ptr(x), self._ptr(st), S,
+                                       self._ptr(ix), int(pad), self._ptr(w), self._ptr(b), act,
+                                       self._ptr(y))
+        if rc < 0:
+            raise RuntimeError(f"oracle_update_ex failed ({rc})")
+        return rc, (y if rc == 0 else None), st
 
     # -- packed sequences, initial / final state, activation ---------------------------------
     @staticmethod
@@ -225,6 +255,14 @@ def validate(*a, **k):
 
 def update(*a, **k):
     return get().update(*a, **k)
+
+
+def update_ex(*a, **k):
+    return get().update_ex(*a, **k)
+
+
+def validate_pad(*a, **k):
+    return get().validate_pad(*a, **k)
 
 
 def fwd_seq(*a, **k):

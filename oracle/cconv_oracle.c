@@ -311,3 +311,60 @@ int oracle_update(int64_t N, int64_t D, int W, const uint16_t* x, uint16_t* stat
   }
   return 0;
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Decode update, general form (the variants the cuDNN decode-update PR names): a state of
+ * Ls >= W-1 entries per channel whose newest W-1 feed the window (Ls = W keeps one older
+ * token); optional padding rows (pad != 0: an index of -1 marks a row that reads and writes
+ * no state and produces no output -- its y row is left NaN here); activation silu (act = 0)
+ * or none (act = 1).  Other negative, out-of-range or repeated indices fail closed as in
+ * oracle_update.  Returns 0, the offence mask (> 0, nothing written), or -1 on a bad shape.
+ * --------------------------------------------------------------------------------------- */
+int oracle_validate_pad(int64_t N, int64_t S, const int32_t* idx, int pad) {
+  int off = 0;
+  for (int64_t i = 0; i < N; ++i) {
+    const int32_t v = idx[i];
+    if (pad && v == -1) continue; /* a padding row */
+    if (v < 0) off |= ORACLE_IDX_NEGATIVE;
+    else if (v >= S) off |= ORACLE_IDX_OUT_OF_RANGE;
+    else
+      for (int64_t k = 0; k < i; ++k)
+        if (idx[k] == v) off |= ORACLE_IDX_DUPLICATE;
+  }
+  return off;
+}
+
+int oracle_update_ex(int64_t N, int64_t D, int W, int Ls, const uint16_t* x, uint16_t* state,
+                     int64_t S, const int32_t* idx, int pad, const double* w, const double* bias,
+                     int act, double* y) {
+  if (N < 0 || D < 0 || W < 1 || W > 8 || Ls < W - 1 || Ls > 8 || S < 0) return -1;
+  if (act != 0 && act != 1) return -1;
+  if (idx) {
+    const int off = oracle_validate_pad(N, S, idx, pad);
+    if (off) return off;
+  } else if (S < N) {
+    return -1;
+  }
+  uint16_t win[8];
+  for (int64_t i = 0; i < N; ++i) {
+    const int64_t slot = idx ? (int64_t)idx[i] : i;
+    if (idx && pad && idx[i] == -1) {
+      for (int64_t d = 0; d < D; ++d) y[i * D + d] = NAN;
+      continue;
+    }
+    if (slot < 0 || slot >= S) return -1; /* unreachable after a correct validation */
+    for (int64_t d = 0; d < D; ++d) {
+      uint16_t* cell = state + (slot * D + d) * Ls;
+      /* window: the newest W-1 state entries, then the token */
+      for (int j = 0; j < W - 1; ++j) win[j] = cell[Ls - (W - 1) + j];
+      win[W - 1] = x[i * D + d];
+      double zd = bias ? bias[d] : 0.0;
+      for (int j = 0; j < W; ++j) zd += w[d * W + j] * bf16_to_double(win[j]);
+      y[i * D + d] = act == 0 ? silu(zd) : zd;
+      /* the state drops its oldest entry and takes the token */
+      for (int j = 0; j + 1 < Ls; ++j) cell[j] = cell[j + 1];
+      if (Ls > 0) cell[Ls - 1] = x[i * D + d];
+    }
+  }
+  return 0;
+}

@@ -464,6 +464,90 @@ def pin_act_none_linear(o):
     _close(dxa, dxb, 0.0, "act=None: dx independent of x")
 
 
+# ---------------------------------------------------------------------------------------
+# general decode update: longer state, padding rows, activation
+# ---------------------------------------------------------------------------------------
+
+def pin_update_ex_state_lengths(o):
+    """Single-token updates from a zero state of Ls >= W-1 entries reproduce every row of the
+    forward, and leave the last Ls tokens in the state (oldest first), bit for bit."""
+    rng = _rng(14)
+    for W, Ls, T in ((4, 4, 9), (4, 3, 7), (3, 5, 4), (2, 2, 6), (1, 1, 3), (1, 0, 2)):
+        N, D, S = 2, 3, 4
+        x = _bf16_values(rng, (N, T, D))
+        w = rng.uniform(-0.5, 0.5, (D, W))
+        bias = rng.uniform(-0.1, 0.1, D)
+        for act in ("silu", None):
+            y_full = o.fwd_seq(x.reshape(N * T, D), np.arange(N + 1) * T, w, bias, None, act)
+            y_full = y_full.reshape(N, T, D)
+            idx = np.array([3, 1], np.int32)
+            state = np.zeros((S, D, Ls), np.uint16)
+            xb = _bf16_bits(x)
+            for t in range(T):
+                status, y, state = o.update_ex(xb[:, t, :], state, idx, w, bias, activation=act)
+                assert status == 0
+                _close(y, y_full[:, t, :], 1e-15, f"W={W} Ls={Ls} act={act} step {t}")
+            for n in range(N):
+                expect = np.zeros((D, Ls), np.uint16)
+                for j in range(Ls):
+                    t = T - Ls + j
+                    if t >= 0:
+                        expect[:, j] = xb[n, t, :]
+                assert np.array_equal(state[idx[n]], expect), f"W={W} Ls={Ls}: final state"
+
+
+def pin_update_ex_is_update(o):
+    """Ls = W-1, no padding, SiLU: the general form is the plain decode update."""
+    rng = _rng(15)
+    S, N, D, W = 7, 4, 5, 4
+    state = _bf16_bits(_bf16_values(rng, (S, D, W - 1)))
+    x = _bf16_bits(_bf16_values(rng, (N, D)))
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    bias = rng.uniform(-0.1, 0.1, D)
+    for idx in (np.array([6, 0, 3, 2], np.int32), None, np.array([1, -1, 2, 3], np.int32)):
+        a = o.update(x, state, idx, w, bias)
+        b = o.update_ex(x, state, idx, w, bias)
+        assert a[0] == b[0] and np.array_equal(a[2], b[2])
+        if a[0] == 0:
+            _close(b[1], a[1], 0.0, "update_ex vs update")
+
+
+def _validate_pad_by_sets(idx, S, pad):
+    live = [v for v in idx if not (pad and v == -1)]
+    return _validate_by_sets(live, S)
+
+
+def pin_validate_pad_exhaustive(o):
+    for S in range(0, 4):
+        for N in range(0, 4):
+            for idx in itertools.product(range(-2, S + 2), repeat=N):
+                for pad in (False, True):
+                    got = o.validate_pad(np.array(idx, np.int32), S, pad)
+                    assert got == _validate_pad_by_sets(idx, S, pad), f"{idx} S={S} pad={pad}"
+
+
+def pin_update_ex_padding_rows(o):
+    """Padding rows (index -1) read and write no state and give no output; the other rows
+    are exactly the update without them."""
+    rng = _rng(16)
+    S, D, W, Ls = 6, 4, 4, 4
+    state = _bf16_bits(_bf16_values(rng, (S, D, Ls)))
+    x = _bf16_bits(_bf16_values(rng, (5, D)))
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    idx = np.array([2, -1, 5, -1, 0], np.int32)
+    status, y, st = o.update_ex(x, state, idx, w, None, pad=True)
+    assert status == 0
+    live = idx >= 0
+    status2, y2, st2 = o.update_ex(x[live], state, idx[live], w, None)
+    assert status2 == 0
+    assert np.array_equal(st, st2), "padding rows changed the pool"
+    _close(y[live], y2, 0.0, "rows beside padding rows")
+    assert np.all(np.isnan(y[~live])), "padding rows produced output"
+    # without the padding mode, -1 is a negative index and the call fails closed
+    status3, y3, st3 = o.update_ex(x, state, idx, w, None, pad=False)
+    assert status3 == 1 and y3 is None and np.array_equal(st3, state)
+
+
 ALL_PINS = [
     pin_fwd_lfilter,
     pin_fwd_bwd_torch,
@@ -481,4 +565,8 @@ ALL_PINS = [
     pin_seq_decode_handoff,
     pin_seq_equal_lengths_batch,
     pin_act_none_linear,
+    pin_update_ex_state_lengths,
+    pin_update_ex_is_update,
+    pin_validate_pad_exhaustive,
+    pin_update_ex_padding_rows,
 ]

@@ -45,6 +45,14 @@ MUTANTS = {
     "seq_dinit_window": ("if (u + k >= s && u + k < e) ai", "if (u + k > s && u + k < e) ai"),
     "act_none_ignored_fwd": ("y[t * D + d] = act == 0 ? silu(zs) : zs;", "y[t * D + d] = silu(zs);"),
     "act_none_ignored_bwd": ("if (act == 0) {\n          const double zv", "if (1) {\n          const double zv"),
+    # general decode update
+    "upd_ex_window_oldest": ("win[j] = cell[Ls - (W - 1) + j];", "win[j] = cell[j];"),
+    "upd_ex_no_shift": ("cell[j] = cell[j + 1];", "cell[j] = cell[j];"),
+    "upd_ex_pad_not_skipped_validate": ("if (pad && v == -1) continue;", "if (pad && v == -2) continue;"),
+    "upd_ex_pad_not_skipped_update": ("if (idx && pad && idx[i] == -1) {", "if (idx && pad && idx[i] == -2) {"),
+    "upd_ex_act_ignored": ("y[i * D + d] = act == 0 ? silu(zd) : zd;", "y[i * D + d] = silu(zd);"),
+    "upd_ex_no_duplicates": ("if (idx[k] == v) off |= ORACLE_IDX_DUPLICATE;",
+                             "if (idx[k] == v && 0) off |= ORACLE_IDX_DUPLICATE;"),
 }
 
 
