@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     cconv_fwd_varlen,
     cconv_status_str,
     cconv_update,
+    cconv_update_ex,
     header_functions,
     lib_path,
     load,

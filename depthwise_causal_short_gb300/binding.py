@@ -79,6 +79,9 @@ def load(path: str | Path | None = None):
     lib.cconv_bwd_varlen.argtypes = [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _INT, _INT,
                                      _INT, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.cconv_bwd_varlen.restype = _INT
+    lib.cconv_update_ex.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _P, _INT,
+                                    _INT, _INT, _P, _P, _P]
+    lib.cconv_update_ex.restype = _INT
     lib.cconv_status_str.argtypes = [_INT]
     lib.cconv_status_str.restype = ctypes.c_char_p
     lib.cconv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -340,6 +343,34 @@ def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "cconv_bwd_varlen")
     return dx, dw, (dbias if want_dbias else None), (d_initial_state if want_dinit else None)
+
+
+def cconv_update_ex(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
+                    bias: torch.Tensor | None = None, state_indices: torch.Tensor | None = None,
+                    *, pad_rows: bool = False, activation="silu", y: torch.Tensor | None = None,
+                    status: torch.Tensor | None = None, stream=None):
+    """One decode step with the variants: state [S, D, L] with L = W-1 or W; pad_rows: index
+    -1 marks a padding row (no state access, y row not written); activation 'silu' or None.
+    Returns (y [N,D], status int32[2] on the device)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [N,D] bfloat16 with channel stride 1")
+    N, D = x.shape
+    W = w.shape[1]
+    if state.dtype != torch.bfloat16 or state.dim() != 3 or not state.is_contiguous():
+        raise ValueError("state must be a contiguous [S,D,L] bfloat16 tensor")
+    S, L = state.shape[0], state.shape[2]
+    if y is None:
+        y = torch.empty((N, D), dtype=torch.bfloat16, device=x.device)
+    if status is None:
+        status = torch.empty(2, dtype=torch.int32, device=x.device)
+    if state_indices is not None and state_indices.dtype != torch.int32:
+        raise TypeError("state_indices must be int32")
+    rc = load().cconv_update_ex(_ptr(x), N, D, x.stride(0), _ptr(state), S, L,
+                                _ptr(state_indices), int(bool(pad_rows)), _ptr(w), _ptr(bias),
+                                _wdt(w), W, _act(activation), _ptr(y), _ptr(status),
+                                _stream(stream))
+    _check(rc, "cconv_update_ex")
+    return y, status
 
 
 def cconv_status_str(status: int) -> str:

@@ -30,6 +30,8 @@ struct UpdArgs {
   int32_t* status;    // [2]
   int64_t N, D, ldx, S;
   int wdt;
+  int pad;            // nonzero: index -1 marks a padding row
+  int act;            // CCONV_ACT_SILU or CCONV_ACT_NONE
 };
 
 constexpr int kUpdThreads = 256;
@@ -95,17 +97,21 @@ __device__ __forceinline__ void load_update_taps(const UpdArgs& p, int64_t d0,
   }
 }
 
-// VEC = channels per thread (8: 16-byte vectors; 1: scalar path), L = W - 1, ROWS = rows
+// VEC = channels per thread (8: 16-byte vectors; 1: scalar path), W taps, L = state entries
+// per channel (W - 1, or W to keep one older token: the newest W - 1 feed the window, and
+// the new state is the last L of (old state, token), i.e. window[W - L + j]), ROWS = rows
 // per thread.  Grid: x over channel vectors, y over groups of ROWS rows.
 //
 // Latency is what this kernel is about (a decode step moves ~17 MB, mostly L2-resident), so
 // every independent load is issued before the index check needs to finish: this thread's
 // slot ids, token rows, taps and bias first, then the CTA's pass over all N indices; the
 // state rows of in-range slots are fetched while the check completes.  Only the writes wait
-// for the verdict.
-template <int VEC, int L, int ROWS>
+// for the verdict.  Padding rows (p.pad, index -1) are left out of the check and touch
+// neither the state nor y.
+template <int VEC, int W, int L, int ROWS>
 __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs p) {
-  constexpr int W = L + 1;
+  static_assert(L == W - 1 || L == W, "state length is W-1 or W");
+  constexpr int OFF = L - (W - 1);  // state entries older than the window (0 or 1)
   extern __shared__ uint32_t bitmap[];
   __shared__ int s_bad;
 
@@ -121,21 +127,23 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
   const int64_t i0 = static_cast<int64_t>(blockIdx.y) * ROWS;
 
   // ---- this thread's rows: slot ids, token rows, taps ------------------------------------
+  // slot[r] < 0: no row, or a padding row (nothing to do for it)
   int64_t slot[ROWS];
   uint16_t win[ROWS][VEC][W];
 #pragma unroll
   for (int r = 0; r < ROWS; ++r) {
     const int64_t i = i0 + r;
     slot[r] = (mine && i < p.N) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
+    if (p.pad && slot[r] == -1) continue;
     if (mine && i < p.N) {
       const uint16_t* xr = p.x + i * p.ldx + d0;
       if constexpr (VEC == 8) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xr);
         const uint16_t* xh = reinterpret_cast<const uint16_t*>(&xv);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) win[r][c][L] = xh[c];
+        for (int c = 0; c < VEC; ++c) win[r][c][W - 1] = xh[c];
       } else {
-        win[r][0][L] = xr[0];
+        win[r][0][W - 1] = xr[0];
       }
     }
   }
@@ -149,6 +157,7 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
     int off = 0;
     for (int64_t i = threadIdx.x; i < p.N; i += kUpdThreads) {
       const int32_t v = p.idx[i];
+      if (p.pad && v == -1) continue;  // a padding row
       if (v < 0) {
         off |= CCONV_IDX_NEGATIVE;
       } else if (v >= p.S) {
@@ -175,10 +184,10 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
 #pragma unroll
       for (int c = 0; c < VEC; ++c)
 #pragma unroll
-        for (int j = 0; j < L; ++j) win[r][c][j] = sh[c * L + j];
+        for (int j = 0; j < W - 1; ++j) win[r][c][j] = sh[c * L + OFF + j];
     } else {
 #pragma unroll
-      for (int j = 0; j < L; ++j) win[r][0][j] = st[j];
+      for (int j = 0; j < W - 1; ++j) win[r][0][j] = st[OFF + j];
     }
   }
 
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
       float z = tb[c];
 #pragma unroll
       for (int j = 0; j < W; ++j) z = fmaf(tw[c][j], bf16_to_f32(win[r][c][j]), z);
-      yo[c] = f32_to_bf16(silu_f(z));
+      yo[c] = f32_to_bf16(p.act == CCONV_ACT_NONE ? z : silu_f(z));
     }
     uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
     uint16_t* yr = p.y + (i0 + r) * p.D + d0;
@@ -215,51 +224,53 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
 #pragma unroll
         for (int c = 0; c < VEC; ++c)
 #pragma unroll
-          for (int j = 0; j < L; ++j) nh[c * L + j] = win[r][c][j + 1];
+          for (int j = 0; j < L; ++j) nh[c * L + j] = win[r][c][W - L + j];
 #pragma unroll
         for (int u = 0; u < L; ++u) reinterpret_cast<uint4*>(st)[u] = nv[u];
       }
     } else {
       yr[0] = yo[0];
 #pragma unroll
-      for (int j = 0; j < L; ++j) st[j] = win[r][0][j + 1];
+      for (int j = 0; j < L; ++j) st[j] = win[r][0][W - L + j];
     }
   }
 }
 
 typedef void (*UpdKernel)(const UpdArgs);
 
-template <int VEC, int ROWS>
+template <int VEC, int ROWS, int OFF>
 static UpdKernel pick_update_kernel_w(int W) {
   switch (W) {
-    case 1: return cconv_update_kernel<VEC, 0, ROWS>;
-    case 2: return cconv_update_kernel<VEC, 1, ROWS>;
-    case 3: return cconv_update_kernel<VEC, 2, ROWS>;
-    default: return cconv_update_kernel<VEC, 3, ROWS>;
+    case 1: return cconv_update_kernel<VEC, 1, 0 + OFF, ROWS>;
+    case 2: return cconv_update_kernel<VEC, 2, 1 + OFF, ROWS>;
+    case 3: return cconv_update_kernel<VEC, 3, 2 + OFF, ROWS>;
+    default: return cconv_update_kernel<VEC, 4, 3 + OFF, ROWS>;
   }
 }
 
+// L = W - 1 + off.  The longer state takes fewer row counts (1 and 4).
 template <int VEC>
-static UpdKernel pick_update_kernel(int W, int rows) {
+static UpdKernel pick_update_kernel(int W, int rows, int off) {
+  if (off) return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1>(W) : pick_update_kernel_w<VEC, 1, 1>(W);
   switch (rows) {
-    case 1: return pick_update_kernel_w<VEC, 1>(W);
-    case 2: return pick_update_kernel_w<VEC, 2>(W);
-    case 4: return pick_update_kernel_w<VEC, 4>(W);
-    case 8: return pick_update_kernel_w<VEC, 8>(W);
-    default: return pick_update_kernel_w<VEC, 16>(W);
+    case 1: return pick_update_kernel_w<VEC, 1, 0>(W);
+    case 2: return pick_update_kernel_w<VEC, 2, 0>(W);
+    case 4: return pick_update_kernel_w<VEC, 4, 0>(W);
+    case 8: return pick_update_kernel_w<VEC, 8, 0>(W);
+    default: return pick_update_kernel_w<VEC, 16, 0>(W);
   }
 }
 
-}  // namespace cconv
-
-extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx,
-                                      void* state, int64_t S, const int32_t* state_indices,
-                                      const void* w, const void* bias, cconv_dtype wdt, int W,
-                                      void* y, int32_t* status_dev, cconv_stream_t stream) {
-  using namespace cconv;
+// The decode update with every option: state length L (W - 1 or W), padding rows, activation.
+static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* state, int64_t S,
+                       int L, const int32_t* state_indices, int pad, const void* w,
+                       const void* bias, cconv_dtype wdt, int W, cconv_activation act, void* y,
+                       int32_t* status_dev, cconv_stream_t stream) {
   if (!x || !w || !y || !status_dev) return CCONV_ERR_NULL;
   if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
-  if (W > 1 && !state) return CCONV_ERR_NULL;
+  if (L != W - 1 && L != W) return CCONV_ERR_SHAPE;
+  if (act != CCONV_ACT_SILU && act != CCONV_ACT_NONE) return CCONV_ERR_SHAPE;
+  if (L > 0 && !state) return CCONV_ERR_NULL;
   if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
   if (N < 1 || D < 1 || S < 0 || N > (int64_t(1) << 31) - 1 || D > (int64_t(1) << 31) - 8)
     return CCONV_ERR_SHAPE;
@@ -304,9 +315,11 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
     return (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ? v : 0;
   }();
   if (rows_override) rows = rows_override;
+  const int off = L - (W - 1);
+  if (off && rows != 4) rows = 1;  // the longer state is built for 1 and 4 rows only
   const int64_t gy = (N + rows - 1) / rows;
   if (gx > 2147483647 || gy > 65535) return CCONV_ERR_SHAPE;
-  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows) : pick_update_kernel<1>(W, rows);
+  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows, off) : pick_update_kernel<1>(W, rows, off);
 
   UpdArgs a;
   a.x = static_cast<const uint16_t*>(x);
@@ -321,6 +334,8 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
   a.ldx = ldx;
   a.S = S;
   a.wdt = wdt;
+  a.pad = pad ? 1 : 0;
+  a.act = act;
 
   const size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
   // Dynamic plus static shared memory above 48 KB needs the per-function opt-in.
@@ -335,3 +350,23 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
              : CCONV_ERR_CUDA;
 }
 
+
+}  // namespace cconv
+
+extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx,
+                                      void* state, int64_t S, const int32_t* state_indices,
+                                      const void* w, const void* bias, cconv_dtype wdt, int W,
+                                      void* y, int32_t* status_dev, cconv_stream_t stream) {
+  return cconv::update_impl(x, N, D, ldx, state, S, W - 1, state_indices, 0, w, bias, wdt, W,
+                            CCONV_ACT_SILU, y, status_dev, stream);
+}
+
+extern "C" CCONV_API int cconv_update_ex(const void* x, int64_t N, int64_t D, int64_t ldx,
+                                         void* state, int64_t S, int L,
+                                         const int32_t* state_indices, int pad_rows,
+                                         const void* w, const void* bias, cconv_dtype wdt, int W,
+                                         cconv_activation act, void* y, int32_t* status_dev,
+                                         cconv_stream_t stream) {
+  return cconv::update_impl(x, N, D, ldx, state, S, L, state_indices, pad_rows, w, bias, wdt, W,
+                            act, y, status_dev, stream);
+}

@@ -161,6 +161,28 @@ CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx, voi
                            int32_t* status_dev, cconv_stream_t stream);
 
 /*
+ * cconv_update_ex -- cconv_update with the decode variants the cuDNN decode-update PR names
+ * ("Add experimental causal conv1d decode update - #797", NVIDIA/cudnn-frontend, PR
+ * summary: state length L in {3, 4} for W = 4; index -1 as a non-mutating padding row) and
+ * fla's activation keyword.  cconv_update(...) is cconv_update_ex(..., L = W-1,
+ * pad_rows = 0, act = CCONV_ACT_SILU).
+ *
+ *   state    [S, D, L] bf16 contiguous pool, L = W-1 or L = W.  The newest W-1 entries and
+ *            the token form the window; the new state is the last L of (old state, token),
+ *            so L = W keeps one token more than the convolution needs.
+ *   pad_rows nonzero: a state index of -1 marks a padding row, which reads and writes no
+ *            state and whose y row is not written; it is left out of the validation.
+ *            Other negative indices are invalid as before.  Zero: -1 is invalid.
+ *   act      CCONV_ACT_SILU or CCONV_ACT_NONE.
+ * Everything else, including the status words and the fail-closed rule, is cconv_update's.
+ */
+CCONV_API int cconv_update_ex(const void* x, int64_t N, int64_t D, int64_t ldx, void* state,
+                              int64_t S, int L, const int32_t* state_indices, int pad_rows,
+                              const void* w, const void* bias, cconv_dtype wdt, int W,
+                              cconv_activation act, void* y, int32_t* status_dev,
+                              cconv_stream_t stream);
+
+/*
  * cconv_bwd_noalloc -- cconv_bwd without a workspace argument, for callers that cannot
  * allocate device memory where they run the backward (a runtime that hands out memory only
  * from a pre-sized arena, a plugin inside a framework that owns every allocation, a thread

@@ -24,7 +24,8 @@ def test_exports_match_header(lib):
     assert set(declared) == {"cconv_fwd", "cconv_bwd_workspace_bytes", "cconv_bwd",
                              "cconv_bwd_noalloc", "cconv_update", "cconv_status_str",
                              "cconv_device_fault", "cconv_fwd_varlen",
-                             "cconv_bwd_varlen_workspace_bytes", "cconv_bwd_varlen"}
+                             "cconv_bwd_varlen_workspace_bytes", "cconv_bwd_varlen",
+                             "cconv_update_ex"}
     for name in declared:
         assert hasattr(lib, name), f"{name} declared in cconv.h but not exported"
 
@@ -135,3 +136,18 @@ def _bwdv(lib, x=P, sxt=64, dy=P, sdt=64, total=64, D=64, cu=P, nseq=2, w=P, bia
 ])
 def test_bwd_varlen_rejects(lib, kw, expect):
     assert _bwdv(lib, **kw) == expect
+
+
+def _updx(lib, x=P, N=4, D=64, ldx=64, state=P, S=8, L=3, idx=P, pad=0, w=P, bias=None,
+          wdt=F32, W=4, act=0, y=P, status=P):
+    return lib.cconv_update_ex(x, N, D, ldx, state, S, L, idx, pad, w, bias, wdt, W, act, y,
+                               status, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(L=2), ESHAPE), (dict(L=5), ESHAPE), (dict(W=2, L=3), ESHAPE), (dict(act=3), ESHAPE),
+    (dict(status=None), ENULL), (dict(state=None), ENULL), (dict(W=1, L=1, state=None), ENULL),
+    (dict(W=7, L=6), EWIDTH), (dict(ldx=60), ESTRIDE), (dict(x=None), ENULL),
+])
+def test_update_ex_rejects(lib, kw, expect):
+    assert _updx(lib, **kw) == expect
