@@ -15,12 +15,15 @@ from .binding import (  # noqa: F401
     IDX_OUT_OF_RANGE,
     CConvError,
     cconv_bwd,
+    cconv_bwd_multi,
+    cconv_bwd_multi_workspace_bytes,
     cconv_bwd_noalloc,
     cconv_bwd_varlen,
     cconv_bwd_varlen_workspace_bytes,
     cconv_bwd_workspace_bytes,
     cconv_device_fault,
     cconv_fwd,
+    cconv_fwd_multi,
     cconv_fwd_varlen,
     cconv_status_str,
     cconv_update,

@@ -82,6 +82,17 @@ def load(path: str | Path | None = None):
     lib.cconv_update_ex.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _P, _INT,
                                     _INT, _INT, _P, _P, _P]
     lib.cconv_update_ex.restype = _INT
+    _PA = ctypes.POINTER(ctypes.c_void_p)
+    _IA = ctypes.POINTER(ctypes.c_int64)
+    lib.cconv_fwd_multi.argtypes = [_INT, _PA, _IA, _IA, _IA, _PA, _PA, _PA, _I64, _I64, _INT, _INT,
+                                    _P]
+    lib.cconv_fwd_multi.restype = _INT
+    lib.cconv_bwd_multi_workspace_bytes.argtypes = [_INT, _IA, _I64, _I64, _INT,
+                                                    ctypes.POINTER(ctypes.c_size_t)]
+    lib.cconv_bwd_multi_workspace_bytes.restype = _INT
+    lib.cconv_bwd_multi.argtypes = [_INT, _PA, _IA, _IA, _PA, _IA, _IA, _IA, _PA, _PA, _PA, _PA,
+                                    _PA, _I64, _I64, _INT, _INT, _P, ctypes.c_size_t, _P]
+    lib.cconv_bwd_multi.restype = _INT
     lib.cconv_status_str.argtypes = [_INT]
     lib.cconv_status_str.restype = ctypes.c_char_p
     lib.cconv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -371,6 +382,75 @@ def cconv_update_ex(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
                                 _stream(stream))
     _check(rc, "cconv_update_ex")
     return y, status
+
+
+def _parr(ts):
+    """Host array of device pointers (NULL for None)."""
+    return (ctypes.c_void_p * len(ts))(*[None if t is None else t.data_ptr() for t in ts])
+
+
+def _iarr(vals):
+    return (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+
+
+def cconv_fwd_multi(xs, ws, biases=None, *, ys=None, stream=None):
+    """One launch over several [B,T,D_k] problems sharing B, T, W and the weight dtype (the
+    q, k, v convolutions of a layer).  Returns the list of outputs."""
+    n = len(xs)
+    for k, x in enumerate(xs):
+        _bf16_rows(x, f"x[{k}]")
+    B, T = xs[0].shape[:2]
+    if any(x.shape[:2] != (B, T) for x in xs):
+        raise ValueError("every problem must have the same B and T")
+    W = ws[0].shape[1]
+    if ys is None:
+        ys = [torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) for x in xs]
+    biases = biases if biases is not None else [None] * n
+    rc = load().cconv_fwd_multi(n, _parr(xs), _iarr([x.shape[2] for x in xs]),
+                                _iarr([x.stride(0) for x in xs]), _iarr([x.stride(1) for x in xs]),
+                                _parr(ws), _parr(biases), _parr(ys), B, T, _wdt(ws[0]), W,
+                                _stream(stream))
+    _check(rc, "cconv_fwd_multi")
+    return ys
+
+
+def cconv_bwd_multi_workspace_bytes(Ds, B: int, T: int, W: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().cconv_bwd_multi_workspace_bytes(len(Ds), _iarr(Ds), B, T, W, ctypes.byref(n)),
+           "cconv_bwd_multi_workspace_bytes")
+    return int(n.value)
+
+
+def cconv_bwd_multi(xs, dys, ws, biases=None, *, want_dbias: bool | None = None, dxs=None,
+                    dws=None, dbiases=None, workspace=None, stream=None):
+    """Backward of cconv_fwd_multi: lists (dx, dw, dbias or None) per problem."""
+    n = len(xs)
+    for k in range(n):
+        _bf16_rows(xs[k], f"x[{k}]")
+        _bf16_rows(dys[k], f"dy[{k}]")
+    B, T = xs[0].shape[:2]
+    W = ws[0].shape[1]
+    Ds = [x.shape[2] for x in xs]
+    biases = biases if biases is not None else [None] * n
+    if want_dbias is None:
+        want_dbias = any(b is not None for b in biases) or dbiases is not None
+    if dxs is None:
+        dxs = [torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) for x in xs]
+    if dws is None:
+        dws = [torch.empty((D, W), dtype=w.dtype, device=w.device) for D, w in zip(Ds, ws)]
+    if want_dbias and dbiases is None:
+        dbiases = [torch.empty((D,), dtype=w.dtype, device=w.device) for D, w in zip(Ds, ws)]
+    if workspace is None:
+        workspace = torch.empty(cconv_bwd_multi_workspace_bytes(Ds, B, T, W), dtype=torch.uint8,
+                                device=xs[0].device)
+    rc = load().cconv_bwd_multi(
+        n, _parr(xs), _iarr([x.stride(0) for x in xs]), _iarr([x.stride(1) for x in xs]),
+        _parr(dys), _iarr([d.stride(0) for d in dys]), _iarr([d.stride(1) for d in dys]),
+        _iarr(Ds), _parr(ws), _parr(biases), _parr(dxs), _parr(dws),
+        _parr(dbiases) if want_dbias else None, B, T, _wdt(ws[0]), W, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "cconv_bwd_multi")
+    return dxs, dws, (dbiases if want_dbias else [None] * n)
 
 
 def cconv_status_str(status: int) -> str:

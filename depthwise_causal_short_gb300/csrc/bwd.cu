@@ -202,10 +202,11 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
 // runs its own TMA pipeline; the RW partial sums of each strip are added inside the CTA.
 // MODE: kModeVarlen walks packed sequences (rows of [total, D], each sequence's ring from
 // its initial state, its gradient written); kModeActNone leaves out the SiLU.
+// The CTA's work is strip group sg (strips sg*SW .. sg*SW + SW - 1 of the problem) and range
+// group rg; its partial-sum record slots are those of CTA blockIdx.x.
 template <int VEC, int R, int S, int NW, int SW, int MODE>
-__global__ void __launch_bounds__(NW * 32, 1)
-    cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
-                     const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
+__device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMap* tmdy,
+                                        const BwdArgs& p, int sg, int rg) {
   static_assert(NW % SW == 0, "SW strips must divide the CTA's warps");
   constexpr bool VL = (MODE & kModeVarlen) != 0;
   constexpr bool ACT = (MODE & kModeActNone) == 0;
@@ -219,9 +220,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_sg = (p.n_cb + SW - 1) / SW;  // strip groups
-  const int sg = blockIdx.x % n_sg;
-  const int rg = blockIdx.x / n_sg;          // range group
   const int si = warp % SW;
   const int cb = sg * SW + si;
   const int k = rg * RW + warp / SW;
@@ -238,8 +236,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const bool all_active = c0 + CB <= p.D;  // uniform over the warp
 
   if (has_work && lane == 0) {
-    prefetch_tensormap(&tmx);
-    prefetch_tensormap(&tmdy);
+    prefetch_tensormap(tmx);
+    prefetch_tensormap(tmdy);
 #pragma unroll
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -269,8 +267,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int s = 0; s < S; ++s) {
         if (!pc.done) {
           mbar_arrive_expect_tx(&bars[s], STAGE);
-          tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-          tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+          tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b, pol);
+          tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b, pol);
           pc.advance();
         }
       }
@@ -342,8 +340,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       if (lane == 0 && !pc.done) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars[s], STAGE);
-        tma_load_3d(stages + s * STAGE, &tmx, &bars[s], c0, pc.tt, pc.b, pol);
-        tma_load_3d(stages + s * STAGE + TILE, &tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+        tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b, pol);
+        tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b, pol);
         pc.advance();
       }
       cc.advance();
@@ -399,15 +397,65 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
 }
 
+template <int VEC, int R, int S, int NW, int SW, int MODE>
+__global__ void __launch_bounds__(NW * 32, 1)
+    cconv_bwd_kernel(const __grid_constant__ CUtensorMap tmx,
+                     const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
+  const int n_sg = (p.n_cb + SW - 1) / SW;  // strip groups
+  bwd_cta<VEC, R, S, NW, SW, MODE>(&tmx, &tmdy, p, blockIdx.x % n_sg, blockIdx.x / n_sg);
+}
+
+// ------------------------------------------------------------------------------------
+// Several problems in one launch (the q, k and v convolutions of a layer): the same rows
+// and width, each its own x, dy, weights, outputs and D.  Each problem's strips are grouped
+// SW at a time on their own (no CTA straddles two problems); CTA -> (strip group over all
+// problems, range group), so every problem's records sit in one workspace.
+// ------------------------------------------------------------------------------------
+constexpr int kMaxProblems = 4;
+
+struct BwdMulti {
+  CUtensorMap mx[kMaxProblems];
+  CUtensorMap mdy[kMaxProblems];
+  BwdArgs base;                      // shared: ws, T, BT, wpc, W, wdt
+  const void* w[kMaxProblems];
+  const void* bias[kMaxProblems];
+  uint16_t* dx[kMaxProblems];
+  int64_t D[kMaxProblems];
+  int n_cb[kMaxProblems];
+  int sg0[kMaxProblems + 1];         // first strip group of each problem
+  int n;
+};
+
+template <int VEC, int R, int S, int NW, int SW>
+__global__ void __launch_bounds__(NW * 32, 1)
+    cconv_bwd_multi_kernel(const __grid_constant__ BwdMulti m) {
+  const int n_sg = m.sg0[m.n];
+  const int sga = blockIdx.x % n_sg;
+  int k = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxProblems; ++j)
+    if (j < m.n && sga >= m.sg0[j]) k = j;
+  BwdArgs q = m.base;
+  q.w = m.w[k];
+  q.bias = m.bias[k];
+  q.dx = m.dx[k];
+  q.D = m.D[k];
+  q.n_cb = m.n_cb[k];
+  bwd_cta<VEC, R, S, NW, SW, 0>(&m.mx[k], &m.mdy[k], q, sga - m.sg0[k], blockIdx.x / n_sg);
+}
+
 // dw[d, W-1-lag] and dbias[d]: strip cb's records are slot cb % SW of the CTAs of strip group
-// cb / SW, one per range group.  CTA = 32 channels x kRedGroups groups for one record row j
-// (blockIdx.y): group g adds range groups g, g + G, g + 2G, ... and the G group sums are then
-// added in group order.  Deterministic; no atomics; a few independent loads per thread.
+// cb / SW (plus the problem's first strip group), one per range group.  CTA = 32 channels x
+// kRedGroups groups for one record row j (blockIdx.y): group g adds range groups g, g + G,
+// g + 2G, ... and the G group sums are then added in group order.  Deterministic; no
+// atomics; a few independent loads per thread.  blockIdx.x runs over the 32-channel blocks
+// of every problem in turn.
 constexpr int kRedGroups = 8;
 
+// One problem: the same sum with scalar arguments.
 __global__ void __launch_bounds__(32 * kRedGroups)
-    cconv_bwd_reduce_kernel(const float* __restrict__ ws, int cb_width, int sw, int n_sg,
-                            int n_rg, int64_t D, int W, int wdt, void* dw, void* dbias) {
+    cconv_bwd_reduce1_kernel(const float* __restrict__ ws, int cb_width, int sw, int n_sg,
+                             int n_rg, int64_t D, int W, int wdt, void* dw, void* dbias) {
   __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
@@ -453,6 +501,92 @@ __global__ void __launch_bounds__(32 * kRedGroups)
     else
       static_cast<uint16_t*>(dbias)[d] = f32_to_bf16(t);
   }
+}
+
+struct RedArgs {
+  const float* ws;
+  int cb_width, sw, n_sg, n_rg;      // n_sg: strip groups of all problems
+  int W, wdt, n;
+  void* dw[kMaxProblems];
+  void* dbias[kMaxProblems];
+  int64_t D[kMaxProblems];
+  int sg0[kMaxProblems];
+  int blk0[kMaxProblems + 1];        // first 32-channel block of each problem
+};
+
+__global__ void __launch_bounds__(32 * kRedGroups) cconv_bwd_reduce_kernel(const RedArgs r) {
+  __shared__ float part[kRedGroups][33];
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int grp = threadIdx.x >> 5;
+  const int j = blockIdx.y;
+  int k = 0;
+#pragma unroll
+  for (int u = 1; u < kMaxProblems; ++u)
+    if (u < r.n && static_cast<int>(blockIdx.x) >= r.blk0[u]) k = u;
+  const int64_t D = r.D[k];
+  const int64_t d = static_cast<int64_t>(blockIdx.x - r.blk0[k]) * 32 + lane;
+  float a = 0.f;
+  if (d < D) {
+    const int64_t cb = d / r.cb_width;
+    const int c = static_cast<int>(d - cb * r.cb_width);
+    const int64_t rec = static_cast<int64_t>(kRec) * r.cb_width;
+    const int64_t sg = r.sg0[k] + cb / r.sw;
+    const int64_t si = cb % r.sw;
+    const float* base = r.ws + (sg * r.sw + si) * rec + static_cast<int64_t>(j) * r.cb_width + c;
+    const int64_t step = static_cast<int64_t>(r.n_sg) * r.sw * rec;  // next range group's CTA
+    float a0 = 0.f, a1 = 0.f;
+    int q = grp;
+    for (; q + kRedGroups < r.n_rg; q += 2 * kRedGroups) {
+      a0 += base[q * step];
+      a1 += base[(q + kRedGroups) * step];
+    }
+    if (q < r.n_rg) a0 += base[q * step];
+    a = a0 + a1;
+  }
+  part[grp][lane] = a;
+  __syncthreads();
+  if (grp != 0 || d >= D) return;
+  float t = 0.f;
+#pragma unroll
+  for (int g = 0; g < kRedGroups; ++g) t += part[g][lane];
+  const int W = r.W;
+  if (j < 4) {
+    const int lag = j;
+    if (lag < W) {
+      const int64_t o = d * W + (W - 1 - lag);
+      if (r.wdt == CCONV_F32)
+        static_cast<float*>(r.dw[k])[o] = t;
+      else
+        static_cast<uint16_t*>(r.dw[k])[o] = f32_to_bf16(t);
+    }
+  } else if (r.dbias[k]) {
+    if (r.wdt == CCONV_F32)
+      static_cast<float*>(r.dbias[k])[d] = t;
+    else
+      static_cast<uint16_t*>(r.dbias[k])[d] = f32_to_bf16(t);
+  }
+}
+
+// One problem's reduction arguments.
+static RedArgs red_args_one(const float* ws, int cb_width, int sw, int n_sg, int n_rg, int64_t D,
+                            int W, int wdt, void* dw, void* dbias) {
+  RedArgs r{};
+  r.ws = ws;
+  r.cb_width = cb_width;
+  r.sw = sw;
+  r.n_sg = n_sg;
+  r.n_rg = n_rg;
+  r.W = W;
+  r.wdt = wdt;
+  r.n = 1;
+  r.dw[0] = dw;
+  r.dbias[0] = dbias;
+  r.D[0] = D;
+  r.sg0[0] = 0;
+  r.blk0[0] = 0;
+  r.blk0[1] = static_cast<int>((D + 31) / 32);
+  return r;
 }
 
 struct BwdConfig {
@@ -599,10 +733,10 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   const int n_sg = plan.n_sg;
   const int n_rg = plan.n_rg;
   const int wdt_i = static_cast<int>(wdt);
-  if (launch_pdl(cconv_bwd_reduce_kernel,
+  if (launch_pdl(cconv_bwd_reduce1_kernel,
                  dim3(static_cast<unsigned>((D + 31) / 32), dbias ? kRec : W),
-                 dim3(32 * kRedGroups), 0,
-                 st, wsp, cbw, sw, n_sg, n_rg, D, W, wdt_i, dw, dbias) != cudaSuccess)
+                 dim3(32 * kRedGroups), 0, st, wsp, cbw, sw, n_sg, n_rg, D, W, wdt_i, dw,
+                 dbias) != cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;
 }
@@ -764,9 +898,10 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
                      static_cast<uint16_t*>(d_initial_state), n) != cudaSuccess)
         return CCONV_ERR_CUDA;
     }
-    const float* none = nullptr;
-    if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, none,
-                   32 * cfg.vec, cfg.sw, plan.n_sg, 0, D, W, wdt_i, dw, dbias) != cudaSuccess)
+    const RedArgs ra = red_args_one(nullptr, 32 * cfg.vec, cfg.sw, plan.n_sg, 0, D, W, wdt_i,
+                                    dw, dbias);
+    if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, ra) !=
+        cudaSuccess)
       return CCONV_ERR_CUDA;
     return CCONV_OK;
   }
@@ -808,10 +943,172 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
   if (launch_pdl(kern, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
-  const float* wsp = a.ws;
-  if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, wsp,
-                 32 * cfg.vec, cfg.sw, plan.n_sg, plan.n_rg, D, W, wdt_i, dw, dbias) !=
+  const RedArgs ra = red_args_one(a.ws, 32 * cfg.vec, cfg.sw, plan.n_sg, plan.n_rg, D, W, wdt_i,
+                                  dw, dbias);
+  if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, ra) !=
       cudaSuccess)
+    return CCONV_ERR_CUDA;
+  return CCONV_OK;
+}
+
+}  // extern "C"
+
+namespace cconv {
+
+// Work split of the multi-problem backward (default tile shape): strip groups of every
+// problem side by side, range groups sized so the grid is about one wave.
+struct MultiPlan {
+  int n_cb[kMaxProblems], sg0[kMaxProblems + 1];
+  int n_rg, wpc, grid;
+  size_t ws_bytes;
+};
+
+static const BwdConfig kBwdMultiConfig = {4, 12, 3, 8, 4, nullptr};
+
+static int multi_plan(int n, const int64_t* D, int64_t B, int64_t T, MultiPlan* mp) {
+  const BwdConfig& cfg = kBwdMultiConfig;
+  int sms = 0;
+  const int rc = sm_count_current_device(&sms, nullptr);
+  if (rc != CCONV_OK) return rc;
+  const int rw = cfg.warps / cfg.sw;
+  const int64_t cbw = 32 * cfg.vec;
+  int n_sg = 0;
+  for (int k = 0; k < n; ++k) {
+    mp->n_cb[k] = static_cast<int>((D[k] + cbw - 1) / cbw);
+    mp->sg0[k] = n_sg;
+    n_sg += (mp->n_cb[k] + cfg.sw - 1) / cfg.sw;
+  }
+  mp->sg0[n] = n_sg;
+  int64_t n_rg = sms / n_sg;
+  const int64_t by_rows = (B * T) / (32 * rw);
+  if (n_rg > by_rows) n_rg = by_rows;
+  if (n_rg < 1) n_rg = 1;
+  mp->n_rg = static_cast<int>(n_rg);
+  mp->wpc = mp->n_rg * rw;
+  mp->grid = n_sg * mp->n_rg;
+  mp->ws_bytes = static_cast<size_t>(mp->grid) * cfg.sw * kRec * cbw * sizeof(float);
+  return CCONV_OK;
+}
+
+static int check_multi_sizes(int n, const int64_t* D, int64_t B, int64_t T, int W) {
+  if (n < 1 || n > kMaxProblems) return CCONV_ERR_SHAPE;
+  for (int k = 0; k < n; ++k) {
+    const int rc = check_sizes(B, T, D[k], W);
+    if (rc != CCONV_OK) return rc;
+  }
+  return CCONV_OK;
+}
+
+}  // namespace cconv
+
+extern "C" {
+
+CCONV_API int cconv_bwd_multi_workspace_bytes(int n, const int64_t* D, int64_t B, int64_t T,
+                                              int W, size_t* bytes) {
+  using namespace cconv;
+  if (!bytes || !D) return CCONV_ERR_NULL;
+  int rc = check_multi_sizes(n, D, B, T, W);
+  if (rc != CCONV_OK) return rc;
+  MultiPlan mp;
+  rc = multi_plan(n, D, B, T, &mp);
+  if (rc != CCONV_OK) return rc;
+  *bytes = mp.ws_bytes;
+  return CCONV_OK;
+}
+
+CCONV_API int cconv_bwd_multi(int n, const void* const* x, const int64_t* sxb,
+                              const int64_t* sxt, const void* const* dy, const int64_t* sdb,
+                              const int64_t* sdt, const int64_t* D, const void* const* w,
+                              const void* const* bias, void* const* dx, void* const* dw,
+                              void* const* dbias, int64_t B, int64_t T, cconv_dtype wdt, int W,
+                              void* workspace, size_t workspace_bytes, cconv_stream_t stream) {
+  using namespace cconv;
+  if (!x || !sxb || !sxt || !dy || !sdb || !sdt || !D || !w || !dx || !dw) return CCONV_ERR_NULL;
+  if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
+  int rc = check_multi_sizes(n, D, B, T, W);
+  if (rc != CCONV_OK) return rc;
+  const int ew = wdt == CCONV_F32 ? 4 : 2;
+  bool any_dbias = false;
+  for (int k = 0; k < n; ++k) {
+    const void* bk = bias ? bias[k] : nullptr;
+    void* dbk = dbias ? dbias[k] : nullptr;
+    any_dbias = any_dbias || dbk;
+    if (!x[k] || !dy[k] || !w[k] || !dx[k] || !dw[k]) return CCONV_ERR_NULL;
+    rc = check_rows_tensor(x[k], B, T, D[k], sxb[k], sxt[k]);
+    if (rc != CCONV_OK) return rc;
+    rc = check_rows_tensor(dy[k], B, T, D[k], sdb[k], sdt[k]);
+    if (rc != CCONV_OK) return rc;
+    if (reinterpret_cast<uintptr_t>(dx[k]) % 16 != 0) return CCONV_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(w[k]) % ew != 0 || reinterpret_cast<uintptr_t>(dw[k]) % ew != 0)
+      return CCONV_ERR_ALIGN;
+    if ((bk && reinterpret_cast<uintptr_t>(bk) % ew != 0) ||
+        (dbk && reinterpret_cast<uintptr_t>(dbk) % ew != 0))
+      return CCONV_ERR_ALIGN;
+  }
+  MultiPlan mp;
+  rc = multi_plan(n, D, B, T, &mp);
+  if (rc != CCONV_OK) return rc;
+  if (!workspace || workspace_bytes < mp.ws_bytes) return CCONV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return CCONV_ERR_ALIGN;
+
+  const BwdConfig& cfg = kBwdMultiConfig;
+  BwdMulti m;
+  BwdArgs& a = m.base;
+  a = BwdArgs{};
+  a.ws = static_cast<float*>(workspace);
+  a.T = static_cast<int>(T);
+  a.BT = static_cast<int>(B * T);
+  a.wpc = mp.wpc;
+  a.W = W;
+  a.wdt = wdt;
+  RedArgs ra{};
+  ra.ws = a.ws;
+  ra.cb_width = 32 * cfg.vec;
+  ra.sw = cfg.sw;
+  ra.n_sg = mp.sg0[n];
+  ra.n_rg = mp.n_rg;
+  ra.W = W;
+  ra.wdt = static_cast<int>(wdt);
+  ra.n = n;
+  int blk = 0;
+  for (int k = 0; k < kMaxProblems; ++k) {
+    const int src = k < n ? k : n - 1;  // unused slots: copies of the last problem
+    int64_t sb = sxb[src], st = sxt[src], db = sdb[src], dt = sdt[src];
+    normalise_strides(B, T, D[src], sb, st);
+    normalise_strides(B, T, D[src], db, dt);
+    rc = encode_rows_map(&m.mx[k], x[src], B, T, D[src], sb, st, 32 * cfg.vec, cfg.rows);
+    if (rc != CCONV_OK) return rc;
+    rc = encode_rows_map(&m.mdy[k], dy[src], B, T, D[src], db, dt, 32 * cfg.vec, cfg.rows);
+    if (rc != CCONV_OK) return rc;
+    m.w[k] = w[src];
+    m.bias[k] = bias ? bias[src] : nullptr;
+    m.dx[k] = static_cast<uint16_t*>(dx[src]);
+    m.D[k] = D[src];
+    m.n_cb[k] = mp.n_cb[src];
+    m.sg0[k] = k < n ? mp.sg0[k] : mp.sg0[n];
+    ra.dw[k] = dw[src];
+    ra.dbias[k] = dbias ? dbias[src] : nullptr;
+    ra.D[k] = D[src];
+    ra.sg0[k] = mp.sg0[src];
+    ra.blk0[k] = blk;
+    if (k < n) blk += static_cast<int>((D[k] + 31) / 32);
+  }
+  m.sg0[kMaxProblems] = mp.sg0[n];
+  ra.blk0[kMaxProblems] = blk;
+  for (int k = n; k <= kMaxProblems; ++k) ra.blk0[k] = blk;
+  m.n = n;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto kern = cconv_bwd_multi_kernel<4, 12, 3, 8, 4>;
+  int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
+  const int red_bytes = cfg.warps * kRec * 32 * cfg.vec * static_cast<int>(sizeof(float));
+  if (smem < red_bytes) smem = red_bytes;
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+  if (rc != CCONV_OK) return rc;
+  if (launch_pdl(kern, dim3(mp.grid), dim3(cfg.warps * 32), smem, st, m) != cudaSuccess)
+    return CCONV_ERR_CUDA;
+  if (launch_pdl(cconv_bwd_reduce_kernel, dim3(static_cast<unsigned>(blk), any_dbias ? kRec : W),
+                 dim3(32 * kRedGroups), 0, st, ra) != cudaSuccess)
     return CCONV_ERR_CUDA;
   return CCONV_OK;
 }

@@ -179,9 +179,12 @@ __device__ __forceinline__ void final_of_empty(const FwdArgs& p, int first, int 
 // warp 0 re-arms each stage once every consumer has released it.  Stage layout: NC boxes of
 // R rows x CB channels.  MODE: kModeVarlen walks packed sequences (rows of [total, D], ring
 // from each sequence's initial state); kModeActNone leaves out the SiLU.
-template <int VEC, int R, int S, int NC, int MINB, bool SEP, int MODE>
-__global__ void __maxnreg__(regs_for(NC + SEP, MINB))
-cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
+//
+// The CTA's work is channel group cg of the rows' range `part`; the kernels below pick them
+// (and, for several problems in one launch, the problem) from blockIdx.x.
+template <int VEC, int R, int S, int NC, bool SEP, int MODE>
+__device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p, int cg,
+                                        int part) {
   constexpr bool VL = (MODE & kModeVarlen) != 0;
   constexpr bool ACT = (MODE & kModeActNone) == 0;
   static_assert(SEP || !VL, "packed sequences use the producer warp to check cu_seqlens");
@@ -194,8 +197,6 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int cg = blockIdx.x / p.cpc;
-  const int part = blockIdx.x - cg * p.cpc;
   const int r0 = static_cast<int>(static_cast<int64_t>(part) * p.BT / p.cpc);
   const int r1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.BT / p.cpc);
   const int c0 = cg * NC * CB;
@@ -203,7 +204,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
   if (nact > NC) nact = NC;
 
   if (threadIdx.x == 0) {
-    prefetch_tensormap(&tmx);
+    prefetch_tensormap(tmx);
 #pragma unroll
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -236,7 +237,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
           }
           eph ^= 1u << s;
         }
-        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, cur, nact, c0, pol);
+        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, cur, nact, c0, pol);
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }
@@ -252,7 +253,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     Cursor pc = cur;  // the leader's producer cursor, S tiles ahead
     if (leader && lane == 0) {
       for (int s = 0; s < S && !pc.done; ++s) {
-        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, pc, nact, c0, pol);
+        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0, pol);
         pc.advance();
       }
     }
@@ -323,7 +324,7 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
         if (lane == 0 && !pc.done) {
           fine = mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs);
           if (fine) {
-            fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], &tmx, pc, nact, c0, pol);
+            fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0, pol);
             pc.advance();
           } else {
             atomicOr(&g_fault_fwd, kFaultFwdWait);
@@ -337,6 +338,47 @@ cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
     }
   }
   grid_launch_dependents();
+}
+
+template <int VEC, int R, int S, int NC, int MINB, bool SEP, int MODE>
+__global__ void __maxnreg__(regs_for(NC + SEP, MINB))
+cconv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, const FwdArgs p) {
+  const int cg = blockIdx.x / p.cpc;
+  fwd_cta<VEC, R, S, NC, SEP, MODE>(&tmx, p, cg, blockIdx.x - cg * p.cpc);
+}
+
+// ------------------------------------------------------------------------------------
+// Several problems in one launch (the q, k and v convolutions of a layer): the same rows
+// (B, T) and width, each its own x, weights, output and D.  The grid is every problem's
+// channel groups x cpc row ranges; CTA -> (problem, channel group, range).
+// ------------------------------------------------------------------------------------
+constexpr int kMaxProblems = 4;
+
+struct FwdMulti {
+  CUtensorMap map[kMaxProblems];
+  FwdArgs base;                      // shared: T, BT, cpc, W, wdt
+  const void* w[kMaxProblems];
+  const void* bias[kMaxProblems];
+  uint16_t* y[kMaxProblems];
+  int64_t D[kMaxProblems];
+  int cg0[kMaxProblems + 1];         // first channel group of each problem
+  int n;
+};
+
+template <int VEC, int R, int S, int NC, int MINB, bool SEP>
+__global__ void __maxnreg__(regs_for(NC + SEP, MINB))
+cconv_fwd_multi_kernel(const __grid_constant__ FwdMulti m) {
+  const int cga = blockIdx.x / m.base.cpc;
+  int k = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxProblems; ++j)
+    if (j < m.n && cga >= m.cg0[j]) k = j;
+  FwdArgs q = m.base;
+  q.w = m.w[k];
+  q.bias = m.bias[k];
+  q.y = m.y[k];
+  q.D = m.D[k];
+  fwd_cta<VEC, R, S, NC, SEP, 0>(&m.map[k], q, cga - m.cg0[k], blockIdx.x - cga * m.base.cpc);
 }
 
 // ------------------------------------------------------------------------------------
@@ -667,4 +709,78 @@ extern "C" CCONV_API int cconv_fwd_varlen(const void* x, int64_t total, int64_t 
       return CCONV_ERR_CUDA;
   }
   return CCONV_OK;
+}
+
+extern "C" CCONV_API int cconv_fwd_multi(int n, const void* const* x, const int64_t* D,
+                                         const int64_t* sxb, const int64_t* sxt,
+                                         const void* const* w, const void* const* bias,
+                                         void* const* y, int64_t B, int64_t T, cconv_dtype wdt,
+                                         int W, cconv_stream_t stream) {
+  using namespace cconv;
+  if (!x || !D || !sxb || !sxt || !w || !y) return CCONV_ERR_NULL;
+  if (n < 1 || n > kMaxProblems) return CCONV_ERR_SHAPE;
+  if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
+  if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
+  if (B < 1 || T < 1 || B * T > (int64_t(1) << 31) - 16) return CCONV_ERR_SHAPE;
+  const int ew = wdt == CCONV_F32 ? 4 : 2;
+  constexpr int kVec = 4, kRows = 8, kStages = 10, kNc = 8;
+  constexpr int64_t kGroup = int64_t(kNc) * 32 * kVec;
+  FwdMulti m;
+  int cg_total = 0;
+  for (int k = 0; k < n; ++k) {
+    const void* bk = bias ? bias[k] : nullptr;
+    if (!x[k] || !w[k] || !y[k]) return CCONV_ERR_NULL;
+    if (D[k] < 1 || D[k] > (int64_t(1) << 31) - 8) return CCONV_ERR_SHAPE;
+    if (D[k] % 8 != 0) return CCONV_ERR_ALIGN;
+    int rc = check_rows_tensor(x[k], B, T, D[k], sxb[k], sxt[k]);
+    if (rc != CCONV_OK) return rc;
+    if (reinterpret_cast<uintptr_t>(y[k]) % 16 != 0) return CCONV_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(w[k]) % ew != 0 ||
+        (bk && reinterpret_cast<uintptr_t>(bk) % ew != 0))
+      return CCONV_ERR_ALIGN;
+    m.cg0[k] = cg_total;
+    cg_total += static_cast<int>((D[k] + kGroup - 1) / kGroup);
+  }
+  m.cg0[n] = cg_total;
+  int sms = 0;
+  int rc = sm_count_current_device(&sms, nullptr);
+  if (rc != CCONV_OK) return rc;
+  int64_t cpc = sms / cg_total;
+  if (cpc < 1) cpc = 1;
+  const int64_t by_rows = (B * T) / 32 > 0 ? (B * T) / 32 : 1;
+  if (cpc > by_rows) cpc = by_rows;
+  for (int k = 0; k < n; ++k) {
+    int64_t sb = sxb[k], st = sxt[k];
+    normalise_strides(B, T, D[k], sb, st);
+    rc = encode_rows_map(&m.map[k], x[k], B, T, D[k], sb, st, 32 * kVec, kRows);
+    if (rc != CCONV_OK) return rc;
+    m.w[k] = w[k];
+    m.bias[k] = bias ? bias[k] : nullptr;
+    m.y[k] = static_cast<uint16_t*>(y[k]);
+    m.D[k] = D[k];
+  }
+  for (int k = n; k < kMaxProblems; ++k) {  // unused slots: copies of the last problem
+    m.map[k] = m.map[n - 1];
+    m.w[k] = m.w[n - 1];
+    m.bias[k] = m.bias[n - 1];
+    m.y[k] = m.y[n - 1];
+    m.D[k] = m.D[n - 1];
+    m.cg0[k + 1 > kMaxProblems ? kMaxProblems : k + 1] = cg_total;
+  }
+  m.n = n;
+  FwdArgs& a = m.base;
+  a = FwdArgs{};
+  a.T = static_cast<int>(T);
+  a.BT = static_cast<int>(B * T);
+  a.cpc = static_cast<int>(cpc);
+  a.W = W;
+  a.wdt = wdt;
+  auto kern = cconv_fwd_multi_kernel<kVec, kRows, kStages, kNc, 1, true>;
+  const int smem = kStages * (kNc * kRows * 32 * kVec * 2 + 16);
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+  if (rc != CCONV_OK) return rc;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(cg_total * cpc)), dim3((kNc + 1) * 32), smem,
+                    reinterpret_cast<cudaStream_t>(stream), m) == cudaSuccess
+             ? CCONV_OK
+             : CCONV_ERR_CUDA;
 }

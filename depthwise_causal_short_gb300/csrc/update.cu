@@ -107,11 +107,15 @@ __device__ __forceinline__ void load_update_taps(const UpdArgs& p, int64_t d0,
 // slot ids, token rows, taps and bias first, then the CTA's pass over all N indices; the
 // state rows of in-range slots are fetched while the check completes.  Only the writes wait
 // for the verdict.  Padding rows (p.pad, index -1) are left out of the check and touch
-// neither the state nor y.
-template <int VEC, int W, int L, int ROWS>
+// neither the state nor y.  GEN: the padding mode and the activation are read from p;
+// otherwise they are fixed to "off" and SiLU at compile time (the plain decode call, whose
+// latency the runtime tests measurably add to).
+template <int VEC, int W, int L, int ROWS, bool GEN>
 __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs p) {
   static_assert(L == W - 1 || L == W, "state length is W-1 or W");
   constexpr int OFF = L - (W - 1);  // state entries older than the window (0 or 1)
+  const bool pad = GEN && p.pad != 0;
+  const bool act_none = GEN && p.act == CCONV_ACT_NONE;
   extern __shared__ uint32_t bitmap[];
   __shared__ int s_bad;
 
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
   for (int r = 0; r < ROWS; ++r) {
     const int64_t i = i0 + r;
     slot[r] = (mine && i < p.N) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
-    if (p.pad && slot[r] == -1) continue;
+    if (pad && slot[r] == -1) continue;
     if (mine && i < p.N) {
       const uint16_t* xr = p.x + i * p.ldx + d0;
       if constexpr (VEC == 8) {
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
     int off = 0;
     for (int64_t i = threadIdx.x; i < p.N; i += kUpdThreads) {
       const int32_t v = p.idx[i];
-      if (p.pad && v == -1) continue;  // a padding row
+      if (pad && v == -1) continue;  // a padding row
       if (v < 0) {
         off |= CCONV_IDX_NEGATIVE;
       } else if (v >= p.S) {
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
       float z = tb[c];
 #pragma unroll
       for (int j = 0; j < W; ++j) z = fmaf(tw[c][j], bf16_to_f32(win[r][c][j]), z);
-      yo[c] = f32_to_bf16(p.act == CCONV_ACT_NONE ? z : silu_f(z));
+      yo[c] = f32_to_bf16(act_none ? z : silu_f(z));
     }
     uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
     uint16_t* yr = p.y + (i0 + r) * p.D + d0;
@@ -238,26 +242,33 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
 
 typedef void (*UpdKernel)(const UpdArgs);
 
-template <int VEC, int ROWS, int OFF>
+template <int VEC, int ROWS, int OFF, bool GEN>
 static UpdKernel pick_update_kernel_w(int W) {
   switch (W) {
-    case 1: return cconv_update_kernel<VEC, 1, 0 + OFF, ROWS>;
-    case 2: return cconv_update_kernel<VEC, 2, 1 + OFF, ROWS>;
-    case 3: return cconv_update_kernel<VEC, 3, 2 + OFF, ROWS>;
-    default: return cconv_update_kernel<VEC, 4, 3 + OFF, ROWS>;
+    case 1: return cconv_update_kernel<VEC, 1, 0 + OFF, ROWS, GEN>;
+    case 2: return cconv_update_kernel<VEC, 2, 1 + OFF, ROWS, GEN>;
+    case 3: return cconv_update_kernel<VEC, 3, 2 + OFF, ROWS, GEN>;
+    default: return cconv_update_kernel<VEC, 4, 3 + OFF, ROWS, GEN>;
   }
 }
 
-// L = W - 1 + off.  The longer state takes fewer row counts (1 and 4).
+// L = W - 1 + off.  gen: padding rows or another activation asked for.  The general kernels
+// take fewer row counts (1 and 4).
 template <int VEC>
-static UpdKernel pick_update_kernel(int W, int rows, int off) {
-  if (off) return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1>(W) : pick_update_kernel_w<VEC, 1, 1>(W);
+static UpdKernel pick_update_kernel(int W, int rows, int off, bool gen) {
+  if (off || gen) {
+    if (off)
+      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, true>(W)
+                       : pick_update_kernel_w<VEC, 1, 1, true>(W);
+    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, true>(W)
+                     : pick_update_kernel_w<VEC, 1, 0, true>(W);
+  }
   switch (rows) {
-    case 1: return pick_update_kernel_w<VEC, 1, 0>(W);
-    case 2: return pick_update_kernel_w<VEC, 2, 0>(W);
-    case 4: return pick_update_kernel_w<VEC, 4, 0>(W);
-    case 8: return pick_update_kernel_w<VEC, 8, 0>(W);
-    default: return pick_update_kernel_w<VEC, 16, 0>(W);
+    case 1: return pick_update_kernel_w<VEC, 1, 0, false>(W);
+    case 2: return pick_update_kernel_w<VEC, 2, 0, false>(W);
+    case 4: return pick_update_kernel_w<VEC, 4, 0, false>(W);
+    case 8: return pick_update_kernel_w<VEC, 8, 0, false>(W);
+    default: return pick_update_kernel_w<VEC, 16, 0, false>(W);
   }
 }
 
@@ -316,10 +327,12 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
   }();
   if (rows_override) rows = rows_override;
   const int off = L - (W - 1);
-  if (off && rows != 4) rows = 1;  // the longer state is built for 1 and 4 rows only
+  const bool gen = pad != 0 || act != CCONV_ACT_SILU;
+  if ((off || gen) && rows != 4) rows = 1;  // the general kernels are built for 1 and 4 rows
   const int64_t gy = (N + rows - 1) / rows;
   if (gx > 2147483647 || gy > 65535) return CCONV_ERR_SHAPE;
-  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows, off) : pick_update_kernel<1>(W, rows, off);
+  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows, off, gen)
+                        : pick_update_kernel<1>(W, rows, off, gen);
 
   UpdArgs a;
   a.x = static_cast<const uint16_t*>(x);

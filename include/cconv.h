@@ -285,6 +285,34 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
                                void* dx, void* dw, void* dbias, void* d_initial_state,
                                void* workspace, size_t workspace_bytes, cconv_stream_t stream);
 
+/*
+ * Several convolutions in one launch: the q, k and v short convolutions of a KDA layer
+ * (kernel-fun 0.2.0.dev1 wheel, kernel_fun/cconv/__init__.py module docstring: three calls
+ * per layer forward, q and k at D = n_heads*128 and v at twice that).  Each problem k has
+ * its own x, weights, bias and outputs and its own D[k]; B, T, W and the weight dtype are
+ * shared.  The arrays of pointers, strides and sizes are HOST arrays of n entries
+ * (1 <= n <= 4); the pointers in them are device pointers with the rules of cconv_fwd /
+ * cconv_bwd.  One stream kernel covers every problem (plus one reduction kernel for the
+ * backward), so the per-launch tails are paid once.  Results are those of n separate
+ * calls: y and dx bit for bit, dw and dbias up to the order of the partial sums.
+ */
+CCONV_API int cconv_fwd_multi(int n, const void* const* x, const int64_t* D, const int64_t* sxb,
+                              const int64_t* sxt, const void* const* w, const void* const* bias,
+                              void* const* y, int64_t B, int64_t T, cconv_dtype wdt, int W,
+                              cconv_stream_t stream);
+
+/* Workspace cconv_bwd_multi needs on the current device. */
+CCONV_API int cconv_bwd_multi_workspace_bytes(int n, const int64_t* D, int64_t B, int64_t T,
+                                              int W, size_t* bytes);
+
+/* bias and dbias may be NULL arrays (no bias / no dbias for any problem) or hold NULLs. */
+CCONV_API int cconv_bwd_multi(int n, const void* const* x, const int64_t* sxb,
+                              const int64_t* sxt, const void* const* dy, const int64_t* sdb,
+                              const int64_t* sdt, const int64_t* D, const void* const* w,
+                              const void* const* bias, void* const* dx, void* const* dw,
+                              void* const* dbias, int64_t B, int64_t T, cconv_dtype wdt, int W,
+                              void* workspace, size_t workspace_bytes, cconv_stream_t stream);
+
 /* Human-readable name of a cconv_status value (static storage). */
 CCONV_API const char* cconv_status_str(int status);
 

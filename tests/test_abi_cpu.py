@@ -25,7 +25,8 @@ def test_exports_match_header(lib):
                              "cconv_bwd_noalloc", "cconv_update", "cconv_status_str",
                              "cconv_device_fault", "cconv_fwd_varlen",
                              "cconv_bwd_varlen_workspace_bytes", "cconv_bwd_varlen",
-                             "cconv_update_ex"}
+                             "cconv_update_ex", "cconv_fwd_multi",
+                             "cconv_bwd_multi_workspace_bytes", "cconv_bwd_multi"}
     for name in declared:
         assert hasattr(lib, name), f"{name} declared in cconv.h but not exported"
 
@@ -151,3 +152,37 @@ def _updx(lib, x=P, N=4, D=64, ldx=64, state=P, S=8, L=3, idx=P, pad=0, w=P, bia
 ])
 def test_update_ex_rejects(lib, kw, expect):
     assert _updx(lib, **kw) == expect
+
+
+def _arr(ctype, vals):
+    return (ctype * len(vals))(*vals)
+
+
+def _fwdm(lib, n=3, x=(P, P, P), D=(64, 64, 128), sxb=(16 * 64, 16 * 64, 16 * 128),
+          sxt=(64, 64, 128), w=(P, P, P), bias=None, y=(P, P, P), B=2, T=16, wdt=F32, W=4):
+    V, I = ctypes.c_void_p, ctypes.c_int64
+    return lib.cconv_fwd_multi(n, _arr(V, x), _arr(I, D), _arr(I, sxb), _arr(I, sxt), _arr(V, w),
+                               None if bias is None else _arr(V, bias), _arr(V, y), B, T, wdt, W,
+                               None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(n=0), ESHAPE), (dict(n=5, x=(P,) * 5, D=(64,) * 5, sxb=(1024,) * 5, sxt=(64,) * 5,
+                                 w=(P,) * 5, y=(P,) * 5), ESHAPE),
+    (dict(x=(P, None, P)), ENULL), (dict(y=(P, P, None)), ENULL), (dict(W=5), EWIDTH),
+    (dict(wdt=4), EDTYPE), (dict(T=0), ESHAPE), (dict(D=(64, 60, 128)), EALIGN),
+    (dict(D=(64, 0, 128)), ESHAPE), (dict(y=(P, P + 8, P)), EALIGN), (dict(sxt=(64, 64, 0)), ESTRIDE),
+    (dict(bias=(None, P + 1, None)), EALIGN),
+])
+def test_fwd_multi_rejects(lib, kw, expect):
+    assert _fwdm(lib, **kw) == expect
+
+
+def test_bwd_multi_workspace_query_rejects(lib):
+    n = ctypes.c_size_t(0)
+    D = _arr(ctypes.c_int64, [64, 64])
+    assert lib.cconv_bwd_multi_workspace_bytes(2, D, 2, 16, 4, None) == ENULL
+    assert lib.cconv_bwd_multi_workspace_bytes(0, D, 2, 16, 4, ctypes.byref(n)) == ESHAPE
+    assert lib.cconv_bwd_multi_workspace_bytes(2, D, 2, 16, 6, ctypes.byref(n)) == EWIDTH
+    assert lib.cconv_bwd_multi_workspace_bytes(2, _arr(ctypes.c_int64, [64, 12]), 2, 16, 4,
+                                               ctypes.byref(n)) == EALIGN
