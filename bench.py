@@ -337,6 +337,52 @@ def run_ours(args, world, rank, local):
     vb_us = loop_us(vbwd, K)
     del vxs, vdys
 
+    # ---- q, k, v of a layer in one launch: D = 1024, 1024, 2048 (same rows and bytes) -------
+    qkv_D = [FWD.D // 4, FWD.D // 4, FWD.D // 2]
+    qsets = []
+    for k in range(NSET):
+        pr = [inputs.fwd_bwd_inputs(FWD.B, FWD.T, D, FWD.W, False, seed=rank * 100 + 10 * k + j)
+              for j, D in enumerate(qkv_D)]
+        qsets.append(([t[0].to(dev) for t in pr], [t[1].to(dev) for t in pr]))
+    qw = [inputs.fwd_bwd_inputs(1, 1, D, FWD.W, False, seed=j)[2].to(dev)
+          for j, D in enumerate(qkv_D)]
+    qys = [[torch.empty(FWD.B, FWD.T, D, dtype=torch.bfloat16, device=dev) for D in qkv_D]
+           for _ in range(NSET)]
+    qdxs = [[torch.empty(FWD.B, FWD.T, D, dtype=torch.bfloat16, device=dev) for D in qkv_D]
+            for _ in range(NSET)]
+    qdws = [torch.empty(D, FWD.W, device=dev) for D in qkv_D]
+    qws = torch.empty(cc.cconv_bwd_multi_workspace_bytes(qkv_D, FWD.B, FWD.T, FWD.W),
+                      dtype=torch.uint8, device=dev)
+    qws1 = [torch.empty(cc.cconv_bwd_workspace_bytes(FWD.B, FWD.T, D, FWD.W), dtype=torch.uint8,
+                        device=dev) for D in qkv_D]
+
+    def qfwd(i):
+        k = i % NSET
+        cc.cconv_fwd_multi(qsets[k][0], qw, ys=qys[k], stream=stream)
+
+    def qbwd(i):
+        k = i % NSET
+        cc.cconv_bwd_multi(qsets[k][0], qsets[k][1], qw, want_dbias=False, dxs=qdxs[k], dws=qdws,
+                           workspace=qws, stream=stream)
+
+    def qfwd3(i):
+        k = i % NSET
+        for j in range(3):
+            cc.cconv_fwd(qsets[k][0][j], qw[j], None, y=qys[k][j], stream=stream)
+
+    def qbwd3(i):
+        k = i % NSET
+        for j in range(3):
+            cc.cconv_bwd(qsets[k][0][j], qsets[k][1][j], qw[j], None, want_dbias=False,
+                         dx=qdxs[k][j], dw=qdws[j], workspace=qws1[j], stream=stream)
+
+    for fn in (qfwd, qbwd, qfwd3, qbwd3):
+        for i in range(3):
+            fn(i)
+    qf_us, qb_us = loop_us(qfwd, K), loop_us(qbwd, K)
+    qf3_us, qb3_us = loop_us(qfwd3, K), loop_us(qbwd3, K)
+    del qsets
+
     # ---- end to end through the public API with host buffers ------------------------------
     e2e = run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
 
@@ -383,7 +429,18 @@ def run_ours(args, world, rank, local):
                            "tbps": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e12, 4),
                            "frac_of_peak": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e9 / peak_gbs, 4),
                            "note": f"{VL_NSEQ} packed sequences of mixed lengths, same rows; "
-                                   "initial states in, final states out (stream + state kernel)"},
+                                   "initial states in, final states out (one stream kernel; "
+                                   "final states from its register ring)"},
+            "fwd_qkv_one_launch": {"us": round(qf_us, 3),
+                                   "tbps": round(FWD_BYTES / (qf_us * 1e-6) / 1e12, 4),
+                                   "frac_of_peak": round(FWD_BYTES / (qf_us * 1e-6) / 1e9 / peak_gbs, 4),
+                                   "three_calls_us": round(qf3_us, 3),
+                                   "note": "q, k, v convolutions of a layer (D = 1024, 1024, 2048, "
+                                           "same B, T) in one launch vs three cconv_fwd calls"},
+            "bwd_qkv_one_launch": {"us": round(qb_us, 3),
+                                   "tbps": round(BWD_BYTES / (qb_us * 1e-6) / 1e12, 4),
+                                   "frac_of_peak": round(BWD_BYTES / (qb_us * 1e-6) / 1e9 / peak_gbs, 4),
+                                   "three_calls_us": round(qb3_us, 3)},
             "bwd_varlen": {"us": round(vb_us, 3),
                            "tbps": round(VL_BWD_BYTES / (vb_us * 1e-6) / 1e12, 4),
                            "frac_of_peak": round(VL_BWD_BYTES / (vb_us * 1e-6) / 1e9 / peak_gbs, 4),
