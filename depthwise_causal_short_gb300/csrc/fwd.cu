@@ -275,6 +275,9 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
       if (!cur.done && cur.from == cur.ss) {
         init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
         hin_seq = cur.i;
+      } else if (!cur.done && cur.se < cur.r1 && cur.i + 1 < p.nseq) {  // the next sequence's
+        init_ring<VEC>(p.init, seq_slot(p, cur.i + 1), p.D, p.W, d0, active, hin);
+        hin_seq = cur.i + 1;
       }
     }
 

@@ -6,7 +6,7 @@ empty, one-row and shorter-than-the-ring sequences, every width, both activation
 without initial states, bias and bf16 weights, at sizes spanning many tiles and CTA ranges
 and at the production row count.  Final states must equal the oracle's bit for bit (they
 are copies of bf16 rows).  Also: equal lengths without states reproduce the batched calls
-bit for bit; the final state written in place into a decode pool through state indices
+bit for bit (dw, dbias up to the grouping of their partial sums); the final state written in place into a decode pool through state indices
 continues the sequences under cconv_update; invalid indices fail closed; no rows at all;
 an ill-formed cu_seqlens is reported through the device fault word.
 """
@@ -113,7 +113,10 @@ def test_equal_lengths_match_batched_bitwise():
     torch.cuda.synchronize()
     assert torch.equal(y_b.view(B * T, D).view(torch.int16), y_v.view(torch.int16))
     assert torch.equal(dx_b.view(B * T, D).view(torch.int16), dx_v.view(torch.int16))
-    assert torch.equal(dw_b, dw_v) and torch.equal(db_b, db_v)
+    # dw / dbias: the same fp32 terms, but the two calls may group the partial sums
+    # differently (each call's grouping is fixed, so each is deterministic on its own)
+    assert torch.allclose(dw_b, dw_v, rtol=1e-5, atol=1e-5 * float(dw_b.abs().max()))
+    assert torch.allclose(db_b, db_v, rtol=1e-5, atol=1e-5 * float(db_b.abs().max()))
 
 
 def test_strided_rows():
