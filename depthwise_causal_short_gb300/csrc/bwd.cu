@@ -228,8 +228,18 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
   uint8_t* stages = smem + warp * (S * STAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
 
-  const int r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
-  const int r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
+  int r0, r1;
+  if constexpr (VL) {
+    // Equal cost per range: a sequence boundary costs a warp the pulled-back last tile, the
+    // halo, the ring refill and two tiles on the per-row path; 40-48 rows balanced 16 and
+    // 128 mixed sequences and 8 short clustered ones best (measured).
+    constexpr int kBoundaryRows = 44;
+    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k, p.wpc, lane);
+    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k + 1, p.wpc, lane);
+  } else {
+    r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
+    r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
+  }
   const int c0 = cb * CB;
   const int64_t d0 = c0 + lane * VEC;
   const bool active = has_work && d0 < p.D;

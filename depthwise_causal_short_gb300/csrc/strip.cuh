@@ -137,6 +137,38 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int nseq, int total, 
   return lo;
 }
 
+// Packed sequences: where range `num` of `den` starts when ranges get equal COST rather than
+// equal rows.  A sequence boundary costs a warp about `c` rows of work (the extra tile and
+// the ring refill around it), so the cost up to row r of sequence i is r + c*i and the
+// total is total + c*(nseq - 1).  The split row is found with the same warp-wide search as
+// find_seq, on the keys cu[i] + c*i (non-decreasing when cu is): the largest i whose key is
+// at most the target, then the row inside sequence i that reaches it (or the sequence's
+// end).  Split rows are non-decreasing in `num`, start at 0 and end at total.  Must be
+// called by all 32 lanes.
+__device__ __forceinline__ int cost_split(const int32_t* cu, int nseq, int total, int c,
+                                          int num, int den, int lane) {
+  if (num <= 0) return 0;
+  if (num >= den) return total;
+  const int64_t cost = static_cast<int64_t>(total) + static_cast<int64_t>(c) * (nseq - 1);
+  const int64_t tau = cost * num / den;
+  int lo = 0, n = nseq;
+  while (n > 1) {
+    const int step = (n + 31) / 32;
+    const int pos = lo + lane * step;
+    const bool le = lane == 0 ||
+                    (pos < lo + n &&
+                     clamp_row(cu[pos], total) + static_cast<int64_t>(c) * pos <= tau);
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    lo += (31 - __clz(m)) * step;
+    const int left = nseq - lo;
+    n = step < left ? step : left;
+  }
+  const int64_t r = tau - static_cast<int64_t>(c) * lo;
+  const int a = clamp_row(cu[lo], total);
+  const int e = clamp_row(cu[lo + 1], total);
+  return r < a ? a : (r > e ? e : static_cast<int>(r));
+}
+
 // The tile walk of TileCursor over a range [r0, r1) of packed rows.  A segment is the part
 // of the range inside one sequence [ss, se): rows [a, e).  Each segment's first tile starts
 // at a - kRing (rows that fill the ring) but rows before the sequence start ss are skipped:
