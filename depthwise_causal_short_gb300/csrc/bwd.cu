@@ -145,12 +145,10 @@ __device__ __forceinline__ void store_dinit(uint16_t* dinit, int i, int64_t D, i
 // stores dx[t-3].  Otherwise rows before `from` were done with the previous tile, rows
 // before a only fill the x ring, halo rows after e give g (for the last dx rows) only.
 // STORE: this lane's channels exist, so stores need no per-row test.  The dx row pointer
-// (row t-3) advances by D per row.  VL (packed sequences): halo rows past the sequence's
-// end have g = 0, and in a segment that starts its sequence the dx formula for the W-1
-// rows before it gives the initial state's gradient.
-template <int VEC, int R, bool FULL, bool STORE, bool VL, bool ACT, class Cursor>
+// (row t-3) advances by D per row.
+template <int VEC, int R, bool FULL, bool STORE, bool ACT>
 __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, int lane,
-                                         const Cursor& c, bool active, const BwdArgs& p,
+                                         const TileCursor& c, bool active, const BwdArgs& p,
                                          int64_t d0, const f2 (&tap)[4][VEC / 2],
                                          const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
                                          f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2]) {
@@ -164,28 +162,14 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
       f2 x[P], g[P];
       smem_row<VEC>(xt + i * ROWB, lane, x);
       if (FULL || t >= c.a) {
-        bool live = true;
-        if constexpr (VL) live = FULL || t < c.se;
-        if (live) {
-          f2 dy[P];
-          smem_row<VEC>(dyt + i * ROWB, lane, dy);
-          bwd_g<P, ACT>(x, dy, h, tap, bias2, g);
-        } else {
-#pragma unroll
-          for (int q = 0; q < P; ++q) g[q] = 0ull;
-        }
+        f2 dy[P];
+        smem_row<VEC>(dyt + i * ROWB, lane, dy);
+        bwd_g<P, ACT>(x, dy, h, tap, bias2, g);
         if (FULL || t < c.e) bwd_acc<P>(x, h, g, acc);
         if (FULL || (t - kRing >= c.a && t - kRing < c.e)) {
           f2 dxv[P];
           bwd_dx<P>(g, gr, tap, dxv);
           if (STORE || active) store_row<VEC>(dxrow, dxv);
-        } else if constexpr (VL && !FULL) {
-          if (p.dinit && c.a == c.ss && t - kRing < c.a && t - kRing >= c.a - (p.W - 1)) {
-            f2 dxv[P];
-            bwd_dx<P>(g, gr, tap, dxv);
-            if (active)
-              store_dinit<VEC>(p.dinit, c.i, p.D, p.W, t - kRing - (c.a - (p.W - 1)), d0, dxv);
-          }
         }
       } else {
 #pragma unroll
@@ -194,6 +178,108 @@ __device__ __forceinline__ void bwd_tile(const uint8_t* xt, const uint8_t* dyt, 
       rings_push<P>(h, gr, x, g);
     }
     dxrow += p.D;
+  }
+}
+
+// Packed sequences: the dx formula's value at row u lands in dx (u in the sequence that
+// starts at ss, inside [a, e)) or in the gradient of sequence i's initial state (u among the
+// W-1 rows before ss, when this range holds the sequence's first row).
+template <int VEC>
+__device__ __forceinline__ void bwd_put(int u, int i, int ss, int se, const TileCursor& c,
+                                        bool active, const BwdArgs& p, int64_t d0,
+                                        const f2 (&v)[VEC / 2]) {
+  if (!active) return;
+  if (u >= ss && u >= c.a && u < c.e) {
+    store_row<VEC>(p.dx + static_cast<int64_t>(u) * p.D + d0, v);
+  } else if (p.dinit && i >= 0 && u < ss && u >= ss - (p.W - 1) && ss >= c.a && ss < c.e &&
+             ss < se) {
+    store_dinit<VEC>(p.dinit, i, p.D, p.W, u - (ss - (p.W - 1)), d0, v);
+  }
+}
+
+// Packed sequences: the event at row t, where the current sequence ends and the next
+// non-empty one starts.  The ending sequence's last W-1 dx rows (or, for a short sequence,
+// its last initial-state gradient rows) are finished with g = 0 past its end; then both
+// rings restart: x from the new sequence's initial state (fetched one sequence ahead), g
+// from zeros.
+template <int VEC>
+__device__ __forceinline__ void bwd_boundary(int t, const TileCursor& c, SeqTracker& sq,
+                                             bool active, const BwdArgs& p, int64_t d0,
+                                             const f2 (&tap)[4][VEC / 2], f2 (&h)[3][VEC / 2],
+                                             f2 (&gr)[3][VEC / 2], f2 (&hin)[3][VEC / 2],
+                                             int& hin_seq) {
+  constexpr int P = VEC / 2;
+  f2 zero[P];
+#pragma unroll
+  for (int q = 0; q < P; ++q) zero[q] = 0ull;
+#pragma unroll
+  for (int m = 0; m < kRing; ++m) {
+    f2 v[P];
+    bwd_dx<P>(zero, gr, tap, v);
+    bwd_put<VEC>(t - kRing + m, sq.i, sq.ss, t, c, active, p, d0, v);
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      gr[2][q] = gr[1][q];
+      gr[1][q] = gr[0][q];
+      gr[0][q] = 0ull;
+    }
+  }
+  sq.next(t);
+  if (hin_seq != sq.i) init_ring<VEC>(p.init, sq.i, p.D, p.W, d0, active, hin);
+#pragma unroll
+  for (int q = 0; q < P; ++q)
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      h[j][q] = hin[j][q];
+      gr[j][q] = 0ull;
+    }
+  hin_seq = -1;
+  if (sq.i + 1 < p.nseq) {
+    init_ring<VEC>(p.init, sq.i + 1, p.D, p.W, d0, active, hin);
+    hin_seq = sq.i + 1;
+  }
+}
+
+// Packed sequences, a tile on the per-row path (the range's first and last tiles and tiles
+// holding a sequence boundary or the rows just after one): rows before a fill the x ring,
+// rows from a on give g (dw / dbias only inside [a, e)) and the dx value of row t - 3,
+// which bwd_put files as dx or as initial-state gradient; a boundary event runs before the
+// first row of each new sequence.  Halo rows past e finish the range's last dx rows.
+template <int VEC, int R, bool ACT>
+__device__ __forceinline__ void bwd_tile_vl(const uint8_t* xt, const uint8_t* dyt, int lane,
+                                            const TileCursor& c, SeqTracker& sq, bool active,
+                                            const BwdArgs& p, int64_t d0,
+                                            const f2 (&tap)[4][VEC / 2],
+                                            const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
+                                            f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2],
+                                            f2 (&hin)[3][VEC / 2], int& hin_seq) {
+  constexpr int P = VEC / 2;
+  constexpr int ROWB = 32 * VEC * 2;
+  // Not unrolled: unrolling the boundary event into every row made the whole kernel slower
+  // (one sequence: 74.5 against 76.9 us), and running the rows between boundaries through an
+  // unrolled loop with a row test was slower still with many sequences (128: 92.8 against
+  // 87.1 us), measured.
+#pragma unroll 1
+  for (int i = 0; i < R; ++i) {
+    const int t = c.tt + i;
+    if (t >= c.from) {
+      if (sq.at(t)) bwd_boundary<VEC>(t, c, sq, active, p, d0, tap, h, gr, hin, hin_seq);
+      f2 x[P], g[P];
+      smem_row<VEC>(xt + i * ROWB, lane, x);
+      if (t >= c.a) {
+        f2 dy[P];
+        smem_row<VEC>(dyt + i * ROWB, lane, dy);
+        bwd_g<P, ACT>(x, dy, h, tap, bias2, g);
+        if (t < c.e) bwd_acc<P>(x, h, g, acc);
+        f2 dxv[P];
+        bwd_dx<P>(g, gr, tap, dxv);
+        bwd_put<VEC>(t - kRing, sq.i, sq.ss, sq.nb, c, active, p, d0, dxv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < P; ++q) g[q] = 0ull;  // rows before the range: only the x ring
+      }
+      rings_push<P>(h, gr, x, g);
+    }
   }
 }
 
@@ -210,7 +296,7 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
   static_assert(NW % SW == 0, "SW strips must divide the CTA's warps");
   constexpr bool VL = (MODE & kModeVarlen) != 0;
   constexpr bool ACT = (MODE & kModeActNone) == 0;
-  using Cursor = typename std::conditional<VL, SeqCursor, TileCursor>::type;
+  using Cursor = TileCursor;  // packed sequences: one batch row of T = total rows
   constexpr int RW = NW / SW;
   constexpr int CB = 32 * VEC;
   constexpr int P = VEC / 2;
@@ -266,10 +352,7 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
 
   if (has_work) {
     Cursor pc, cc;
-    if constexpr (VL)
-      pc.init(r0, r1, p.cu, p.nseq, p.BT, kRing, R, lane);  // all lanes of the warp
-    else
-      pc.init(r0, r1, p.T, kRing, R);
+    pc.init(r0, r1, p.T, kRing, R);
     cc = pc;
     const uint64_t pol = policy_evict_first();
     if (lane == 0) {
@@ -296,17 +379,16 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
         h[j][q] = 0ull;
         gr[j][q] = 0ull;
       }
-    // Packed sequences: hin holds the initial x ring of sequence hin_seq, fetched one
-    // sequence ahead so that its loads overlap the rows before it.
+    // Packed sequences: the sequence of the rows walked (from the first ring-fill row on),
+    // and hin, the initial x ring of sequence hin_seq, fetched one sequence ahead.
+    SeqTracker sq;
     f2 hin[3][P];
     int hin_seq = -1;
     if constexpr (VL) {
-      if (!cc.done && cc.from == cc.ss) {
-        init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
-        hin_seq = cc.i;
-      } else if (!cc.done && cc.se < cc.r1 && cc.i + 1 < p.nseq) {
-        init_ring<VEC>(p.init, cc.i + 1, p.D, p.W, d0, active, hin);  // the next sequence's
-        hin_seq = cc.i + 1;
+      sq.init(p.cu, p.nseq, p.BT, r0 - kRing, lane);  // all lanes of the warp
+      if (sq.i + 1 < p.nseq) {
+        init_ring<VEC>(p.init, sq.i + 1, p.D, p.W, d0, active, hin);
+        hin_seq = sq.i + 1;
       }
     }
 
@@ -324,30 +406,20 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
       }
       parity ^= 1u << s;
       const uint8_t* xt = stages + s * STAGE;
-      if constexpr (VL) {
-        if (cc.first && cc.from == cc.ss) {  // the segment starts its sequence's rings
-          if (hin_seq != cc.i) init_ring<VEC>(p.init, cc.i, p.D, p.W, d0, active, hin);
-#pragma unroll
-          for (int q = 0; q < P; ++q)
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-              h[j][q] = hin[j][q];
-              gr[j][q] = 0ull;
-            }
-          hin_seq = -1;
-          if (cc.se < cc.r1 && cc.i + 1 < p.nseq) {  // the next sequence starts in range
-            init_ring<VEC>(p.init, cc.i + 1, p.D, p.W, d0, active, hin);
-            hin_seq = cc.i + 1;
-          }
-        }
-      }
-      if (cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e) {
+      bool full_tile = cc.from == cc.tt && cc.tt >= cc.a + kRing && cc.tt + R <= cc.e;
+      if constexpr (VL)  // and no boundary inside, nor one within the 3 rows before
+        full_tile = full_tile && cc.tt - kRing >= sq.ss &&
+                    !(sq.i + 1 < p.nseq && sq.nb >= cc.tt && sq.nb < cc.tt + R);
+      if (full_tile) {
         if (all_active)
-          bwd_tile<VEC, R, true, true, VL, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+          bwd_tile<VEC, R, true, true, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
         else
-          bwd_tile<VEC, R, true, false, VL, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+          bwd_tile<VEC, R, true, false, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+      } else if constexpr (VL) {
+        bwd_tile_vl<VEC, R, ACT>(xt, xt + TILE, lane, cc, sq, active, p, d0, tap, bias2, h, gr,
+                                 acc, hin, hin_seq);
       } else {
-        bwd_tile<VEC, R, false, false, VL, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
+        bwd_tile<VEC, R, false, false, ACT>(xt, xt + TILE, lane, cc, active, p, d0, tap, bias2, h, gr, acc);
       }
       __syncwarp();
       if (lane == 0 && !pc.done) {

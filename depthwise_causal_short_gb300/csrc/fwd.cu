@@ -79,11 +79,11 @@ __device__ __forceinline__ void ring_push(f2 (&h)[3][P], const f2 (&x)[P]) {
 
 // Rows of one tile for this lane.  FULL: every row lies inside the segment.  Otherwise rows
 // before `from` were done with the previous tile, rows before a only fill the ring, and rows
-// from e on are not needed (VL: not even pushed, so the ring ends on the segment's last row).
-// STORE: this lane's channels exist (every lane of a CTA whose channel group lies inside D),
-// so stores need no per-row test.  The output row pointer advances by D per row.
-template <int VEC, int R, bool FULL, bool STORE, bool ACT, bool VL, class Cursor>
-__device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Cursor& c,
+// from e on are not needed.  STORE: this lane's channels exist (every lane of a CTA whose
+// channel group lies inside D), so stores need no per-row test.  The output row pointer
+// advances by D per row.
+template <int VEC, int R, bool FULL, bool STORE, bool ACT>
+__device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const TileCursor& c,
                                          bool active, const FwdArgs& p, int64_t d0,
                                          const f2 (&tap)[4][VEC / 2], const f2 (&bias2)[VEC / 2],
                                          f2 (&h)[3][VEC / 2]) {
@@ -101,7 +101,7 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Cu
         fwd_row<P, ACT>(x, h, tap, bias2, yv);
         if (STORE || active) store_row<VEC>(yrow, yv);
       }
-      if (!VL || FULL || t < c.e) ring_push<P>(h, x);
+      ring_push<P>(h, x);
     }
     yrow += p.D;
   }
@@ -174,6 +174,62 @@ __device__ __forceinline__ void final_of_empty(const FwdArgs& p, int first, int 
   }
 }
 
+// Packed sequences: the event at row t, where the current sequence ends and the next
+// non-empty one starts.  The ending sequence's final state is its ring (if its last row is
+// in this range); the ring then restarts from the new sequence's initial state, which was
+// fetched one sequence ahead (hin); the one after it is fetched now.
+template <int VEC>
+__device__ __forceinline__ void fwd_boundary(int t, const TileCursor& c, SeqTracker& sq,
+                                             bool active, const FwdArgs& p, int64_t d0,
+                                             f2 (&h)[3][VEC / 2], f2 (&hin)[3][VEC / 2],
+                                             int& hin_seq) {
+  if (p.fin && active && sq.i >= 0 && sq.ss < t && t > c.a && t <= c.e)
+    store_final<VEC>(p.fin, sq.i, p.D, p.W, d0, h);
+  sq.next(t);
+  if (hin_seq != sq.i) init_ring<VEC>(p.init, seq_slot(p, sq.i), p.D, p.W, d0, active, hin);
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+#pragma unroll
+    for (int q = 0; q < VEC / 2; ++q) h[j][q] = hin[j][q];
+  hin_seq = -1;
+  if (sq.i + 1 < p.nseq) {
+    init_ring<VEC>(p.init, seq_slot(p, sq.i + 1), p.D, p.W, d0, active, hin);
+    hin_seq = sq.i + 1;
+  }
+}
+
+// Packed sequences, a tile on the per-row path (the range's first and last tiles and tiles
+// holding a sequence boundary): rows before a fill the ring, rows in [a, e) are computed,
+// and a boundary event runs before the first row of each new sequence.  The ring stops at
+// the range's last row, so after the loop it holds the final state of a sequence ending
+// there.
+template <int VEC, int R, bool ACT>
+__device__ __forceinline__ void fwd_tile_vl(const uint8_t* tile, int lane, const TileCursor& c,
+                                            SeqTracker& sq, bool active, const FwdArgs& p,
+                                            int64_t d0, const f2 (&tap)[4][VEC / 2],
+                                            const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
+                                            f2 (&hin)[3][VEC / 2], int& hin_seq) {
+  constexpr int P = VEC / 2;
+  constexpr int ROWB = 32 * VEC * 2;
+  uint16_t* yrow = p.y + static_cast<int64_t>(c.tt) * p.D + d0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int t = c.tt + i;
+    if (t >= c.from && t < c.e) {
+      if (sq.at(t)) fwd_boundary<VEC>(t, c, sq, active, p, d0, h, hin, hin_seq);
+      f2 x[P];
+      smem_row<VEC>(tile + i * ROWB, lane, x);
+      if (t >= c.a) {
+        f2 yv[P];
+        fwd_row<P, ACT>(x, h, tap, bias2, yv);
+        if (active) store_row<VEC>(yrow, yv);
+      }
+      ring_push<P>(h, x);
+    }
+    yrow += p.D;
+  }
+}
+
 // CTA: NC consumer warps (warp w owns channels c0 + w*CB .. c0 + (w+1)*CB - 1 of every tile).
 // SEP: a separate producer warp (index NC) streams the stages; otherwise lane 0 of consumer
 // warp 0 re-arms each stage once every consumer has released it.  Stage layout: NC boxes of
@@ -191,7 +247,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
   constexpr bool VL = (MODE & kModeVarlen) != 0;
   constexpr bool ACT = (MODE & kModeActNone) == 0;
   static_assert(SEP || !VL, "packed sequences use the producer warp to check cu_seqlens");
-  using Cursor = typename std::conditional<VL, SeqCursor, TileCursor>::type;
+  using Cursor = TileCursor;
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
   constexpr int STAGE = NC * TILE;
@@ -227,11 +283,8 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
   // completed.
   grid_dependency_wait();
 
-  Cursor cur;
-  if constexpr (VL)
-    cur.init(r0, r1, p.cu, p.nseq, p.BT, 0, R, lane);  // all lanes of every warp
-  else
-    cur.init(r0, r1, p.T, 0, R);
+  Cursor cur;  // packed sequences: one batch row of T = total rows
+  cur.init(r0, r1, p.T, 0, R);
   const uint64_t pol = policy_evict_first();
   if (SEP && warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
@@ -276,17 +329,16 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
     for (int j = 0; j < 3; ++j)
 #pragma unroll
       for (int q = 0; q < VEC / 2; ++q) h[j][q] = 0ull;
-    // Packed sequences: hin holds the initial ring of sequence hin_seq, fetched one sequence
-    // ahead so that its loads overlap the rows before it.
+    // Packed sequences: the sequence of the rows walked (from the first ring-fill row on),
+    // and hin, the initial ring of sequence hin_seq, fetched one sequence ahead.
+    SeqTracker sq;
     f2 hin[3][VEC / 2];
     int hin_seq = -1;
     if constexpr (VL) {
-      if (!cur.done && cur.from == cur.ss) {
-        init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
-        hin_seq = cur.i;
-      } else if (!cur.done && cur.se < cur.r1 && cur.i + 1 < p.nseq) {  // the next sequence's
-        init_ring<VEC>(p.init, seq_slot(p, cur.i + 1), p.D, p.W, d0, active, hin);
-        hin_seq = cur.i + 1;
+      sq.init(p.cu, p.nseq, p.BT, r0 - kRing, lane);  // all lanes of the warp
+      if (sq.i + 1 < p.nseq) {
+        init_ring<VEC>(p.init, seq_slot(p, sq.i + 1), p.D, p.W, d0, active, hin);
+        hin_seq = sq.i + 1;
       }
     }
 
@@ -301,32 +353,18 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
       }
       fph ^= 1u << s;
       const uint8_t* tile = smem + s * STAGE + warp * TILE;
-      if constexpr (VL) {
-        if (cur.first && cur.from == cur.ss) {  // the segment starts its sequence's ring
-          if (hin_seq != cur.i) init_ring<VEC>(p.init, seq_slot(p, cur.i), p.D, p.W, d0, active, hin);
-#pragma unroll
-          for (int j = 0; j < 3; ++j)
-#pragma unroll
-            for (int q = 0; q < VEC / 2; ++q) h[j][q] = hin[j][q];
-          hin_seq = -1;
-          if (cur.se < cur.r1 && cur.i + 1 < p.nseq) {  // the next sequence starts in range
-            init_ring<VEC>(p.init, seq_slot(p, cur.i + 1), p.D, p.W, d0, active, hin);
-            hin_seq = cur.i + 1;
-          }
-        }
-      }
-      if (cur.from == cur.tt && cur.tt >= cur.a && cur.tt + R <= cur.e) {
+      bool full_tile = cur.from == cur.tt && cur.tt >= cur.a && cur.tt + R <= cur.e;
+      if constexpr (VL)  // and no sequence boundary inside
+        full_tile = full_tile && !(sq.i + 1 < p.nseq && sq.nb >= cur.tt && sq.nb < cur.tt + R);
+      if (full_tile) {
         if (all_active)
-          fwd_tile<VEC, R, true, true, ACT, VL>(tile, lane, cur, active, p, d0, tap, bias2, h);
+          fwd_tile<VEC, R, true, true, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
         else
-          fwd_tile<VEC, R, true, false, ACT, VL>(tile, lane, cur, active, p, d0, tap, bias2, h);
+          fwd_tile<VEC, R, true, false, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
+      } else if constexpr (VL) {
+        fwd_tile_vl<VEC, R, ACT>(tile, lane, cur, sq, active, p, d0, tap, bias2, h, hin, hin_seq);
       } else {
-        fwd_tile<VEC, R, false, false, ACT, VL>(tile, lane, cur, active, p, d0, tap, bias2, h);
-      }
-      if constexpr (VL) {
-        // The tile held the last row of a sequence that ends in this range.
-        if (p.fin && cur.e == cur.se && cur.tt + R >= cur.e && active)
-          store_final<VEC>(p.fin, cur.i, p.D, p.W, d0, h);
+        fwd_tile<VEC, R, false, false, ACT>(tile, lane, cur, active, p, d0, tap, bias2, h);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -347,6 +385,10 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
       }
       cur.advance();
       s = (s + 1 == S) ? 0 : s + 1;
+    }
+    if constexpr (VL) {  // a sequence that ends exactly at the range's end
+      if (p.fin && active && sq.i >= 0 && sq.nb == r1 && sq.ss < r1 && r0 < r1)
+        store_final<VEC>(p.fin, sq.i, p.D, p.W, d0, h);
     }
   }
   grid_launch_dependents();

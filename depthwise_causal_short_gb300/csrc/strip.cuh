@@ -10,7 +10,7 @@
 // order in lockstep, keeping the W-1 previous rows in registers (the ring).  Where a range
 // starts inside a sequence, its first tile starts 3 rows early to fill the ring; where it
 // starts a sequence, those 3 rows lie at t < 0 and the copy engine fills them with zeros,
-// which is exactly the causal zero padding.  Packed sequences of any lengths (SeqCursor)
+// which is exactly the causal zero padding.  Packed sequences of any lengths (SeqTracker)
 // take their ring at a sequence start from the sequence's initial state instead.
 #pragma once
 
@@ -169,96 +169,59 @@ __device__ __forceinline__ int cost_split(const int32_t* cu, int nseq, int total
   return r < a ? a : (r > e ? e : static_cast<int>(r));
 }
 
-// The tile walk of TileCursor over a range [r0, r1) of packed rows.  A segment is the part
-// of the range inside one sequence [ss, se): rows [a, e).  Each segment's first tile starts
-// at a - kRing (rows that fill the ring) but rows before the sequence start ss are skipped:
-// `from` starts at max(a - kRing, ss), and when it starts at ss the caller loads the ring
-// from the sequence's initial state instead (`first && from == ss`).  Empty sequences are
-// stepped over.  Every row touched lies in [r0 - kRing, r1 + tail) and every written row in
-// [r0, r1), whatever cu holds.
-struct SeqCursor {
+// Packed sequences: which sequence the rows a warp walks belong to.  A range of packed rows
+// is walked like one batch row of a [1, total, D] tensor (TileCursor with T = total), and
+// sequence boundaries are events at single rows inside the tiles: at row nb the current
+// sequence ends and the next non-empty one starts.  The tracker keeps the current sequence
+// i (-1 before the first), its first row ss, its end nb and the end of sequence i + 1 (nb2,
+// loaded one boundary ahead so that crossing a boundary waits on no load).  Values of cu are
+// clamped to [0, total]; an ill-formed cu only makes events come early, late or not at all.
+struct SeqTracker {
   const int32_t* cu;
-  int nseq, total, r1;
-  int i;          // current sequence
-  int ss, se;     // its rows, clamped to [0, total]
-  int nse;        // end of sequence i + 1 (loaded one sequence ahead), or total
-  int a, e;       // current segment
-  int tt, from;   // current tile
-  int b;          // always 0: rows are packed
-  int tail, R;
-  bool done, first;
+  int nseq, total;
+  int i, ss, nb, nb2;
 
   __device__ __forceinline__ int ld(int k) const { return clamp_row(cu[k], total); }
 
-  __device__ __forceinline__ void place(int start) {
-    from = start;
-    tt = start;
-    const int lim = e + tail;
-    if (tt + R > lim) {
-      const int back = lim - R;
-      tt = back > a - kRing ? back : a - kRing;
-    }
-  }
-
-  // Segment of sequence i from row a, given its rows [ss, se).  The next sequence's end is
-  // requested now and only needed at the next boundary, so crossing one waits on no load.
-  __device__ __forceinline__ void begin_segment() {
-    if (se < ss) se = ss;
-    nse = i + 2 <= nseq ? ld(i + 2) : total;
-    e = se < r1 ? se : r1;
-    if (e < a) e = a;
-    place(a - kRing);
-    if (from < ss) from = ss;
-    first = true;
-  }
-
-  // Warp-collective (all 32 lanes): positions the cursor on the first tile of [r0, r1_).
-  __device__ __forceinline__ void init(int r0, int r1_, const int32_t* cu_, int nseq_,
-                                       int total_, int tail_, int R_, int lane) {
+  // Warp-collective (all 32 lanes): the state for walking rows from f0 (which may be
+  // negative: rows before 0 read as zeros).  If a sequence starts at or after f0 the walk
+  // begins "before" it, so that its start is an event (and its ring comes from its state).
+  __device__ __forceinline__ void init(const int32_t* cu_, int nseq_, int total_, int f0,
+                                       int lane) {
     cu = cu_;
     nseq = nseq_;
     total = total_;
-    r1 = r1_;
-    tail = tail_;
-    R = R_;
-    b = 0;
-    done = r0 >= r1_ || nseq_ < 1;
-    i = done ? 0 : find_seq(cu_, nseq_, total_, r0, lane);
-    a = r0;
-    if (!done) {
-      ss = ld(i);
-      se = ld(i + 1);
-      begin_segment();
+    const int row = f0 > 0 ? (f0 < total_ ? f0 : total_ - 1) : 0;
+    const int i0 = find_seq(cu_, nseq_, total_, row, lane);
+    const int s0 = ld(i0);
+    if (s0 >= f0) {
+      i = i0 - 1;
+      ss = s0;
+      nb = s0;
+      nb2 = ld(i0 + 1);
+    } else {
+      i = i0;
+      ss = s0;
+      nb = ld(i0 + 1);
+      nb2 = i0 + 2 <= nseq_ ? ld(i0 + 2) : total_;
     }
   }
 
-  __device__ __forceinline__ void advance() {
-    const int next = tt + R;
-    if (next >= e + tail) {
-      if (e >= r1 || i + 1 >= nseq) {
-        done = true;
-        return;
-      }
-      // Sequence i + 1 normally starts where this segment ended; step over empty ones.
-      int j = i + 1;
-      int je = nse;
-      while (je <= e && j + 1 < nseq) {
-        ++j;
-        je = ld(j + 1);
-      }
-      if (je <= e) {
-        done = true;
-        return;
-      }
-      ss = (j == i + 1) ? se : ld(j);
-      i = j;
-      se = je;
-      a = e;
-      begin_segment();
-      return;
+  // An event is due at row t.
+  __device__ __forceinline__ bool at(int t) const { return t == nb && i + 1 < nseq; }
+
+  // At row t == nb: step to the sequence that starts at t, past empty ones.
+  __device__ __forceinline__ void next(int t) {
+    int j = i + 1;
+    int je = nb2;
+    while (je <= t && j + 1 < nseq) {
+      ++j;
+      je = ld(j + 1);
     }
-    first = false;
-    place(next);
+    i = j;
+    ss = t;
+    nb = je;
+    nb2 = j + 2 <= nseq ? ld(j + 2) : total;
   }
 };
 
