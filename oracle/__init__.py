@@ -59,6 +59,9 @@ class Oracle:
         lib.oracle_update_ex.argtypes = [_I64, _I64, ctypes.c_int, ctypes.c_int, _P, _P, _I64, _P,
                                          ctypes.c_int, _P, _P, ctypes.c_int, _P]
         lib.oracle_update_ex.restype = ctypes.c_int
+        lib.oracle_update_ring.argtypes = [_I64, _I64, ctypes.c_int, ctypes.c_int, _P, _P, _I64,
+                                           _P, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P]
+        lib.oracle_update_ring.restype = ctypes.c_int
         lib.oracle_fwd_seq.argtypes = [_I64, _P, _I64, ctypes.c_int, _P, _P, _P, _P, ctypes.c_int,
                                        _P, _P]
         lib.oracle_fwd_seq.restype = ctypes.c_int
@@ -174,6 +177,29 @@ class Oracle:
             raise RuntimeError(f"oracle_update_ex failed ({rc})")
         return rc, (y if rc == 0 else None), st
 
+    def update_ring(self, x_bits, state_bits, idx, pos, w, bias=None, *, pad: bool = False,
+                    activation="silu"):
+        """Circular-buffer decode update: state [S, D, Ls] is a ring per channel, pos [N]
+        the tokens each row's slot has seen; the token goes to ring entry pos mod Ls and the
+        window is the W-1 entries before it.  Returns (status, y, new_state)."""
+        x = self._bits(x_bits)
+        N, D = x.shape
+        st = np.array(self._bits(state_bits), copy=True)
+        S, _, Ls = st.shape
+        w = self._f64(w)
+        W = w.shape[1]
+        b = self._f64(bias)
+        ix = None if idx is None else np.ascontiguousarray(idx, dtype=np.int32)
+        ps = np.ascontiguousarray(pos, dtype=np.int32)
+        act = {"silu": 0, None: 1, "none": 1}[activation]
+        y = np.empty((N, D), np.float64)
+        rc = self.lib.oracle_update_ring(N, D, W, Ls, self._ptr(x), self._ptr(st), S,
+                                         self._ptr(ix), int(pad), self._ptr(ps), self._ptr(w),
+                                         self._ptr(b), act, self._ptr(y))
+        if rc < 0:
+            raise RuntimeError(f"oracle_update_ring failed ({rc})")
+        return rc, (y if rc == 0 else None), st
+
     # -- packed sequences, initial / final state, activation ---------------------------------
     @staticmethod
     def _cu(cu_seqlens):
@@ -263,6 +289,10 @@ def update_ex(*a, **k):
 
 def validate_pad(*a, **k):
     return get().validate_pad(*a, **k)
+
+
+def update_ring(*a, **k):
+    return get().update_ring(*a, **k)
 
 
 def fwd_seq(*a, **k):

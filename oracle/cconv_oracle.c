@@ -368,3 +368,49 @@ int oracle_update_ex(int64_t N, int64_t D, int W, int Ls, const uint16_t* x, uin
   }
   return 0;
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Decode update, circular-buffer form (the cache_seqlens mode the cuDNN decode-update PR
+ * reserves).  Reading: the state of a slot is a ring of Ls >= W-1 entries per channel, and
+ * pos[i] counts the tokens slot s has already seen.  The new token goes to ring entry
+ * pos[i] mod Ls (taken non-negative); the window is the W-1 ring entries before it
+ * (positions pos-(W-1) .. pos-1 mod Ls, oldest first), then the token.  Nothing is shifted;
+ * the caller advances pos.  Padding rows, activation and validation as oracle_update_ex.
+ * --------------------------------------------------------------------------------------- */
+static int64_t ring_mod(int64_t a, int64_t m) {
+  const int64_t r = a % m;
+  return r < 0 ? r + m : r;
+}
+
+int oracle_update_ring(int64_t N, int64_t D, int W, int Ls, const uint16_t* x, uint16_t* state,
+                       int64_t S, const int32_t* idx, int pad, const int32_t* pos,
+                       const double* w, const double* bias, int act, double* y) {
+  if (N < 0 || D < 0 || W < 1 || W > 8 || Ls < W - 1 || Ls < 1 || Ls > 8 || S < 0) return -1;
+  if (act != 0 && act != 1) return -1;
+  if (idx) {
+    const int off = oracle_validate_pad(N, S, idx, pad);
+    if (off) return off;
+  } else if (S < N) {
+    return -1;
+  }
+  uint16_t ring_win[8];
+  for (int64_t i = 0; i < N; ++i) {
+    if (pad && idx && idx[i] == -1) { /* a padding row: no state access, no output */
+      for (int64_t d = 0; d < D; ++d) y[i * D + d] = NAN;
+      continue;
+    }
+    const int64_t slot = idx ? (int64_t)idx[i] : i;
+    if (slot < 0 || slot >= S) return -1;
+    const int64_t head = ring_mod(pos[i], Ls); /* where the new token goes */
+    for (int64_t d = 0; d < D; ++d) {
+      uint16_t* ring = state + (slot * D + d) * Ls;
+      for (int j = 0; j < W - 1; ++j) ring_win[j] = ring[ring_mod(head - (W - 1) + j, Ls)];
+      ring_win[W - 1] = x[i * D + d];
+      double zr = bias ? bias[d] : 0.0;
+      for (int j = 0; j < W; ++j) zr += w[d * W + j] * bf16_to_double(ring_win[j]);
+      y[i * D + d] = act == 0 ? silu(zr) : zr;
+      ring[head] = x[i * D + d];
+    }
+  }
+  return 0;
+}

@@ -548,6 +548,49 @@ def pin_update_ex_padding_rows(o):
     assert status3 == 1 and y3 is None and np.array_equal(st3, state)
 
 
+def pin_update_ring_vs_shift(o):
+    """The circular-buffer form against the shifting form: T single-token steps from a zero
+    state, the ring fed pos = t, give the same y at every step, and the final ring is the
+    shifted state rotated by T (ring[(T - Ls + j) mod Ls] = shifted[j])."""
+    rng = _rng(17)
+    for W, Ls, T in ((4, 3, 9), (4, 4, 10), (3, 2, 7), (2, 1, 5), (1, 1, 4), (4, 5, 11)):
+        N, D, S = 3, 2, 5
+        x = _bf16_bits(_bf16_values(rng, (T, N, D)))
+        w = rng.uniform(-0.5, 0.5, (D, W))
+        bias = rng.uniform(-0.1, 0.1, D)
+        idx = np.array([4, 0, 2], np.int32)
+        ring = np.zeros((S, D, Ls), np.uint16)
+        shift = np.zeros((S, D, Ls), np.uint16)
+        for t in range(T):
+            for act in ("silu",):
+                st1, y1, ring = o.update_ring(x[t], ring, idx, np.full(N, t, np.int32), w, bias,
+                                              activation=act)
+                st2, y2, shift = o.update_ex(x[t], shift, idx, w, bias, activation=act)
+                assert st1 == 0 and st2 == 0
+                _close(y1, y2, 0.0, f"W={W} Ls={Ls} step {t}")
+        for j in range(Ls):
+            assert np.array_equal(ring[idx][:, :, (T - Ls + j) % Ls], shift[idx][:, :, j]), \
+                f"W={W} Ls={Ls}: ring is not the rotated shifted state"
+
+
+def pin_update_ring_positions(o):
+    """Closed form on one slot: a ring holding known tokens, read at several positions."""
+    D, W, Ls = 1, 3, 4
+    w = np.array([[0.25, 0.5, 1.0]])          # taps on (older, newer, token)
+    vals = np.array([1.0, 2.0, 4.0, 8.0])     # ring entries 0..3, exact in bf16
+    ring = _bf16_bits(vals.reshape(1, 1, Ls))
+    x = _bf16_bits(np.array([[16.0]]))
+    for p in (0, 1, 2, 3, 4, 7, -1):
+        h = p % Ls
+        want_z = 0.25 * vals[(h - 2) % Ls] + 0.5 * vals[(h - 1) % Ls] + 16.0
+        st, y, new = o.update_ring(x, ring, None, np.array([p], np.int32), w, None,
+                                   activation=None)
+        assert st == 0 and y[0, 0] == want_z, f"pos {p}: {y[0, 0]} != {want_z}"
+        expect = ring.copy()
+        expect[0, 0, h] = x[0, 0]
+        assert np.array_equal(new, expect), f"pos {p}: token not at entry {h}"
+
+
 ALL_PINS = [
     pin_fwd_lfilter,
     pin_fwd_bwd_torch,
@@ -569,4 +612,6 @@ ALL_PINS = [
     pin_update_ex_is_update,
     pin_validate_pad_exhaustive,
     pin_update_ex_padding_rows,
+    pin_update_ring_vs_shift,
+    pin_update_ring_positions,
 ]

@@ -53,6 +53,13 @@ MUTANTS = {
     "upd_ex_act_ignored": ("y[i * D + d] = act == 0 ? silu(zd) : zd;", "y[i * D + d] = silu(zd);"),
     "upd_ex_no_duplicates": ("if (idx[k] == v) off |= ORACLE_IDX_DUPLICATE;",
                              "if (idx[k] == v && 0) off |= ORACLE_IDX_DUPLICATE;"),
+    # circular-buffer decode
+    "ring_head_off_by_one": ("const int64_t head = ring_mod(pos[i], Ls);",
+                             "const int64_t head = ring_mod(pos[i] + 1, Ls);"),
+    "ring_window_reversed": ("ring_win[j] = ring[ring_mod(head - (W - 1) + j, Ls)];",
+                             "ring_win[j] = ring[ring_mod(head - 1 - j, Ls)];"),
+    "ring_token_not_stored": ("      ring[head] = x[i * D + d];\n", "      (void)0;\n"),
+    "ring_mod_negative": ("return r < 0 ? r + m : r;", "return r < 0 ? 0 : r;"),
 }
 
 
