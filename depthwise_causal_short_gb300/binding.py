@@ -79,8 +79,8 @@ def load(path: str | Path | None = None):
     lib.cconv_bwd_varlen.argtypes = [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _INT, _INT,
                                      _INT, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.cconv_bwd_varlen.restype = _INT
-    lib.cconv_update_ex.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _P, _INT,
-                                    _INT, _INT, _P, _P, _P]
+    lib.cconv_update_ex.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _P, _P,
+                                    _INT, _INT, _INT, _P, _P, _P]
     lib.cconv_update_ex.restype = _INT
     _PA = ctypes.POINTER(ctypes.c_void_p)
     _IA = ctypes.POINTER(ctypes.c_int64)
@@ -358,11 +358,13 @@ def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor
 
 def cconv_update_ex(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
                     bias: torch.Tensor | None = None, state_indices: torch.Tensor | None = None,
-                    *, pad_rows: bool = False, activation="silu", y: torch.Tensor | None = None,
+                    *, pad_rows: bool = False, cache_seqlens: torch.Tensor | None = None,
+                    activation="silu", y: torch.Tensor | None = None,
                     status: torch.Tensor | None = None, stream=None):
     """One decode step with the variants: state [S, D, L] with L = W-1 or W; pad_rows: index
-    -1 marks a padding row (no state access, y row not written); activation 'silu' or None.
-    Returns (y [N,D], status int32[2] on the device)."""
+    -1 marks a padding row (no state access, y row not written); cache_seqlens int32 [N]:
+    the state is a ring and the token goes to entry cache_seqlens mod L; activation 'silu'
+    or None.  Returns (y [N,D], status int32[2] on the device)."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be [N,D] bfloat16 with channel stride 1")
     N, D = x.shape
@@ -376,10 +378,13 @@ def cconv_update_ex(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
         status = torch.empty(2, dtype=torch.int32, device=x.device)
     if state_indices is not None and state_indices.dtype != torch.int32:
         raise TypeError("state_indices must be int32")
+    if cache_seqlens is not None and (cache_seqlens.dtype != torch.int32 or
+                                      not cache_seqlens.is_contiguous()):
+        raise TypeError("cache_seqlens must be a contiguous int32 tensor")
     rc = load().cconv_update_ex(_ptr(x), N, D, x.stride(0), _ptr(state), S, L,
-                                _ptr(state_indices), int(bool(pad_rows)), _ptr(w), _ptr(bias),
-                                _wdt(w), W, _act(activation), _ptr(y), _ptr(status),
-                                _stream(stream))
+                                _ptr(state_indices), int(bool(pad_rows)), _ptr(cache_seqlens),
+                                _ptr(w), _ptr(bias), _wdt(w), W, _act(activation), _ptr(y),
+                                _ptr(status), _stream(stream))
     _check(rc, "cconv_update_ex")
     return y, status
 

@@ -32,7 +32,17 @@ struct UpdArgs {
   int wdt;
   int pad;            // nonzero: index -1 marks a padding row
   int act;            // CCONV_ACT_SILU or CCONV_ACT_NONE
+  const int32_t* pos; // [N] circular-buffer positions (ring mode), or null
 };
+
+// Kernel modes: the plain decode call; the general one (padding rows, activation read from
+// the arguments); the general one on circular-buffer states.
+enum : int { kUpdPlain = 0, kUpdGeneral = 1, kUpdRing = 2 };
+
+__device__ __forceinline__ int ring_mod(int64_t a, int m) {
+  const int r = static_cast<int>(a % m);
+  return r < 0 ? r + m : r;
+}
 
 constexpr int kUpdThreads = 256;
 
@@ -107,12 +117,17 @@ __device__ __forceinline__ void load_update_taps(const UpdArgs& p, int64_t d0,
 // slot ids, token rows, taps and bias first, then the CTA's pass over all N indices; the
 // state rows of in-range slots are fetched while the check completes.  Only the writes wait
 // for the verdict.  Padding rows (p.pad, index -1) are left out of the check and touch
-// neither the state nor y.  GEN: the padding mode and the activation are read from p;
-// otherwise they are fixed to "off" and SiLU at compile time (the plain decode call, whose
-// latency the runtime tests measurably add to).
-template <int VEC, int W, int L, int ROWS, bool GEN>
+// neither the state nor y.  MODE kUpdGeneral: the padding mode and the activation are read
+// from p; kUpdPlain fixes them to "off" and SiLU at compile time (the plain decode call,
+// whose latency the runtime tests measurably add to).  kUpdRing: the state of a slot is a
+// ring of L entries; the token goes to entry head = pos[i] mod L, the window is the W-1
+// entries before it (oldest first), and only the head entry is written.
+template <int VEC, int W, int L, int ROWS, int MODE>
 __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs p) {
   static_assert(L == W - 1 || L == W, "state length is W-1 or W");
+  static_assert(MODE != kUpdRing || L > 0, "a ring needs at least one entry");
+  constexpr bool GEN = MODE != kUpdPlain;
+  constexpr bool RING = MODE == kUpdRing;
   constexpr int OFF = L - (W - 1);  // state entries older than the window (0 or 1)
   const bool pad = GEN && p.pad != 0;
   const bool act_none = GEN && p.act == CCONV_ACT_NONE;
@@ -133,11 +148,13 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
   // ---- this thread's rows: slot ids, token rows, taps ------------------------------------
   // slot[r] < 0: no row, or a padding row (nothing to do for it)
   int64_t slot[ROWS];
+  int head[ROWS];  // ring mode: the entry the token goes to
   uint16_t win[ROWS][VEC][W];
 #pragma unroll
   for (int r = 0; r < ROWS; ++r) {
     const int64_t i = i0 + r;
     slot[r] = (mine && i < p.N) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
+    if constexpr (RING) head[r] = (mine && i < p.N) ? ring_mod(p.pos[i], L) : 0;
     if (pad && slot[r] == -1) continue;
     if (mine && i < p.N) {
       const uint16_t* xr = p.x + i * p.ldx + d0;
@@ -185,10 +202,28 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
 #pragma unroll
       for (int u = 0; u < L; ++u) sv[u] = reinterpret_cast<const uint4*>(st)[u];
       const uint16_t* sh = reinterpret_cast<const uint16_t*>(sv);
+      if constexpr (RING) {
 #pragma unroll
-      for (int c = 0; c < VEC; ++c)
+        for (int j = 0; j < W - 1; ++j) {
+          const int e = ring_mod(head[r] - (W - 1) + j, L);
 #pragma unroll
-        for (int j = 0; j < W - 1; ++j) win[r][c][j] = sh[c * L + OFF + j];
+          for (int c = 0; c < VEC; ++c) {
+            uint16_t v = 0;
+#pragma unroll
+            for (int m = 0; m < L; ++m)  // select in registers (no local-memory indexing)
+              if (m == e) v = sh[c * L + m];
+            win[r][c][j] = v;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c)
+#pragma unroll
+          for (int j = 0; j < W - 1; ++j) win[r][c][j] = sh[c * L + OFF + j];
+      }
+    } else if constexpr (RING) {
+#pragma unroll
+      for (int j = 0; j < W - 1; ++j) win[r][0][j] = st[ring_mod(head[r] - (W - 1) + j, L)];
     } else {
 #pragma unroll
       for (int j = 0; j < W - 1; ++j) win[r][0][j] = st[OFF + j];
@@ -220,7 +255,14 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
     }
     uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
     uint16_t* yr = p.y + (i0 + r) * p.D + d0;
-    if constexpr (VEC == 8) {
+    if constexpr (RING) {
+      if constexpr (VEC == 8)
+        *reinterpret_cast<uint4*>(yr) = *reinterpret_cast<const uint4*>(yo);
+      else
+        yr[0] = yo[0];
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) st[c * L + head[r]] = win[r][c][W - 1];  // the token
+    } else if constexpr (VEC == 8) {
       *reinterpret_cast<uint4*>(yr) = *reinterpret_cast<const uint4*>(yo);
       if constexpr (L > 0) {
         uint4 nv[L];
@@ -242,44 +284,64 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
 
 typedef void (*UpdKernel)(const UpdArgs);
 
-template <int VEC, int ROWS, int OFF, bool GEN>
+// No kernel for a ring of zero entries (the host refuses it before choosing).
+template <int VEC, int W, int L, int ROWS, int MODE>
+static UpdKernel update_kernel() {
+  if constexpr (MODE == kUpdRing && L == 0)
+    return nullptr;
+  else
+    return cconv_update_kernel<VEC, W, L, ROWS, MODE>;
+}
+
+template <int VEC, int ROWS, int OFF, int MODE>
 static UpdKernel pick_update_kernel_w(int W) {
   switch (W) {
-    case 1: return cconv_update_kernel<VEC, 1, 0 + OFF, ROWS, GEN>;
-    case 2: return cconv_update_kernel<VEC, 2, 1 + OFF, ROWS, GEN>;
-    case 3: return cconv_update_kernel<VEC, 3, 2 + OFF, ROWS, GEN>;
-    default: return cconv_update_kernel<VEC, 4, 3 + OFF, ROWS, GEN>;
+    case 1: return update_kernel<VEC, 1, 0 + OFF, ROWS, MODE>();
+    case 2: return update_kernel<VEC, 2, 1 + OFF, ROWS, MODE>();
+    case 3: return update_kernel<VEC, 3, 2 + OFF, ROWS, MODE>();
+    default: return update_kernel<VEC, 4, 3 + OFF, ROWS, MODE>();
   }
 }
 
-// L = W - 1 + off.  gen: padding rows or another activation asked for.  The general kernels
-// take fewer row counts (1 and 4).
+// L = W - 1 + off.  mode: kUpdGeneral when padding rows or another activation are asked
+// for, kUpdRing for circular-buffer states.  The general kernels take fewer row counts (1
+// and 4).
 template <int VEC>
-static UpdKernel pick_update_kernel(int W, int rows, int off, bool gen) {
-  if (off || gen) {
+static UpdKernel pick_update_kernel(int W, int rows, int off, int mode) {
+  if (mode == kUpdRing) {
     if (off)
-      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, true>(W)
-                       : pick_update_kernel_w<VEC, 1, 1, true>(W);
-    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, true>(W)
-                     : pick_update_kernel_w<VEC, 1, 0, true>(W);
+      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, kUpdRing>(W)
+                       : pick_update_kernel_w<VEC, 1, 1, kUpdRing>(W);
+    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, kUpdRing>(W)
+                     : pick_update_kernel_w<VEC, 1, 0, kUpdRing>(W);
+  }
+  if (off || mode == kUpdGeneral) {
+    if (off)
+      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, kUpdGeneral>(W)
+                       : pick_update_kernel_w<VEC, 1, 1, kUpdGeneral>(W);
+    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, kUpdGeneral>(W)
+                     : pick_update_kernel_w<VEC, 1, 0, kUpdGeneral>(W);
   }
   switch (rows) {
-    case 1: return pick_update_kernel_w<VEC, 1, 0, false>(W);
-    case 2: return pick_update_kernel_w<VEC, 2, 0, false>(W);
-    case 4: return pick_update_kernel_w<VEC, 4, 0, false>(W);
-    case 8: return pick_update_kernel_w<VEC, 8, 0, false>(W);
-    default: return pick_update_kernel_w<VEC, 16, 0, false>(W);
+    case 1: return pick_update_kernel_w<VEC, 1, 0, kUpdPlain>(W);
+    case 2: return pick_update_kernel_w<VEC, 2, 0, kUpdPlain>(W);
+    case 4: return pick_update_kernel_w<VEC, 4, 0, kUpdPlain>(W);
+    case 8: return pick_update_kernel_w<VEC, 8, 0, kUpdPlain>(W);
+    default: return pick_update_kernel_w<VEC, 16, 0, kUpdPlain>(W);
   }
 }
 
 // The decode update with every option: state length L (W - 1 or W), padding rows, activation.
 static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* state, int64_t S,
-                       int L, const int32_t* state_indices, int pad, const void* w,
-                       const void* bias, cconv_dtype wdt, int W, cconv_activation act, void* y,
-                       int32_t* status_dev, cconv_stream_t stream) {
+                       int L, const int32_t* state_indices, int pad, const int32_t* pos,
+                       const void* w, const void* bias, cconv_dtype wdt, int W,
+                       cconv_activation act, void* y, int32_t* status_dev,
+                       cconv_stream_t stream) {
   if (!x || !w || !y || !status_dev) return CCONV_ERR_NULL;
   if (W < 1 || W > 4) return CCONV_ERR_WIDTH;
   if (L != W - 1 && L != W) return CCONV_ERR_SHAPE;
+  if (pos && L < 1) return CCONV_ERR_SHAPE;  // a ring needs at least one entry
+  if (pos && reinterpret_cast<uintptr_t>(pos) % 4 != 0) return CCONV_ERR_ALIGN;
   if (act != CCONV_ACT_SILU && act != CCONV_ACT_NONE) return CCONV_ERR_SHAPE;
   if (L > 0 && !state) return CCONV_ERR_NULL;
   if (wdt != CCONV_BF16 && wdt != CCONV_F32) return CCONV_ERR_DTYPE;
@@ -327,12 +389,13 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
   }();
   if (rows_override) rows = rows_override;
   const int off = L - (W - 1);
-  const bool gen = pad != 0 || act != CCONV_ACT_SILU;
-  if ((off || gen) && rows != 4) rows = 1;  // the general kernels are built for 1 and 4 rows
+  const int mode = pos ? kUpdRing : (pad != 0 || act != CCONV_ACT_SILU) ? kUpdGeneral : kUpdPlain;
+  if ((off || mode != kUpdPlain) && rows != 4) rows = 1;  // general kernels: 1 and 4 rows
   const int64_t gy = (N + rows - 1) / rows;
   if (gx > 2147483647 || gy > 65535) return CCONV_ERR_SHAPE;
-  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows, off, gen)
-                        : pick_update_kernel<1>(W, rows, off, gen);
+  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows, off, mode)
+                        : pick_update_kernel<1>(W, rows, off, mode);
+  if (!kern) return CCONV_ERR_SHAPE;
 
   UpdArgs a;
   a.x = static_cast<const uint16_t*>(x);
@@ -349,6 +412,7 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
   a.wdt = wdt;
   a.pad = pad ? 1 : 0;
   a.act = act;
+  a.pos = pos;
 
   const size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
   // Dynamic plus static shared memory above 48 KB needs the per-function opt-in.
@@ -370,16 +434,17 @@ extern "C" CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64
                                       void* state, int64_t S, const int32_t* state_indices,
                                       const void* w, const void* bias, cconv_dtype wdt, int W,
                                       void* y, int32_t* status_dev, cconv_stream_t stream) {
-  return cconv::update_impl(x, N, D, ldx, state, S, W - 1, state_indices, 0, w, bias, wdt, W,
-                            CCONV_ACT_SILU, y, status_dev, stream);
+  return cconv::update_impl(x, N, D, ldx, state, S, W - 1, state_indices, 0, nullptr, w, bias,
+                            wdt, W, CCONV_ACT_SILU, y, status_dev, stream);
 }
 
 extern "C" CCONV_API int cconv_update_ex(const void* x, int64_t N, int64_t D, int64_t ldx,
                                          void* state, int64_t S, int L,
                                          const int32_t* state_indices, int pad_rows,
-                                         const void* w, const void* bias, cconv_dtype wdt, int W,
+                                         const int32_t* cache_seqlens, const void* w,
+                                         const void* bias, cconv_dtype wdt, int W,
                                          cconv_activation act, void* y, int32_t* status_dev,
                                          cconv_stream_t stream) {
-  return cconv::update_impl(x, N, D, ldx, state, S, L, state_indices, pad_rows, w, bias, wdt, W,
-                            act, y, status_dev, stream);
+  return cconv::update_impl(x, N, D, ldx, state, S, L, state_indices, pad_rows, cache_seqlens, w,
+                            bias, wdt, W, act, y, status_dev, stream);
 }

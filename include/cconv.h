@@ -163,9 +163,10 @@ CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx, voi
 /*
  * cconv_update_ex -- cconv_update with the decode variants the cuDNN decode-update PR names
  * ("Add experimental causal conv1d decode update - #797", NVIDIA/cudnn-frontend, PR
- * summary: state length L in {3, 4} for W = 4; index -1 as a non-mutating padding row) and
- * fla's activation keyword.  cconv_update(...) is cconv_update_ex(..., L = W-1,
- * pad_rows = 0, act = CCONV_ACT_SILU).
+ * summary: state length L in {3, 4} for W = 4; index -1 as a non-mutating padding row;
+ * circular-buffer cache_seqlens metadata) and fla's activation keyword.  cconv_update(...)
+ * is cconv_update_ex(..., L = W-1, pad_rows = 0, cache_seqlens = NULL,
+ * act = CCONV_ACT_SILU).
  *
  *   state    [S, D, L] bf16 contiguous pool, L = W-1 or L = W.  The newest W-1 entries and
  *            the token form the window; the new state is the last L of (old state, token),
@@ -173,14 +174,21 @@ CCONV_API int cconv_update(const void* x, int64_t N, int64_t D, int64_t ldx, voi
  *   pad_rows nonzero: a state index of -1 marks a padding row, which reads and writes no
  *            state and whose y row is not written; it is left out of the validation.
  *            Other negative indices are invalid as before.  Zero: -1 is invalid.
+ *   cache_seqlens  int32[N] in device memory, or NULL.  Given, the state is a circular
+ *            buffer (the mode the PR's signature reserves; the reading taken here): the
+ *            state of a slot is a ring of L entries per channel, cache_seqlens[i] counts the
+ *            tokens row i's slot has already seen, the token is written to ring entry
+ *            cache_seqlens[i] mod L (taken non-negative), and the window is the W-1 entries
+ *            before it, oldest first.  Nothing is shifted and cache_seqlens is not changed
+ *            (the caller advances it).  Needs L >= 1.
  *   act      CCONV_ACT_SILU or CCONV_ACT_NONE.
  * Everything else, including the status words and the fail-closed rule, is cconv_update's.
  */
 CCONV_API int cconv_update_ex(const void* x, int64_t N, int64_t D, int64_t ldx, void* state,
                               int64_t S, int L, const int32_t* state_indices, int pad_rows,
-                              const void* w, const void* bias, cconv_dtype wdt, int W,
-                              cconv_activation act, void* y, int32_t* status_dev,
-                              cconv_stream_t stream);
+                              const int32_t* cache_seqlens, const void* w, const void* bias,
+                              cconv_dtype wdt, int W, cconv_activation act, void* y,
+                              int32_t* status_dev, cconv_stream_t stream);
 
 /*
  * cconv_bwd_noalloc -- cconv_bwd without a workspace argument, for callers that cannot

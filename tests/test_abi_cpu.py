@@ -139,9 +139,9 @@ def test_bwd_varlen_rejects(lib, kw, expect):
     assert _bwdv(lib, **kw) == expect
 
 
-def _updx(lib, x=P, N=4, D=64, ldx=64, state=P, S=8, L=3, idx=P, pad=0, w=P, bias=None,
-          wdt=F32, W=4, act=0, y=P, status=P):
-    return lib.cconv_update_ex(x, N, D, ldx, state, S, L, idx, pad, w, bias, wdt, W, act, y,
+def _updx(lib, x=P, N=4, D=64, ldx=64, state=P, S=8, L=3, idx=P, pad=0, pos=None, w=P,
+          bias=None, wdt=F32, W=4, act=0, y=P, status=P):
+    return lib.cconv_update_ex(x, N, D, ldx, state, S, L, idx, pad, pos, w, bias, wdt, W, act, y,
                                status, None)
 
 
@@ -149,6 +149,7 @@ def _updx(lib, x=P, N=4, D=64, ldx=64, state=P, S=8, L=3, idx=P, pad=0, w=P, bia
     (dict(L=2), ESHAPE), (dict(L=5), ESHAPE), (dict(W=2, L=3), ESHAPE), (dict(act=3), ESHAPE),
     (dict(status=None), ENULL), (dict(state=None), ENULL), (dict(W=1, L=1, state=None), ENULL),
     (dict(W=7, L=6), EWIDTH), (dict(ldx=60), ESTRIDE), (dict(x=None), ENULL),
+    (dict(W=1, L=0, pos=P), ESHAPE), (dict(pos=P + 2), EALIGN),
 ])
 def test_update_ex_rejects(lib, kw, expect):
     assert _updx(lib, **kw) == expect

@@ -4,7 +4,8 @@ Each case draws its shape and options from a fixed-seed generator, so a failure 
 reproducible case: batched forward / backward with random B, T, D tails, widths, bias,
 weight dtype and row strides; packed sequences with random length mixes (empty and short
 ones included), states, activation; decode updates with random pools, state lengths,
-padding rows and layouts; several problems in one launch.  Sizes stay small enough for
+padding rows and layouts, shifting or circular (random positions); several problems in one
+launch.  Sizes stay small enough for
 the fp64 oracle to finish in milliseconds.
 """
 import random
@@ -167,3 +168,40 @@ def test_multi(case):
         rdx, rdw, rdb = oracle_bwd(x, dy, w, b, want_dbias=True)
         for name, gt, ref in (("dx", dxs[k], rdx), ("dw", dws[k], rdw), ("dbias", dbs[k], rdb)):
             assert rel_err(f64(gt), ref) <= BWD_TOL, f"{what}: {name}"
+
+
+@pytest.mark.parametrize("case", range(N_CASES // 2))
+def test_decode_ring(case):
+    r = random.Random(5000 + case)
+    W = r.randint(1, 4)
+    L = max(1, W - 1 + (r.random() < 0.4))
+    S = r.randint(1, 80)
+    N = r.randint(1, min(S, 70))
+    D = r.choice([8 * r.randint(1, 64), r.randint(1, 300)])
+    pad_rows = r.random() < 0.3
+    act = r.choice(["silu", None])
+    g = torch.Generator().manual_seed(case)
+    state = torch.randn(S, D, L, generator=g).to(torch.bfloat16)
+    x = torch.randn(N, D, generator=g).to(torch.bfloat16)
+    w = torch.rand(D, W, generator=g) - 0.5
+    b = torch.rand(D, generator=g) - 0.5 if r.random() < 0.5 else None
+    idx = torch.randperm(S, generator=g)[:N].to(torch.int32)
+    if pad_rows:
+        for i in range(N):
+            if r.random() < 0.3:
+                idx[i] = -1
+    pos = torch.tensor([r.randint(-20, 1000) for _ in range(N)], dtype=torch.int32)
+    dev = torch.device("cuda", 0)
+    sg = state.to(dev)
+    y = torch.zeros(N, D, dtype=torch.bfloat16, device=dev)
+    _, status = cc.cconv_update_ex(x.to(dev), sg, w.to(dev), None if b is None else b.to(dev),
+                                   idx.to(dev), pad_rows=pad_rows, cache_seqlens=pos.to(dev),
+                                   activation=act, y=y)
+    torch.cuda.synchronize()
+    what = f"ring W={W} L={L} S={S} N={N} D={D} pad={pad_rows} act={act}"
+    rc, y_ref, st_ref = oracle.update_ring(bits(x), bits(state), idx.numpy(), pos.numpy(),
+                                           f64(w), f64(b), pad=pad_rows, activation=act)
+    assert status.tolist() == [0 if rc == 0 else -8, rc], what
+    assert np.array_equal(bits(sg), st_ref), f"{what}: pool"
+    live = (idx >= 0).numpy()
+    assert rel_err(f64(y)[live], y_ref[live]) <= FWD_TOL, f"{what}: y"

@@ -120,3 +120,63 @@ def test_invalid_with_padding_mode(pad, idx, mask):
     assert status.tolist() == [-8, mask]
     assert torch.equal(state.view(torch.int16), before.view(torch.int16))
     assert not y.float().any(), "y written on a rejected call"
+
+
+def _ring_steps(W, L, D, ldpad, pad, act, idx_rows, steps, seed, start):
+    """Circular-buffer decode: `steps` steps with cache_seqlens = start + step, against the
+    oracle's circular form; pools bit for bit, y within tolerance, padding y untouched."""
+    S = max(29, max(idx_rows) + 1)
+    N = len(idx_rows)
+    _, xr, _, w, b = inputs.decode_inputs(S, N, D, W, True, n_x=steps, seed=seed)
+    state = _pool(S, D, L, seed + 1)
+    rows = torch.zeros(steps, N, D + ldpad, dtype=torch.bfloat16)
+    rows[:, :, :D] = xr
+    rows_g = rows.cuda()
+    state_g, wg, bg = state.cuda(), w.cuda(), b.cuda()
+    idx = torch.tensor(idx_rows, dtype=torch.int32)
+    idx_g = idx.cuda()
+    st_ref = bits(state)
+    live = idx >= 0
+    for k in range(steps):
+        pos = torch.tensor([start[i] + k for i in range(N)], dtype=torch.int32)
+        y = torch.full((N, D), 0, dtype=torch.int16)
+        y[:] = SENTINEL
+        y = y.view(torch.bfloat16).cuda()
+        _, status = cc.cconv_update_ex(rows_g[k, :, :D], state_g, wg, bg, idx_g, pad_rows=pad,
+                                       cache_seqlens=pos.cuda(), activation=act, y=y)
+        torch.cuda.synchronize()
+        assert status.tolist() == [0, 0], f"step {k}: status {status.tolist()}"
+        rc, y_ref, st_ref = oracle.update_ring(bits(xr[k]), st_ref, idx.numpy(), pos.numpy(),
+                                               f64(w), f64(b), pad=pad, activation=act)
+        assert rc == 0
+        yc = y.cpu()
+        e = rel_err(f64(yc[live]), y_ref[live.numpy()])
+        assert e <= FWD_TOL, f"ring W={W} L={L} step {k}: y err {e:.2e}"
+        assert np.all(bits(yc[~live]) == SENTINEL), "a padding row's y was written"
+    assert np.array_equal(bits(state_g), st_ref), f"ring W={W} L={L}: pool differs"
+
+
+@pytest.mark.parametrize("W,L", [(4, 3), (4, 4), (3, 2), (3, 3), (2, 1), (2, 2), (1, 1)])
+@pytest.mark.parametrize("D,ldpad", [(4096, 0), (1000, 8), (1001, 0)])
+def test_circular_buffer(W, L, D, ldpad):
+    start = [0, 1, 5, 2, 7, 100, 3]        # different positions per row, wrapping
+    _ring_steps(W, L, D, ldpad, False, "silu", [4, 17, 0, 28, 9, 3, 11], steps=5, seed=W + L,
+                start=start)
+
+
+def test_circular_buffer_padding_and_no_activation():
+    start = [3, 0, 9, 0, 1, 4, 0, 2, 6]
+    _ring_steps(4, 4, 2048, 0, True, None, [5, -1, 12, -1, -1, 0, 27, 6, -1], steps=4, seed=90,
+                start=start)
+
+
+def test_circular_buffer_many_rows():
+    g = torch.Generator().manual_seed(91)
+    idx = torch.randperm(512, generator=g)[:256].tolist()
+    start = torch.randint(0, 50, (256,), generator=g).tolist()
+    _ring_steps(4, 3, 4096, 0, False, "silu", idx, steps=4, seed=91, start=start)
+
+
+def test_circular_buffer_negative_position():
+    """cache_seqlens is taken modulo L, non-negative: -1 is entry L - 1."""
+    _ring_steps(4, 3, 512, 0, False, "silu", [0, 1, 2], steps=3, seed=92, start=[-1, -5, -3])
