@@ -1,4 +1,5 @@
-// bwd.cu -- cconv_bwd: the backward stream plus a deterministic reduction (two kernels).
+// bwd.cu -- cconv_bwd and its packed-sequence and multi-problem forms: the backward stream
+// plus a deterministic reduction (two kernels).
 //
 // With z recomputed from x and g = dy * sigmoid(z) * (1 + z * (1 - sigmoid(z))):
 //   dx[b,t,d]    = sum_{k<W} w[d,W-1-k] * g[b,t+k,d]     (g = 0 for t+k >= T)
@@ -10,13 +11,18 @@
 // from a g ring three rows later, a 3-row halo after each range, and a fixed-shape
 // reduction of fp32 partials instead of atomics.
 //
-// GB300 layout: the same warp-specialised CTA pipeline as the forward (a stage holds the x
-// and the dy boxes of every consumer warp and completes on one mbarrier), packed f32x2
-// arithmetic, and one fp32 partial record per consumer warp ([5][32*VEC]: four lags of dw,
-// then dbias).  Because each lane owns its channels for the whole range, the time sum needs
-// no shuffles; the cross-CTA sum is a second small kernel that adds each channel's records in
-// a fixed order, launched as a programmatic dependent of the first so its launch overlaps
-// the stream's tail.
+// GB300 layout: every warp runs its own TMA pipeline over one 128-channel strip of a row
+// range (S stages of x and dy tiles on the warp's own mbarriers, issued by lane 0); a CTA is
+// SW neighbouring strips x (8 / SW) consecutive ranges.  Arithmetic is packed f32x2, and
+// each warp keeps one fp32 partial record ([5][32*VEC]: four lags of dw, then dbias).
+// Because each lane owns its channels for the whole range, the time sum needs no shuffles.
+// The CTA adds its ranges' records per strip in a fixed order in shared memory; a second
+// small kernel adds each channel's records across CTAs in a fixed order, launched as a
+// programmatic dependent of the first so that its launch overlaps the stream's tail.
+//
+// The same body also serves packed sequences (kModeVarlen: sequence boundaries are events
+// at single rows, with the initial state's gradient written), no activation (kModeActNone),
+// and several problems in one launch (cconv_bwd_multi_kernel).
 #include <mutex>
 #include <type_traits>
 

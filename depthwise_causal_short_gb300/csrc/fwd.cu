@@ -1,4 +1,4 @@
-// fwd.cu -- cconv_fwd: the forward stream (one kernel).
+// fwd.cu -- cconv_fwd and its packed-sequence and multi-problem forms: the forward stream.
 //
 // y[b,t,d] = silu(bias[d] + sum_{k<W} w[d,W-1-k] * x[b,t-k,d]), x = 0 left of the sequence.
 // Definition: kernel-fun 0.2.0.dev1 wheel, kernel_fun/cconv/_kernels/strip.py (`_tap`,
@@ -15,6 +15,11 @@
 // lockstep keeps the warps of an SM finishing together.  The 3 ring rows before a range and
 // the zero padding before t = 0 come from the same tiled copy (out-of-range rows fill with
 // zeros).  Arithmetic is packed f32x2; the sigmoid is 0.5 * tanh.approx(z/2) + 0.5.
+//
+// The same body also serves packed sequences (kModeVarlen: rows of [total, D], sequence
+// boundaries as events at single rows, final states from the register ring, plus
+// cconv_fwd_state_kernel for in-place or indexed states), no activation (kModeActNone), and
+// several problems in one launch (cconv_fwd_multi_kernel).
 #include <type_traits>
 
 #include "strip.cuh"

@@ -2,8 +2,9 @@
 //
 // A channel group is NC * 32 * VEC consecutive channels: one CTA tile row, split among NC
 // consumer warps of 32 lanes with VEC channels each, so each warp reads its part of a row as
-// one coalesced 16-byte (VEC=8), 8-byte (VEC=4) or 4-byte (VEC=2) access per lane.  Each group's rows,
-// flattened over (b, t), are cut into `cpc` equal contiguous ranges, one per CTA, so every
+// one coalesced 16-byte (VEC=8), 8-byte (VEC=4) or 4-byte (VEC=2) access per lane.  Each
+// group's rows, flattened over (b, t), are cut into `cpc` equal contiguous ranges, one per
+// CTA, so every
 // CTA gets the same number of rows (to within one) and the grid is one wave of resident
 // CTAs.  Inside a CTA a producer warp streams tiles of R rows x the group's channels into a
 // ring of S shared-memory stages with TMA; the consumer warps walk the same tiles in time
@@ -11,7 +12,10 @@
 // starts inside a sequence, its first tile starts 3 rows early to fill the ring; where it
 // starts a sequence, those 3 rows lie at t < 0 and the copy engine fills them with zeros,
 // which is exactly the causal zero padding.  Packed sequences of any lengths (SeqTracker)
-// take their ring at a sequence start from the sequence's initial state instead.
+// take their ring at a sequence start from the sequence's initial state instead, and their
+// ranges are of equal cost (cost_split) rather than equal rows.  The backward cuts the rows
+// the same way but per warp: each warp walks its own range of one channel strip with its
+// own pipeline (bwd.cu).
 #pragma once
 
 #include "common.cuh"

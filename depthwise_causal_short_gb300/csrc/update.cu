@@ -1,4 +1,5 @@
-// update.cu -- cconv_update: single-token decode update of a pooled conv state (one kernel).
+// update.cu -- cconv_update / cconv_update_ex: single-token decode update of a pooled conv
+// state (one kernel).
 //
 // Per row i with slot s = state_indices[i] (or i):
 //   window     = (state[s,d,0..W-2], x[i,d])          state[...,0] is the oldest
@@ -14,6 +15,10 @@
 // vector no CTA writes anything but CTA 0's status words (state rows are only read, and
 // only for in-range slots).  This replaces the pages' per-CTA O(N^2) scan and device trap
 // with an O(N + S/32) check and a status word.
+//
+// cconv_update_ex runs the same kernel with the PR's variants: a state of L = W entries
+// (the window takes the newest W-1), -1 as a padding row, circular-buffer states (the token
+// goes to entry cache_seqlens[i] mod L and nothing shifts), and no activation.
 #include <cstdlib>
 
 #include "common.cuh"
