@@ -82,3 +82,22 @@ def test_problem_counts(Ds):
 
 def test_short_rows():
     _run_and_check(2, 3, [64, 8, 72], 2, [True, True, False], seed=40)
+
+
+def test_backward_deterministic():
+    B, T, W = 2, 1000, 4
+    Ds = [512, 512, 1024]
+    probs = [inputs.fwd_bwd_inputs(B, T, D, W, True, seed=60 + k) for k, D in enumerate(Ds)]
+    xs = [p[0].cuda() for p in probs]
+    dys = [p[1].cuda() for p in probs]
+    ws = [p[2].cuda() for p in probs]
+    bs = [p[3].cuda() for p in probs]
+    a = cc.cconv_bwd_multi(xs, dys, ws, bs, want_dbias=True)
+    c = cc.cconv_bwd_multi(xs, dys, ws, bs, want_dbias=True)
+    torch.cuda.synchronize()
+    for u_list, v_list in zip(a, c):
+        for u, v in zip(u_list, v_list):
+            if u.dtype == torch.bfloat16:
+                assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+            else:
+                assert torch.equal(u, v)

@@ -158,3 +158,16 @@ def test_gpu_side_argument_errors():
 
 def test_no_device_fault_recorded():
     assert cc.cconv_device_fault() == 0
+
+
+@pytest.mark.parametrize("scale", [1e-4, 30.0, 1e3], ids=["tiny", "saturating", "huge"])
+def test_extreme_magnitudes(scale):
+    """x scaled far from N(0,1): tiny values, values where tanh saturates (|z| >> 1, the
+    SiLU's linear and zero sides), and huge ones; all within the forward / backward
+    tolerances of the oracle."""
+    B, T, D, W = 2, 300, 520, 4
+    x, dy, w, b = inputs.fwd_bwd_inputs(B, T, D, W, True, seed=95)
+    x = (x.float() * scale).to(torch.bfloat16)
+    y, dx, dw, db = _run(x, dy, w, b, want_dbias=True)
+    assert torch.isfinite(y.float()).all() and torch.isfinite(dx.float()).all()
+    _check(x, dy, w, b, y, dx, dw, db, f"scale {scale}")
