@@ -5,6 +5,7 @@ thin Python binding with the same names, plus the build step and the seeded synt
 input generators.  Importing the package does not load the library; the first call does,
 and raises if it has not been built.
 """
+from .autograd import causal_conv1d  # noqa: F401
 from .binding import (  # noqa: F401
     CCONV_ACT_NONE,
     CCONV_ACT_SILU,

@@ -22,10 +22,49 @@ cudaError_t report_cuda(const char* what, cudaError_t e) {
   return e;
 }
 
+static PFN_cuCtxGetCurrent_v4000 ctx_get_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  return fn;
+}
+
+// The driver call made here (cuTensorMapEncodeTiled) needs a context current on the
+// calling thread.  A thread that has so far made only runtime calls that bind none
+// (cudaGetDevice, cudaDeviceGetAttribute, stream-ordered allocator hits) has none:
+// autograd's per-device worker thread, for example, can reach a backward call before any
+// kernel launch of its own.  If no context is current, cudaSetDevice on the device already
+// current binds that device's primary context (the runtime creates it there since CUDA
+// 12) without changing which device is current; a context the caller made current itself,
+// primary or not, is left alone.  Checked once per thread and device.
+static int bind_current_context(int* device) {
+  thread_local int checked = -1;
+  int dev = 0;
+  if (report_cuda("cudaGetDevice", cudaGetDevice(&dev)) != cudaSuccess) return CCONV_ERR_CUDA;
+  if (checked != dev) {
+    PFN_cuCtxGetCurrent_v4000 get = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+      if (report_cuda("cudaSetDevice", cudaSetDevice(dev)) != cudaSuccess)
+        return CCONV_ERR_CUDA;
+    }
+    checked = dev;
+  }
+  if (device) *device = dev;
+  return CCONV_OK;
+}
+
 int sm_count_current_device(int* sms, int* device) {
   static std::atomic<int> cache[64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CCONV_ERR_CUDA;
+  if (bind_current_context(&dev) != CCONV_OK) return CCONV_ERR_CUDA;
   if (device) *device = dev;
   if (dev >= 0 && dev < 64) {
     const int c = cache[dev].load(std::memory_order_relaxed);
@@ -35,7 +74,10 @@ int sm_count_current_device(int* sms, int* device) {
     }
   }
   int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+  if (report_cuda("cudaDeviceGetAttribute",
+                  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) !=
+          cudaSuccess ||
+      n <= 0)
     return CCONV_ERR_CUDA;
   if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   *sms = n;
@@ -61,7 +103,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int encode_rows_map(CUtensorMap* map, const void* base, int64_t B, int64_t T, int64_t D,
                     int64_t sb, int64_t st, int box_c, int box_r) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc) return CCONV_ERR_CUDA;
+  if (!enc) {
+    report_cuda("cuTensorMapEncodeTiled lookup", cudaErrorSymbolNotFound);
+    return CCONV_ERR_CUDA;
+  }
+  if (bind_current_context(nullptr) != CCONV_OK) return CCONV_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)st * 2u, (cuuint64_t)sb * 2u};
   cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)box_r, 1u};
@@ -69,7 +115,12 @@ int encode_rows_map(CUtensorMap* map, const void* base, int64_t B, int64_t T, in
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? CCONV_OK : CCONV_ERR_CUDA;
+  if (r != CUDA_SUCCESS) {
+    static const bool debug = getenv("CCONV_DEBUG") != nullptr;
+    if (debug) fprintf(stderr, "cconv: cuTensorMapEncodeTiled failed: CUresult %d\n", (int)r);
+    return CCONV_ERR_CUDA;
+  }
+  return CCONV_OK;
 }
 
 int set_max_dynamic_smem(const void* func, int bytes) {

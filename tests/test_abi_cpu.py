@@ -3,6 +3,7 @@ include/cconv.h declares, and rejects bad arguments on the host before any CUDA 
 import ctypes
 
 import pytest
+import torch
 
 import depthwise_causal_short_gb300 as cc
 from depthwise_causal_short_gb300 import _build
@@ -187,3 +188,9 @@ def test_bwd_multi_workspace_query_rejects(lib):
     assert lib.cconv_bwd_multi_workspace_bytes(2, D, 2, 16, 6, ctypes.byref(n)) == EWIDTH
     assert lib.cconv_bwd_multi_workspace_bytes(2, _arr(ctypes.c_int64, [64, 12]), 2, 16, 4,
                                                ctypes.byref(n)) == EALIGN
+
+
+def test_causal_conv1d_rejects_unknown_activation():
+    x = torch.zeros(1, 4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        cc.causal_conv1d(x, torch.zeros(8, 4), activation="gelu")
