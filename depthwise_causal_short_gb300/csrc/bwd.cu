@@ -23,6 +23,10 @@
 // The same body also serves packed sequences (kModeVarlen: sequence boundaries are events
 // at single rows, with the initial state's gradient written), no activation (kModeActNone),
 // and several problems in one launch (cconv_bwd_multi_kernel).
+//
+// Batched rows of at least 8 strips take a lockstep form instead (cconv_bwd_ls_kernel): a
+// producer warp loads 8 neighbouring strips of one row range per stage, for x and dy
+// together, and 8 consumer warps run the same per-warp tile code on their strip of it.
 #include <mutex>
 #include <type_traits>
 
@@ -496,6 +500,149 @@ __global__ void __launch_bounds__(NW * 32, 1)
   bwd_cta<VEC, R, S, NW, SW, MODE>(&tmx, &tmdy, p, blockIdx.x % n_sg, blockIdx.x / n_sg);
 }
 
+// Lockstep form of the batched backward: NC consumer warps own the NC neighbouring channel
+// strips of one row range, and a producer warp (index NC) loads each stage's NC x tiles and
+// NC dy tiles together, so a stage is R rows of NC*CB contiguous channels of both tensors.
+// A stage is re-armed once every consumer has released it (full / empty mbarriers).  Each
+// consumer runs the same per-warp tile code as the independent-pipeline form; the partial
+// records have the same layout (SW = NC strips, one range per CTA).
+template <int VEC, int R, int S, int NC, int MODE>
+__device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtensorMap* tmdy,
+                                           const BwdArgs& p, int sg, int rg) {
+  constexpr bool ACT = (MODE & kModeActNone) == 0;
+  static_assert((MODE & kModeVarlen) == 0, "the lockstep form walks batched rows only");
+  constexpr int CB = 32 * VEC;
+  constexpr int P = VEC / 2;
+  constexpr int TILE = R * CB * 2;
+  constexpr int STAGE = 2 * NC * TILE;  // NC x tiles, then NC dy tiles
+  constexpr int REC = kRec * CB;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+  uint64_t* empty = full + S;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r0 = static_cast<int>(static_cast<int64_t>(rg) * p.BT / p.wpc);
+  const int r1 = static_cast<int>(static_cast<int64_t>(rg + 1) * p.BT / p.wpc);
+  const int c0 = sg * NC * CB;
+  int nact = static_cast<int>((p.D - c0 + CB - 1) / CB);  // consumer warps with channels
+  if (nact > NC) nact = NC;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(tmx);
+    prefetch_tensormap(tmdy);
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nact);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_dependency_wait();
+
+  f2 acc[kRec][P];
+#pragma unroll
+  for (int q = 0; q < P; ++q)
+#pragma unroll
+    for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
+
+  TileCursor cur;
+  cur.init(r0, r1, p.T, kRing, R);
+  if (warp == NC) {
+    // ---- producer warp -------------------------------------------------------------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t eph = 0;
+      int s = 0;
+      for (int i = 0; !cur.done; ++i) {
+        if (i >= S) {  // wait until every consumer has released this stage
+          if (!mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs)) {
+            atomicOr(&g_fault_bwd, kFaultBwdWait);
+            break;
+          }
+          eph ^= 1u << s;
+        }
+        uint8_t* st = smem + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], 2 * nact * TILE);
+        for (int w = 0; w < nact; ++w)
+          tma_load_3d(st + w * TILE, tmx, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
+        for (int w = 0; w < nact; ++w)
+          tma_load_3d(st + (NC + w) * TILE, tmdy, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
+        cur.advance();
+        s = (s + 1 == S) ? 0 : s + 1;
+      }
+    }
+  } else if (warp < nact) {
+    // ---- consumer ------------------------------------------------------------------------
+    const int64_t d0 = c0 + warp * CB + lane * VEC;
+    const bool active = d0 < p.D;
+    const bool all_active = c0 + nact * CB <= p.D && nact == NC;  // uniform over the CTA
+    f2 tap[4][P], bias2[P];
+    load_taps<VEC>(p.w, p.bias, p.wdt, p.W, d0, active, tap, bias2);
+    f2 h[3][P], gr[3][P];
+#pragma unroll
+    for (int q = 0; q < P; ++q)
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        h[j][q] = 0ull;
+        gr[j][q] = 0ull;
+      }
+    uint32_t fph = 0;
+    int s = 0;
+    while (!cur.done) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (fph >> s) & 1u,
+                                                               kWaitLimitNs));
+      if (!ok) {
+        if (lane == 0) atomicOr(&g_fault_bwd, kFaultBwdWait);
+        // Let the copies already issued land (bounded) before the stages are reused.
+        for (int j = 0; j < S; ++j)
+          (void)mbar_wait_bounded(&full[j], (fph >> j) & 1u, 100000000ull);
+        break;
+      }
+      fph ^= 1u << s;
+      const uint8_t* xt = smem + s * STAGE + warp * TILE;
+      const uint8_t* dyt = xt + NC * TILE;
+      const bool full_tile = cur.from == cur.tt && cur.tt >= cur.a + kRing && cur.tt + R <= cur.e;
+      if (full_tile) {
+        if (all_active)
+          bwd_tile<VEC, R, true, true, ACT>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+        else
+          bwd_tile<VEC, R, true, false, ACT>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+      } else {
+        bwd_tile<VEC, R, false, false, ACT>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      cur.advance();
+      s = (s + 1 == S) ? 0 : s + 1;
+    }
+  }
+  grid_launch_dependents();
+
+  // ---- the CTA's partial sums: one record per strip (one range per CTA) -------------------
+  __syncthreads();
+  float* rec = p.ws + static_cast<int64_t>(blockIdx.x) * NC * REC;
+  if (warp < NC) {
+#pragma unroll
+    for (int j = 0; j < kRec; ++j) {
+      float v[VEC];
+#pragma unroll
+      for (int q = 0; q < P; ++q)
+        f2_unpack(f2_mul(acc[j][q], f2_splat(0.5f)), v[2 * q], v[2 * q + 1]);
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) rec[warp * REC + j * CB + lane * VEC + q] = v[q];
+    }
+  }
+}
+
+template <int VEC, int R, int S, int NC, int MINB, int MODE>
+__global__ void __launch_bounds__((NC + 1) * 32, MINB)
+    cconv_bwd_ls_kernel(const __grid_constant__ CUtensorMap tmx,
+                        const __grid_constant__ CUtensorMap tmdy, const BwdArgs p) {
+  const int n_sg = (p.n_cb + NC - 1) / NC;
+  bwd_cta_ls<VEC, R, S, NC, MODE>(&tmx, &tmdy, p, blockIdx.x % n_sg, blockIdx.x / n_sg);
+}
+
 // ------------------------------------------------------------------------------------
 // Several problems in one launch (the q, k and v convolutions of a layer): the same rows
 // and width, each its own x, dy, weights, outputs and D.  Each problem's strips are grouped
@@ -682,32 +829,42 @@ static RedArgs red_args_one(const float* ws, int cb_width, int sw, int n_sg, int
 
 struct BwdConfig {
   int vec, rows, stages, warps, sw;
+  int producer;  // 1: a producer warp beside the warps consumer warps (lockstep form)
+  int minb;      // CTAs resident per SM
   void (*kernel)(const CUtensorMap, const CUtensorMap, const BwdArgs);
 };
 
 #define CCONV_BWD_CFG(V, R, S, NW, SW) \
-  BwdConfig { V, R, S, NW, SW, cconv_bwd_kernel<V, R, S, NW, SW, 0> }
+  BwdConfig { V, R, S, NW, SW, 0, 1, cconv_bwd_kernel<V, R, S, NW, SW, 0> }
+#define CCONV_BWD_LS_CFG(V, R, S, NC, M) \
+  BwdConfig { V, R, S, NC, NC, 1, M, cconv_bwd_ls_kernel<V, R, S, NC, M, 0> }
 
+// Entry 0 is the default from 2048 channels (16 strips of 128) up; narrower rows take entry
+// 1, whose 2-strip CTAs leave no consumer warp idle.  Measured at B=2 T=8192 (us, entry 0
+// against entry 1): D=1024 27.5 / 25.4, 1536 39.6 / 34.5, 2048 40.4 / 40.5, 3072 56.4 / 57.4,
+// 4096 69.7 / 72.4, 8192 130.2 / 148.8.  The others are for sweeps (CCONV_BWD_CONFIG =
+// index).
 static const BwdConfig kBwdConfigs[] = {
-    CCONV_BWD_CFG(4, 12, 3, 8, 2),  // measured fastest at B=2 T=8192 D=4096
-    CCONV_BWD_CFG(4, 12, 3, 8, 8),
+    CCONV_BWD_LS_CFG(4, 12, 4, 8, 1),
+    CCONV_BWD_CFG(4, 12, 3, 8, 2),
     CCONV_BWD_CFG(4, 12, 3, 8, 4),  // packed sequences and several problems use this shape
+    CCONV_BWD_CFG(4, 12, 3, 8, 8),
     CCONV_BWD_CFG(4, 16, 3, 8, 4),
-    CCONV_BWD_CFG(4, 12, 4, 8, 4),
-    CCONV_BWD_CFG(4, 18, 2, 8, 4),
-    CCONV_BWD_CFG(4, 24, 2, 8, 4),
     CCONV_BWD_CFG(4, 12, 2, 12, 4),
+    CCONV_BWD_LS_CFG(4, 16, 3, 8, 1),
+    CCONV_BWD_LS_CFG(4, 12, 4, 4, 2),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
-static int bwd_config_index() {
-  static int idx = -1;
-  if (idx < 0) {
+static const BwdConfig& bwd_config(int64_t D) {
+  static const int override_idx = [] {
     const char* e = getenv("CCONV_BWD_CONFIG");
-    int v = e ? atoi(e) : 0;
-    idx = (v >= 0 && v < kNumBwdConfigs) ? v : 0;
-  }
-  return idx;
+    const int v = e ? atoi(e) : -1;
+    return (v >= 0 && v < kNumBwdConfigs) ? v : -1;
+  }();
+  if (override_idx >= 0) return kBwdConfigs[override_idx];
+  const BwdConfig& ls = kBwdConfigs[0];
+  return D >= 2 * static_cast<int64_t>(ls.warps) * 32 * ls.vec ? ls : kBwdConfigs[1];
 }
 
 // Work split of the backward: strips of 32*VEC channels in groups of SW, each strip's rows in
@@ -726,7 +883,7 @@ static int bwd_plan(int64_t B, int64_t T, int64_t D, const BwdConfig& cfg, BwdPl
   const int64_t cbw = 32 * cfg.vec;
   plan->n_cb = static_cast<int>((D + cbw - 1) / cbw);
   plan->n_sg = (plan->n_cb + cfg.sw - 1) / cfg.sw;
-  int64_t n_rg = sms / plan->n_sg;                       // CTAs per strip group
+  int64_t n_rg = static_cast<int64_t>(sms) * cfg.minb / plan->n_sg;  // CTAs per strip group
   const int64_t by_rows = (B * T) / (32 * rw);           // ranges of at least 32 rows
   if (n_rg > by_rows) n_rg = by_rows;
   if (n_rg < 1) n_rg = 1;
@@ -755,7 +912,7 @@ CCONV_API int cconv_bwd_workspace_bytes(int64_t B, int64_t T, int64_t D, int W, 
   int rc = check_sizes(B, T, D, W);
   if (rc != CCONV_OK) return rc;
   BwdPlan plan;
-  return bwd_plan(B, T, D, kBwdConfigs[bwd_config_index()], &plan, bytes);
+  return bwd_plan(B, T, D, bwd_config(D), &plan, bytes);
 }
 
 CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy, int64_t sdb,
@@ -780,7 +937,7 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
       (dbias && reinterpret_cast<uintptr_t>(dbias) % ew != 0))
     return CCONV_ERR_ALIGN;
 
-  const BwdConfig& cfg = kBwdConfigs[bwd_config_index()];
+  const BwdConfig& cfg = bwd_config(D);
   BwdPlan plan;
   size_t need = 0;
   rc = bwd_plan(B, T, D, cfg, &plan, &need);
@@ -815,7 +972,8 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   if (smem < red_bytes) smem = red_bytes;  // the stage memory doubles as the reduction buffer
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(cfg.kernel), smem);
   if (rc != CCONV_OK) return rc;
-  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
+  if (launch_pdl(cfg.kernel, dim3(plan.grid), dim3((cfg.warps + cfg.producer) * 32), smem, st,
+                 tmx, tmdy, a) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
   const float* wsp = a.ws;
@@ -908,7 +1066,7 @@ static void (*const kBwdVarlenKernels[2])(const CUtensorMap, const CUtensorMap, 
     cconv_bwd_kernel<4, 12, 3, 8, 4, kModeVarlen>,
     cconv_bwd_kernel<4, 12, 3, 8, 4, kModeVarlen | kModeActNone>,
 };
-static const BwdConfig kBwdVarlenConfig = {4, 12, 3, 8, 4, nullptr};
+static const BwdConfig kBwdVarlenConfig = {4, 12, 3, 8, 4, 0, 1, nullptr};
 
 // Zeroes n bf16 values (the initial-state gradient when there are no rows at all).
 __global__ void cconv_zero_u16_kernel(uint16_t* p, int64_t n) {
@@ -1056,7 +1214,7 @@ struct MultiPlan {
   size_t ws_bytes;
 };
 
-static const BwdConfig kBwdMultiConfig = {4, 12, 3, 8, 4, nullptr};
+static const BwdConfig kBwdMultiConfig = {4, 12, 3, 8, 4, 0, 1, nullptr};
 
 static int multi_plan(int n, const int64_t* D, int64_t B, int64_t T, MultiPlan* mp) {
   const BwdConfig& cfg = kBwdMultiConfig;
