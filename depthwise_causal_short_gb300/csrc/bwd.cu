@@ -500,17 +500,18 @@ __global__ void __launch_bounds__(NW * 32, 1)
   bwd_cta<VEC, R, S, NW, SW, MODE>(&tmx, &tmdy, p, blockIdx.x % n_sg, blockIdx.x / n_sg);
 }
 
-// Lockstep form of the batched backward: NC consumer warps own the NC neighbouring channel
-// strips of one row range, and a producer warp (index NC) loads each stage's NC x tiles and
-// NC dy tiles together, so a stage is R rows of NC*CB contiguous channels of both tensors.
-// A stage is re-armed once every consumer has released it (full / empty mbarriers).  Each
-// consumer runs the same per-warp tile code as the independent-pipeline form; the partial
-// records have the same layout (SW = NC strips, one range per CTA).
+// Lockstep form of the backward: NC consumer warps own the NC neighbouring channel strips
+// of one row range, and a producer warp (index NC) loads each stage's NC x tiles and NC dy
+// tiles together, so a stage is R rows of NC*CB contiguous channels of both tensors.  A
+// stage is re-armed once every consumer has released it (full / empty mbarriers).  Each
+// consumer runs the same per-warp tile code as the independent-pipeline form (for packed
+// sequences, with its own sequence tracking); the partial records have the same layout
+// (SW = NC strips, one range per CTA).
 template <int VEC, int R, int S, int NC, int MODE>
 __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtensorMap* tmdy,
                                            const BwdArgs& p, int sg, int rg) {
+  constexpr bool VL = (MODE & kModeVarlen) != 0;
   constexpr bool ACT = (MODE & kModeActNone) == 0;
-  static_assert((MODE & kModeVarlen) == 0, "the lockstep form walks batched rows only");
   constexpr int CB = 32 * VEC;
   constexpr int P = VEC / 2;
   constexpr int TILE = R * CB * 2;
@@ -521,8 +522,15 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
   uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int r0 = static_cast<int>(static_cast<int64_t>(rg) * p.BT / p.wpc);
-  const int r1 = static_cast<int>(static_cast<int64_t>(rg + 1) * p.BT / p.wpc);
+  int r0, r1;
+  if constexpr (VL) {  // equal cost per range, as in the independent-pipeline form
+    constexpr int kBoundaryRows = 44;
+    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg, p.wpc, lane);
+    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg + 1, p.wpc, lane);
+  } else {
+    r0 = static_cast<int>(static_cast<int64_t>(rg) * p.BT / p.wpc);
+    r1 = static_cast<int>(static_cast<int64_t>(rg + 1) * p.BT / p.wpc);
+  }
   const int c0 = sg * NC * CB;
   int nact = static_cast<int>((p.D - c0 + CB - 1) / CB);  // consumer warps with channels
   if (nact > NC) nact = NC;
@@ -546,7 +554,7 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
 #pragma unroll
     for (int j = 0; j < kRec; ++j) acc[j][q] = 0ull;
 
-  TileCursor cur;
+  TileCursor cur;  // packed sequences: one batch row of T = total rows
   cur.init(r0, r1, p.T, kRing, R);
   if (warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
@@ -587,6 +595,18 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
         h[j][q] = 0ull;
         gr[j][q] = 0ull;
       }
+    // Packed sequences: the sequence of the rows walked (from the first ring-fill row on),
+    // and hin, the initial x ring of sequence hin_seq, fetched one sequence ahead.
+    SeqTracker sq;
+    f2 hin[3][P];
+    int hin_seq = -1;
+    if constexpr (VL) {
+      sq.init(p.cu, p.nseq, p.BT, r0 - kRing, lane);  // all lanes of the warp
+      if (sq.i + 1 < p.nseq) {
+        init_ring<VEC>(p.init, sq.i + 1, p.D, p.W, d0, active, hin);
+        hin_seq = sq.i + 1;
+      }
+    }
     uint32_t fph = 0;
     int s = 0;
     while (!cur.done) {
@@ -602,12 +622,18 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
       fph ^= 1u << s;
       const uint8_t* xt = smem + s * STAGE + warp * TILE;
       const uint8_t* dyt = xt + NC * TILE;
-      const bool full_tile = cur.from == cur.tt && cur.tt >= cur.a + kRing && cur.tt + R <= cur.e;
+      bool full_tile = cur.from == cur.tt && cur.tt >= cur.a + kRing && cur.tt + R <= cur.e;
+      if constexpr (VL)  // and no boundary inside, nor one within the 3 rows before
+        full_tile = full_tile && cur.tt - kRing >= sq.ss &&
+                    !(sq.i + 1 < p.nseq && sq.nb >= cur.tt && sq.nb < cur.tt + R);
       if (full_tile) {
         if (all_active)
           bwd_tile<VEC, R, true, true, ACT>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
         else
           bwd_tile<VEC, R, true, false, ACT>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
+      } else if constexpr (VL) {
+        bwd_tile_vl<VEC, R, ACT>(xt, dyt, lane, cur, sq, active, p, d0, tap, bias2, h, gr, acc,
+                                 hin, hin_seq);
       } else {
         bwd_tile<VEC, R, false, false, ACT>(xt, dyt, lane, cur, active, p, d0, tap, bias2, h, gr, acc);
       }
@@ -617,10 +643,31 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }
+  if constexpr (VL) {
+    // Empty sequences get a zero initial-state gradient (CTA i, i + grid, ...), and warp 0
+    // of CTA 0 checks cu_seqlens.
+    if (p.dinit && p.W > 1) {
+      const int64_t n = p.D * (p.W - 1);
+      for (int i = blockIdx.x; i < p.nseq; i += gridDim.x) {
+        if (clamp_row(p.cu[i + 1], p.BT) > clamp_row(p.cu[i], p.BT)) continue;
+        uint16_t* o = p.dinit + static_cast<int64_t>(i) * n;
+        for (int64_t k = threadIdx.x; k < n; k += (NC + 1) * 32) o[k] = 0;
+      }
+    }
+    if (blockIdx.x == 0 && warp == 0) {
+      bool bad = false;
+      for (int k = lane; k <= p.nseq; k += 32) {
+        const int v = p.cu[k];
+        if (v < 0 || v > p.BT || (k == 0 && v != 0) || (k == p.nseq && v != p.BT) ||
+            (k > 0 && p.cu[k - 1] > v))
+          bad = true;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_fault_bwd, kFaultSeqlens);
+    }
+  }
   grid_launch_dependents();
 
   // ---- the CTA's partial sums: one record per strip (one range per CTA) -------------------
-  __syncthreads();
   float* rec = p.ws + static_cast<int64_t>(blockIdx.x) * NC * REC;
   if (warp < NC) {
 #pragma unroll
@@ -680,6 +727,25 @@ __global__ void __launch_bounds__(NW * 32, 1)
   q.D = m.D[k];
   q.n_cb = m.n_cb[k];
   bwd_cta<VEC, R, S, NW, SW, 0>(&m.mx[k], &m.mdy[k], q, sga - m.sg0[k], blockIdx.x / n_sg);
+}
+
+// The same in the lockstep form (strip groups of NC strips per problem, one range per CTA).
+template <int VEC, int R, int S, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32, 1)
+    cconv_bwd_ls_multi_kernel(const __grid_constant__ BwdMulti m) {
+  const int n_sg = m.sg0[m.n];
+  const int sga = blockIdx.x % n_sg;
+  int k = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxProblems; ++j)
+    if (j < m.n && sga >= m.sg0[j]) k = j;
+  BwdArgs q = m.base;
+  q.w = m.w[k];
+  q.bias = m.bias[k];
+  q.dx = m.dx[k];
+  q.D = m.D[k];
+  q.n_cb = m.n_cb[k];
+  bwd_cta_ls<VEC, R, S, NC, 0>(&m.mx[k], &m.mdy[k], q, sga - m.sg0[k], blockIdx.x / n_sg);
 }
 
 // dw[d, W-1-lag] and dbias[d]: strip cb's records are slot cb % SW of the CTAs of strip group
@@ -1067,6 +1133,16 @@ static void (*const kBwdVarlenKernels[2])(const CUtensorMap, const CUtensorMap, 
     cconv_bwd_kernel<4, 12, 3, 8, 4, kModeVarlen | kModeActNone>,
 };
 static const BwdConfig kBwdVarlenConfig = {4, 12, 3, 8, 4, 0, 1, nullptr};
+// From 2048 channels on, the lockstep form (as for batched rows).
+static void (*const kBwdVarlenLsKernels[2])(const CUtensorMap, const CUtensorMap, const BwdArgs) = {
+    cconv_bwd_ls_kernel<4, 12, 4, 8, 1, kModeVarlen>,
+    cconv_bwd_ls_kernel<4, 12, 4, 8, 1, kModeVarlen | kModeActNone>,
+};
+static const BwdConfig kBwdVarlenLsConfig = {4, 12, 4, 8, 8, 1, 1, nullptr};
+
+static const BwdConfig& varlen_config(int64_t D) {
+  return D >= 2048 ? kBwdVarlenLsConfig : kBwdVarlenConfig;
+}
 
 // Zeroes n bf16 values (the initial-state gradient when there are no rows at all).
 __global__ void cconv_zero_u16_kernel(uint16_t* p, int64_t n) {
@@ -1096,7 +1172,7 @@ CCONV_API int cconv_bwd_varlen_workspace_bytes(int64_t total, int64_t D, int W, 
   int rc = check_varlen_sizes(total, D, W, 1);
   if (rc != CCONV_OK) return rc;
   BwdPlan plan;
-  return bwd_plan(1, total, D, kBwdVarlenConfig, &plan, bytes);
+  return bwd_plan(1, total, D, varlen_config(D), &plan, bytes);
 }
 
 CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64_t sdt,
@@ -1131,7 +1207,7 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
                 (d_initial_state && reinterpret_cast<uintptr_t>(d_initial_state) % 2 != 0)))
     return CCONV_ERR_ALIGN;
 
-  const BwdConfig& cfg = kBwdVarlenConfig;
+  const BwdConfig& cfg = varlen_config(D);
   BwdPlan plan;
   size_t need = 0;
   rc = bwd_plan(1, total, D, cfg, &plan, &need);
@@ -1185,14 +1261,14 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
   a.dinit = L > 0 ? static_cast<uint16_t*>(d_initial_state) : nullptr;
   a.nseq = static_cast<int>(nseq);
 
-  auto kern = kBwdVarlenKernels[act == CCONV_ACT_NONE ? 1 : 0];
+  auto kern = (cfg.producer ? kBwdVarlenLsKernels : kBwdVarlenKernels)[act == CCONV_ACT_NONE ? 1 : 0];
   int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
   const int red_bytes = cfg.warps * kRec * 32 * cfg.vec * static_cast<int>(sizeof(float));
   if (smem < red_bytes) smem = red_bytes;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (rc != CCONV_OK) return rc;
-  if (launch_pdl(kern, dim3(plan.grid), dim3(cfg.warps * 32), smem, st, tmx, tmdy, a) !=
-      cudaSuccess)
+  if (launch_pdl(kern, dim3(plan.grid), dim3((cfg.warps + cfg.producer) * 32), smem, st, tmx,
+                 tmdy, a) != cudaSuccess)
     return CCONV_ERR_CUDA;
   const RedArgs ra = red_args_one(a.ws, 32 * cfg.vec, cfg.sw, plan.n_sg, plan.n_rg, D, W, wdt_i,
                                   dw, dbias);
@@ -1215,9 +1291,22 @@ struct MultiPlan {
 };
 
 static const BwdConfig kBwdMultiConfig = {4, 12, 3, 8, 4, 0, 1, nullptr};
+static const BwdConfig kBwdMultiLsConfig = {4, 12, 4, 8, 8, 1, 1, nullptr};
+
+// The lockstep form when every problem fills a group of 8 strips (D > 896) and there are at
+// least two groups in all, as for the batched call from 2048 channels on.
+static const BwdConfig& multi_config(int n, const int64_t* D) {
+  int64_t strips = 0;
+  for (int k = 0; k < n; ++k) {
+    const int64_t c = (D[k] + 127) / 128;
+    if (c < 8) return kBwdMultiConfig;
+    strips += c;
+  }
+  return strips >= 16 ? kBwdMultiLsConfig : kBwdMultiConfig;
+}
 
 static int multi_plan(int n, const int64_t* D, int64_t B, int64_t T, MultiPlan* mp) {
-  const BwdConfig& cfg = kBwdMultiConfig;
+  const BwdConfig& cfg = multi_config(n, D);
   int sms = 0;
   const int rc = sm_count_current_device(&sms, nullptr);
   if (rc != CCONV_OK) return rc;
@@ -1302,7 +1391,7 @@ CCONV_API int cconv_bwd_multi(int n, const void* const* x, const int64_t* sxb,
   if (!workspace || workspace_bytes < mp.ws_bytes) return CCONV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return CCONV_ERR_ALIGN;
 
-  const BwdConfig& cfg = kBwdMultiConfig;
+  const BwdConfig& cfg = multi_config(n, D);
   BwdMulti m;
   BwdArgs& a = m.base;
   a = BwdArgs{};
@@ -1350,13 +1439,15 @@ CCONV_API int cconv_bwd_multi(int n, const void* const* x, const int64_t* sxb,
   m.n = n;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  auto kern = cconv_bwd_multi_kernel<4, 12, 3, 8, 4>;
+  auto kern = cfg.producer ? cconv_bwd_ls_multi_kernel<4, 12, 4, 8>
+                           : cconv_bwd_multi_kernel<4, 12, 3, 8, 4>;
   int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
   const int red_bytes = cfg.warps * kRec * 32 * cfg.vec * static_cast<int>(sizeof(float));
   if (smem < red_bytes) smem = red_bytes;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (rc != CCONV_OK) return rc;
-  if (launch_pdl(kern, dim3(mp.grid), dim3(cfg.warps * 32), smem, st, m) != cudaSuccess)
+  if (launch_pdl(kern, dim3(mp.grid), dim3((cfg.warps + cfg.producer) * 32), smem, st, m) !=
+      cudaSuccess)
     return CCONV_ERR_CUDA;
   if (launch_pdl(cconv_bwd_reduce_kernel, dim3(static_cast<unsigned>(blk), any_dbias ? kRec : W),
                  dim3(32 * kRedGroups), 0, st, ra) != cudaSuccess)
