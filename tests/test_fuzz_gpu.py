@@ -5,8 +5,9 @@ reproducible case: batched forward / backward with random B, T, D tails, widths,
 weight dtype and row strides; packed sequences with random length mixes (empty and short
 ones included), states, activation; decode updates with random pools, state lengths,
 padding rows and layouts, shifting or circular (random positions); several problems in one
-launch.  Sizes stay small enough for
-the fp64 oracle to finish in milliseconds.
+launch; and the same three backward calls at widths of 2048 channels and more, where they
+take the lockstep kernels (with ragged last strip groups and short ranges).  Sizes stay
+small enough for the fp64 oracle to finish in milliseconds.
 """
 import random
 
@@ -205,3 +206,84 @@ def test_decode_ring(case):
     assert np.array_equal(bits(sg), st_ref), f"{what}: pool"
     live = (idx >= 0).numpy()
     assert rel_err(f64(y)[live], y_ref[live]) <= FWD_TOL, f"{what}: y"
+
+
+# Widths from 2048 channels on take the lockstep backward kernels (a producer warp streams 8
+# strips per stage); these cases cover them with ragged last strip groups, rows that give
+# short ranges, strided x, and every width and weight dtype.
+@pytest.mark.parametrize("case", range(N_CASES // 4))
+def test_lockstep_batched(case):
+    r = random.Random(6000 + case)
+    B, T = r.randint(1, 3), r.choice([1, 3, 17, 64, 130, 333])
+    D = 8 * r.randint(256, 640)
+    W = r.randint(1, 4)
+    has_bias = r.random() < 0.6
+    wdt = r.choice([torch.float32, torch.bfloat16])
+    pad = 8 * r.randint(0, 2)
+    x, dy, w, b = inputs.fwd_bwd_inputs(B, T, D, W, has_bias, wdtype=wdt, seed=6000 + case)
+    dev = torch.device("cuda", 0)
+    xg, dyg = _strided(x, pad, dev), _strided(dy, 0, dev)
+    bg = None if b is None else b.to(dev)
+    dx, dw, db = cc.cconv_bwd(xg, dyg, w.to(dev), bg, want_dbias=True)
+    torch.cuda.synchronize()
+    what = f"B={B} T={T} D={D} W={W} bias={has_bias} {wdt} pad={pad}"
+    rdx, rdw, rdb = oracle_bwd(x, dy, w, b, want_dbias=True)
+    for name, g, ref in (("dx", dx, rdx), ("dw", dw, rdw), ("dbias", db, rdb)):
+        assert rel_err(f64(g), ref) <= BWD_TOL, f"{what}: {name}"
+
+
+@pytest.mark.parametrize("case", range(N_CASES // 4))
+def test_lockstep_packed(case):
+    r = random.Random(7000 + case)
+    nseq = r.randint(1, 10)
+    lens = [r.choice([0, 1, 2, 3, r.randint(4, 40), r.randint(40, 300)]) for _ in range(nseq)]
+    if sum(lens) == 0:
+        lens[-1] = 5
+    D = 8 * r.randint(256, 520)
+    W = r.randint(1, 4)
+    act = r.choice(["silu", None])
+    with_init = r.random() < 0.7
+    x, dy, cu, w, b, init = inputs.varlen_inputs(lens, D, W, bias=r.random() < 0.5,
+                                                 wdtype=r.choice([torch.float32,
+                                                                  torch.bfloat16]),
+                                                 seed=7000 + case)
+    init = init if with_init else None
+    dev = torch.device("cuda", 0)
+    ig = None if init is None else init.to(dev)
+    bg = None if b is None else b.to(dev)
+    dx, dw, db, di = cc.cconv_bwd_varlen(x.to(dev), dy.to(dev), cu.to(dev), w.to(dev), bg,
+                                         activation=act, initial_state=ig, want_dbias=True,
+                                         want_dinit=True)
+    torch.cuda.synchronize()
+    what = f"lens={lens} D={D} W={W} act={act} init={with_init}"
+    rdx, rdw, rdb, rdi = oracle.bwd_seq(f64(x), f64(dy), cu.numpy(), f64(w), f64(b), f64(init),
+                                        act, want_dinit=True)
+    for name, g, ref in (("dx", dx, rdx), ("dw", dw, rdw), ("dbias", db, rdb),
+                         ("d_initial_state", di, rdi)):
+        assert rel_err(f64(g), ref) <= BWD_TOL, f"{what}: {name}"
+
+
+@pytest.mark.parametrize("case", range(N_CASES // 4))
+def test_lockstep_multi(case):
+    r = random.Random(8000 + case)
+    n = r.randint(1, 4)
+    B, T = r.randint(1, 2), r.choice([1, 4, 33, 300])
+    W = r.randint(1, 4)
+    Ds = [8 * r.randint(113, 300) for _ in range(n)]  # each fills a group of 8 strips
+    if sum(Ds) < 2048:
+        Ds[0] = 2048
+    wdt = r.choice([torch.float32, torch.bfloat16])
+    probs = [inputs.fwd_bwd_inputs(B, T, D, W, r.random() < 0.5, wdtype=wdt,
+                                   seed=8000 + case * 10 + k) for k, D in enumerate(Ds)]
+    dev = torch.device("cuda", 0)
+    xs = [p[0].to(dev) for p in probs]
+    dys = [p[1].to(dev) for p in probs]
+    ws = [p[2].to(dev) for p in probs]
+    bs = [None if p[3] is None else p[3].to(dev) for p in probs]
+    dxs, dws, dbs = cc.cconv_bwd_multi(xs, dys, ws, bs, want_dbias=True)
+    torch.cuda.synchronize()
+    for k, (x, dy, w, b) in enumerate(probs):
+        what = f"n={n} B={B} T={T} Ds={Ds} W={W} problem {k}"
+        rdx, rdw, rdb = oracle_bwd(x, dy, w, b, want_dbias=True)
+        for name, gt, ref in (("dx", dxs[k], rdx), ("dw", dws[k], rdw), ("dbias", dbs[k], rdb)):
+            assert rel_err(f64(gt), ref) <= BWD_TOL, f"{what}: {name}"
