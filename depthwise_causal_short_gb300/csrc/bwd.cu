@@ -293,6 +293,31 @@ __device__ __forceinline__ void bwd_tile_vl(const uint8_t* xt, const uint8_t* dy
   }
 }
 
+// Packed sequences, once per CTA after its rows: empty sequences get a zero initial-state
+// gradient (CTA i, i + grid, ...; all nthreads threads), and warp 0 of CTA 0 checks
+// cu_seqlens (a malformed one sets the fault word).
+__device__ __forceinline__ void bwd_varlen_tail(const BwdArgs& p, int nthreads, int warp,
+                                                int lane) {
+  if (p.dinit && p.W > 1) {
+    const int64_t n = p.D * (p.W - 1);
+    for (int i = blockIdx.x; i < p.nseq; i += gridDim.x) {
+      if (clamp_row(p.cu[i + 1], p.BT) > clamp_row(p.cu[i], p.BT)) continue;
+      uint16_t* o = p.dinit + static_cast<int64_t>(i) * n;
+      for (int64_t k = threadIdx.x; k < n; k += nthreads) o[k] = 0;
+    }
+  }
+  if (blockIdx.x == 0 && warp == 0) {
+    bool bad = false;
+    for (int k = lane; k <= p.nseq; k += 32) {
+      const int v = p.cu[k];
+      if (v < 0 || v > p.BT || (k == 0 && v != 0) || (k == p.nseq && v != p.BT) ||
+          (k > 0 && p.cu[k - 1] > v))
+        bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_fault_bwd, kFaultSeqlens);
+  }
+}
+
 // CTA: NW warps = SW neighbouring strips x RW = NW/SW consecutive row ranges (strips fastest,
 // so at any time the CTA reads SW*32*VEC contiguous channels of the same rows); each warp
 // runs its own TMA pipeline; the RW partial sums of each strip are added inside the CTA.
@@ -443,28 +468,7 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }
-  if constexpr (VL) {
-    // Empty sequences get a zero initial-state gradient (CTA i, i + grid, ...), and warp 0
-    // of CTA 0 checks cu_seqlens.
-    if (p.dinit && p.W > 1) {
-      const int64_t n = p.D * (p.W - 1);
-      for (int i = blockIdx.x; i < p.nseq; i += gridDim.x) {
-        if (clamp_row(p.cu[i + 1], p.BT) > clamp_row(p.cu[i], p.BT)) continue;
-        uint16_t* o = p.dinit + static_cast<int64_t>(i) * n;
-        for (int64_t k = threadIdx.x; k < n; k += NW * 32) o[k] = 0;
-      }
-    }
-    if (blockIdx.x == 0 && warp == 0) {
-      bool bad = false;
-      for (int k = lane; k <= p.nseq; k += 32) {
-        const int v = p.cu[k];
-        if (v < 0 || v > p.BT || (k == 0 && v != 0) || (k == p.nseq && v != p.BT) ||
-            (k > 0 && p.cu[k - 1] > v))
-          bad = true;
-      }
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_fault_bwd, kFaultSeqlens);
-    }
-  }
+  if constexpr (VL) bwd_varlen_tail(p, NW * 32, warp, lane);
   grid_launch_dependents();
 
   // ---- the CTA's partial sums, added in a fixed order ------------------------------------
@@ -643,28 +647,7 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }
-  if constexpr (VL) {
-    // Empty sequences get a zero initial-state gradient (CTA i, i + grid, ...), and warp 0
-    // of CTA 0 checks cu_seqlens.
-    if (p.dinit && p.W > 1) {
-      const int64_t n = p.D * (p.W - 1);
-      for (int i = blockIdx.x; i < p.nseq; i += gridDim.x) {
-        if (clamp_row(p.cu[i + 1], p.BT) > clamp_row(p.cu[i], p.BT)) continue;
-        uint16_t* o = p.dinit + static_cast<int64_t>(i) * n;
-        for (int64_t k = threadIdx.x; k < n; k += (NC + 1) * 32) o[k] = 0;
-      }
-    }
-    if (blockIdx.x == 0 && warp == 0) {
-      bool bad = false;
-      for (int k = lane; k <= p.nseq; k += 32) {
-        const int v = p.cu[k];
-        if (v < 0 || v > p.BT || (k == 0 && v != 0) || (k == p.nseq && v != p.BT) ||
-            (k > 0 && p.cu[k - 1] > v))
-          bad = true;
-      }
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_fault_bwd, kFaultSeqlens);
-    }
-  }
+  if constexpr (VL) bwd_varlen_tail(p, (NC + 1) * 32, warp, lane);
   grid_launch_dependents();
 
   // ---- the CTA's partial sums: one record per strip (one range per CTA) -------------------
