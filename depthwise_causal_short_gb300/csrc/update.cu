@@ -49,7 +49,10 @@ __device__ __forceinline__ int ring_mod(int64_t a, int m) {
   return r < 0 ? r + m : r;
 }
 
+// Threads per CTA: 256, or 64 for small decode batches on the vector path (more CTAs over
+// the same rows; the host picks).
 constexpr int kUpdThreads = 256;
+constexpr int kUpdThreadsSmall = 64;
 
 __device__ __forceinline__ float load_w(const void* p, int64_t i, int wdt) {
   return wdt == CCONV_F32 ? static_cast<const float*>(p)[i]
@@ -127,8 +130,8 @@ __device__ __forceinline__ void load_update_taps(const UpdArgs& p, int64_t d0,
 // whose latency the runtime tests measurably add to).  kUpdRing: the state of a slot is a
 // ring of L entries; the token goes to entry head = pos[i] mod L, the window is the W-1
 // entries before it (oldest first), and only the head entry is written.
-template <int VEC, int W, int L, int ROWS, int MODE>
-__global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs p) {
+template <int VEC, int W, int L, int ROWS, int MODE, int NT>
+__global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
   static_assert(L == W - 1 || L == W, "state length is W-1 or W");
   static_assert(MODE != kUpdRing || L > 0, "a ring needs at least one entry");
   constexpr bool GEN = MODE != kUpdPlain;
@@ -142,11 +145,11 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
   if (p.idx) {  // shared-memory set-up only: no global access before the dependency wait
     if (threadIdx.x == 0) s_bad = 0;
     const int nwords = static_cast<int>((p.S + 31) / 32);
-    for (int i = threadIdx.x; i < nwords; i += kUpdThreads) bitmap[i] = 0u;
+    for (int i = threadIdx.x; i < nwords; i += NT) bitmap[i] = 0u;
   }
   grid_dependency_wait();
 
-  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kUpdThreads + threadIdx.x) * VEC;
+  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * NT + threadIdx.x) * VEC;
   const bool mine = d0 < p.D;
   const int64_t i0 = static_cast<int64_t>(blockIdx.y) * ROWS;
 
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
   if (p.idx) {
     __syncthreads();  // the zeroed bitmap is visible
     int off = 0;
-    for (int64_t i = threadIdx.x; i < p.N; i += kUpdThreads) {
+    for (int64_t i = threadIdx.x; i < p.N; i += NT) {
       const int32_t v = p.idx[i];
       if (pad && v == -1) continue;  // a padding row
       if (v < 0) {
@@ -290,49 +293,57 @@ __global__ void __launch_bounds__(kUpdThreads) cconv_update_kernel(const UpdArgs
 typedef void (*UpdKernel)(const UpdArgs);
 
 // No kernel for a ring of zero entries (the host refuses it before choosing).
-template <int VEC, int W, int L, int ROWS, int MODE>
+template <int VEC, int W, int L, int ROWS, int MODE, int NT>
 static UpdKernel update_kernel() {
   if constexpr (MODE == kUpdRing && L == 0)
     return nullptr;
   else
-    return cconv_update_kernel<VEC, W, L, ROWS, MODE>;
+    return cconv_update_kernel<VEC, W, L, ROWS, MODE, NT>;
 }
 
-template <int VEC, int ROWS, int OFF, int MODE>
+template <int VEC, int ROWS, int OFF, int MODE, int NT>
 static UpdKernel pick_update_kernel_w(int W) {
   switch (W) {
-    case 1: return update_kernel<VEC, 1, 0 + OFF, ROWS, MODE>();
-    case 2: return update_kernel<VEC, 2, 1 + OFF, ROWS, MODE>();
-    case 3: return update_kernel<VEC, 3, 2 + OFF, ROWS, MODE>();
-    default: return update_kernel<VEC, 4, 3 + OFF, ROWS, MODE>();
+    case 1: return update_kernel<VEC, 1, 0 + OFF, ROWS, MODE, NT>();
+    case 2: return update_kernel<VEC, 2, 1 + OFF, ROWS, MODE, NT>();
+    case 3: return update_kernel<VEC, 3, 2 + OFF, ROWS, MODE, NT>();
+    default: return update_kernel<VEC, 4, 3 + OFF, ROWS, MODE, NT>();
   }
 }
 
 // L = W - 1 + off.  mode: kUpdGeneral when padding rows or another activation are asked
 // for, kUpdRing for circular-buffer states.  The general kernels take fewer row counts (1
-// and 4).
-template <int VEC>
+// and 4), and the 64-thread plain kernels 1, 2 and 4.
+template <int VEC, int NT>
 static UpdKernel pick_update_kernel(int W, int rows, int off, int mode) {
   if (mode == kUpdRing) {
     if (off)
-      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, kUpdRing>(W)
-                       : pick_update_kernel_w<VEC, 1, 1, kUpdRing>(W);
-    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, kUpdRing>(W)
-                     : pick_update_kernel_w<VEC, 1, 0, kUpdRing>(W);
+      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, kUpdRing, NT>(W)
+                       : pick_update_kernel_w<VEC, 1, 1, kUpdRing, NT>(W);
+    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, kUpdRing, NT>(W)
+                     : pick_update_kernel_w<VEC, 1, 0, kUpdRing, NT>(W);
   }
   if (off || mode == kUpdGeneral) {
     if (off)
-      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, kUpdGeneral>(W)
-                       : pick_update_kernel_w<VEC, 1, 1, kUpdGeneral>(W);
-    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, kUpdGeneral>(W)
-                     : pick_update_kernel_w<VEC, 1, 0, kUpdGeneral>(W);
+      return rows >= 4 ? pick_update_kernel_w<VEC, 4, 1, kUpdGeneral, NT>(W)
+                       : pick_update_kernel_w<VEC, 1, 1, kUpdGeneral, NT>(W);
+    return rows >= 4 ? pick_update_kernel_w<VEC, 4, 0, kUpdGeneral, NT>(W)
+                     : pick_update_kernel_w<VEC, 1, 0, kUpdGeneral, NT>(W);
   }
-  switch (rows) {
-    case 1: return pick_update_kernel_w<VEC, 1, 0, kUpdPlain>(W);
-    case 2: return pick_update_kernel_w<VEC, 2, 0, kUpdPlain>(W);
-    case 4: return pick_update_kernel_w<VEC, 4, 0, kUpdPlain>(W);
-    case 8: return pick_update_kernel_w<VEC, 8, 0, kUpdPlain>(W);
-    default: return pick_update_kernel_w<VEC, 16, 0, kUpdPlain>(W);
+  if constexpr (NT == kUpdThreadsSmall) {
+    switch (rows) {
+      case 1: return pick_update_kernel_w<VEC, 1, 0, kUpdPlain, NT>(W);
+      case 2: return pick_update_kernel_w<VEC, 2, 0, kUpdPlain, NT>(W);
+      default: return pick_update_kernel_w<VEC, 4, 0, kUpdPlain, NT>(W);
+    }
+  } else {
+    switch (rows) {
+      case 1: return pick_update_kernel_w<VEC, 1, 0, kUpdPlain, NT>(W);
+      case 2: return pick_update_kernel_w<VEC, 2, 0, kUpdPlain, NT>(W);
+      case 4: return pick_update_kernel_w<VEC, 4, 0, kUpdPlain, NT>(W);
+      case 8: return pick_update_kernel_w<VEC, 8, 0, kUpdPlain, NT>(W);
+      default: return pick_update_kernel_w<VEC, 16, 0, kUpdPlain, NT>(W);
+    }
   }
 }
 
@@ -379,27 +390,47 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
   int sms = 0;
   int rc = sm_count_current_device(&sms, nullptr);
   if (rc != CCONV_OK) return rc;
-  // Rows per thread: 4 measured fastest for the decode workload (N=256, D=4096: 128 CTAs,
-  // 5.1 us per step in a CUDA graph against 8.0 us with one row): every CTA repeats the O(N)
-  // index check, so fewer, fuller CTAs cost less, and each thread keeps four rows' loads in
-  // flight.  Fewer rows only when four would leave more than half of the SMs idle.
+  const int off = L - (W - 1);
+  const int mode = pos ? kUpdRing : (pad != 0 || act != CCONV_ACT_SILU) ? kUpdGeneral : kUpdPlain;
   const int64_t nvec = (D + vec - 1) / vec;
-  const int64_t gx = (nvec + kUpdThreads - 1) / kUpdThreads;
+  // Small batches on the vector path: 64-thread CTAs, with the fewest rows per thread (1, 2
+  // or 4) that keep the grid within one wave, as long as that grid stays within two waves.
+  // Measured at S=512 D=4096 W=4 in a CUDA graph (us per step, 64- against 256-thread
+  // CTAs): N=1 1.44 / 2.79, 16 1.89 / 3.11, 64 2.45 / 3.04, 128 3.29 / 4.64; from N=192 on
+  // the 256-thread CTAs win (256: 4.97 against 5.88).
+  int nt = kUpdThreads;
   int rows = 4;
-  while (rows > 1 && 2 * gx * ((N + rows - 1) / rows) < static_cast<int64_t>(sms)) rows /= 2;
+  if (vec == 8) {
+    const int64_t gx_small = (nvec + kUpdThreadsSmall - 1) / kUpdThreadsSmall;
+    int r = 1;
+    while (r < 4 && gx_small * ((N + r - 1) / r) > sms) r *= 2;
+    if (gx_small * ((N + r - 1) / r) <= 2 * static_cast<int64_t>(sms)) {
+      nt = kUpdThreadsSmall;
+      rows = r;
+    }
+  }
+  const int64_t gx = (nvec + nt - 1) / nt;
+  if (nt == kUpdThreads) {
+    // Rows per thread: 4 measured fastest for the decode workload (N=256, D=4096: 128 CTAs,
+    // 5.1 us per step in a CUDA graph against 8.0 us with one row): every CTA repeats the
+    // O(N) index check, so fewer, fuller CTAs cost less, and each thread keeps four rows'
+    // loads in flight.  Fewer rows only when four would leave more than half of the SMs idle.
+    while (rows > 1 && 2 * gx * ((N + rows - 1) / rows) < static_cast<int64_t>(sms)) rows /= 2;
+  }
   static const int rows_override = [] {  // sweeps only: CCONV_UPDATE_ROWS = 1, 2, 4, 8 or 16
     const char* e = getenv("CCONV_UPDATE_ROWS");
     const int v = e ? atoi(e) : 0;
     return (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ? v : 0;
   }();
   if (rows_override) rows = rows_override;
-  const int off = L - (W - 1);
-  const int mode = pos ? kUpdRing : (pad != 0 || act != CCONV_ACT_SILU) ? kUpdGeneral : kUpdPlain;
+  if (nt == kUpdThreadsSmall && rows > 4) rows = 4;
   if ((off || mode != kUpdPlain) && rows != 4) rows = 1;  // general kernels: 1 and 4 rows
   const int64_t gy = (N + rows - 1) / rows;
   if (gx > 2147483647 || gy > 65535) return CCONV_ERR_SHAPE;
-  UpdKernel kern = vec8 ? pick_update_kernel<8>(W, rows, off, mode)
-                        : pick_update_kernel<1>(W, rows, off, mode);
+  UpdKernel kern = vec8 ? (nt == kUpdThreadsSmall
+                               ? pick_update_kernel<8, kUpdThreadsSmall>(W, rows, off, mode)
+                               : pick_update_kernel<8, kUpdThreads>(W, rows, off, mode))
+                        : pick_update_kernel<1, kUpdThreads>(W, rows, off, mode);
   if (!kern) return CCONV_ERR_SHAPE;
 
   UpdArgs a;
@@ -426,7 +457,7 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
       return CCONV_ERR_CUDA;
   }
   return launch_pdl(kern, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
-                    dim3(kUpdThreads), smem, reinterpret_cast<cudaStream_t>(stream), a) ==
+                    dim3(nt), smem, reinterpret_cast<cudaStream_t>(stream), a) ==
                  cudaSuccess
              ? CCONV_OK
              : CCONV_ERR_CUDA;
