@@ -286,26 +286,33 @@ def run_ours(args, world, rank, local):
     u_us = loop_us(upd, K)
 
     # ---- decode: 1000 steps replayed from one CUDA graph --------------------------------
-    g = torch.cuda.CUDAGraph()
-    s2 = torch.cuda.Stream(device=dev)
-    s2.wait_stream(stream)
-    with torch.cuda.stream(s2):
-        cc.cconv_update(xr[0], st, wd, bd, idx, y=yd, status=status, stream=s2)
-        with torch.cuda.graph(g, stream=s2):
-            for j in range(DEC.steps):
-                cc.cconv_update(xr[j % xr.shape[0]], st, wd, bd, idx, y=yd, status=status,
-                                stream=s2)
-    torch.cuda.synchronize()
-    g.replay()
-    torch.cuda.synchronize()
-    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 5
-    ga.record(stream)
-    for _ in range(reps):
+    def decode_graph_us(n_rows):
+        """us per decode step of the first n_rows rows (and slots), from one CUDA graph."""
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(device=dev)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            cc.cconv_update(xr[0][:n_rows], st, wd, bd, idx[:n_rows], y=yd[:n_rows],
+                            status=status, stream=s2)
+            with torch.cuda.graph(g, stream=s2):
+                for j in range(DEC.steps):
+                    cc.cconv_update(xr[j % xr.shape[0]][:n_rows], st, wd, bd, idx[:n_rows],
+                                    y=yd[:n_rows], status=status, stream=s2)
+        torch.cuda.synchronize()
         g.replay()
-    gb.record(stream)
-    torch.cuda.synchronize()
-    dec_graph_us = ga.elapsed_time(gb) * 1e3 / (reps * DEC.steps)
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        ga.record(stream)
+        for _ in range(reps):
+            g.replay()
+        gb.record(stream)
+        torch.cuda.synchronize()
+        return ga.elapsed_time(gb) * 1e3 / (reps * DEC.steps)
+
+    dec_graph_us = decode_graph_us(DEC.N)
+    dec_small_us = {n: decode_graph_us(n) for n in (1, 16, 64)}
+    assert status.tolist() == [0, 0]
 
     # ---- packed sequences: same rows, 16 mixed lengths, with states ------------------------
     lens = inputs.seqlen_mix(FWD.B * FWD.T, VL_NSEQ, seed=rank)
@@ -425,6 +432,9 @@ def run_ours(args, world, rank, local):
             "decode_update": {"us_per_step_stream": round(u_us, 3),
                               "us_per_step_graph": round(dec_graph_us, 3),
                               "bytes_per_step": DEC_BYTES},
+            "decode_update_small_batches": {
+                "us_per_step_graph": {str(n): round(v, 3) for n, v in dec_small_us.items()},
+                "note": "the same pool, weights and tokens, first N rows and slots only"},
             "fwd_varlen": {"us": round(vf_us, 3),
                            "tbps": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e12, 4),
                            "frac_of_peak": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e9 / peak_gbs, 4),
