@@ -389,14 +389,13 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
     Cursor pc, cc;
     pc.init(r0, r1, p.T, kRing, R);
     cc = pc;
-    const uint64_t pol = policy_evict_first();
     if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < S; ++s) {
         if (!pc.done) {
           mbar_arrive_expect_tx(&bars[s], STAGE);
-          tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b, pol);
-          tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+          tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b);
+          tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b);
           pc.advance();
         }
       }
@@ -460,8 +459,8 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
       if (lane == 0 && !pc.done) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars[s], STAGE);
-        tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b, pol);
-        tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b, pol);
+        tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b);
+        tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b);
         pc.advance();
       }
       cc.advance();
@@ -563,8 +562,7 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
   if (warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      uint32_t eph = 0;
+        uint32_t eph = 0;
       int s = 0;
       for (int i = 0; !cur.done; ++i) {
         if (i >= S) {  // wait until every consumer has released this stage
@@ -577,9 +575,9 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
         uint8_t* st = smem + s * STAGE;
         mbar_arrive_expect_tx(&full[s], 2 * nact * TILE);
         for (int w = 0; w < nact; ++w)
-          tma_load_3d(st + w * TILE, tmx, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
+          tma_load_3d(st + w * TILE, tmx, &full[s], c0 + w * CB, cur.tt, cur.b);
         for (int w = 0; w < nact; ++w)
-          tma_load_3d(st + (NC + w) * TILE, tmdy, &full[s], c0 + w * CB, cur.tt, cur.b, pol);
+          tma_load_3d(st + (NC + w) * TILE, tmdy, &full[s], c0 + w * CB, cur.tt, cur.b);
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }

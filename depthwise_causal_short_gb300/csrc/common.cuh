@@ -91,26 +91,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 // Coordinates are (innermost, middle, outermost) = (channel, row, batch).  Rows outside
-// [0, T) and channels outside [0, D) are filled with zeros by the copy engine.
+// [0, T) and channels outside [0, D) are filled with zeros by the copy engine.  No L2 cache
+// hint: with an evict_first policy the stream kernels were slower (backward 70.2 against
+// 67.0 us, forward 43.4 against 42.0 us at B=2 T=8192 D=4096, with streaming row stores in
+// both; an evict_normal policy gave 67.3 and 43.0 us).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c, int r, int b, uint64_t policy) {
+                                            int c, int r, int b) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(b), "r"(smem_addr(bar)),
-      "l"(policy)
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(b), "r"(smem_addr(bar))
       : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// L2 eviction policy for data read exactly once.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 __device__ __forceinline__ uint4 lds128(const void* p) {

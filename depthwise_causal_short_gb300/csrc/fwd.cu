@@ -115,12 +115,12 @@ __device__ __forceinline__ void fwd_tile(const uint8_t* tile, int lane, const Ti
 // Loads one tile (rows cur.tt .. cur.tt+R-1, one box per consumer warp) into a stage.
 template <int VEC, int R, int NC, class Cursor>
 __device__ __forceinline__ void fwd_issue(uint8_t* st, uint64_t* full, const CUtensorMap* tmx,
-                                          const Cursor& cur, int nact, int c0, uint64_t pol) {
+                                          const Cursor& cur, int nact, int c0) {
   constexpr int CB = 32 * VEC;
   constexpr int TILE = R * CB * 2;
   mbar_arrive_expect_tx(full, nact * TILE);
   for (int w = 0; w < nact; ++w)
-    tma_load_3d(st + w * TILE, tmx, full, c0 + w * CB, cur.tt, cur.b, pol);
+    tma_load_3d(st + w * TILE, tmx, full, c0 + w * CB, cur.tt, cur.b);
 }
 
 // Slot of sequence i in the state arrays, or -1 when the index is unusable (the state
@@ -290,7 +290,6 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
 
   Cursor cur;  // packed sequences: one batch row of T = total rows
   cur.init(r0, r1, p.T, 0, R);
-  const uint64_t pol = policy_evict_first();
   if (SEP && warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
     if (lane == 0) {
@@ -304,7 +303,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
           }
           eph ^= 1u << s;
         }
-        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, cur, nact, c0, pol);
+        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, cur, nact, c0);
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }
@@ -320,7 +319,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
     Cursor pc = cur;  // the leader's producer cursor, S tiles ahead
     if (leader && lane == 0) {
       for (int s = 0; s < S && !pc.done; ++s) {
-        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0, pol);
+        fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0);
         pc.advance();
       }
     }
@@ -379,7 +378,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
         if (lane == 0 && !pc.done) {
           fine = mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs);
           if (fine) {
-            fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0, pol);
+            fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0);
             pc.advance();
           } else {
             atomicOr(&g_fault_fwd, kFaultFwdWait);

@@ -312,7 +312,10 @@ __device__ __forceinline__ void smem_row(const uint8_t* row, int lane, f2 (&x)[V
   }
 }
 
-// Stores one row of this lane's VEC channels (fp32 pairs -> bf16, nearest even).
+// Stores one row of this lane's VEC channels (fp32 pairs -> bf16, nearest even).  Streaming
+// stores (st.global.cs): y and dx are written once and not read back by the kernel; the
+// plain stores measured 1.8 us slower in the backward and 0.8 us in the forward (B=2
+// T=8192 D=4096).
 template <int VEC>
 __device__ __forceinline__ void store_row(uint16_t* dst, const f2 (&v)[VEC / 2]) {
   if constexpr (VEC == 8) {
@@ -321,14 +324,14 @@ __device__ __forceinline__ void store_row(uint16_t* dst, const f2 (&v)[VEC / 2])
     o.y = f2_to_bf16x2(v[1]);
     o.z = f2_to_bf16x2(v[2]);
     o.w = f2_to_bf16x2(v[3]);
-    *reinterpret_cast<uint4*>(dst) = o;
+    __stcs(reinterpret_cast<uint4*>(dst), o);
   } else if constexpr (VEC == 4) {
     uint2 o;
     o.x = f2_to_bf16x2(v[0]);
     o.y = f2_to_bf16x2(v[1]);
-    *reinterpret_cast<uint2*>(dst) = o;
+    __stcs(reinterpret_cast<uint2*>(dst), o);
   } else {
-    *reinterpret_cast<uint32_t*>(dst) = f2_to_bf16x2(v[0]);
+    __stcs(reinterpret_cast<unsigned int*>(dst), f2_to_bf16x2(v[0]));
   }
 }
 
