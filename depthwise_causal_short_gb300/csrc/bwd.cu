@@ -389,13 +389,14 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
     Cursor pc, cc;
     pc.init(r0, r1, p.T, kRing, R);
     cc = pc;
+    const uint64_t pol = policy_evict_first();
     if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < S; ++s) {
         if (!pc.done) {
           mbar_arrive_expect_tx(&bars[s], STAGE);
-          tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b);
-          tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b);
+          tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b, pol);
+          tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b, pol);
           pc.advance();
         }
       }
@@ -459,8 +460,8 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
       if (lane == 0 && !pc.done) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars[s], STAGE);
-        tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b);
-        tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b);
+        tma_load_3d(stages + s * STAGE, tmx, &bars[s], c0, pc.tt, pc.b, pol);
+        tma_load_3d(stages + s * STAGE + TILE, tmdy, &bars[s], c0, pc.tt, pc.b, pol);
         pc.advance();
       }
       cc.advance();

@@ -92,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 // Coordinates are (innermost, middle, outermost) = (channel, row, batch).  Rows outside
 // [0, T) and channels outside [0, D) are filled with zeros by the copy engine.  No L2 cache
-// hint: with an evict_first policy the stream kernels were slower (backward 70.2 against
+// hint: with an evict_first policy the lockstep kernels were slower (backward 70.2 against
 // 67.0 us, forward 43.4 against 42.0 us at B=2 T=8192 D=4096, with streaming row stores in
 // both; an evict_normal policy gave 67.3 and 43.0 us).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -102,6 +102,27 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(b), "r"(smem_addr(bar))
       : "memory");
+}
+
+// The same with an L2 cache-policy operand.  The independent-pipeline backward (rows under
+// 2048 channels) is faster with evict_first loads: D=512 17.9 against 18.6 us, D=1024 25.5
+// against 25.9 us, D=1536 34.2 against 35.1 us (B=2 T=8192), while the lockstep kernels
+// are faster without a hint.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c, int r, int b, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(b), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// L2 eviction policy for data read exactly once.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
