@@ -105,8 +105,9 @@ CCONV_API int cconv_fwd(const void* x, int64_t B, int64_t T, int64_t D, int64_t 
                         void* y, cconv_stream_t stream);
 
 /*
- * cconv_bwd_workspace_bytes -- scratch that cconv_bwd needs for its per-warp fp32 partial
- * sums of dw and dbias, for the CURRENT device (the split of work follows its SM count).
+ * cconv_bwd_workspace_bytes -- scratch that cconv_bwd needs for its fp32 partial sums of dw
+ * and dbias (one record per channel strip and CTA), for the CURRENT device (the split of
+ * work follows its SM count and D).
  * Returns CCONV_OK and writes *bytes, or an error for invalid sizes / no device.
  */
 CCONV_API int cconv_bwd_workspace_bytes(int64_t B, int64_t T, int64_t D, int W,
@@ -116,7 +117,7 @@ CCONV_API int cconv_bwd_workspace_bytes(int64_t B, int64_t T, int64_t D, int W,
  * cconv_bwd -- backward: dx, dw and (optionally) dbias, with z recomputed from x.
  * Source: kernel-fun 0.2.0.dev1 wheel, cconv/_kernels/strip.py (`_dsilu`, `_bwd4`,
  * `cconv_bwd_strip`, `cconv_bwd`): one streaming pass, then a fixed-order (deterministic,
- * atomic-free) reduction of per-warp partial sums.  Two kernels on `stream`.
+ * atomic-free) reduction of the partial sums.  Two kernels on `stream`.
  *
  *   x, dy   [B,T,D] bf16 with strides (sxb, sxt) and (sdb, sdt); same rules as cconv_fwd.
  *   w, bias as cconv_fwd (bias may be NULL).
