@@ -24,9 +24,10 @@
 // at single rows, with the initial state's gradient written), no activation (kModeActNone),
 // and several problems in one launch (cconv_bwd_multi_kernel).
 //
-// Batched rows of at least 8 strips take a lockstep form instead (cconv_bwd_ls_kernel): a
-// producer warp loads 8 neighbouring strips of one row range per stage, for x and dy
-// together, and 8 consumer warps run the same per-warp tile code on their strip of it.
+// Rows of 512 channels or more take a lockstep form instead (cconv_bwd_ls_kernel): a
+// producer warp loads 8 (from 2048 channels) or 4 neighbouring strips of one row range per
+// stage, for x and dy together, and as many consumer warps run the same per-warp tile code
+// on their strip of it.
 #include <mutex>
 #include <type_traits>
 
@@ -891,20 +892,23 @@ struct BwdConfig {
 #define CCONV_BWD_LS_CFG(V, R, S, NC, M) \
   BwdConfig { V, R, S, NC, NC, 1, M, cconv_bwd_ls_kernel<V, R, S, NC, M, 0> }
 
-// Entry 0 is the default from 2048 channels (16 strips of 128) up; narrower rows take entry
-// 1, whose 2-strip CTAs leave no consumer warp idle.  Measured at B=2 T=8192 (us, entry 0
-// against entry 1): D=1024 27.5 / 25.4, 1536 39.6 / 34.5, 2048 40.4 / 40.5, 3072 56.4 / 57.4,
-// 4096 69.7 / 72.4, 8192 130.2 / 148.8.  The others are for sweeps (CCONV_BWD_CONFIG =
-// index).
+// Entry 0 is the default from 2048 channels (16 strips of 128) up, entry 1 (4-strip
+// lockstep CTAs) from 512 channels, and entry 2 (independent warp pipelines, 2-strip CTAs)
+// below that.  Measured at B=2 T=8192 (us, entry 0 / 1 / 2):
+//   D=512 17.7 / 16.9 / 17.1, 1024 27.2 / 24.4 / 25.2, 1536 39.7 / 33.4 / 34.3,
+//   2048 40.3 / 40.5 / 40.3, 4096 66.9 / 74.5 / 72.2.
+// The others are for sweeps (CCONV_BWD_CONFIG = index).
 static const BwdConfig kBwdConfigs[] = {
     CCONV_BWD_LS_CFG(4, 12, 4, 8, 1),
+    CCONV_BWD_LS_CFG(4, 12, 6, 4, 1),
     CCONV_BWD_CFG(4, 12, 3, 8, 2),
-    CCONV_BWD_CFG(4, 12, 3, 8, 4),  // packed sequences and several problems use this shape
+    CCONV_BWD_CFG(4, 12, 3, 8, 4),  // packed sequences and several problems below 512 channels
     CCONV_BWD_CFG(4, 12, 3, 8, 8),
     CCONV_BWD_CFG(4, 16, 3, 8, 4),
     CCONV_BWD_CFG(4, 12, 2, 12, 4),
     CCONV_BWD_LS_CFG(4, 16, 3, 8, 1),
     CCONV_BWD_LS_CFG(4, 12, 4, 4, 2),
+    CCONV_BWD_LS_CFG(4, 12, 8, 4, 1),
 };
 static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
@@ -915,8 +919,8 @@ static const BwdConfig& bwd_config(int64_t D) {
     return (v >= 0 && v < kNumBwdConfigs) ? v : -1;
   }();
   if (override_idx >= 0) return kBwdConfigs[override_idx];
-  const BwdConfig& ls = kBwdConfigs[0];
-  return D >= 2 * static_cast<int64_t>(ls.warps) * 32 * ls.vec ? ls : kBwdConfigs[1];
+  if (D >= 2048) return kBwdConfigs[0];
+  return D >= 512 ? kBwdConfigs[1] : kBwdConfigs[2];
 }
 
 // Work split of the backward: strips of 32*VEC channels in groups of SW, each strip's rows in
@@ -1119,15 +1123,22 @@ static void (*const kBwdVarlenKernels[2])(const CUtensorMap, const CUtensorMap, 
     cconv_bwd_kernel<4, 12, 3, 8, 4, kModeVarlen | kModeActNone>,
 };
 static const BwdConfig kBwdVarlenConfig = {4, 12, 3, 8, 4, 0, 1, nullptr};
-// From 2048 channels on, the lockstep form (as for batched rows).
+// From 512 channels on, the lockstep forms (as for batched rows): 8 strips per CTA from
+// 2048 channels, 4 below.
 static void (*const kBwdVarlenLsKernels[2])(const CUtensorMap, const CUtensorMap, const BwdArgs) = {
     cconv_bwd_ls_kernel<4, 12, 4, 8, 1, kModeVarlen>,
     cconv_bwd_ls_kernel<4, 12, 4, 8, 1, kModeVarlen | kModeActNone>,
 };
+static void (*const kBwdVarlenLs4Kernels[2])(const CUtensorMap, const CUtensorMap, const BwdArgs) = {
+    cconv_bwd_ls_kernel<4, 12, 6, 4, 1, kModeVarlen>,
+    cconv_bwd_ls_kernel<4, 12, 6, 4, 1, kModeVarlen | kModeActNone>,
+};
 static const BwdConfig kBwdVarlenLsConfig = {4, 12, 4, 8, 8, 1, 1, nullptr};
+static const BwdConfig kBwdVarlenLs4Config = {4, 12, 6, 4, 4, 1, 1, nullptr};
 
 static const BwdConfig& varlen_config(int64_t D) {
-  return D >= 2048 ? kBwdVarlenLsConfig : kBwdVarlenConfig;
+  if (D >= 2048) return kBwdVarlenLsConfig;
+  return D >= 512 ? kBwdVarlenLs4Config : kBwdVarlenConfig;
 }
 
 // Zeroes n bf16 values (the initial-state gradient when there are no rows at all).
@@ -1247,7 +1258,9 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
   a.dinit = L > 0 ? static_cast<uint16_t*>(d_initial_state) : nullptr;
   a.nseq = static_cast<int>(nseq);
 
-  auto kern = (cfg.producer ? kBwdVarlenLsKernels : kBwdVarlenKernels)[act == CCONV_ACT_NONE ? 1 : 0];
+  auto kern = (!cfg.producer ? kBwdVarlenKernels
+                : cfg.warps == 8 ? kBwdVarlenLsKernels
+                                 : kBwdVarlenLs4Kernels)[act == CCONV_ACT_NONE ? 1 : 0];
   int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
   const int red_bytes = cfg.warps * kRec * 32 * cfg.vec * static_cast<int>(sizeof(float));
   if (smem < red_bytes) smem = red_bytes;
@@ -1278,17 +1291,21 @@ struct MultiPlan {
 
 static const BwdConfig kBwdMultiConfig = {4, 12, 3, 8, 4, 0, 1, nullptr};
 static const BwdConfig kBwdMultiLsConfig = {4, 12, 4, 8, 8, 1, 1, nullptr};
+static const BwdConfig kBwdMultiLs4Config = {4, 12, 6, 4, 4, 1, 1, nullptr};
 
-// The lockstep form when every problem fills a group of 8 strips (D > 896) and there are at
-// least two groups in all, as for the batched call from 2048 channels on.
+// The 8-strip lockstep form when every problem fills a group of 8 strips (D > 896) and
+// there are at least two groups in all, as for the batched call from 2048 channels on; the
+// 4-strip lockstep form when every problem fills a group of 4 (D > 384); else independent
+// warp pipelines.
 static const BwdConfig& multi_config(int n, const int64_t* D) {
-  int64_t strips = 0;
+  int64_t strips = 0, least = int64_t(1) << 62;
   for (int k = 0; k < n; ++k) {
     const int64_t c = (D[k] + 127) / 128;
-    if (c < 8) return kBwdMultiConfig;
     strips += c;
+    if (c < least) least = c;
   }
-  return strips >= 16 ? kBwdMultiLsConfig : kBwdMultiConfig;
+  if (least >= 8 && strips >= 16) return kBwdMultiLsConfig;
+  return least >= 4 ? kBwdMultiLs4Config : kBwdMultiConfig;
 }
 
 static int multi_plan(int n, const int64_t* D, int64_t B, int64_t T, MultiPlan* mp) {
@@ -1425,8 +1442,9 @@ CCONV_API int cconv_bwd_multi(int n, const void* const* x, const int64_t* sxb,
   m.n = n;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  auto kern = cfg.producer ? cconv_bwd_ls_multi_kernel<4, 12, 4, 8>
-                           : cconv_bwd_multi_kernel<4, 12, 3, 8, 4>;
+  auto kern = !cfg.producer   ? cconv_bwd_multi_kernel<4, 12, 3, 8, 4>
+              : cfg.warps == 8 ? cconv_bwd_ls_multi_kernel<4, 12, 4, 8>
+                               : cconv_bwd_ls_multi_kernel<4, 12, 6, 4>;
   int smem = cfg.warps * cfg.stages * (2 * cfg.rows * 32 * cfg.vec * 2 + 8);
   const int red_bytes = cfg.warps * kRec * 32 * cfg.vec * static_cast<int>(sizeof(float));
   if (smem < red_bytes) smem = red_bytes;
