@@ -379,6 +379,7 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
   // Everything above touches no global memory; from here on the previous kernel on the
   // stream has completed.
   grid_dependency_wait();
+  grid_launch_dependents();  // the reduction waits for this grid in griddepcontrol.wait
 
   f2 acc[kRec][P];
 #pragma unroll
@@ -470,7 +471,6 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
     }
   }
   if constexpr (VL) bwd_varlen_tail(p, NW * 32, warp, lane);
-  grid_launch_dependents();
 
   // ---- the CTA's partial sums, added in a fixed order ------------------------------------
   // Every warp has consumed all its tiles, so the stage memory is free for NW records.
@@ -556,6 +556,10 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
   }
   __syncthreads();
   grid_dependency_wait();
+  // The reduction launched after this kernel waits for its completion in
+  // griddepcontrol.wait, so it may be scheduled now: its CTAs then sit resident and start
+  // the moment this grid finishes (0.7 us per call at B=2 T=8192 D=4096, measured).
+  grid_launch_dependents();
 
   f2 acc[kRec][P];
 #pragma unroll
@@ -652,7 +656,6 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
     }
   }
   if constexpr (VL) bwd_varlen_tail(p, (NC + 1) * 32, warp, lane);
-  grid_launch_dependents();
 
   // ---- the CTA's partial sums: one record per strip (one range per CTA) -------------------
   float* rec = p.ws + static_cast<int64_t>(blockIdx.x) * NC * REC;
@@ -749,6 +752,7 @@ __global__ void __launch_bounds__(32 * kRedGroups)
                              int n_rg, int64_t D, int W, int wdt, void* dw, void* dbias) {
   __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
+  grid_launch_dependents();  // the next kernel waits for this grid in griddepcontrol.wait
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x >> 5;
   const int j = blockIdx.y;
@@ -808,6 +812,7 @@ struct RedArgs {
 __global__ void __launch_bounds__(32 * kRedGroups) cconv_bwd_reduce_kernel(const RedArgs r) {
   __shared__ float part[kRedGroups][33];
   grid_dependency_wait();
+  grid_launch_dependents();  // the next kernel waits for this grid in griddepcontrol.wait
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x >> 5;
   const int j = blockIdx.y;
