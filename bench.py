@@ -70,7 +70,7 @@ LAUNCHES_PER_STEP = 4                        # fwd, bwd stream, bwd reduce, upda
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel (the
 # backward stream kernel) from the ncu capture summarised under profiles/; None when the
 # kernel has changed since the counters were taken.
-BWD_TRAFFIC_BYTES = 368_817_664  # cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>, profiles/cconv_fwd_bwd_update_kernels_b2_t8192_d4096.md
+BWD_TRAFFIC_BYTES = 367_960_064  # cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>, profiles/cconv_fwd_bwd_update_kernels_b2_t8192_d4096.md
 
 WORKLOAD = ("fwd+bwd B=2 T=8192 D=4096 W=4 no bias (bf16 x/dy, f32 w) + 1 decode update "
             "S=512 N=256 D=4096 W=4 bias per step")
