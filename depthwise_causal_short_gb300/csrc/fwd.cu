@@ -287,6 +287,9 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
   // Nothing above touches global memory; from here on the previous kernel on the stream has
   // completed.
   grid_dependency_wait();
+  // The next kernel waits for this whole grid in griddepcontrol.wait, so it may be
+  // scheduled now and start the moment this grid finishes.
+  grid_launch_dependents();
 
   Cursor cur;  // packed sequences: one batch row of T = total rows
   cur.init(r0, r1, p.T, 0, R);
@@ -395,7 +398,6 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
         store_final<VEC>(p.fin, sq.i, p.D, p.W, d0, h);
     }
   }
-  grid_launch_dependents();
 }
 
 template <int VEC, int R, int S, int NC, int MINB, bool SEP, int MODE>
