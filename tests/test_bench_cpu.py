@@ -1,0 +1,56 @@
+"""bench.py's host-side helpers on CPU: the clock summary taken from nvidia-smi samples.
+
+The summary decides the `clocks` object of the benchmark line (median SM clock under load,
+maximum clock, throttle reasons seen), so its parsing is checked here on synthetic lines in
+nvidia-smi's `--format=csv,noheader,nounits` layout, without a GPU.
+"""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _line(sm, smax=2070, power=900.0, active="0x0000000000000000", hw="Not Active",
+          hw_thermal="Not Active", sw_thermal="Not Active", sw_power="Not Active"):
+    return f"0, {sm}, {smax}, {power}, {active}, {hw}, {hw_thermal}, {sw_thermal}, {sw_power}"
+
+
+def _summary(lines):
+    s = bench.ClockSampler("0")
+    s.lines = list(lines)
+    return s.summary()
+
+
+def test_loaded_median_and_no_reasons():
+    out = _summary([_line(2070), _line(2070), _line(2055), _line(2070)])
+    assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 4}
+
+
+def test_idle_samples_left_out_of_the_median():
+    # samples before the load starts (idle clocks) do not pull the median down
+    out = _summary([_line(345), _line(345), _line(2070), _line(2070), _line(2070)])
+    assert out["sm_mhz"] == 2070.0
+    assert out["samples"] == 5
+
+
+def test_throttle_reasons_are_reported():
+    out = _summary([_line(1980, sw_power="Active"), _line(2070),
+                    _line(1800, hw_thermal="Active"), _line(2000, hw="Active")])
+    assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+    out = _summary([_line(2070, sw_thermal="Active")])
+    assert out["reasons"] == ["sw_thermal_slowdown"]
+
+
+def test_no_samples_and_unparsable_samples():
+    assert _summary([])["reasons"] == ["nvidia-smi unavailable"]
+    bad = _summary(["[N/A], [N/A]", "0, [Not Supported], 2070, 1, 0x0, x, x, x, x"])
+    assert bad["reasons"] == ["no parsable samples"] and bad["samples"] == 0
+
+
+def test_aggregate_is_whole_job_throughput():
+    # units all ranks processed over the slowest rank's time
+    assert bench.aggregate(100.0, 2.0, 1) == 50.0
+    assert bench.aggregate(100.0, 2.0, 4) == 200.0
