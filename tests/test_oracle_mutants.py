@@ -25,6 +25,11 @@ MUTANTS = {
     "dx_tap_reversed": ("acc += w[d * W + (W - 1 - k)] * g[", "acc += w[d * W + k] * g["),
     "dw_index_reversed": ("dw[d * W + (W - 1 - k)] += gg", "dw[d * W + k] += gg"),
     "dbias_dropped": ("if (dbias) dbias[d] += gg;", "if (dbias) dbias[d] += 0.0 * gg;"),
+    "dw_lag_shifted": ("if (t - k < 0) continue;\n          dw[d * W + (W - 1 - k)] += gg * x[(b * T + (t - k)) * D + d];",
+                       "if (t - k - 1 < 0) continue;\n          dw[d * W + (W - 1 - k)] += gg * x[(b * T + (t - k - 1)) * D + d];"),
+    "dx_reads_the_past": ("if (t + k >= T) continue;\n          acc += w[d * W + (W - 1 - k)] * g[(b * T + (t + k)) * D + d];",
+                          "if (t - k < 0) continue;\n          acc += w[d * W + (W - 1 - k)] * g[(b * T + (t - k)) * D + d];"),
+    "dx_tail_dropped": ("if (t + k >= T) continue;\n          acc +=", "if (t + k >= T - 1) continue;\n          acc +="),
     "decode_no_shift": ("st[j] = window[j + 1];", "st[j] = window[j];"),
     "decode_tap_reversed": ("z += w[d * W + j] * bf16_to_double(window[j]);",
                             "z += w[d * W + (W - 1 - j)] * bf16_to_double(window[j]);"),
