@@ -81,6 +81,13 @@ def causal_conv1d(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | No
     with final_state None unless output_final_state.  See the module docstring for layouts."""
     if activation not in ("silu", "swish", None, "none"):
         raise ValueError(f"activation must be 'silu' or None, got {activation!r}")
+    if not isinstance(x, torch.Tensor) or x.dim() != 3:
+        raise ValueError("x must be a [B, T, D] tensor")
+    if initial_state is not None:
+        n = x.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+        if not isinstance(initial_state, torch.Tensor) or initial_state.dim() != 3 or \
+                initial_state.shape[0] != n:
+            raise ValueError(f"initial_state must be [{n}, D, W-1]: one state per sequence")
     act = "silu" if activation in ("silu", "swish") else None
     return _CausalConv1d.apply(x, weight, bias, initial_state, cu_seqlens, act,
                                output_final_state)
