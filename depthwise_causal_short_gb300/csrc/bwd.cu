@@ -28,7 +28,6 @@
 // producer warp loads 8 (from 2048 channels) or 4 neighbouring strips of one row range per
 // stage, for x and dy together, and as many consumer warps run the same per-warp tile code
 // on their strip of it.
-#include <mutex>
 #include <type_traits>
 
 #include "strip.cuh"
@@ -350,18 +349,6 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
   uint8_t* stages = smem + warp * (S * STAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S * STAGE) + warp * S;
 
-  int r0, r1;
-  if constexpr (VL) {
-    // Equal cost per range: a sequence boundary costs a warp the pulled-back last tile, the
-    // halo, the ring refill and two tiles on the per-row path; 40-48 rows balanced 16 and
-    // 128 mixed sequences and 8 short clustered ones best (measured).
-    constexpr int kBoundaryRows = 44;
-    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k, p.wpc, lane);
-    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k + 1, p.wpc, lane);
-  } else {
-    r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
-    r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
-  }
   const int c0 = cb * CB;
   const int64_t d0 = c0 + lane * VEC;
   const bool active = has_work && d0 < p.D;
@@ -380,6 +367,21 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
   // stream has completed.
   grid_dependency_wait();
   grid_launch_dependents();  // the reduction waits for this grid in griddepcontrol.wait
+
+  // The warp's row range, after the wait: packed sequences split it by cu_seqlens, which
+  // the previous kernel on the stream may have written.
+  int r0, r1;
+  if constexpr (VL) {
+    // Equal cost per range: a sequence boundary costs a warp the pulled-back last tile, the
+    // halo, the ring refill and two tiles on the per-row path; 40-48 rows balanced 16 and
+    // 128 mixed sequences and 8 short clustered ones best (measured).
+    constexpr int kBoundaryRows = 44;
+    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k, p.wpc, lane);
+    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k + 1, p.wpc, lane);
+  } else {
+    r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
+    r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
+  }
 
   f2 acc[kRec][P];
 #pragma unroll
@@ -527,19 +529,6 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
   uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int r0, r1;
-  if constexpr (VL) {
-    // Equal cost per range.  A boundary costs fewer rows here than in the independent-
-    // pipeline form (whose 44 gave 75.0 / 89.3 us for 16 / 128 mixed sequences over 16384 x
-    // 4096 rows); measured: 16 rows 75.2 / 86.2, 24: 74.7 / 84.3, 32: 73.9 / 85.3, 64:
-    // 75.7 / 95.2 us.
-    constexpr int kBoundaryRows = 32;
-    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg, p.wpc, lane);
-    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg + 1, p.wpc, lane);
-  } else {
-    r0 = static_cast<int>(static_cast<int64_t>(rg) * p.BT / p.wpc);
-    r1 = static_cast<int>(static_cast<int64_t>(rg + 1) * p.BT / p.wpc);
-  }
   const int c0 = sg * NC * CB;
   int nact = static_cast<int>((p.D - c0 + CB - 1) / CB);  // consumer warps with channels
   if (nact > NC) nact = NC;
@@ -561,6 +550,22 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
   // the moment this grid finishes (0.7 us per call at B=2 T=8192 D=4096, measured).
   grid_launch_dependents();
 
+  // The row range, after the wait: packed sequences split it by cu_seqlens, which the
+  // previous kernel on the stream may have written.
+  int r0, r1;
+  if constexpr (VL) {
+    // Equal cost per range.  A boundary costs fewer rows here than in the independent-
+    // pipeline form (whose 44 gave 75.0 / 89.3 us for 16 / 128 mixed sequences over 16384 x
+    // 4096 rows); measured: 16 rows 75.2 / 86.2, 24: 74.7 / 84.3, 32: 73.9 / 85.3, 64:
+    // 75.7 / 95.2 us.
+    constexpr int kBoundaryRows = 32;
+    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg, p.wpc, lane);
+    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg + 1, p.wpc, lane);
+  } else {
+    r0 = static_cast<int>(static_cast<int64_t>(rg) * p.BT / p.wpc);
+    r1 = static_cast<int>(static_cast<int64_t>(rg + 1) * p.BT / p.wpc);
+  }
+
   f2 acc[kRec][P];
 #pragma unroll
   for (int q = 0; q < P; ++q)
@@ -572,9 +577,9 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
   if (warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
     if (lane == 0) {
-        uint32_t eph = 0;
-      int s = 0;
-      for (int i = 0; !cur.done; ++i) {
+      uint32_t eph = 0;
+      int s = 0, i = 0;
+      for (; !cur.done; ++i) {
         if (i >= S) {  // wait until every consumer has released this stage
           if (!mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs)) {
             atomicOr(&g_fault_bwd, kFaultBwdWait);
@@ -591,6 +596,7 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }
+      drain_issued<S>(full, i);  // i stages issued
     }
   } else if (warp < nact) {
     // ---- consumer ------------------------------------------------------------------------
@@ -902,28 +908,35 @@ struct BwdConfig {
 // below that.  Measured at B=2 T=8192 (us, entry 0 / 1 / 2):
 //   D=512 17.7 / 16.9 / 17.1, 1024 27.2 / 24.4 / 25.2, 1536 39.7 / 33.4 / 34.3,
 //   2048 40.3 / 40.5 / 40.3, 4096 66.9 / 74.5 / 72.2.
-// The others are for sweeps (CCONV_BWD_CONFIG = index).
+// Building with -DCCONV_TILE_SWEEP adds the other shapes that were measured against them,
+// one of which the environment variable CCONV_BWD_CONFIG (an index into the table) then
+// forces for every D; that build is for tile sweeps only, and its extra shapes are not
+// covered by the parity tests.
 static const BwdConfig kBwdConfigs[] = {
     CCONV_BWD_LS_CFG(4, 12, 4, 8, 1),
     CCONV_BWD_LS_CFG(4, 12, 6, 4, 1),
     CCONV_BWD_CFG(4, 12, 3, 8, 2),
-    CCONV_BWD_CFG(4, 12, 3, 8, 4),  // packed sequences and several problems below 512 channels
+#ifdef CCONV_TILE_SWEEP
+    CCONV_BWD_CFG(4, 12, 3, 8, 4),
     CCONV_BWD_CFG(4, 12, 3, 8, 8),
     CCONV_BWD_CFG(4, 16, 3, 8, 4),
     CCONV_BWD_CFG(4, 12, 2, 12, 4),
     CCONV_BWD_LS_CFG(4, 16, 3, 8, 1),
     CCONV_BWD_LS_CFG(4, 12, 4, 4, 2),
     CCONV_BWD_LS_CFG(4, 12, 8, 4, 1),
+#endif
 };
-static const int kNumBwdConfigs = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
 
 static const BwdConfig& bwd_config(int64_t D) {
+#ifdef CCONV_TILE_SWEEP
   static const int override_idx = [] {
+    constexpr int n = sizeof(kBwdConfigs) / sizeof(kBwdConfigs[0]);
     const char* e = getenv("CCONV_BWD_CONFIG");
     const int v = e ? atoi(e) : -1;
-    return (v >= 0 && v < kNumBwdConfigs) ? v : -1;
+    return (v >= 0 && v < n) ? v : -1;
   }();
   if (override_idx >= 0) return kBwdConfigs[override_idx];
+#endif
   if (D >= 2048) return kBwdConfigs[0];
   return D >= 512 ? kBwdConfigs[1] : kBwdConfigs[2];
 }
@@ -1068,36 +1081,31 @@ namespace cconv {
 // inputs and outputs; nothing here calls cudaMalloc, cudaFree or any allocating routine.
 //
 // Host code cannot use the array's name as a device address (it names a host-side
-// stand-in), so the first call on each device, with that device current, looks the
-// address up with cudaGetSymbolAddress and keeps it.  That first call should therefore
-// happen before any stream capture.  All calls on a device share the array, which keeps
-// whatever the last call left in it; nothing in it needs to start at zero, because every
-// record is fully written before it is read.  Calls whose work overlaps on the GPU (for
-// example on two streams) race on the array and must be serialised by the caller.
+// stand-in), so every call looks the address up with cudaGetSymbolAddress in the context
+// current on the calling thread.  That lookup is cheap once the library's device code is
+// loaded in the context; the first call in a context may load it, which reserves the array
+// there and is not a stream operation, so make that first call before any stream capture
+// (and before sizing a memory arena, which the array then no longer competes with).  No
+// address is cached, so a device reset or another context current on the same device is
+// safe.  All calls on a device share the array, which keeps whatever the last call left in
+// it; nothing in it needs to start at zero, because every record is fully written before it
+// is read.  Calls whose work overlaps on the GPU (for example on two streams) race on the
+// array and must be serialised by the caller.
 // ------------------------------------------------------------------------------------
 constexpr size_t kBwdNoallocScratchBytes = size_t(8) << 20;  // 8 MiB
 
 static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[kBwdNoallocScratchBytes];
 
 static void* bwd_noalloc_scratch_address(int* status) {
-  static void* addr[64] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  void* p = nullptr;
+  if (report_cuda("cudaGetSymbolAddress", cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch)) !=
+          cudaSuccess ||
+      !p) {
     *status = CCONV_ERR_CUDA;
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || !p) {
-      *status = CCONV_ERR_CUDA;
-      return nullptr;
-    }
-    addr[dev] = p;
-  }
   *status = CCONV_OK;
-  return addr[dev];
+  return p;
 }
 
 }  // namespace cconv

@@ -89,6 +89,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Nanoseconds the thread that issued a CTA's tile copies waits, per stage, for them to land
+// before it returns.
+constexpr unsigned long long kDrainLimitNs = 100000000ull;
+
+// The thread that issued `issued` tile copies into stages 0, 1, ..., S-1, 0, ... (each
+// completing on its stage's full barrier) waits until every one of them has landed before it
+// returns.  A CTA's shared memory stays allocated until its last thread exits, so with this
+// wait at the end of the issuing thread no copy can land in the shared memory of a CTA that
+// has exited, whichever of its threads gave up a bounded wait first.  In a run where nothing
+// gave up, it only waits for the last few stages, which the consumers are waiting for too.
+template <int S>
+__device__ __forceinline__ void drain_issued(uint64_t* full, int issued) {
+  for (int s = 0; s < S && s < issued; ++s) {
+    const int armed = (issued - 1 - s) / S + 1;  // phases of stage s that were armed
+    (void)mbar_wait_bounded(&full[s], static_cast<uint32_t>(armed - 1) & 1u, kDrainLimitNs);
+  }
+}
+
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 // Coordinates are (innermost, middle, outermost) = (channel, row, batch).  Rows outside
 // [0, T) and channels outside [0, D) are filled with zeros by the copy engine.  No L2 cache

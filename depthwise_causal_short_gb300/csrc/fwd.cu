@@ -261,14 +261,6 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
   uint64_t* empty = full + S;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int r0, r1;
-  if constexpr (VL) {  // equal cost: a sequence boundary counts as kBoundaryRows rows
-    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, part, p.cpc, lane);
-    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, part + 1, p.cpc, lane);
-  } else {
-    r0 = static_cast<int>(static_cast<int64_t>(part) * p.BT / p.cpc);
-    r1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.BT / p.cpc);
-  }
   const int c0 = cg * NC * CB;
   int nact = static_cast<int>((p.D - c0 + CB - 1) / CB);  // consumer warps with channels
   if (nact > NC) nact = NC;
@@ -291,14 +283,24 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
   // scheduled now and start the moment this grid finishes.
   grid_launch_dependents();
 
+  // The row range, after the wait: packed sequences split it by cu_seqlens, which the
+  // previous kernel on the stream may have written.
+  int r0, r1;
+  if constexpr (VL) {  // equal cost: a sequence boundary counts as kBoundaryRows rows
+    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, part, p.cpc, lane);
+    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, part + 1, p.cpc, lane);
+  } else {
+    r0 = static_cast<int>(static_cast<int64_t>(part) * p.BT / p.cpc);
+    r1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.BT / p.cpc);
+  }
   Cursor cur;  // packed sequences: one batch row of T = total rows
   cur.init(r0, r1, p.T, 0, R);
   if (SEP && warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
     if (lane == 0) {
       uint32_t eph = 0;
-      int s = 0;
-      for (int i = 0; !cur.done; ++i) {
+      int s = 0, i = 0;
+      for (; !cur.done; ++i) {
         if (i >= S) {  // wait until every consumer has released this stage
           if (!mbar_wait_bounded(&empty[s], (eph >> s) & 1u, kWaitLimitNs)) {
             atomicOr(&g_fault_fwd, kFaultFwdWait);
@@ -310,6 +312,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }
+      drain_issued<S>(full, i);  // i tiles issued
     }
     if constexpr (VL) {
       __syncwarp();
@@ -320,10 +323,12 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
     // ---- consumer ------------------------------------------------------------------------
     const bool leader = !SEP && warp == 0;
     Cursor pc = cur;  // the leader's producer cursor, S tiles ahead
+    int issued = 0;   // tiles the leader has issued
     if (leader && lane == 0) {
       for (int s = 0; s < S && !pc.done; ++s) {
         fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0);
         pc.advance();
+        ++issued;
       }
     }
     const int64_t d0 = c0 + warp * CB + lane * VEC;
@@ -383,6 +388,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
           if (fine) {
             fwd_issue<VEC, R, NC>(smem + s * STAGE, &full[s], tmx, pc, nact, c0);
             pc.advance();
+            ++issued;
           } else {
             atomicOr(&g_fault_fwd, kFaultFwdWait);
           }
@@ -393,6 +399,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
       cur.advance();
       s = (s + 1 == S) ? 0 : s + 1;
     }
+    if (leader && lane == 0) drain_issued<S>(full, issued);
     if constexpr (VL) {  // a sequence that ends exactly at the range's end
       if (p.fin && active && sq.i >= 0 && sq.nb == r1 && sq.ss < r1 && r0 < r1)
         store_final<VEC>(p.fin, sq.i, p.D, p.W, d0, h);
@@ -552,7 +559,12 @@ __global__ void __launch_bounds__(kStateThreads) cconv_fwd_state_kernel(const St
 }
 
 // ------------------------------------------------------------------------------------
-// launch configurations (compile-time tile shapes; the first is the default)
+// launch configuration (a compile-time tile shape)
+//
+// The product build has one forward tile shape, measured fastest at B=2 T=8192 D=4096.
+// Building with -DCCONV_TILE_SWEEP adds the other shapes that were measured against it,
+// selected by the environment variable CCONV_FWD_CONFIG (an index into the table); that
+// build is for tile sweeps only, and its extra shapes are not covered by the parity tests.
 // ------------------------------------------------------------------------------------
 struct FwdConfig {
   int vec, rows, stages, nc, ctas_per_sm, sep;
@@ -563,7 +575,8 @@ struct FwdConfig {
   FwdConfig { V, R, S, NC, M, SEP, cconv_fwd_kernel<V, R, S, NC, M, SEP, 0> }
 
 static const FwdConfig kFwdConfigs[] = {
-    CCONV_FWD_CFG(4, 8, 10, 8, 1, true),  // measured fastest at B=2 T=8192 D=4096
+    CCONV_FWD_CFG(4, 8, 10, 8, 1, true),
+#ifdef CCONV_TILE_SWEEP
     CCONV_FWD_CFG(4, 12, 6, 8, 1, true),
     CCONV_FWD_CFG(4, 16, 6, 8, 1, true),
     CCONV_FWD_CFG(4, 24, 4, 8, 1, true),
@@ -571,17 +584,21 @@ static const FwdConfig kFwdConfigs[] = {
     CCONV_FWD_CFG(8, 8, 6, 8, 1, true),
     CCONV_FWD_CFG(4, 8, 5, 8, 2, false),
     CCONV_FWD_CFG(4, 4, 20, 8, 1, true),
+#endif
 };
-static const int kNumFwdConfigs = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
 
 static int fwd_config_index() {
-  static int idx = -1;
-  if (idx < 0) {
+#ifdef CCONV_TILE_SWEEP
+  static const int idx = [] {
+    constexpr int n = sizeof(kFwdConfigs) / sizeof(kFwdConfigs[0]);
     const char* e = getenv("CCONV_FWD_CONFIG");
-    int v = e ? atoi(e) : 0;
-    idx = (v >= 0 && v < kNumFwdConfigs) ? v : 0;
-  }
+    const int v = e ? atoi(e) : 0;
+    return (v >= 0 && v < n) ? v : 0;
+  }();
   return idx;
+#else
+  return 0;
+#endif
 }
 
 }  // namespace cconv

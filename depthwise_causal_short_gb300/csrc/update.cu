@@ -340,9 +340,11 @@ static UpdKernel pick_update_kernel(int W, int rows, int off, int mode) {
     switch (rows) {
       case 1: return pick_update_kernel_w<VEC, 1, 0, kUpdPlain, NT>(W);
       case 2: return pick_update_kernel_w<VEC, 2, 0, kUpdPlain, NT>(W);
-      case 4: return pick_update_kernel_w<VEC, 4, 0, kUpdPlain, NT>(W);
+#ifdef CCONV_TILE_SWEEP
       case 8: return pick_update_kernel_w<VEC, 8, 0, kUpdPlain, NT>(W);
-      default: return pick_update_kernel_w<VEC, 16, 0, kUpdPlain, NT>(W);
+      case 16: return pick_update_kernel_w<VEC, 16, 0, kUpdPlain, NT>(W);
+#endif
+      default: return pick_update_kernel_w<VEC, 4, 0, kUpdPlain, NT>(W);
     }
   }
 }
@@ -417,12 +419,15 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
     // loads in flight.  Fewer rows only when four would leave more than half of the SMs idle.
     while (rows > 1 && 2 * gx * ((N + rows - 1) / rows) < static_cast<int64_t>(sms)) rows /= 2;
   }
-  static const int rows_override = [] {  // sweeps only: CCONV_UPDATE_ROWS = 1, 2, 4, 8 or 16
+#ifdef CCONV_TILE_SWEEP
+  // Sweep builds only: CCONV_UPDATE_ROWS = 1, 2, 4, 8 or 16 forces the rows per thread.
+  static const int rows_override = [] {
     const char* e = getenv("CCONV_UPDATE_ROWS");
     const int v = e ? atoi(e) : 0;
     return (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ? v : 0;
   }();
   if (rows_override) rows = rows_override;
+#endif
   if (nt == kUpdThreadsSmall && rows > 4) rows = 4;
   if ((off || mode != kUpdPlain) && rows != 4) rows = 1;  // general kernels: 1 and 4 rows
   const int64_t gy = (N + rows - 1) / rows;

@@ -24,9 +24,11 @@
  *     rounded to nearest-even on store.  The sigmoid uses the hardware tanh approximation
  *     (sigmoid(z) = 0.5 * tanh(z / 2) + 0.5), whose relative error is about 2^-11.
  *   - All pointers are DEVICE pointers owned by the caller; the library allocates nothing,
- *     keeps no tensor cache and never aliases one call's buffers into another.
+ *     keeps no tensor cache and never aliases one call's buffers into another (the one
+ *     fixed device array of cconv_bwd_noalloc aside).
  *   - All work is enqueued on `stream` (NULL = the legacy default stream) with no host
- *     synchronisation, so every call may be captured in a CUDA graph.
+ *     synchronisation.  The forward, backward, decode, packed-sequence and multi-problem
+ *     calls may be captured in a CUDA graph.
  *   - Argument errors are found on the host, before anything is enqueued: the call returns
  *     a negative cconv_status and launches nothing.  CCONV_OK means "enqueued".
  *   - Strides are in elements.  The channel stride is 1 for every [.., D] tensor.
@@ -198,13 +200,19 @@ CCONV_API int cconv_update_ex(const void* x, int64_t N, int64_t D, int64_t ldx, 
  * that must not call cudaMalloc because it can synchronise the device).  The pages have no
  * counterpart to this call; it exists for those callers.
  *
- * Arguments and results are those of cconv_bwd minus (workspace, workspace_bytes).  The
- * partial sums live in a fixed 8 MiB device array inside the library (held by every GPU
- * that loads it until the process exits); a problem whose cconv_bwd_workspace_bytes()
- * exceeds 8 MiB returns CCONV_ERR_WORKSPACE.  The call allocates nothing.  Its first call on
- * a device (with that device current) looks up the array's device address, so make that
- * first call before any stream capture.  All calls on a device share the array: calls whose
- * work overlaps on the GPU race and must be serialised by the caller.
+ * Arguments and results are those of cconv_bwd minus (workspace, workspace_bytes), and so
+ * are the results: the same kernels run with the same work split, so dx, dw and dbias are
+ * bit-identical to cconv_bwd's.  The partial sums live in a fixed 8 MiB device array inside
+ * the library (held by every GPU that loads it until the process exits); a problem whose
+ * cconv_bwd_workspace_bytes() exceeds 8 MiB returns CCONV_ERR_WORKSPACE before anything is
+ * enqueued.  The call itself never calls cudaMalloc, cudaFree or any allocating routine.
+ * Set-up: the first call in a context (with that device current) may load the library's
+ * device code there, which reserves the 8 MiB array, and looks up the array's device
+ * address; so make one warm-up call before any stream capture and before sizing a memory
+ * arena from the free memory.  Every call repeats the address lookup, which is cheap once
+ * the code is loaded and stays valid after a device reset.  All calls on a device share the
+ * array: calls whose work overlaps on the GPU (e.g. on two streams) race on it and must be
+ * serialised by the caller.  Calls queued one after another on one stream do not overlap.
  */
 CCONV_API int cconv_bwd_noalloc(const void* x, int64_t sxb, int64_t sxt, const void* dy,
                                 int64_t sdb, int64_t sdt, int64_t B, int64_t T, int64_t D,
