@@ -5,7 +5,8 @@
 One step is one pass of the whole hot path over one batch of synthetic input:
   * cconv_fwd  on the production-length workload  B=2 T=8192 D=4096 W=4, no bias,
     bf16 activations, fp32 weights;
-  * cconv_bwd  (dx, dw; stream kernel + deterministic reduction) on the same workload;
+  * cconv_bwd  (dx, dw and dbias; stream kernel + deterministic reduction) on the same
+    workload, dw / dbias reduced over its 16384 rows;
   * cconv_update, one decode step of the decode workload: pool [512, 4096, 3] bf16,
     256 active rows, W=4, bias.
 The reported value is achieved HBM throughput, algorithmic bytes over device time, in
@@ -15,9 +16,12 @@ reported beside it.  Inputs are rotated so that no kernel reads data the previou
 touched, and every per-launch working set (>= 268 MB) is larger than the 129 MB L2.
 
 Timing: the K steps of the timed region run back to back between two CUDA events on the
-launching stream (max over ranks); the per-part figures come from K back-to-back calls of
-each entry point, timed the same way; the decode update is also timed as 1000 updates
-replayed from one CUDA graph.
+launching stream (max over ranks).  Each part's device time per call comes from calls of
+that entry point captured in one CUDA graph and replayed between two events, so host-side
+time (argument checks, ctypes) cannot leak into it; the eager per-call time is reported
+beside it.  The decode update is also timed as 1000 updates replayed from one CUDA graph.
+Each part lists the kernels it launches with their registers per thread, local (spill)
+bytes, shared memory and resident CTAs per SM (the library's launch descriptions).
 
 Under torchrun (N > 1) every rank runs the same step on its own data (weak scaling, no
 collective on the data path); the timed region is bracketed by a barrier and
@@ -67,13 +71,31 @@ VL_FWD_BYTES = FWD_BYTES + 2 * VL_STATE_BYTES    # + initial states read, final 
 VL_BWD_BYTES = BWD_BYTES + 2 * VL_STATE_BYTES    # + initial states read, gradient written
 LAUNCHES_PER_STEP = 4                        # fwd, bwd stream, bwd reduce, update
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel (the
-# backward stream kernel) from the ncu capture summarised under profiles/; None when the
-# kernel has changed since the counters were taken.
-BWD_TRAFFIC_BYTES = 367_960_064  # cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>, profiles/cconv_fwd_bwd_update_kernels_b2_t8192_d4096.md
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant call (the
+# backward: stream kernel + reduction), averaged over back-to-back launches in one ncu
+# capture (profiles/, file named below), together with the hash of the kernel sources it
+# was taken on.  `traffic` is reported only while the sources still hash the same.
+BWD_TRAFFIC = {"bytes_per_call": None, "sources_sha16": None, "profile": None}
+TRAFFIC_SOURCES = ("csrc/bwd.cu", "csrc/strip.cuh", "csrc/common.cuh")
 
 WORKLOAD = ("fwd+bwd B=2 T=8192 D=4096 W=4 no bias (bf16 x/dy, f32 w) + 1 decode update "
             "S=512 N=256 D=4096 W=4 bias per step")
+
+
+def sources_sha16() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(HERE, "depthwise_causal_short_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def bwd_traffic():
+    """Measured DRAM bytes per backward call, or None if the kernels changed since."""
+    if BWD_TRAFFIC["bytes_per_call"] is None or BWD_TRAFFIC["sources_sha16"] != sources_sha16():
+        return None
+    return BWD_TRAFFIC["bytes_per_call"]
 
 
 def measured_peak():
@@ -198,6 +220,30 @@ def gpu_id(dev) -> str:
 # our arm
 # ---------------------------------------------------------------------------------------
 
+def short_name(name: str) -> str:
+    """cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0> from the demangled signature."""
+    n = name.split("(")[0]
+    n = n.replace("void ", "").replace("cconv::", "")
+    return n.strip()
+
+
+def kernels_of(cc, fn, max_threads_per_sm: int):
+    """The kernels fn() launches, with their resources (launch descriptions, nothing runs)."""
+    out = []
+    for d in cc.describe(fn):
+        out.append({
+            "kernel": short_name(d["name"]),
+            "registers": d["registers"],
+            "local_bytes_per_thread": d["local_bytes"],
+            "smem_bytes": d["static_shared_bytes"] + d["dynamic_shared_bytes"],
+            "threads": d["threads"],
+            "ctas": d["ctas"],
+            "ctas_per_sm": d["ctas_per_sm"],
+            "theoretical_occupancy": round(d["ctas_per_sm"] * d["threads"] / max_threads_per_sm, 4),
+        })
+    return out
+
+
 def run_ours(args, world, rank, local):
     import depthwise_causal_short_gb300 as cc
     from depthwise_causal_short_gb300 import _build
@@ -208,6 +254,8 @@ def run_ours(args, world, rank, local):
         _build.build()
     barrier(world)
     cc.load()
+    props = torch.cuda.get_device_properties(dev)
+    max_thr = props.max_threads_per_multi_processor
 
     # ---- inputs (seeded, synthetic), resident in HBM before the timed region ----------
     x, dy, w, _ = inputs.fwd_bwd_inputs(FWD.B, FWD.T, FWD.D, FWD.W, FWD.bias, seed=rank)
@@ -219,6 +267,7 @@ def run_ours(args, world, rank, local):
     dxs = [torch.empty_like(xf[0]) for _ in range(NSET)]
     wg = w.to(dev)
     dw = torch.empty_like(wg)
+    db = torch.empty(FWD.D, dtype=wg.dtype, device=dev)
     ws = torch.empty(cc.cconv_bwd_workspace_bytes(FWD.B, FWD.T, FWD.D, FWD.W), dtype=torch.uint8,
                      device=dev)
     st, xr, idx, wd, bd = inputs.decode_inputs(DEC.S, DEC.N, DEC.D, DEC.W, DEC.bias, n_x=8,
@@ -228,17 +277,18 @@ def run_ours(args, world, rank, local):
     status = torch.zeros(2, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
+    # Every part runs on the current stream (the launching stream, or the capture stream).
     def fwd(i):
         k = i % NSET
-        cc.cconv_fwd(xf[k], wg, None, y=ys[k], stream=stream)
+        cc.cconv_fwd(xf[k], wg, None, y=ys[k])
 
     def bwd(i):
         k = i % NSET
-        cc.cconv_bwd(xb[k], dyb[k], wg, None, want_dbias=False, dx=dxs[k], dw=dw, workspace=ws,
-                     stream=stream)
+        cc.cconv_bwd(xb[k], dyb[k], wg, None, want_dbias=True, dx=dxs[k], dw=dw, dbias=db,
+                     workspace=ws)
 
     def upd(i):
-        cc.cconv_update(xr[i % xr.shape[0]], st, wd, bd, idx, y=yd, status=status, stream=stream)
+        cc.cconv_update(xr[i % xr.shape[0]], st, wd, bd, idx, y=yd, status=status)
 
     def step(i):
         fwd(i)
@@ -246,7 +296,8 @@ def run_ours(args, world, rank, local):
         upd(i)
 
     def loop_us(fn, n):
-        """Average device time of fn over n back-to-back calls (CUDA events on the stream)."""
+        """Average time per call of fn over n back-to-back eager calls (CUDA events on the
+        stream; includes whatever host time the calls take beyond the device's)."""
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for i in range(n):
@@ -254,6 +305,31 @@ def run_ours(args, world, rank, local):
         b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / n
+
+    def graph_us(fn, n):
+        """Device time per call of fn: min(n, 50) calls captured in one CUDA graph, the
+        graph replayed until about n calls have run, between two CUDA events."""
+        per = max(2, min(n, 50))
+        reps = max(1, n // per)
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn(0)
+            with torch.cuda.graph(g, stream=side):
+                for i in range(per):
+                    fn(i)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * per)
 
     for i in range(args.warmup):
         step(i)
@@ -277,13 +353,12 @@ def run_ours(args, world, rank, local):
     elapsed_max = max_over_ranks(elapsed, world, dev)
     assert status.tolist() == [0, 0]
 
-    # ---- per-kernel averages: each call back to back, K times ------------------------------
+    # ---- per-part device time (graph replay) and eager time per call ---------------------
     for fn in (fwd, bwd):
         for i in range(3):
             fn(i)
-    f_us = loop_us(fwd, K)
-    b_us = loop_us(bwd, K)
-    u_us = loop_us(upd, K)
+    f_us, b_us, u_us = graph_us(fwd, K), graph_us(bwd, K), graph_us(upd, K)
+    f_eager, b_eager, u_eager = loop_us(fwd, K), loop_us(bwd, K), loop_us(upd, K)
 
     # ---- decode: 1000 steps replayed from one CUDA graph --------------------------------
     def decode_graph_us(n_rows):
@@ -293,11 +368,11 @@ def run_ours(args, world, rank, local):
         s2.wait_stream(stream)
         with torch.cuda.stream(s2):
             cc.cconv_update(xr[0][:n_rows], st, wd, bd, idx[:n_rows], y=yd[:n_rows],
-                            status=status, stream=s2)
+                            status=status)
             with torch.cuda.graph(g, stream=s2):
                 for j in range(DEC.steps):
                     cc.cconv_update(xr[j % xr.shape[0]][:n_rows], st, wd, bd, idx[:n_rows],
-                                    y=yd[:n_rows], status=status, stream=s2)
+                                    y=yd[:n_rows], status=status)
         torch.cuda.synchronize()
         g.replay()
         torch.cuda.synchronize()
@@ -329,20 +404,18 @@ def run_ours(args, world, rank, local):
     def vfwd(i):
         k = i % NSET
         cc.cconv_fwd_varlen(vxs[k], vcu, vw, None, initial_state=vinits[k], final_state=vfin,
-                            y=ys[k].view(-1, FWD.D), stream=stream)
+                            y=ys[k].view(-1, FWD.D))
 
     def vbwd(i):
         k = i % NSET
         cc.cconv_bwd_varlen(vxs[k], vdys[k], vcu, vw, None, initial_state=vinits[k],
-                            want_dbias=False, dx=dxs[k].view(-1, FWD.D), dw=dw,
-                            d_initial_state=vdinit, workspace=vws, stream=stream)
+                            want_dbias=True, dx=dxs[k].view(-1, FWD.D), dw=dw, dbias=db,
+                            d_initial_state=vdinit, workspace=vws)
 
     for fn in (vfwd, vbwd):
         for i in range(3):
             fn(i)
-    vf_us = loop_us(vfwd, K)
-    vb_us = loop_us(vbwd, K)
-    del vxs, vdys
+    vf_us, vb_us = graph_us(vfwd, K), graph_us(vbwd, K)
 
     # ---- q, k, v of a layer in one launch: D = 1024, 1024, 2048 (same rows and bytes) -------
     qkv_D = [FWD.D // 4, FWD.D // 4, FWD.D // 2]
@@ -358,6 +431,7 @@ def run_ours(args, world, rank, local):
     qdxs = [[torch.empty(FWD.B, FWD.T, D, dtype=torch.bfloat16, device=dev) for D in qkv_D]
             for _ in range(NSET)]
     qdws = [torch.empty(D, FWD.W, device=dev) for D in qkv_D]
+    qdbs = [torch.empty(D, device=dev) for D in qkv_D]
     qws = torch.empty(cc.cconv_bwd_multi_workspace_bytes(qkv_D, FWD.B, FWD.T, FWD.W),
                       dtype=torch.uint8, device=dev)
     qws1 = [torch.empty(cc.cconv_bwd_workspace_bytes(FWD.B, FWD.T, D, FWD.W), dtype=torch.uint8,
@@ -365,43 +439,62 @@ def run_ours(args, world, rank, local):
 
     def qfwd(i):
         k = i % NSET
-        cc.cconv_fwd_multi(qsets[k][0], qw, ys=qys[k], stream=stream)
+        cc.cconv_fwd_multi(qsets[k][0], qw, ys=qys[k])
 
     def qbwd(i):
         k = i % NSET
-        cc.cconv_bwd_multi(qsets[k][0], qsets[k][1], qw, want_dbias=False, dxs=qdxs[k], dws=qdws,
-                           workspace=qws, stream=stream)
+        cc.cconv_bwd_multi(qsets[k][0], qsets[k][1], qw, want_dbias=True, dxs=qdxs[k], dws=qdws,
+                           dbiases=qdbs, workspace=qws)
 
     def qfwd3(i):
         k = i % NSET
         for j in range(3):
-            cc.cconv_fwd(qsets[k][0][j], qw[j], None, y=qys[k][j], stream=stream)
+            cc.cconv_fwd(qsets[k][0][j], qw[j], None, y=qys[k][j])
 
     def qbwd3(i):
         k = i % NSET
         for j in range(3):
-            cc.cconv_bwd(qsets[k][0][j], qsets[k][1][j], qw[j], None, want_dbias=False,
-                         dx=qdxs[k][j], dw=qdws[j], workspace=qws1[j], stream=stream)
+            cc.cconv_bwd(qsets[k][0][j], qsets[k][1][j], qw[j], None, want_dbias=True,
+                         dx=qdxs[k][j], dw=qdws[j], dbias=qdbs[j], workspace=qws1[j])
 
     for fn in (qfwd, qbwd, qfwd3, qbwd3):
         for i in range(3):
             fn(i)
-    qf_us, qb_us = loop_us(qfwd, K), loop_us(qbwd, K)
-    qf3_us, qb3_us = loop_us(qfwd3, K), loop_us(qbwd3, K)
+    qf_us, qb_us = graph_us(qfwd, K), graph_us(qbwd, K)
+    qf3_us, qb3_us = graph_us(qfwd3, K), graph_us(qbwd3, K)
+
+    # ---- what each part launches (launch descriptions: nothing runs) -----------------------
+    kern = {name: kernels_of(cc, lambda f=f: f(0), max_thr)
+            for name, f in (("fwd", fwd), ("bwd", bwd), ("decode_update", upd),
+                            ("fwd_varlen", vfwd), ("bwd_varlen", vbwd),
+                            ("fwd_qkv_one_launch", qfwd), ("bwd_qkv_one_launch", qbwd))}
     del qsets
 
     # ---- end to end through the public API with host buffers ------------------------------
     e2e = run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
+        cpu_all = cpu_baseline_all_cores(args.cpu_seconds, cpu)
 
     if rank != 0:
         return None
     peak_gbs, peak_kind = measured_peak()
-    fwd_tbps = FWD_BYTES / (f_us * 1e-6) / 1e12
-    bwd_tbps = BWD_BYTES / (b_us * 1e-6) / 1e12
+
+    def tb(nbytes, us):
+        return nbytes / (us * 1e-6) / 1e12
+
+    def part(nbytes, us, eager=None, **extra):
+        row = {"us": round(us, 3), "tbps": round(tb(nbytes, us), 4),
+               "frac_of_peak": round(tb(nbytes, us) * 1e3 / peak_gbs, 4),
+               "algorithmic_bytes": nbytes}
+        if eager is not None:
+            row["us_eager"] = round(eager, 3)
+        row.update(extra)
+        return row
+
+    bwd_tbps = tb(BWD_BYTES, b_us)
     value = aggregate(STEP_BYTES * K, elapsed_max, world) / 1e12
     out = {
         "metric": METRIC,
@@ -424,38 +517,30 @@ def run_ours(args, world, rank, local):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "parts": {
-            "fwd": {"us": round(f_us, 3), "tbps": round(fwd_tbps, 4),
-                    "frac_of_peak": round(fwd_tbps * 1e3 / peak_gbs, 4)},
-            "bwd": {"us": round(b_us, 3), "tbps": round(bwd_tbps, 4),
-                    "frac_of_peak": round(bwd_tbps * 1e3 / peak_gbs, 4),
-                    "note": "stream kernel + deterministic reduction kernel"},
-            "decode_update": {"us_per_step_stream": round(u_us, 3),
-                              "us_per_step_graph": round(dec_graph_us, 3),
-                              "bytes_per_step": DEC_BYTES},
+            "fwd": part(FWD_BYTES, f_us, f_eager, kernels=kern["fwd"]),
+            "bwd": part(BWD_BYTES, b_us, b_eager, kernels=kern["bwd"],
+                        note="stream kernel + deterministic reduction kernel; dx, dw, dbias"),
+            "decode_update": {"us_per_step_graph_1000": round(dec_graph_us, 3),
+                              "us_per_call_graph": round(u_us, 3),
+                              "us_per_call_eager": round(u_eager, 3),
+                              "bytes_per_step": DEC_BYTES, "kernels": kern["decode_update"]},
             "decode_update_small_batches": {
                 "us_per_step_graph": {str(n): round(v, 3) for n, v in dec_small_us.items()},
                 "note": "the same pool, weights and tokens, first N rows and slots only"},
-            "fwd_varlen": {"us": round(vf_us, 3),
-                           "tbps": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e12, 4),
-                           "frac_of_peak": round(VL_FWD_BYTES / (vf_us * 1e-6) / 1e9 / peak_gbs, 4),
-                           "note": f"{VL_NSEQ} packed sequences of mixed lengths, same rows; "
-                                   "initial states in, final states out (one stream kernel; "
-                                   "final states from its register ring)"},
-            "fwd_qkv_one_launch": {"us": round(qf_us, 3),
-                                   "tbps": round(FWD_BYTES / (qf_us * 1e-6) / 1e12, 4),
-                                   "frac_of_peak": round(FWD_BYTES / (qf_us * 1e-6) / 1e9 / peak_gbs, 4),
-                                   "three_calls_us": round(qf3_us, 3),
-                                   "note": "q, k, v convolutions of a layer (D = 1024, 1024, 2048, "
-                                           "same B, T) in one launch vs three cconv_fwd calls"},
-            "bwd_qkv_one_launch": {"us": round(qb_us, 3),
-                                   "tbps": round(BWD_BYTES / (qb_us * 1e-6) / 1e12, 4),
-                                   "frac_of_peak": round(BWD_BYTES / (qb_us * 1e-6) / 1e9 / peak_gbs, 4),
-                                   "three_calls_us": round(qb3_us, 3)},
-            "bwd_varlen": {"us": round(vb_us, 3),
-                           "tbps": round(VL_BWD_BYTES / (vb_us * 1e-6) / 1e12, 4),
-                           "frac_of_peak": round(VL_BWD_BYTES / (vb_us * 1e-6) / 1e9 / peak_gbs, 4),
-                           "note": "same packing; initial states in, their gradient out "
-                                   "(stream + reduction kernel)"},
+            "fwd_varlen": part(VL_FWD_BYTES, vf_us, kernels=kern["fwd_varlen"],
+                               note=f"{VL_NSEQ} packed sequences of mixed lengths, same rows; "
+                                    "initial states in, final states out (one stream kernel; "
+                                    "final states from its register ring)"),
+            "bwd_varlen": part(VL_BWD_BYTES, vb_us, kernels=kern["bwd_varlen"],
+                               note="same packing; initial states in, dx, dw, dbias and the "
+                                    "initial-state gradient out (stream + reduction kernel)"),
+            "fwd_qkv_one_launch": part(FWD_BYTES, qf_us, kernels=kern["fwd_qkv_one_launch"],
+                                       three_calls_us=round(qf3_us, 3),
+                                       note="q, k, v convolutions of a layer (D = 1024, 1024, "
+                                            "2048, same B, T) in one launch vs three cconv_fwd "
+                                            "calls"),
+            "bwd_qkv_one_launch": part(BWD_BYTES, qb_us, kernels=kern["bwd_qkv_one_launch"],
+                                       three_calls_us=round(qb3_us, 3)),
         },
         "roofline": {
             "kernel": "cconv_bwd (stream + reduction)",
@@ -465,19 +550,23 @@ def run_ours(args, world, rank, local):
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(bwd_tbps * 1e3 / peak_gbs, 4),
-            "traffic": BWD_TRAFFIC_BYTES,
+            "traffic": bwd_traffic(),
+            "traffic_profile": BWD_TRAFFIC["profile"],
             "algorithmic_bytes_per_launch": BWD_BYTES,
         },
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K,
-        "timing": "value: K whole steps between two CUDA events on the launching stream; parts: "
-                  "K back-to-back calls of each entry point between two events; decode graph: "
+        "timing": "value: K whole steps (eager calls) between two CUDA events on the launching "
+                  "stream; parts: device time per call from calls captured in one CUDA graph and "
+                  "replayed between two events (us_eager: K back-to-back eager calls); decode: "
                   "1000 updates replayed from one CUDA graph",
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 4),
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
+    if cpu_all is not None:
+        out["cpu_baseline_all_cores"] = cpu_all
     return out
 
 
@@ -496,12 +585,14 @@ def run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
     hy = [torch.empty_like(hx[0]).pin_memory() for _ in range(NB)]
     hdx = [torch.empty_like(hx[0]).pin_memory() for _ in range(NB)]
     hdw = [torch.empty(wg.shape, dtype=wg.dtype).pin_memory() for _ in range(NB)]
+    hdb = [torch.empty(wg.shape[0], dtype=wg.dtype).pin_memory() for _ in range(NB)]
     hyd = [torch.empty(DEC.N, DEC.D, dtype=torch.bfloat16).pin_memory() for _ in range(NB)]
     x_ = [torch.empty(x.shape, dtype=torch.bfloat16, device=dev) for _ in range(NB)]
     dy_ = [torch.empty_like(x_[0]) for _ in range(NB)]
     y_ = [torch.empty_like(x_[0]) for _ in range(NB)]
     dx_ = [torch.empty_like(x_[0]) for _ in range(NB)]
     dw_ = [torch.empty_like(wg) for _ in range(NB)]
+    db_ = [torch.empty(wg.shape[0], dtype=wg.dtype, device=dev) for _ in range(NB)]
     xd_ = [torch.empty(DEC.N, DEC.D, dtype=torch.bfloat16, device=dev) for _ in range(NB)]
     yd_ = [torch.empty_like(xd_[0]) for _ in range(NB)]
     status = torch.zeros(2, dtype=torch.int32, device=dev)
@@ -527,8 +618,8 @@ def run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
         stream.wait_event(uploaded[k])
         stream.wait_event(downloaded[k])    # step i-NB's results have been copied out
         cc.cconv_fwd(x_[k], wg, None, y=y_[k], stream=stream)
-        cc.cconv_bwd(x_[k], dy_[k], wg, None, want_dbias=False, dx=dx_[k], dw=dw_[k],
-                     workspace=ws, stream=stream)
+        cc.cconv_bwd(x_[k], dy_[k], wg, None, want_dbias=True, dx=dx_[k], dw=dw_[k],
+                     dbias=db_[k], workspace=ws, stream=stream)
         cc.cconv_update(xd_[k], st, wd, bd, idx, y=yd_[k], status=status, stream=stream)
         computed[k].record(stream)
 
@@ -539,6 +630,7 @@ def run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
             hy[k].copy_(y_[k], non_blocking=True)
             hdx[k].copy_(dx_[k], non_blocking=True)
             hdw[k].copy_(dw_[k], non_blocking=True)
+            hdb[k].copy_(db_[k], non_blocking=True)
             hyd[k].copy_(yd_[k], non_blocking=True)
         downloaded[k].record(down)
 
@@ -567,7 +659,8 @@ def run_e2e(cc, dev, stream, args, x, dy, w, wg, ws, xr, st, wd, bd, idx, world)
     torch.cuda.synchronize()
     el = max_over_ranks(a.elapsed_time(b) / 1e3, world, dev)
     h2d = (hx[0].numel() + hdy[0].numel() + hxd[0].numel()) * 2
-    d2h = (hy[0].numel() + hdx[0].numel() + hyd[0].numel()) * 2 + hdw[0].numel() * hdw[0].element_size()
+    d2h = ((hy[0].numel() + hdx[0].numel() + hyd[0].numel()) * 2
+           + (hdw[0].numel() + hdb[0].numel()) * hdw[0].element_size())
     return {"value": round(aggregate(STEP_BYTES * n, el, world) / 1e12, 4), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(el * 1e3 / n, 4), "steps": n,
@@ -597,7 +690,7 @@ def _oracle_step(o, fb, dec):
     one decode update.  Returns the algorithmic bytes it stands for."""
     xd, dyd, wdd = fb
     o.fwd(xd, wdd, None)
-    o.bwd(xd, dyd, wdd, None, want_dbias=False)
+    o.bwd(xd, dyd, wdd, None, want_dbias=True)
     stb, xrb, idx, wdec, bdec = dec
     rc, _, new = o.update(xrb[0], stb, idx, wdec, bdec)
     assert rc == 0
@@ -623,6 +716,71 @@ def cpu_baseline(seconds: float):
             "sample": f"fp64 C oracle, one thread: {steps} whole workload step(s) (fwd+bwd "
                       f"B={FWD.B} T={FWD.T} D={FWD.D} W={FWD.W} + 1 decode update), "
                       f"{dt:.2f} s"}
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _slice_worker(k: int, n: int, steps: int, ready, go, done):
+    """One process of the all-cores oracle run: channels of slice k of n (the convolution is
+    depthwise, so channel slices are independent problems) of the whole workload step."""
+    import oracle
+    d = FWD.D // n + (1 if k < FWD.D % n else 0)
+    x, dy, w, _ = inputs.fwd_bwd_inputs(FWD.B, FWD.T, d, FWD.W, False, seed=k)
+    xd, dyd, wdd = (t.double().numpy() for t in (x, dy, w))
+    st, xr, idx, wdec, bdec = inputs.decode_inputs(DEC.S, DEC.N, d, DEC.W, DEC.bias, n_x=1,
+                                                   seed=k)
+    stb = st.view(torch.int16).numpy().view(np.uint16).copy()
+    xrb = xr[0].view(torch.int16).numpy().view(np.uint16)
+    idxn, wdn, bdn = idx.numpy(), wdec.double().numpy(), bdec.double().numpy()
+    ready.put(k)
+    go.wait()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        o_fwd = oracle.fwd(xd, wdd, None)
+        oracle.bwd(xd, dyd, wdd, None, want_dbias=True)
+        rc, _, new = oracle.update(xrb, stb, idxn, wdn, bdn)
+        assert rc == 0 and o_fwd.shape == xd.shape
+        stb[...] = new
+    done.put((k, time.perf_counter() - t0))
+
+
+def cpu_baseline_all_cores(seconds: float, single: dict | None):
+    """The same oracle on every host core at once: one process per core, each running whole
+    workload steps on its slice of the channels; whole-job throughput over the wall time of
+    the slowest process.  Processes are spawned (never forked after CUDA is initialised)."""
+    import multiprocessing as mp
+    n = _cores()
+    per_step_1 = None
+    if single is not None and single.get("value"):
+        per_step_1 = (FWD_BYTES + BWD_BYTES + DEC_BYTES) / (single["value"] * 1e12)
+    steps = max(1, int(seconds * n / per_step_1 / 1.3)) if per_step_1 else 2
+    ctx = mp.get_context("spawn")
+    ready, done, go = ctx.Queue(), ctx.Queue(), ctx.Event()
+    procs = [ctx.Process(target=_slice_worker, args=(k, n, steps, ready, go, done), daemon=True)
+             for k in range(n)]
+    for pr in procs:
+        pr.start()
+    try:
+        for _ in range(n):
+            ready.get(timeout=600)
+        t0 = time.perf_counter()
+        go.set()
+        times = [done.get(timeout=max(600, 20 * seconds))[1] for _ in range(n)]
+        wall = time.perf_counter() - t0
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+    nbytes = steps * (FWD_BYTES + BWD_BYTES + DEC_BYTES)
+    return {"value": round(nbytes / wall / 1e12, 8), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"fp64 C oracle (unchanged), one process per core, each running {steps} "
+                      f"whole workload step(s) (fwd+bwd B={FWD.B} T={FWD.T} W={FWD.W} + 1 "
+                      f"decode update) on its 1/{n} of the D={FWD.D} channels; wall {wall:.2f} s, "
+                      f"slowest process {max(times):.2f} s"}
 
 
 def run_reference(args, world, rank):

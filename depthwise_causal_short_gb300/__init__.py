@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     cconv_status_str,
     cconv_update,
     cconv_update_ex,
+    describe,
     header_functions,
     lib_path,
     load,

@@ -40,6 +40,14 @@ class CConvError(RuntimeError):
         super().__init__(f"{call}: {STATUS.get(status, status)} ({status})")
 
 
+class KernelDesc(ctypes.Structure):
+    """cconv_kernel_desc of include/cconv.h."""
+    _fields_ = [("name", ctypes.c_char * 160), ("registers", ctypes.c_int),
+                ("local_bytes", ctypes.c_int), ("static_shared_bytes", ctypes.c_int),
+                ("dynamic_shared_bytes", ctypes.c_int), ("threads", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int), ("ctas", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -97,6 +105,10 @@ def load(path: str | Path | None = None):
     lib.cconv_status_str.restype = ctypes.c_char_p
     lib.cconv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.cconv_device_fault.restype = _INT
+    lib.cconv_describe_begin.argtypes = []
+    lib.cconv_describe_begin.restype = _INT
+    lib.cconv_describe_end.argtypes = [ctypes.POINTER(KernelDesc), _INT, ctypes.POINTER(_INT)]
+    lib.cconv_describe_end.restype = _INT
     if path is None:
         _lib = lib
     return lib
@@ -202,43 +214,57 @@ def _bias(b, D: int, w: torch.Tensor, name: str = "bias"):
 
 def _extent(t: torch.Tensor):
     """[first, last) byte range a tensor's elements span."""
-    if t.numel() == 0:
+    n = t.numel()
+    if n == 0:
         return (0, 0)
-    span = 1 + sum((s - 1) * st for s, st in zip(t.shape, t.stride()))
     a = t.data_ptr()
+    if t.is_contiguous():
+        return (a, a + n * t.element_size())
+    span = 1
+    for size, stride in zip(t.shape, t.stride()):
+        span += (size - 1) * stride
     return (a, a + span * t.element_size())
 
 
-def _disjoint(out: torch.Tensor | None, name: str, **inputs):
-    """An output must not overlap what the call reads."""
-    if out is None:
-        return
-    a0, a1 = _extent(out)
-    for n, t in inputs.items():
-        if t is None:
+def _disjoint(outs, ins):
+    """No output may overlap what the call reads.  outs, ins: sequences of (name, tensor or
+    None)."""
+    spans = [(n, _extent(t)) for n, t in ins if t is not None]
+    for on, o in outs:
+        if o is None:
             continue
-        b0, b1 = _extent(t)
-        if a0 < b1 and b0 < a1:
-            raise ValueError(f"{name} overlaps {n}")
+        a0, a1 = _extent(o)
+        for n, (b0, b1) in spans:
+            if a0 < b1 and b0 < a1:
+                raise ValueError(f"{on} overlaps {n}")
 
 
-def _device(**named) -> torch.device:
-    """Every given tensor is a CUDA tensor on the first one's device; returns that device."""
-    dev = None
-    for name, t in named.items():
+def _device(names, tensors) -> torch.device:
+    """Every given tensor (None entries skipped) is a CUDA tensor on the first one's device;
+    returns that device.  names: the tensors' names, a sequence or a function of the
+    position (only used for the error message)."""
+    idx = -2
+    for i, t in enumerate(tensors):
         if t is None:
             continue
-        if not t.is_cuda:
+        d = t.get_device()
+        if d >= 0 and (idx == -2 or d == idx):
+            idx = d
+            continue
+        name = names(i) if callable(names) else names[i]
+        if d < 0:
             raise ValueError(f"{name} must be a CUDA tensor, got device {t.device}")
-        if dev is None:
-            dev = t.device
-        elif t.device != dev:
-            raise ValueError(f"{name} is on {t.device}, but the call's tensors are on {dev}")
-    return dev
+        raise ValueError(f"{name} is on cuda:{d}, but the call's tensors are on cuda:{idx}")
+    return torch.device("cuda", idx)
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream, dev: torch.device) -> ctypes.c_void_p:
     if stream is None:
+        if _raw_stream is not None:
+            return ctypes.c_void_p(_raw_stream(dev.index))
         return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     if hasattr(stream, "cuda_stream"):
         sdev = getattr(stream, "device", None)
@@ -269,8 +295,8 @@ def cconv_fwd(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None = None
     _bias(bias, D, w)
     if y is not None:
         _exact(y, (B, T, D), torch.bfloat16, "y")
-        _disjoint(y, "y", x=x)
-    dev = _device(x=x, w=w, bias=bias, y=y)
+        _disjoint((("y", y),), (("x", x),))
+    dev = _device(("x", "w", "bias", "y"), (x, w, bias, y))
     if y is None:
         y = torch.empty((B, T, D), dtype=torch.bfloat16, device=dev)
     rc = _run(dev, load().cconv_fwd, _ptr(x), B, T, D, x.stride(0), x.stride(1), _ptr(w),
@@ -299,7 +325,7 @@ def _bwd_args(x, dy, w, bias, dx, dw, dbias, want_dbias):
     _bias(bias, D, w)
     if dx is not None:
         _exact(dx, (B, T, D), torch.bfloat16, "dx")
-        _disjoint(dx, "dx", x=x, dy=dy)
+        _disjoint((("dx", dx),), (("x", x), ("dy", dy)))
     if dw is not None:
         _exact(dw, (D, W), w.dtype, "dw")
     if want_dbias and dbias is not None:
@@ -319,8 +345,8 @@ def cconv_bwd(x: torch.Tensor, dy: torch.Tensor, w: torch.Tensor,
     B, T, D, W = _bwd_args(x, dy, w, bias, dx, dw, dbias, want_dbias)
     if workspace is not None:
         _workspace(workspace)
-    dev = _device(x=x, dy=dy, w=w, bias=bias, dx=dx, dw=dw,
-                  dbias=dbias if want_dbias else None, workspace=workspace)
+    dev = _device(("x", "dy", "w", "bias", "dx", "dw", "dbias", "workspace"),
+                  (x, dy, w, bias, dx, dw, dbias if want_dbias else None, workspace))
     if dx is None:
         dx = torch.empty((B, T, D), dtype=torch.bfloat16, device=dev)
     if dw is None:
@@ -346,7 +372,7 @@ def cconv_bwd_noalloc(x: torch.Tensor, dy: torch.Tensor, w: torch.Tensor,
     array instead of a workspace.  Calls that overlap on the GPU race on that array."""
     _bwd_args(x, dy, w, bias, dx, dw, dbias, True)
     B, T, D = x.shape
-    dev = _device(x=x, dy=dy, w=w, bias=bias, dx=dx, dw=dw, dbias=dbias)
+    dev = _device(("x", "dy", "w", "bias", "dx", "dw", "dbias"), (x, dy, w, bias, dx, dw, dbias))
     rc = _run(dev, load().cconv_bwd_noalloc, _ptr(x), x.stride(0), x.stride(1), _ptr(dy),
               dy.stride(0), dy.stride(1), B, T, D, _ptr(w), _ptr(bias), _wdt(w), w.shape[1],
               _ptr(dx), _ptr(dw), _ptr(dbias), _stream(stream, dev))
@@ -386,8 +412,8 @@ def cconv_update(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
         _exact(y, (N, D), torch.bfloat16, "y")
     if status is not None:
         _status(status)
-    dev = _device(x=x, state=state, w=w, bias=bias, state_indices=state_indices, y=y,
-                  status=status)
+    dev = _device(("x", "state", "w", "bias", "state_indices", "y", "status"),
+                  (x, state, w, bias, state_indices, y, status))
     if y is None:
         y = torch.empty((N, D), dtype=torch.bfloat16, device=dev)
     if status is None:
@@ -444,23 +470,24 @@ def cconv_fwd_varlen(x: torch.Tensor, cu_seqlens: torch.Tensor, w: torch.Tensor,
         final_state = None
     if final_state is not None:
         pools.append(_pool(final_state, D, (L,), "final_state")[0])
-        _disjoint(final_state, "final_state", x=x)
+        _disjoint((("final_state", final_state),), (("x", x),))
     if state_indices is not None:
         _int32_vec(state_indices, nseq, "state_indices")
         if status is not None:
             _status(status)
     if y is not None:
         _exact(y, (total, D), torch.bfloat16, "y")
-        _disjoint(y, "y", x=x, final_state=final_state)
+        _disjoint((("y", y),), (("x", x), ("final_state", final_state)))
     S = min(pools) if pools else nseq
     if want_final:
         S = min(S, nseq)
     if state_indices is None and (pools or want_final) and S < nseq:
         raise ValueError(f"without state_indices sequence i uses slot i: state arrays need "
                          f"at least nseq={nseq} slots")
-    dev = _device(x=x, cu_seqlens=cu_seqlens, w=w, bias=bias, initial_state=initial_state,
-                  final_state=final_state, state_indices=state_indices,
-                  status=status if state_indices is not None else None, y=y)
+    dev = _device(("x", "cu_seqlens", "w", "bias", "initial_state", "final_state",
+                   "state_indices", "status", "y"),
+                  (x, cu_seqlens, w, bias, initial_state, final_state, state_indices,
+                   status if state_indices is not None else None, y))
     if want_final:
         final_state = torch.empty((nseq, D, L), dtype=torch.bfloat16, device=dev)
     if state_indices is not None and status is None:
@@ -511,7 +538,7 @@ def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor
         want_dinit = initial_state is not None or d_initial_state is not None
     if dx is not None:
         _exact(dx, (total, D), torch.bfloat16, "dx")
-        _disjoint(dx, "dx", x=x, dy=dy)
+        _disjoint((("dx", dx),), (("x", x), ("dy", dy)))
     if dw is not None:
         _exact(dw, (D, W), w.dtype, "dw")
     if want_dbias and dbias is not None:
@@ -520,9 +547,11 @@ def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor
         _exact(d_initial_state, (nseq, D, L), torch.bfloat16, "d_initial_state")
     if workspace is not None:
         _workspace(workspace)
-    dev = _device(x=x, dy=dy, cu_seqlens=cu_seqlens, w=w, bias=bias, initial_state=initial_state,
-                  dx=dx, dw=dw, dbias=dbias if want_dbias else None,
-                  d_initial_state=d_initial_state if want_dinit else None, workspace=workspace)
+    dev = _device(("x", "dy", "cu_seqlens", "w", "bias", "initial_state", "dx", "dw", "dbias",
+                   "d_initial_state", "workspace"),
+                  (x, dy, cu_seqlens, w, bias, initial_state, dx, dw,
+                   dbias if want_dbias else None, d_initial_state if want_dinit else None,
+                   workspace))
     if dx is None:
         dx = torch.empty((total, D), dtype=torch.bfloat16, device=dev)
     if dw is None:
@@ -568,8 +597,8 @@ def cconv_update_ex(x: torch.Tensor, state: torch.Tensor, w: torch.Tensor,
         _exact(y, (N, D), torch.bfloat16, "y")
     if status is not None:
         _status(status)
-    dev = _device(x=x, state=state, w=w, bias=bias, state_indices=state_indices,
-                  cache_seqlens=cache_seqlens, y=y, status=status)
+    dev = _device(("x", "state", "w", "bias", "state_indices", "cache_seqlens", "y", "status"),
+                  (x, state, w, bias, state_indices, cache_seqlens, y, status))
     if y is None:
         y = torch.empty((N, D), dtype=torch.bfloat16, device=dev)
     if status is None:
@@ -625,8 +654,14 @@ def _outs(ts, n, shapes, dtypes, name):
     return ts
 
 
-def _devices(prefix, ts):
-    return {f"{prefix}{k}": t for k, t in enumerate(ts)}
+def _listed(*groups):
+    """Flattened (tensors, name-of-position) of named lists: groups of (prefix, list)."""
+    ts, where = [], []
+    for prefix, lst in groups:
+        for k, t in enumerate(lst):
+            ts.append(t)
+            where.append((prefix, k))
+    return ts, lambda i: f"{where[i][0]}[{where[i][1]}]"
 
 
 def cconv_fwd_multi(xs, ws, biases=None, *, ys=None, stream=None):
@@ -635,10 +670,9 @@ def cconv_fwd_multi(xs, ws, biases=None, *, ys=None, stream=None):
     n, B, T, Ds, W, biases = _problems(xs, ws, biases)
     if ys is not None:
         ys = _outs(ys, n, [(B, T, D) for D in Ds], [torch.bfloat16] * n, "ys")
-        for k in range(n):
-            _disjoint(ys[k], f"ys[{k}]", **_devices("x", xs))
-    dev = _device(**_devices("x", xs), **_devices("w", ws), **_devices("bias", biases),
-                  **_devices("y", ys or []))
+        _disjoint([(f"ys[{k}]", t) for k, t in enumerate(ys)],
+                  [(f"x[{k}]", t) for k, t in enumerate(xs)])
+    dev = _device(*reversed(_listed(("x", xs), ("w", ws), ("bias", biases), ("ys", ys or []))))
     if ys is None:
         ys = [torch.empty(x.shape, dtype=torch.bfloat16, device=dev) for x in xs]
     rc = _run(dev, load().cconv_fwd_multi, n, _parr(xs), _iarr(Ds),
@@ -674,18 +708,19 @@ def cconv_bwd_multi(xs, dys, ws, biases=None, *, want_dbias: bool | None = None,
     wdtype = ws[0].dtype
     if dxs is not None:
         dxs = _outs(dxs, n, [(B, T, D) for D in Ds], [torch.bfloat16] * n, "dxs")
-        for k in range(n):
-            _disjoint(dxs[k], f"dxs[{k}]", **_devices("x", xs), **_devices("dy", dys))
+        _disjoint([(f"dxs[{k}]", t) for k, t in enumerate(dxs)],
+                  [(f"x[{k}]", t) for k, t in enumerate(xs)] +
+                  [(f"dy[{k}]", t) for k, t in enumerate(dys)])
     if dws is not None:
         dws = _outs(dws, n, [(D, W) for D in Ds], [wdtype] * n, "dws")
     if want_dbias and dbiases is not None:
         dbiases = _outs(dbiases, n, [(D,) for D in Ds], [wdtype] * n, "dbiases")
     if workspace is not None:
         _workspace(workspace)
-    dev = _device(**_devices("x", xs), **_devices("dy", dys), **_devices("w", ws),
-                  **_devices("bias", biases), **_devices("dx", dxs or []),
-                  **_devices("dw", dws or []),
-                  **_devices("dbias", (dbiases or []) if want_dbias else []), workspace=workspace)
+    dev = _device(*reversed(_listed(("x", xs), ("dy", dys), ("w", ws), ("bias", biases),
+                                    ("dxs", dxs or []), ("dws", dws or []),
+                                    ("dbiases", (dbiases or []) if want_dbias else []),
+                                    ("workspace", [workspace]))))
     if dxs is None:
         dxs = [torch.empty(x.shape, dtype=torch.bfloat16, device=dev) for x in xs]
     if dws is None:
@@ -713,3 +748,20 @@ def cconv_device_fault() -> int:
     v = ctypes.c_int32(0)
     _check(load().cconv_device_fault(ctypes.byref(v)), "cconv_device_fault")
     return int(v.value)
+
+
+def describe(fn) -> list[dict]:
+    """The kernels fn() would launch through this library, with their registers per thread,
+    local (spill) bytes, shared memory, threads per CTA, grid size and resident CTAs per SM;
+    fn runs with launches recorded instead of enqueued (nothing runs on the GPU)."""
+    lib = load()
+    _check(lib.cconv_describe_begin(), "cconv_describe_begin")
+    try:
+        fn()
+    finally:
+        buf = (KernelDesc * 16)()
+        n = ctypes.c_int(0)
+        rc = lib.cconv_describe_end(buf, 16, ctypes.byref(n))
+    _check(rc, "cconv_describe_end")
+    return [{f: (getattr(d, f).decode() if f == "name" else getattr(d, f))
+             for f, _ in KernelDesc._fields_} for d in buf[:min(n.value, 16)]]

@@ -248,9 +248,18 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
 // With CCONV_DEBUG set in the environment, failing CUDA calls are reported on stderr.
 cudaError_t report_cuda(const char* what, cudaError_t e);
 
+// Launch recording (cconv_describe_begin / cconv_describe_end, host.cu): while the calling
+// thread records, a launch is described instead of enqueued.
+bool recording_launches();
+void record_launch(const void* func, dim3 grid, dim3 block, size_t smem);
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args... args) {
+  if (recording_launches()) {
+    record_launch(reinterpret_cast<const void*>(kernel), grid, block, smem);
+    return cudaSuccess;
+  }
   cudaLaunchConfig_t lc = {};
   lc.gridDim = grid;
   lc.blockDim = block;

@@ -2,10 +2,14 @@
 // count, TMA descriptor encoding, the fault-word reader.
 #include <cudaTypedefs.h>
 
+#include <cxxabi.h>
+
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -123,6 +127,30 @@ int encode_rows_map(CUtensorMap* map, const void* base, int64_t B, int64_t T, in
   return CCONV_OK;
 }
 
+// ------------------------------------------------------------------------------------
+// launch recording: what each entry point would launch, with the kernels' attributes
+// ------------------------------------------------------------------------------------
+struct LaunchRecord {
+  const void* func;
+  dim3 grid, block;
+  size_t smem;
+};
+
+static thread_local bool t_recording = false;
+static thread_local std::vector<LaunchRecord> t_records;
+
+bool recording_launches() { return t_recording; }
+
+void record_launch(const void* func, dim3 grid, dim3 block, size_t smem) {
+  t_records.push_back(LaunchRecord{func, grid, block, smem});
+}
+
+static void copy_name(char* dst, size_t n, const char* src) {
+  size_t k = 0;
+  for (; src && src[k] && k + 1 < n; ++k) dst[k] = src[k];
+  dst[k] = 0;
+}
+
 int set_max_dynamic_smem(const void* func, int bytes) {
   // Per device and cheap; repeated on every launch rather than cached.
   return report_cuda("cudaFuncSetAttribute",
@@ -151,6 +179,52 @@ CCONV_API const char* cconv_status_str(int status) {
     case CCONV_ERR_DEVICE: return "CCONV_ERR_DEVICE: a kernel gave up a bounded wait";
     default: return "unknown cconv status";
   }
+}
+
+CCONV_API int cconv_describe_begin(void) {
+  cconv::t_records.clear();
+  cconv::t_recording = true;
+  return CCONV_OK;
+}
+
+CCONV_API int cconv_describe_end(cconv_kernel_desc* out, int max, int* count) {
+  using namespace cconv;
+  t_recording = false;
+  if (!count || (max > 0 && !out)) return CCONV_ERR_NULL;
+  *count = static_cast<int>(t_records.size());
+  int rc = CCONV_OK;
+  for (int i = 0; i < max && i < static_cast<int>(t_records.size()); ++i) {
+    const LaunchRecord& r = t_records[i];
+    cconv_kernel_desc& d = out[i];
+    memset(&d, 0, sizeof(d));
+    cudaFuncAttributes fa{};
+    if (report_cuda("cudaFuncGetAttributes", cudaFuncGetAttributes(&fa, r.func)) != cudaSuccess) {
+      rc = CCONV_ERR_CUDA;
+      continue;
+    }
+    const int threads = static_cast<int>(r.block.x * r.block.y * r.block.z);
+    int per_sm = 0;
+    if (report_cuda("cudaOccupancyMaxActiveBlocksPerMultiprocessor",
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, r.func, threads,
+                                                                  r.smem)) != cudaSuccess)
+      rc = CCONV_ERR_CUDA;
+    const char* mangled = nullptr;
+    if (cudaFuncGetName(&mangled, r.func) == cudaSuccess && mangled) {
+      int st = 0;
+      char* dem = abi::__cxa_demangle(mangled, nullptr, nullptr, &st);
+      copy_name(d.name, sizeof(d.name), st == 0 && dem ? dem : mangled);
+      free(dem);
+    }
+    d.registers = fa.numRegs;
+    d.local_bytes = static_cast<int>(fa.localSizeBytes);
+    d.static_shared_bytes = static_cast<int>(fa.sharedSizeBytes);
+    d.dynamic_shared_bytes = static_cast<int>(r.smem);
+    d.threads = threads;
+    d.ctas_per_sm = per_sm;
+    d.ctas = static_cast<int64_t>(r.grid.x) * r.grid.y * r.grid.z;
+  }
+  t_records.clear();
+  return rc;
 }
 
 CCONV_API int cconv_device_fault(int32_t* fault) {

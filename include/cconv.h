@@ -330,6 +330,32 @@ CCONV_API int cconv_bwd_multi(int n, const void* const* x, const int64_t* sxb,
                               void* const* dbias, int64_t B, int64_t T, cconv_dtype wdt, int W,
                               void* workspace, size_t workspace_bytes, cconv_stream_t stream);
 
+/*
+ * Launch descriptions (a measurement and tuning aid; the pages have no counterpart).
+ *
+ * Between cconv_describe_begin() and cconv_describe_end() on one host thread, every call of
+ * this library on that thread runs its host-side checks and planning as usual but records
+ * the kernels it would launch instead of enqueueing them: nothing runs on the GPU and no
+ * output is written.  cconv_describe_end() stops recording, writes up to `max` descriptions
+ * into `out` (in launch order) and sets *count to the number of launches recorded.  The
+ * attributes come from the CUDA runtime (cudaFuncGetAttributes and the occupancy
+ * calculator, for the launch's block size and dynamic shared memory).  Returns CCONV_OK,
+ * CCONV_ERR_NULL, or CCONV_ERR_CUDA if an attribute query failed.
+ */
+typedef struct {
+  char name[160];            /* kernel name with its template arguments (may be truncated) */
+  int registers;             /* registers per thread */
+  int local_bytes;           /* local memory per thread (register spills and stack) */
+  int static_shared_bytes;   /* per CTA */
+  int dynamic_shared_bytes;  /* per CTA, as launched */
+  int threads;               /* per CTA */
+  int ctas_per_sm;           /* CTAs of this launch that fit on one SM at once */
+  int64_t ctas;              /* CTAs in the grid */
+} cconv_kernel_desc;
+
+CCONV_API int cconv_describe_begin(void);
+CCONV_API int cconv_describe_end(cconv_kernel_desc* out, int max, int* count);
+
 /* Human-readable name of a cconv_status value (static storage). */
 CCONV_API const char* cconv_status_str(int status);
 

@@ -27,7 +27,8 @@ def test_exports_match_header(lib):
                              "cconv_device_fault", "cconv_fwd_varlen",
                              "cconv_bwd_varlen_workspace_bytes", "cconv_bwd_varlen",
                              "cconv_update_ex", "cconv_fwd_multi",
-                             "cconv_bwd_multi_workspace_bytes", "cconv_bwd_multi"}
+                             "cconv_bwd_multi_workspace_bytes", "cconv_bwd_multi",
+                             "cconv_describe_begin", "cconv_describe_end"}
     for name in declared:
         assert hasattr(lib, name), f"{name} declared in cconv.h but not exported"
 
@@ -194,3 +195,21 @@ def test_causal_conv1d_rejects_unknown_activation():
     x = torch.zeros(1, 4, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         cc.causal_conv1d(x, torch.zeros(8, 4), activation="gelu")
+
+
+def test_describe_records_nothing_without_calls(lib):
+    n = ctypes.c_int(-1)
+    assert lib.cconv_describe_begin() == OK
+    assert lib.cconv_describe_end(None, 0, ctypes.byref(n)) == OK
+    assert n.value == 0
+    assert lib.cconv_describe_end(None, 0, None) == ENULL
+    assert lib.cconv_describe_end(None, 1, ctypes.byref(n)) == ENULL
+
+
+def test_describe_keeps_host_checks(lib):
+    # A call recorded between begin and end still runs its host checks and launches nothing.
+    n = ctypes.c_int(-1)
+    assert lib.cconv_describe_begin() == OK
+    assert _fwd(lib, W=5) == EWIDTH
+    assert lib.cconv_describe_end(None, 0, ctypes.byref(n)) == OK
+    assert n.value == 0
