@@ -293,20 +293,22 @@ __device__ __forceinline__ void bwd_tile_vl(const uint8_t* xt, const uint8_t* dy
   }
 }
 
-// Packed sequences, once per CTA after its rows: empty sequences get a zero initial-state
-// gradient (CTA i, i + grid, ...; all nthreads threads), and warp 0 of CTA 0 checks
-// cu_seqlens (a malformed one sets the fault word).
-__device__ __forceinline__ void bwd_varlen_tail(const BwdArgs& p, int nthreads, int warp,
-                                                int lane) {
+// Packed sequences, once per CTA: empty sequences get a zero initial-state gradient (CTA i,
+// i + grid, ...), and CTA 0 checks cu_seqlens (a malformed one sets the fault word).  The
+// `nthreads` threads from thread `first` on share the zeroing, and the warp holding thread
+// `first` does the check; every call site runs it with whole warps.
+__device__ __forceinline__ void bwd_varlen_tail(const BwdArgs& p, int first, int nthreads) {
+  const int tid = static_cast<int>(threadIdx.x) - first;
+  const int lane = threadIdx.x & 31;
   if (p.dinit && p.W > 1) {
     const int64_t n = p.D * (p.W - 1);
     for (int i = blockIdx.x; i < p.nseq; i += gridDim.x) {
       if (clamp_row(p.cu[i + 1], p.BT) > clamp_row(p.cu[i], p.BT)) continue;
       uint16_t* o = p.dinit + static_cast<int64_t>(i) * n;
-      for (int64_t k = threadIdx.x; k < n; k += nthreads) o[k] = 0;
+      for (int64_t k = tid; k < n; k += nthreads) o[k] = 0;
     }
   }
-  if (blockIdx.x == 0 && warp == 0) {
+  if (blockIdx.x == 0 && tid < 32) {
     bool bad = false;
     for (int k = lane; k <= p.nseq; k += 32) {
       const int v = p.cu[k];
@@ -376,8 +378,7 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
     // halo, the ring refill and two tiles on the per-row path; 40-48 rows balanced 16 and
     // 128 mixed sequences and 8 short clustered ones best (measured).
     constexpr int kBoundaryRows = 44;
-    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k, p.wpc, lane);
-    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, k + 1, p.wpc, lane);
+    cost_split_range(p.cu, p.nseq, p.BT, kBoundaryRows, k, p.wpc, lane, r0, r1);
   } else {
     r0 = static_cast<int>(static_cast<int64_t>(k) * p.BT / p.wpc);
     r1 = static_cast<int>(static_cast<int64_t>(k + 1) * p.BT / p.wpc);
@@ -472,7 +473,7 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }
-  if constexpr (VL) bwd_varlen_tail(p, NW * 32, warp, lane);
+  if constexpr (VL) bwd_varlen_tail(p, 0, NW * 32);
 
   // ---- the CTA's partial sums, added in a fixed order ------------------------------------
   // Every warp has consumed all its tiles, so the stage memory is free for NW records.
@@ -559,8 +560,7 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
     // 4096 rows); measured: 16 rows 75.2 / 86.2, 24: 74.7 / 84.3, 32: 73.9 / 85.3, 64:
     // 75.7 / 95.2 us.
     constexpr int kBoundaryRows = 32;
-    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg, p.wpc, lane);
-    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, rg + 1, p.wpc, lane);
+    cost_split_range(p.cu, p.nseq, p.BT, kBoundaryRows, rg, p.wpc, lane, r0, r1);
   } else {
     r0 = static_cast<int>(static_cast<int64_t>(rg) * p.BT / p.wpc);
     r1 = static_cast<int>(static_cast<int64_t>(rg + 1) * p.BT / p.wpc);
@@ -661,7 +661,7 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
       s = (s + 1 == S) ? 0 : s + 1;
     }
   }
-  if constexpr (VL) bwd_varlen_tail(p, (NC + 1) * 32, warp, lane);
+  if constexpr (VL) bwd_varlen_tail(p, 0, (NC + 1) * 32);
 
   // ---- the CTA's partial sums: one record per strip (one range per CTA) -------------------
   float* rec = p.ws + static_cast<int64_t>(blockIdx.x) * NC * REC;

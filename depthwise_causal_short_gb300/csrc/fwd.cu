@@ -287,8 +287,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
   // previous kernel on the stream may have written.
   int r0, r1;
   if constexpr (VL) {  // equal cost: a sequence boundary counts as kBoundaryRows rows
-    r0 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, part, p.cpc, lane);
-    r1 = cost_split(p.cu, p.nseq, p.BT, kBoundaryRows, part + 1, p.cpc, lane);
+    cost_split_range(p.cu, p.nseq, p.BT, kBoundaryRows, part, p.cpc, lane, r0, r1);
   } else {
     r0 = static_cast<int>(static_cast<int64_t>(part) * p.BT / p.cpc);
     r1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.BT / p.cpc);
@@ -297,6 +296,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
   cur.init(r0, r1, p.T, 0, R);
   if (SEP && warp == NC) {
     // ---- producer warp -------------------------------------------------------------------
+    int issued = 0;
     if (lane == 0) {
       uint32_t eph = 0;
       int s = 0, i = 0;
@@ -312,13 +312,14 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
         cur.advance();
         s = (s + 1 == S) ? 0 : s + 1;
       }
-      drain_issued<S>(full, i);  // i tiles issued
+      issued = i;
     }
-    if constexpr (VL) {
+    if constexpr (VL) {  // the idle warp's packed-sequence duties overlap the last tiles
       __syncwarp();
       if (blockIdx.x == 0) check_seqlens(p.cu, p.nseq, p.BT, lane, &g_fault_fwd);
       if (p.fin) final_of_empty(p, blockIdx.x, gridDim.x, lane);
     }
+    if (lane == 0) drain_issued<S>(full, issued);
   } else if (warp < nact) {
     // ---- consumer ------------------------------------------------------------------------
     const bool leader = !SEP && warp == 0;

@@ -13,7 +13,7 @@
 // starts a sequence, those 3 rows lie at t < 0 and the copy engine fills them with zeros,
 // which is exactly the causal zero padding.  Packed sequences of any lengths (SeqTracker)
 // take their ring at a sequence start from the sequence's initial state instead, and their
-// ranges are of equal cost (cost_split) rather than equal rows.  The backward cuts the rows
+// ranges are of equal cost (cost_split_range) rather than equal rows.  The backward cuts the rows
 // the same way but per warp: each warp walks its own range of one channel strip with its
 // own pipeline (bwd.cu).
 #pragma once
@@ -141,36 +141,64 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int nseq, int total, 
   return lo;
 }
 
-// Packed sequences: where range `num` of `den` starts when ranges get equal COST rather than
-// equal rows.  A sequence boundary costs a warp about `c` rows of work (the extra tile and
-// the ring refill around it), so the cost up to row r of sequence i is r + c*i and the
-// total is total + c*(nseq - 1).  The split row is found with the same warp-wide search as
-// find_seq, on the keys cu[i] + c*i (non-decreasing when cu is): the largest i whose key is
-// at most the target, then the row inside sequence i that reaches it (or the sequence's
-// end).  Split rows are non-decreasing in `num`, start at 0 and end at total.  Must be
+// Packed sequences: where range `num` of `den` starts and ends when ranges get equal COST
+// rather than equal rows.  A sequence boundary costs a warp about `c` rows of work (the extra
+// tile and the ring refill around it), so the cost up to row r of sequence i is r + c*i and
+// the total is total + c*(nseq - 1).  Each split row is found with a warp-wide search like
+// find_seq's, on the keys cu[i] + c*i (non-decreasing when cu is): the largest i whose key
+// is at most the target, then the row inside sequence i that reaches it (or the sequence's
+// end).  Split rows are non-decreasing in `num`, start at 0 and end at total.
+//
+// r0 = split(num) and r1 = split(num + 1) are searched side by side so that their loads are
+// issued together: each round every lane loads one probe of each search, and the last round
+// (at most 31 candidates left) also loads the entry after the last candidate, so the two
+// entries that bound the answer come from the warp's registers by shuffle instead of two
+// more loads.  For up to 31 sequences the whole split costs one load per lane.  Must be
 // called by all 32 lanes.
-__device__ __forceinline__ int cost_split(const int32_t* cu, int nseq, int total, int c,
-                                          int num, int den, int lane) {
-  if (num <= 0) return 0;
-  if (num >= den) return total;
+__device__ __forceinline__ void cost_split_range(const int32_t* cu, int nseq, int total, int c,
+                                                 int num, int den, int lane, int& r0, int& r1) {
   const int64_t cost = static_cast<int64_t>(total) + static_cast<int64_t>(c) * (nseq - 1);
-  const int64_t tau = cost * num / den;
-  int lo = 0, n = nseq;
-  while (n > 1) {
-    const int step = (n + 31) / 32;
-    const int pos = lo + lane * step;
-    const bool le = lane == 0 ||
-                    (pos < lo + n &&
-                     clamp_row(cu[pos], total) + static_cast<int64_t>(c) * pos <= tau);
-    const unsigned m = __ballot_sync(0xffffffffu, le);
-    lo += (31 - __clz(m)) * step;
-    const int left = nseq - lo;
-    n = step < left ? step : left;
+  const int64_t tau[2] = {cost * num / den, cost * (num + 1) / den};
+  int lo[2] = {0, 0}, n[2] = {nseq, nseq}, idx[2] = {0, 0}, a[2] = {0, 0}, e[2] = {0, 0};
+  bool done[2] = {false, false};
+  while (!(done[0] && done[1])) {
+    int v[2], pos[2];
+    bool fin[2], in[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // both probes' loads first
+      fin[k] = !done[k] && n[k] <= 31;
+      const int step = fin[k] ? 1 : (n[k] + 31) / 32;
+      pos[k] = lo[k] + lane * step;
+      in[k] = !done[k] && (fin[k] ? lane <= n[k] : pos[k] < lo[k] + n[k]);
+      v[k] = in[k] ? clamp_row(cu[pos[k]], total) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (done[k]) continue;  // uniform over the warp
+      const bool cand = fin[k] ? lane < n[k] : in[k];
+      const bool le = lane == 0 || (cand && v[k] + static_cast<int64_t>(c) * pos[k] <= tau[k]);
+      const int last = 31 - __clz(__ballot_sync(0xffffffffu, le));
+      if (fin[k]) {
+        idx[k] = lo[k] + last;
+        a[k] = __shfl_sync(0xffffffffu, v[k], last);
+        e[k] = __shfl_sync(0xffffffffu, v[k], last + 1);
+        done[k] = true;
+      } else {
+        const int step = (n[k] + 31) / 32;
+        lo[k] += last * step;
+        const int left = nseq - lo[k];
+        n[k] = step < left ? step : left;
+      }
+    }
   }
-  const int64_t r = tau - static_cast<int64_t>(c) * lo;
-  const int a = clamp_row(cu[lo], total);
-  const int e = clamp_row(cu[lo + 1], total);
-  return r < a ? a : (r > e ? e : static_cast<int>(r));
+  int r[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int64_t x = tau[k] - static_cast<int64_t>(c) * idx[k];
+    r[k] = x < a[k] ? a[k] : (x > e[k] ? e[k] : static_cast<int>(x));
+  }
+  r0 = num <= 0 ? 0 : (num >= den ? total : r[0]);
+  r1 = num + 1 >= den ? total : r[1];
 }
 
 // Packed sequences: which sequence the rows a warp walks belong to.  A range of packed rows

@@ -2,7 +2,8 @@
 
 While recording, a call runs its host checks and planning and reports the kernels it would
 launch, with their resources, and nothing runs: outputs keep their contents.  The backward
-at the production shape is a one-wave stream kernel (one CTA per SM) plus its reduction.
+at the production shape is a one-wave lockstep stream kernel (one CTA per SM) plus its
+reduction; below 512 channels an independent-pipeline stream kernel plus the reduction.
 """
 import pytest
 import torch
@@ -52,6 +53,10 @@ def test_every_call_describes(dev):
                                                        final_state=True))) == 1
     assert len(cc.describe(lambda: cc.cconv_bwd_varlen(vx, vdy, cu, vw, vb,
                                                        initial_state=init))) == 2
+    narrow = [t[..., :256] for t in (x, dy)]
+    ks = cc.describe(lambda: cc.cconv_bwd(*narrow, w[:256].contiguous()))
+    assert [k["name"].split("(")[0].split("<")[0].split("::")[-1] for k in ks] == [
+        "cconv_bwd_kernel", "cconv_bwd_reduce1_kernel"]
     xs = [x, x[..., :256]]
     ws = [w, w[:256].contiguous()]
     assert len(cc.describe(lambda: cc.cconv_fwd_multi(xs, ws))) == 1
