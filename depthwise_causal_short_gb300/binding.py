@@ -85,7 +85,8 @@ def load(path: str | Path | None = None):
                                                      ctypes.POINTER(ctypes.c_size_t)]
     lib.cconv_bwd_varlen_workspace_bytes.restype = _INT
     lib.cconv_bwd_varlen.argtypes = [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _INT, _INT,
-                                     _INT, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+                                     _INT, _P, _P, _I64, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                     _P]
     lib.cconv_bwd_varlen.restype = _INT
     lib.cconv_update_ex.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _P, _P,
                                     _INT, _INT, _INT, _P, _P, _P]
@@ -513,13 +514,18 @@ def cconv_bwd_varlen_workspace_bytes(total: int, D: int, W: int, device=None) ->
 
 def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor,
                      w: torch.Tensor, bias: torch.Tensor | None = None, *, activation="silu",
-                     initial_state: torch.Tensor | None = None, want_dbias: bool | None = None,
+                     initial_state: torch.Tensor | None = None,
+                     state_indices: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None, want_dbias: bool | None = None,
                      want_dinit: bool | None = None, dx: torch.Tensor | None = None,
                      dw: torch.Tensor | None = None, dbias: torch.Tensor | None = None,
                      d_initial_state: torch.Tensor | None = None,
                      workspace: torch.Tensor | None = None, stream=None):
     """Packed-sequence backward: (dx, dw, dbias or None, d_initial_state or None).
-    initial_state and d_initial_state are [nseq, D, W-1] (slot i is sequence i)."""
+    initial_state is [nseq, D, W-1] (slot i is sequence i), or with state_indices (int32
+    [nseq] on the device) a pool [S, D, W-1] whose slot state_indices[i] is sequence i's;
+    the indices are checked on the device and `status` (int32[2], required with indices)
+    gets the verdict.  d_initial_state is [nseq, D, W-1]."""
     _rows(x, "x", 2)
     _rows(dy, "dy", 2)
     total, D = x.shape
@@ -530,7 +536,15 @@ def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor
     _bias(bias, D, w)
     act = _act(activation)
     L = W - 1
-    if initial_state is not None:
+    S = nseq
+    if state_indices is not None:
+        _int32_vec(state_indices, nseq, "state_indices")
+        if status is None:
+            raise ValueError("status (int32[2] on the device) is required with state_indices")
+        _status(status)
+        if initial_state is not None:
+            S = _pool(initial_state, D, (L,), "initial_state")[0]
+    elif initial_state is not None:
         _exact(initial_state, (nseq, D, L), torch.bfloat16, "initial_state")
     if want_dbias is None:
         want_dbias = bias is not None or dbias is not None
@@ -547,9 +561,10 @@ def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor
         _exact(d_initial_state, (nseq, D, L), torch.bfloat16, "d_initial_state")
     if workspace is not None:
         _workspace(workspace)
-    dev = _device(("x", "dy", "cu_seqlens", "w", "bias", "initial_state", "dx", "dw", "dbias",
-                   "d_initial_state", "workspace"),
-                  (x, dy, cu_seqlens, w, bias, initial_state, dx, dw,
+    dev = _device(("x", "dy", "cu_seqlens", "w", "bias", "initial_state", "state_indices",
+                   "status", "dx", "dw", "dbias", "d_initial_state", "workspace"),
+                  (x, dy, cu_seqlens, w, bias, initial_state, state_indices,
+                   status if state_indices is not None else None, dx, dw,
                    dbias if want_dbias else None, d_initial_state if want_dinit else None,
                    workspace))
     if dx is None:
@@ -565,7 +580,8 @@ def cconv_bwd_varlen(x: torch.Tensor, dy: torch.Tensor, cu_seqlens: torch.Tensor
                                 dtype=torch.uint8, device=dev)
     rc = _run(dev, load().cconv_bwd_varlen,
               _ptr(x), x.stride(0), _ptr(dy), dy.stride(0), total, D, _ptr(cu_seqlens), nseq,
-              _ptr(w), _ptr(bias), _wdt(w), W, act, _ptr(initial_state), _ptr(dx), _ptr(dw),
+              _ptr(w), _ptr(bias), _wdt(w), W, act, _ptr(initial_state), _ptr(state_indices), S,
+              _ptr(status if state_indices is not None else None), _ptr(dx), _ptr(dw),
               _ptr(dbias if want_dbias else None), _ptr(d_initial_state if want_dinit else None),
               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check(rc, "cconv_bwd_varlen")

@@ -56,10 +56,19 @@ struct BwdArgs {
   int W, wdt;
   // packed sequences only
   const int32_t* cu;        // [nseq + 1] row offsets
-  const uint16_t* init;     // [nseq, D, W-1] initial states, or null (zeros)
-  uint16_t* dinit;          // [nseq, D, W-1] their gradient, or null
+  const uint16_t* init;     // [S, D, W-1] initial states, or null (zeros)
+  const int32_t* idx;       // [nseq] slot of each sequence's initial state, or null (slot i)
+  int64_t S;                // slots of init (nseq without idx)
+  uint16_t* dinit;          // [nseq, D, W-1] gradient of each sequence's initial state, or null
   int nseq;
 };
+
+// Slot of sequence i's initial state, or -1 when the index is unusable (negative or >= S:
+// the sequence then starts from zeros, and the index check reports it).
+__device__ __forceinline__ int64_t init_slot(const BwdArgs& p, int i) {
+  const int64_t s = p.idx ? static_cast<int64_t>(p.idx[i]) : i;
+  return (s >= 0 && s < p.S) ? s : -1;
+}
 
 // Kernel modes: the batched [B,T,D] form with SiLU is mode 0.
 enum : int { kModeVarlen = 1, kModeActNone = 2 };
@@ -216,7 +225,7 @@ template <int VEC>
 __device__ __forceinline__ void bwd_boundary(int t, const TileCursor& c, SeqTracker& sq,
                                              bool active, const BwdArgs& p, int64_t d0,
                                              const f2 (&tap)[4][VEC / 2], f2 (&h)[3][VEC / 2],
-                                             f2 (&gr)[3][VEC / 2], f2 (&hin)[3][VEC / 2],
+                                             f2 (&gr)[3][VEC / 2], uint32_t (&hin)[3][VEC / 2],
                                              int& hin_seq) {
   constexpr int P = VEC / 2;
   f2 zero[P];
@@ -235,17 +244,15 @@ __device__ __forceinline__ void bwd_boundary(int t, const TileCursor& c, SeqTrac
     }
   }
   sq.next(t);
-  if (hin_seq != sq.i) init_ring<VEC>(p.init, sq.i, p.D, p.W, d0, active, hin);
+  if (hin_seq != sq.i) init_ring<VEC>(p.init, init_slot(p, sq.i), p.D, p.W, d0, active, hin);
+  ring_of<VEC>(hin, h);
 #pragma unroll
   for (int q = 0; q < P; ++q)
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      h[j][q] = hin[j][q];
-      gr[j][q] = 0ull;
-    }
+    for (int j = 0; j < 3; ++j) gr[j][q] = 0ull;
   hin_seq = -1;
   if (sq.i + 1 < p.nseq) {
-    init_ring<VEC>(p.init, sq.i + 1, p.D, p.W, d0, active, hin);
+    init_ring<VEC>(p.init, init_slot(p, sq.i + 1), p.D, p.W, d0, active, hin);
     hin_seq = sq.i + 1;
   }
 }
@@ -262,7 +269,7 @@ __device__ __forceinline__ void bwd_tile_vl(const uint8_t* xt, const uint8_t* dy
                                             const f2 (&tap)[4][VEC / 2],
                                             const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
                                             f2 (&gr)[3][VEC / 2], f2 (&acc)[kRec][VEC / 2],
-                                            f2 (&hin)[3][VEC / 2], int& hin_seq) {
+                                            uint32_t (&hin)[3][VEC / 2], int& hin_seq) {
   constexpr int P = VEC / 2;
   constexpr int ROWB = 32 * VEC * 2;
   // Not unrolled: unrolling the boundary event into every row made the whole kernel slower
@@ -422,12 +429,12 @@ __device__ __forceinline__ void bwd_cta(const CUtensorMap* tmx, const CUtensorMa
     // Packed sequences: the sequence of the rows walked (from the first ring-fill row on),
     // and hin, the initial x ring of sequence hin_seq, fetched one sequence ahead.
     SeqTracker sq;
-    f2 hin[3][P];
+    uint32_t hin[3][P];
     int hin_seq = -1;
     if constexpr (VL) {
       sq.init(p.cu, p.nseq, p.BT, r0 - kRing, lane);  // all lanes of the warp
       if (sq.i + 1 < p.nseq) {
-        init_ring<VEC>(p.init, sq.i + 1, p.D, p.W, d0, active, hin);
+        init_ring<VEC>(p.init, init_slot(p, sq.i + 1), p.D, p.W, d0, active, hin);
         hin_seq = sq.i + 1;
       }
     }
@@ -616,12 +623,12 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
     // Packed sequences: the sequence of the rows walked (from the first ring-fill row on),
     // and hin, the initial x ring of sequence hin_seq, fetched one sequence ahead.
     SeqTracker sq;
-    f2 hin[3][P];
+    uint32_t hin[3][P];
     int hin_seq = -1;
     if constexpr (VL) {
       sq.init(p.cu, p.nseq, p.BT, r0 - kRing, lane);  // all lanes of the warp
       if (sq.i + 1 < p.nseq) {
-        init_ring<VEC>(p.init, sq.i + 1, p.D, p.W, d0, active, hin);
+        init_ring<VEC>(p.init, init_slot(p, sq.i + 1), p.D, p.W, d0, active, hin);
         hin_seq = sq.i + 1;
       }
     }
@@ -1027,7 +1034,7 @@ CCONV_API int cconv_bwd(const void* x, int64_t sxb, int64_t sxt, const void* dy,
   rc = encode_rows_map(&tmdy, dy, B, T, D, sdb, sdt, 32 * cfg.vec, cfg.rows);
   if (rc != CCONV_OK) return rc;
 
-  BwdArgs a;
+  BwdArgs a{};
   a.w = w;
   a.bias = bias;
   a.dx = static_cast<uint16_t*>(dx);
@@ -1188,9 +1195,10 @@ CCONV_API int cconv_bwd_varlen_workspace_bytes(int64_t total, int64_t D, int W, 
 CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64_t sdt,
                                int64_t total, int64_t D, const int32_t* cu_seqlens, int64_t nseq,
                                const void* w, const void* bias, cconv_dtype wdt, int W,
-                               cconv_activation act, const void* initial_state, void* dx,
-                               void* dw, void* dbias, void* d_initial_state, void* workspace,
-                               size_t workspace_bytes, cconv_stream_t stream) {
+                               cconv_activation act, const void* initial_state,
+                               const int32_t* state_indices, int64_t S, int32_t* status_dev,
+                               void* dx, void* dw, void* dbias, void* d_initial_state,
+                               void* workspace, size_t workspace_bytes, cconv_stream_t stream) {
   using namespace cconv;
   if (!w || !dw || !cu_seqlens) return CCONV_ERR_NULL;
   if (total > 0 && (!x || !dy || !dx)) return CCONV_ERR_NULL;
@@ -1216,6 +1224,18 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
   if (L > 0 && ((initial_state && reinterpret_cast<uintptr_t>(initial_state) % 2 != 0) ||
                 (d_initial_state && reinterpret_cast<uintptr_t>(d_initial_state) % 2 != 0)))
     return CCONV_ERR_ALIGN;
+  if (state_indices) {
+    if (!status_dev) return CCONV_ERR_NULL;
+    if (S < 1 || S > CCONV_UPDATE_MAX_SLOTS) return CCONV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(state_indices) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(status_dev) % 4 != 0)
+      return CCONV_ERR_ALIGN;
+  }
+  // With indices, one small kernel checks them (and writes the status words) after the
+  // gradient kernels; unusable slots are read as zeros by the stream kernel meanwhile.
+  auto check_indices = [&](cudaStream_t s) {
+    return state_indices ? launch_index_check(state_indices, nseq, S, status_dev, s) : CCONV_OK;
+  };
 
   const BwdConfig& cfg = varlen_config(D);
   BwdPlan plan;
@@ -1240,7 +1260,7 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
     if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, ra) !=
         cudaSuccess)
       return CCONV_ERR_CUDA;
-    return CCONV_OK;
+    return check_indices(st);
   }
 
   if (!workspace || workspace_bytes < need) return CCONV_ERR_WORKSPACE;
@@ -1254,7 +1274,7 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
   rc = encode_rows_map(&tmdy, dy, 1, total, D, sdb, sdt, 32 * cfg.vec, cfg.rows);
   if (rc != CCONV_OK) return rc;
 
-  BwdArgs a;
+  BwdArgs a{};
   a.w = w;
   a.bias = bias;
   a.dx = static_cast<uint16_t*>(dx);
@@ -1268,6 +1288,8 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
   a.wdt = wdt;
   a.cu = cu_seqlens;
   a.init = L > 0 ? static_cast<const uint16_t*>(initial_state) : nullptr;
+  a.idx = state_indices;
+  a.S = state_indices ? S : nseq;
   a.dinit = L > 0 ? static_cast<uint16_t*>(d_initial_state) : nullptr;
   a.nseq = static_cast<int>(nseq);
 
@@ -1287,7 +1309,7 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
   if (launch_pdl(cconv_bwd_reduce_kernel, red_grid, dim3(32 * kRedGroups), 0, st, ra) !=
       cudaSuccess)
     return CCONV_ERR_CUDA;
-  return CCONV_OK;
+  return check_indices(st);
 }
 
 }  // extern "C"

@@ -280,6 +280,10 @@ int sm_count_current_device(int* sms, int* device);
 int encode_rows_map(CUtensorMap* map, const void* base, int64_t B, int64_t T, int64_t D,
                     int64_t sb, int64_t st, int box_c, int box_r);
 int set_max_dynamic_smem(const void* func, int bytes);
+// Validates n state indices against a pool of S slots (negative, >= S, repeated), as the
+// decode update does, and writes status[0..1]; nothing else (fwd.cu).
+int launch_index_check(const int32_t* idx, int64_t n, int64_t S, int32_t* status,
+                       cudaStream_t stream);
 
 }  // namespace cconv
 

@@ -186,16 +186,13 @@ __device__ __forceinline__ void final_of_empty(const FwdArgs& p, int first, int 
 template <int VEC>
 __device__ __forceinline__ void fwd_boundary(int t, const TileCursor& c, SeqTracker& sq,
                                              bool active, const FwdArgs& p, int64_t d0,
-                                             f2 (&h)[3][VEC / 2], f2 (&hin)[3][VEC / 2],
+                                             f2 (&h)[3][VEC / 2], uint32_t (&hin)[3][VEC / 2],
                                              int& hin_seq) {
   if (p.fin && active && sq.i >= 0 && sq.ss < t && t > c.a && t <= c.e)
     store_final<VEC>(p.fin, sq.i, p.D, p.W, d0, h);
   sq.next(t);
   if (hin_seq != sq.i) init_ring<VEC>(p.init, seq_slot(p, sq.i), p.D, p.W, d0, active, hin);
-#pragma unroll
-  for (int j = 0; j < 3; ++j)
-#pragma unroll
-    for (int q = 0; q < VEC / 2; ++q) h[j][q] = hin[j][q];
+  ring_of<VEC>(hin, h);
   hin_seq = -1;
   if (sq.i + 1 < p.nseq) {
     init_ring<VEC>(p.init, seq_slot(p, sq.i + 1), p.D, p.W, d0, active, hin);
@@ -213,7 +210,7 @@ __device__ __forceinline__ void fwd_tile_vl(const uint8_t* tile, int lane, const
                                             SeqTracker& sq, bool active, const FwdArgs& p,
                                             int64_t d0, const f2 (&tap)[4][VEC / 2],
                                             const f2 (&bias2)[VEC / 2], f2 (&h)[3][VEC / 2],
-                                            f2 (&hin)[3][VEC / 2], int& hin_seq) {
+                                            uint32_t (&hin)[3][VEC / 2], int& hin_seq) {
   constexpr int P = VEC / 2;
   constexpr int ROWB = 32 * VEC * 2;
   uint16_t* yrow = p.y + static_cast<int64_t>(c.tt) * p.D + d0;
@@ -345,7 +342,7 @@ __device__ __forceinline__ void fwd_cta(const CUtensorMap* tmx, const FwdArgs& p
     // Packed sequences: the sequence of the rows walked (from the first ring-fill row on),
     // and hin, the initial ring of sequence hin_seq, fetched one sequence ahead.
     SeqTracker sq;
-    f2 hin[3][VEC / 2];
+    uint32_t hin[3][VEC / 2];
     int hin_seq = -1;
     if constexpr (VL) {
       sq.init(p.cu, p.nseq, p.BT, r0 - kRing, lane);  // all lanes of the warp
@@ -665,6 +662,24 @@ constexpr int kVarlenVec = 4, kVarlenRows = 8, kVarlenStages = 10, kVarlenNc = 8
 static void (*const kStateKernels[4])(const StateArgs) = {
     cconv_fwd_state_kernel<0>, cconv_fwd_state_kernel<1>, cconv_fwd_state_kernel<2>,
     cconv_fwd_state_kernel<3>};
+
+int launch_index_check(const int32_t* idx, int64_t n, int64_t S, int32_t* status,
+                       cudaStream_t stream) {
+  StateArgs sa{};
+  sa.idx = idx;
+  sa.status = status;
+  sa.S = S;
+  sa.nseq = static_cast<int>(n);
+  sa.fin = nullptr;  // validation and status only: one CTA checks every index
+  auto kern = kStateKernels[0];
+  const size_t smem = static_cast<size_t>((S + 31) / 32) * 4;
+  if (smem > 32 * 1024 &&
+      set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) != CCONV_OK)
+    return CCONV_ERR_CUDA;
+  return launch_pdl(kern, dim3(1), dim3(kStateThreads), smem, stream, sa) == cudaSuccess
+             ? CCONV_OK
+             : CCONV_ERR_CUDA;
+}
 
 }  // namespace cconv
 

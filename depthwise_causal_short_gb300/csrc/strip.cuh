@@ -258,24 +258,35 @@ struct SeqTracker {
 };
 
 // Ring of the W-1 rows before a sequence, from its initial state (bf16 [.., D, W-1], entry
-// j = row ss - (W-1) + j), as this lane's fp32 pairs: h[k-1] = row ss - k, zero for
-// k > W - 1 or without a state (state == nullptr or slot < 0).
+// j = row ss - (W-1) + j), as this lane's bf16 pairs: hr[k-1][q] holds row ss - k for
+// channels (d0 + 2q, d0 + 2q + 1), zero for k > W - 1 or without a state (state == nullptr
+// or slot < 0).  The packed-sequence kernels fetch it one sequence ahead and keep it as bf16
+// (half the registers of fp32 pairs) until the sequence starts (ring_of).
 template <int VEC>
 __device__ __forceinline__ void init_ring(const uint16_t* state, int64_t slot, int64_t D, int W,
-                                          int64_t d0, bool active, f2 (&h)[3][VEC / 2]) {
+                                          int64_t d0, bool active, uint32_t (&hr)[3][VEC / 2]) {
   const int L = W - 1;
 #pragma unroll
   for (int k = 1; k <= 3; ++k)
 #pragma unroll
     for (int q = 0; q < VEC / 2; ++q) {
-      float lo = 0.f, hi = 0.f;
+      uint32_t lo = 0u, hi = 0u;
       if (state && slot >= 0 && active && k <= L) {
         const uint16_t* s0 = state + (slot * D + d0 + 2 * q) * L + (L - k);
-        lo = bf16_to_f32(s0[0]);
-        hi = bf16_to_f32(s0[L]);
+        lo = s0[0];
+        hi = s0[L];
       }
-      h[k - 1][q] = f2_pack(lo, hi);
+      hr[k - 1][q] = lo | (hi << 16);
     }
+}
+
+// The fp32 ring of a sequence from its bf16 initial ring (exact).
+template <int VEC>
+__device__ __forceinline__ void ring_of(const uint32_t (&hr)[3][VEC / 2], f2 (&h)[3][VEC / 2]) {
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+#pragma unroll
+    for (int q = 0; q < VEC / 2; ++q) h[j][q] = bf16x2_to_f2(hr[j][q]);
 }
 
 // Taps of one lane, as fp32 pairs, HALVED: tap[k][p] = w[d, W-1-k] / 2 multiplies x[t-k]

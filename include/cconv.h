@@ -279,7 +279,8 @@ CCONV_API int cconv_bwd_varlen_workspace_bytes(int64_t total, int64_t D, int W, 
 
 /*
  * cconv_bwd_varlen -- backward over packed sequences: dx, dw, dbias and the gradient of
- * the initial states, with z recomputed (two kernels on `stream`, deterministic).
+ * the initial states, with z recomputed (two kernels on `stream`, deterministic; a third,
+ * small one checks state_indices when they are given).
  *
  *   g = dy * silu'(z) (CCONV_ACT_SILU) or dy (CCONV_ACT_NONE)
  *   dx[t]          = sum_{k<W} w[d, W-1-k] g[t+k]   over t+k inside t's sequence
@@ -288,10 +289,21 @@ CCONV_API int cconv_bwd_varlen_workspace_bytes(int64_t total, int64_t D, int W, 
  *   d_initial_state[i][d][j] = sum_{k<W} w[d, W-1-k] g[u+k] over u+k inside sequence i,
  *                              u = cu[i] - (W-1) + j   (zero for an empty sequence)
  *
- *   initial_state    [nseq, D, W-1] bf16 or NULL (zeros); slot i is sequence i.
+ *   initial_state    [S, D, W-1] bf16 or NULL (zeros).  Sequence i's initial state is slot
+ *                    state_indices[i] when indices are given (the decode pool a chunked
+ *                    prefill read from), else slot i (then S is ignored and the array holds
+ *                    nseq slots).
+ *   state_indices    int32[nseq] in device memory, or NULL.  Given, 1 <= S <=
+ *                    CCONV_UPDATE_MAX_SLOTS, status_dev is required, and the indices are
+ *                    checked on the device as cconv_fwd_varlen checks them (negative, >= S,
+ *                    repeated): status_dev gets [CCONV_OK, 0] or [CCONV_ERR_INDEX, offence
+ *                    bits].  A negative or out-of-range slot reads as a zero initial state
+ *                    (as in the forward); repeated slots are read as they are (the backward
+ *                    writes no state).
+ *   status_dev       int32[2] in device memory (only written when state_indices is given).
  *   dx               [total, D] bf16 contiguous, 16-byte aligned, overlapping neither x nor dy.
  *   dw, dbias        as cconv_bwd (dbias may be NULL).
- *   d_initial_state  [nseq, D, W-1] bf16 output, or NULL.
+ *   d_initial_state  [nseq, D, W-1] bf16 output (one per sequence, also with indices), or NULL.
  *   workspace        at least cconv_bwd_varlen_workspace_bytes(total, D, W), 16-byte
  *                    aligned (unused when total == 0).
  */
@@ -299,6 +311,7 @@ CCONV_API int cconv_bwd_varlen(const void* x, int64_t sxt, const void* dy, int64
                                int64_t total, int64_t D, const int32_t* cu_seqlens,
                                int64_t nseq, const void* w, const void* bias, cconv_dtype wdt,
                                int W, cconv_activation act, const void* initial_state,
+                               const int32_t* state_indices, int64_t S, int32_t* status_dev,
                                void* dx, void* dw, void* dbias, void* d_initial_state,
                                void* workspace, size_t workspace_bytes, cconv_stream_t stream);
 

@@ -126,9 +126,10 @@ def test_fwd_varlen_rejects(lib, kw, expect):
 
 
 def _bwdv(lib, x=P, sxt=64, dy=P, sdt=64, total=64, D=64, cu=P, nseq=2, w=P, bias=None,
-          wdt=F32, W=4, act=0, init=None, dx=P, dw=P, dbias=None, dinit=None, ws=P, wsb=1 << 30):
+          wdt=F32, W=4, act=0, init=None, idx=None, S=2, status=None, dx=P, dw=P, dbias=None,
+          dinit=None, ws=P, wsb=1 << 30):
     return lib.cconv_bwd_varlen(x, sxt, dy, sdt, total, D, cu, nseq, w, bias, wdt, W, act, init,
-                                dx, dw, dbias, dinit, ws, wsb, None)
+                                idx, S, status, dx, dw, dbias, dinit, ws, wsb, None)
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -136,6 +137,9 @@ def _bwdv(lib, x=P, sxt=64, dy=P, sdt=64, total=64, D=64, cu=P, nseq=2, w=P, bia
     (dict(dx=None), ENULL), (dict(W=5), EWIDTH), (dict(wdt=9), EDTYPE), (dict(act=-1), ESHAPE),
     (dict(nseq=0), ESHAPE), (dict(D=20), EALIGN), (dict(sdt=-64), ESTRIDE),
     (dict(dx=P + 8), EALIGN), (dict(dinit=P + 1), EALIGN), (dict(cu=P + 1), EALIGN),
+    (dict(init=P, idx=P), ENULL), (dict(init=P, idx=P, status=P, S=0), ESHAPE),
+    (dict(init=P, idx=P, status=P, S=393217), ESHAPE), (dict(idx=P + 2, status=P), EALIGN),
+    (dict(idx=P, status=P + 2), EALIGN),
 ])
 def test_bwd_varlen_rejects(lib, kw, expect):
     assert _bwdv(lib, **kw) == expect

@@ -243,3 +243,86 @@ def test_ill_formed_seqlens_reported():
     out = _run(x, dy, cu, w, b, init, "silu")
     assert cc.cconv_device_fault() == 0
     _check(x, dy, cu, w, b, init, "silu", out, "after an ill-formed call")
+
+
+def _pool_case(lens, D, W, S, seed):
+    """Inputs of a packed call whose initial states live in a decode pool of S slots."""
+    x, dy, cu, w, b, _ = inputs.varlen_inputs(lens, D, W, bias=True, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1000)
+    pool = torch.randn(S, D, W - 1, generator=g).to(torch.bfloat16)
+    idx = torch.randperm(S, generator=g)[:len(lens)].to(torch.int32)
+    return x, dy, cu, w, b, pool, idx
+
+
+@pytest.mark.parametrize("D", [256, 1024, 2048])
+def test_backward_reads_initial_states_from_pool_slots(D):
+    """Packed backward with each sequence's initial state picked from a decode pool by
+    state_indices (the gradient path of a chunked prefill that read from the pool): against
+    the oracle on the gathered states, and bit for bit against the same call on the states
+    gathered into a dense array.  D = 256, 1024 and 2048 take the independent-pipeline and
+    the 4- and 8-strip lockstep kernels."""
+    W, S = 4, 37
+    lens = [700, 1, 0, 2, 129, 3000, 64, 5]
+    x, dy, cu, w, b, pool, idx = _pool_case(lens, D, W, S, seed=D)
+    xg, dyg, cug, wg, bg = (t.cuda() for t in (x, dy, cu, w, b))
+    status = torch.full((2,), 7, dtype=torch.int32, device="cuda")
+    dx, dw, db, di = cc.cconv_bwd_varlen(xg, dyg, cug, wg, bg, initial_state=pool.cuda(),
+                                         state_indices=idx.cuda(), status=status,
+                                         want_dbias=True, want_dinit=True)
+    dense = pool[idx.long()]
+    ref = cc.cconv_bwd_varlen(xg, dyg, cug, wg, bg, initial_state=dense.cuda(), want_dbias=True,
+                              want_dinit=True)
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0]
+    for a, r in zip((dx, dw, db, di), ref):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           r.view(torch.int16) if r.dtype == torch.bfloat16 else r)
+    rdx, rdw, rdb, rdi = oracle.bwd_seq(f64(x), f64(dy), cu.numpy(), f64(w), f64(b), f64(dense),
+                                        "silu", want_dinit=True)
+    for name, g, r in (("dx", dx, rdx), ("dw", dw, rdw), ("dbias", db, rdb),
+                       ("d_initial_state", di, rdi)):
+        assert rel_err(f64(g), r) <= BWD_TOL, name
+
+
+@pytest.mark.parametrize("bad,mask", [([0, -1, 2], 1), ([0, 5, 2], 2), ([3, 1, 3], 4),
+                                      ([-3, 9, 1], 3)])
+def test_backward_pool_indices_checked(bad, mask):
+    """Invalid state indices in the packed backward: the status words report the offence as
+    the forward's check does; negative and out-of-range slots read as zero initial states,
+    repeated slots are read as they are."""
+    D, W, S = 512, 4, 5
+    lens = [10, 20, 30]
+    x, dy, cu, w, b, pool, _ = _pool_case(lens, D, W, S, seed=8)
+    idx = torch.tensor(bad, dtype=torch.int32)
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    dx, dw, db, di = cc.cconv_bwd_varlen(x.cuda(), dy.cuda(), cu.cuda(), w.cuda(), b.cuda(),
+                                         initial_state=pool.cuda(), state_indices=idx.cuda(),
+                                         status=status, want_dbias=True, want_dinit=True)
+    torch.cuda.synchronize()
+    assert status.tolist() == [-8, mask]
+    init = torch.zeros(len(lens), D, W - 1, dtype=torch.bfloat16)
+    for i, s in enumerate(bad):
+        if 0 <= s < S:
+            init[i] = pool[s]
+    rdx, rdw, rdb, rdi = oracle.bwd_seq(f64(x), f64(dy), cu.numpy(), f64(w), f64(b), f64(init),
+                                        "silu", want_dinit=True)
+    for name, g, r in (("dx", dx, rdx), ("dw", dw, rdw), ("dbias", db, rdb),
+                       ("d_initial_state", di, rdi)):
+        assert rel_err(f64(g), r) <= BWD_TOL, name
+
+
+def test_backward_pool_indices_with_no_rows():
+    """No rows at all: the gradients are zero and the indices are still checked."""
+    D, W, S = 64, 3, 4
+    cu = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pool = torch.randn(S, D, W - 1).to(torch.bfloat16).cuda()
+    w = torch.rand(D, W).cuda()
+    x = torch.empty(0, D, dtype=torch.bfloat16).cuda()
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    dx, dw, db, di = cc.cconv_bwd_varlen(x, x, cu, w, initial_state=pool,
+                                         state_indices=torch.tensor([1, 1, 0], dtype=torch.int32,
+                                                                    device="cuda"),
+                                         status=status, want_dbias=True)
+    torch.cuda.synchronize()
+    assert status.tolist() == [-8, 4]
+    assert not dw.any() and not db.any() and not di.float().any()
