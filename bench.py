@@ -75,7 +75,8 @@ LAUNCHES_PER_STEP = 4                        # fwd, bwd stream, bwd reduce, upda
 # backward: stream kernel + reduction), averaged over back-to-back launches in one ncu
 # capture (profiles/, file named below), together with the hash of the kernel sources it
 # was taken on.  `traffic` is reported only while the sources still hash the same.
-BWD_TRAFFIC = {"bytes_per_call": None, "sources_sha16": None, "profile": None}
+BWD_TRAFFIC = {"bytes_per_call": 408_868_032, "sources_sha16": "4acc3333f4cb4e72",
+               "profile": "profiles/cconv_bwd_traffic_b2_t8192_d4096.md"}
 TRAFFIC_SOURCES = ("csrc/bwd.cu", "csrc/strip.cuh", "csrc/common.cuh")
 
 WORKLOAD = ("fwd+bwd B=2 T=8192 D=4096 W=4 no bias (bf16 x/dy, f32 w) + 1 decode update "
