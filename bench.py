@@ -82,6 +82,25 @@ BWD_TRAFFIC = {"bytes_per_call": 408_868_032, "sources_sha16": "4acc3333f4cb4e72
                "profile": "profiles/cconv_bwd_traffic_b2_t8192_d4096.md"}
 TRAFFIC_SOURCES = ("csrc/bwd.cu", "csrc/strip.cuh", "csrc/common.cuh")
 
+# Achieved occupancy (sm__warps_active.avg.pct_of_peak_sustained_active: active warps as a
+# share of the SM's warp slots) of each stream and decode kernel, from the section captures
+# summarised under profiles/.  Reported beside each kernel's live launch description while
+# every kernel source hashes to the value recorded with them.
+ACHIEVED_OCCUPANCY = {
+    "sources_sha16": "cfc91c1228a8523b",
+    "pct": {
+        "cconv_fwd_kernel<4, 8, 10, 8, 1, true, 0>": 14.00,
+        "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>": 13.92,
+        "cconv_update_kernel<8, 4, 3, 4, 0, 256>": 11.86,
+        "cconv_fwd_kernel<4, 8, 10, 8, 1, true, 1>": 14.04,
+        "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 1>": 13.82,
+        "cconv_fwd_multi_kernel<4, 8, 10, 8, 1, true>": 14.07,
+        "cconv_bwd_ls_multi_kernel<4, 12, 4, 8>": 13.82,
+    },
+    "profiles": ["profiles/cconv_fwd_bwd_update_kernels_b2_t8192_d4096.md",
+                 "profiles/cconv_varlen_multi_bwd_kernels_b2_t8192_d4096.md"],
+}
+
 WORKLOAD = ("fwd+bwd B=2 T=8192 D=4096 W=4 no bias (bf16 x/dy, f32 w) + 1 decode update "
             "S=512 N=256 D=4096 W=4 bias per step")
 
@@ -93,6 +112,24 @@ def sources_sha16() -> str:
         with open(os.path.join(HERE, "depthwise_causal_short_gb300", rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def all_sources_sha16() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(os.path.join(HERE, "depthwise_causal_short_gb300", "csrc"))):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(HERE, "depthwise_causal_short_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def achieved_occupancy(kernel: str):
+    """Achieved occupancy (%) of a kernel from the profiles, or None if the kernels changed
+    since they were captured (or the kernel was not captured)."""
+    if ACHIEVED_OCCUPANCY["sources_sha16"] != all_sources_sha16():
+        return None
+    return ACHIEVED_OCCUPANCY["pct"].get(kernel)
 
 
 def bwd_traffic():
@@ -244,6 +281,7 @@ def kernels_of(cc, fn, max_threads_per_sm: int):
             "ctas": d["ctas"],
             "ctas_per_sm": d["ctas_per_sm"],
             "theoretical_occupancy": round(d["ctas_per_sm"] * d["threads"] / max_threads_per_sm, 4),
+            "achieved_occupancy_pct_profiled": achieved_occupancy(short_name(d["name"])),
         })
     return out
 

@@ -54,3 +54,16 @@ def test_aggregate_is_whole_job_throughput():
     # units all ranks processed over the slowest rank's time
     assert bench.aggregate(100.0, 2.0, 1) == 50.0
     assert bench.aggregate(100.0, 2.0, 4) == 200.0
+
+
+def test_profiled_fields_follow_the_kernel_sources(monkeypatch):
+    # traffic and achieved occupancy come from captures of the kernels as they are now; once
+    # a kernel source changes they must read as unmeasured (None), not as stale numbers
+    assert bench.bwd_traffic() == bench.BWD_TRAFFIC["bytes_per_call"]
+    name = "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>"
+    assert bench.achieved_occupancy(name) == bench.ACHIEVED_OCCUPANCY["pct"][name]
+    assert bench.achieved_occupancy("cconv_bwd_reduce1_kernel") is None  # not captured
+    monkeypatch.setitem(bench.BWD_TRAFFIC, "sources_sha16", "0" * 16)
+    monkeypatch.setitem(bench.ACHIEVED_OCCUPANCY, "sources_sha16", "0" * 16)
+    assert bench.bwd_traffic() is None
+    assert bench.achieved_occupancy(name) is None
