@@ -59,8 +59,10 @@ def test_aggregate_is_whole_job_throughput():
 def test_profiled_fields_follow_the_kernel_sources(monkeypatch):
     # traffic and achieved occupancy come from captures of the kernels as they are now; once
     # a kernel source changes they must read as unmeasured (None), not as stale numbers
-    assert bench.bwd_traffic() == bench.BWD_TRAFFIC["bytes_per_call"]
     name = "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>"
+    monkeypatch.setitem(bench.BWD_TRAFFIC, "sources_sha16", bench.sources_sha16())
+    monkeypatch.setitem(bench.ACHIEVED_OCCUPANCY, "sources_sha16", bench.all_sources_sha16())
+    assert bench.bwd_traffic() == bench.BWD_TRAFFIC["bytes_per_call"]
     assert bench.achieved_occupancy(name) == bench.ACHIEVED_OCCUPANCY["pct"][name]
     assert bench.achieved_occupancy("cconv_bwd_reduce1_kernel") is None  # not captured
     monkeypatch.setitem(bench.BWD_TRAFFIC, "sources_sha16", "0" * 16)
