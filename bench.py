@@ -85,9 +85,14 @@ TRAFFIC_SOURCES = ("csrc/bwd.cu", "csrc/strip.cuh", "csrc/common.cuh")
 # Achieved occupancy (sm__warps_active.avg.pct_of_peak_sustained_active: active warps as a
 # share of the SM's warp slots) of each stream and decode kernel, from the section captures
 # summarised under profiles/.  Reported beside each kernel's live launch description while
-# every kernel source hashes to the value recorded with them.
+# the sources of that kernel's family hash to the value recorded for the family.
+OCCUPANCY_SOURCES = {
+    "fwd": ("csrc/fwd.cu", "csrc/strip.cuh", "csrc/common.cuh"),
+    "bwd": ("csrc/bwd.cu", "csrc/strip.cuh", "csrc/common.cuh"),
+    "update": ("csrc/update.cu", "csrc/common.cuh"),
+}
 ACHIEVED_OCCUPANCY = {
-    "sources_sha16": "cfc91c1228a8523b",
+    "sources_sha16": {"fwd": "60f6b29eb63abd65", "bwd": "4acc3333f4cb4e72", "update": "015f449aceb20017"},
     "pct": {
         "cconv_fwd_kernel<4, 8, 10, 8, 1, true, 0>": 14.00,
         "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>": 13.92,
@@ -105,31 +110,32 @@ WORKLOAD = ("fwd+bwd B=2 T=8192 D=4096 W=4 no bias (bf16 x/dy, f32 w) + 1 decode
             "S=512 N=256 D=4096 W=4 bias per step")
 
 
-def sources_sha16() -> str:
+def sources_sha16(files=TRAFFIC_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
-    for rel in TRAFFIC_SOURCES:
+    for rel in files:
         with open(os.path.join(HERE, "depthwise_causal_short_gb300", rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def all_sources_sha16() -> str:
-    import hashlib
-    h = hashlib.sha256()
-    for name in sorted(os.listdir(os.path.join(HERE, "depthwise_causal_short_gb300", "csrc"))):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(HERE, "depthwise_causal_short_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
-    return h.hexdigest()[:16]
+def kernel_family(kernel: str):
+    """fwd, bwd or update: the source family a kernel name belongs to (None if unknown)."""
+    for fam in ("fwd", "bwd", "update"):
+        if kernel.startswith(f"cconv_{fam}_"):
+            return fam
+    return None
 
 
 def achieved_occupancy(kernel: str):
-    """Achieved occupancy (%) of a kernel from the profiles, or None if the kernels changed
-    since they were captured (or the kernel was not captured)."""
-    if ACHIEVED_OCCUPANCY["sources_sha16"] != all_sources_sha16():
+    """Achieved occupancy (%) of a kernel from the profiles, or None if its family's sources
+    changed since they were captured (or the kernel was not captured)."""
+    fam = kernel_family(kernel)
+    if fam is None or kernel not in ACHIEVED_OCCUPANCY["pct"]:
         return None
-    return ACHIEVED_OCCUPANCY["pct"].get(kernel)
+    if ACHIEVED_OCCUPANCY["sources_sha16"][fam] != sources_sha16(OCCUPANCY_SOURCES[fam]):
+        return None
+    return ACHIEVED_OCCUPANCY["pct"][kernel]
 
 
 def bwd_traffic():

@@ -88,6 +88,37 @@ int sm_count_current_device(int* sms, int* device) {
   return CCONV_OK;
 }
 
+int smem_per_sm_current_device(int* per_sm, int* reserved_per_block) {
+  static std::atomic<int> cache_sm[64], cache_res[64];
+  int dev = 0;
+  if (bind_current_context(&dev) != CCONV_OK) return CCONV_ERR_CUDA;
+  if (dev >= 0 && dev < 64) {
+    const int a = cache_sm[dev].load(std::memory_order_relaxed);
+    const int b = cache_res[dev].load(std::memory_order_relaxed);
+    if (a > 0 && b > 0) {
+      *per_sm = a;
+      *reserved_per_block = b - 1;
+      return CCONV_OK;
+    }
+  }
+  int a = 0, b = 0;
+  if (report_cuda("cudaDeviceGetAttribute",
+                  cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+          cudaSuccess ||
+      report_cuda("cudaDeviceGetAttribute",
+                  cudaDeviceGetAttribute(&b, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+          cudaSuccess ||
+      a <= 0 || b < 0)
+    return CCONV_ERR_CUDA;
+  if (dev >= 0 && dev < 64) {
+    cache_res[dev].store(b + 1, std::memory_order_relaxed);  // 0 marks "not cached"
+    cache_sm[dev].store(a, std::memory_order_relaxed);
+  }
+  *per_sm = a;
+  *reserved_per_block = b;
+  return CCONV_OK;
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;

@@ -19,11 +19,16 @@
 // cconv_update_ex runs the same kernel with the PR's variants: a state of L = W entries
 // (the window takes the newest W-1), -1 as a padding row, circular-buffer states (the token
 // goes to entry cache_seqlens[i] mod L and nothing shifts), and no activation.
+#include <algorithm>
 #include <cstdlib>
 
 #include "common.cuh"
 
 namespace cconv {
+
+// Shared memory per SM and the amount reserved per block on the current device (cached;
+// defined in host.cu).
+int smem_per_sm_current_device(int* per_sm, int* reserved_per_block);
 
 struct UpdArgs {
   const uint16_t* x;  // [N, ldx]
@@ -38,6 +43,8 @@ struct UpdArgs {
   int pad;            // nonzero: index -1 marks a padding row
   int act;            // CCONV_ACT_SILU or CCONV_ACT_NONE
   const int32_t* pos; // [N] circular-buffer positions (ring mode), or null
+  int64_t gq;         // row lanes: N / gridDim.y rows per group, plus one for the first
+  int64_t grem;       //   N % gridDim.y groups
 };
 
 // Kernel modes: the plain decode call; the general one (padding rows, activation read from
@@ -115,10 +122,117 @@ __device__ __forceinline__ void load_update_taps(const UpdArgs& p, int64_t d0,
   }
 }
 
+// Taps and bias of a CTA that covers CV channel vectors (8 channels each) with several row
+// lanes: the CTA copies them once into shared memory and every row lane reads them there,
+// so only the few CTAs of one channel block, not every row group, fetch the same taps from
+// L2.  16-byte unit u of channel vector c sits at tap_s[u * CV + c] (taps first, then the
+// bias), so the warp that reads unit u of 32 consecutive channel vectors hits 32 consecutive
+// units without bank conflicts.  A channel vector holds 2W tap units and 2 bias units in
+// fp32, W and 1 in bf16.
+template <int W, int CV>
+constexpr int kTapUnits = CV * 2 * (W + 1);
+
+template <int W, int CV, int NT>
+struct TapStage {
+  static constexpr int K = (kTapUnits<W, CV> + NT - 1) / NT;
+  uint4 v[K];
+  int dst[K];  // destination unit in shared memory, -1 for nothing
+};
+
+// Issue this thread's share of the copy (global loads into registers only).
+template <int W, int CV, int NT>
+__device__ __forceinline__ void tap_stage_load(const UpdArgs& p, int64_t cv0, int64_t nvec,
+                                               TapStage<W, CV, NT>& t) {
+  const bool f32 = p.wdt == CCONV_F32;
+  const int uw = f32 ? 2 * W : W;  // tap units per channel vector
+  const int ub = f32 ? 2 : 1;      // bias units per channel vector
+  const int cvs = static_cast<int>(nvec - cv0 < CV ? nvec - cv0 : CV);
+  const int ntap = cvs * uw, nall = p.bias ? cvs * (uw + ub) : ntap;
+  const int esz = f32 ? 4 : 2;
+  const uint4* wsrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.w) +
+                                                     cv0 * 8 * W * esz);
+  const uint4* bsrc = p.bias ? reinterpret_cast<const uint4*>(
+                                   static_cast<const char*>(p.bias) + cv0 * 8 * esz)
+                             : nullptr;
+#pragma unroll
+  for (int k = 0; k < TapStage<W, CV, NT>::K; ++k) {
+    const int g = threadIdx.x + k * NT;
+    t.dst[k] = -1;
+    if (g < ntap) {
+      const int c = f32 ? g / (2 * W) : g / W, u = g - c * uw;
+      t.v[k] = wsrc[g];
+      t.dst[k] = u * CV + c;
+    } else if (g < nall) {
+      const int h = g - ntap;
+      const int c = f32 ? h >> 1 : h, u = uw + (h - c * ub);
+      t.v[k] = bsrc[h];
+      t.dst[k] = u * CV + c;
+    }
+  }
+}
+
+template <int W, int CV, int NT>
+__device__ __forceinline__ void tap_stage_store(uint4* tap_s, const TapStage<W, CV, NT>& t) {
+#pragma unroll
+  for (int k = 0; k < TapStage<W, CV, NT>::K; ++k)
+    if (t.dst[k] >= 0) tap_s[t.dst[k]] = t.v[k];
+}
+
+// Channel vector c's taps and bias from the staged copy (visible after a barrier).
+template <int W, int CV>
+__device__ __forceinline__ void tap_stage_read(const UpdArgs& p, const uint4* tap_s, int c,
+                                               float (&tw)[8][W], float (&tb)[8]) {
+  if (p.wdt == CCONV_F32) {
+    float4 v[2 * W];
+#pragma unroll
+    for (int u = 0; u < 2 * W; ++u) v[u] = *reinterpret_cast<const float4*>(&tap_s[u * CV + c]);
+    const float* f = reinterpret_cast<const float*>(v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int j = 0; j < W; ++j) tw[k][j] = f[k * W + j];
+    if (p.bias) {
+      const float4 b0 = *reinterpret_cast<const float4*>(&tap_s[2 * W * CV + c]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&tap_s[(2 * W + 1) * CV + c]);
+      tb[0] = b0.x; tb[1] = b0.y; tb[2] = b0.z; tb[3] = b0.w;
+      tb[4] = b1.x; tb[5] = b1.y; tb[6] = b1.z; tb[7] = b1.w;
+    }
+  } else {
+    uint4 v[W];
+#pragma unroll
+    for (int u = 0; u < W; ++u) v[u] = tap_s[u * CV + c];
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int j = 0; j < W; ++j) tw[k][j] = bf16_to_f32(h[k * W + j]);
+    if (p.bias) {
+      const uint4 b = tap_s[W * CV + c];
+      const uint16_t* bh = reinterpret_cast<const uint16_t*>(&b);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) tb[k] = bf16_to_f32(bh[k]);
+    }
+  }
+  if (!p.bias) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tb[k] = 0.f;
+  }
+}
+
+// Channel vectors per CTA row lane: the 256-thread vector kernels run 32 channel vectors x 8
+// row lanes; the others give every thread of a CTA its own channel vector (one row lane).
+template <int VEC, int NT>
+__host__ __device__ constexpr int update_cv() { return (VEC == 8 && NT == 256) ? 32 : NT; }
+
 // VEC = channels per thread (8: 16-byte vectors; 1: scalar path), W taps, L = state entries
 // per channel (W - 1, or W to keep one older token: the newest W - 1 feed the window, and
 // the new state is the last L of (old state, token), i.e. window[W - L + j]), ROWS = rows
-// per thread.  Grid: x over channel vectors, y over groups of ROWS rows.
+// per thread.  A CTA is CV channel vectors x RL = NT / CV row lanes; grid x over blocks of CV
+// channel vectors, y over row groups.  With one row lane a group is ROWS consecutive rows.
+// With several, the N rows are split evenly over gridDim.y groups of at most RL * ROWS rows
+// (the first N % gridDim.y groups one row longer)
+// (so the host can size the grid to the SM count), lane l takes rows l, l + RL, ... of its
+// group, and the CTA stages its taps in shared memory once.
 //
 // Latency is what this kernel is about (a decode step moves ~17 MB, mostly L2-resident), so
 // every independent load is issued before the index check needs to finish: this thread's
@@ -139,8 +253,12 @@ __global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
   constexpr int OFF = L - (W - 1);  // state entries older than the window (0 or 1)
   const bool pad = GEN && p.pad != 0;
   const bool act_none = GEN && p.act == CCONV_ACT_NONE;
+  constexpr int CV = update_cv<VEC, NT>();
+  constexpr int RL = NT / CV;
+  static_assert(RL * CV == NT && (RL == 1 || VEC == 8), "row lanes need the vector path");
   extern __shared__ uint32_t bitmap[];
   __shared__ int s_bad;
+  __shared__ uint4 tap_s[RL > 1 ? kTapUnits<W, CV> : 1];
 
   if (p.idx) {  // shared-memory set-up only: no global access before the dependency wait
     if (threadIdx.x == 0) s_bad = 0;
@@ -149,9 +267,16 @@ __global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
   }
   grid_dependency_wait();
 
-  const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * NT + threadIdx.x) * VEC;
+  const int cl = RL > 1 ? static_cast<int>(threadIdx.x % CV) : static_cast<int>(threadIdx.x);
+  const int rl = RL > 1 ? static_cast<int>(threadIdx.x / CV) : 0;
+  const int64_t cv0 = static_cast<int64_t>(blockIdx.x) * CV;
+  const int64_t d0 = (cv0 + cl) * VEC;
   const bool mine = d0 < p.D;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * ROWS;
+  // rows of this thread: row_of(r) for r < ROWS, valid while below iend
+  const int64_t by = blockIdx.y;
+  const int64_t ib = RL > 1 ? p.gq * by + (by < p.grem ? by : p.grem) : by * ROWS;
+  const int64_t iend = RL > 1 ? ib + p.gq + (by < p.grem ? 1 : 0) : p.N;
+  auto row_of = [&](int r) -> int64_t { return ib + static_cast<int64_t>(r) * RL + rl; };
 
   // ---- this thread's rows: slot ids, token rows, taps ------------------------------------
   // slot[r] < 0: no row, or a padding row (nothing to do for it)
@@ -160,11 +285,11 @@ __global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
   uint16_t win[ROWS][VEC][W];
 #pragma unroll
   for (int r = 0; r < ROWS; ++r) {
-    const int64_t i = i0 + r;
-    slot[r] = (mine && i < p.N) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
-    if constexpr (RING) head[r] = (mine && i < p.N) ? ring_mod(p.pos[i], L) : 0;
+    const int64_t i = row_of(r);
+    slot[r] = (mine && i < iend) ? (p.idx ? static_cast<int64_t>(p.idx[i]) : i) : -1;
+    if constexpr (RING) head[r] = (mine && i < iend) ? ring_mod(p.pos[i], L) : 0;
     if (pad && slot[r] == -1) continue;
-    if (mine && i < p.N) {
+    if (mine && i < iend) {
       const uint16_t* xr = p.x + i * p.ldx + d0;
       if constexpr (VEC == 8) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xr);
@@ -177,7 +302,11 @@ __global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
     }
   }
   float tw[VEC][W], tb[VEC];
-  if (mine) load_update_taps<VEC, W>(p, d0, tw, tb);
+  TapStage<W, CV, NT> stage;
+  if constexpr (RL > 1)
+    tap_stage_load<W, CV, NT>(p, cv0, (p.D + VEC - 1) / VEC, stage);
+  else if (mine)
+    load_update_taps<VEC, W>(p, d0, tw, tb);
 
   // ---- validation: identical verdict in every CTA --------------------------------------
   int bad = 0;
@@ -238,9 +367,10 @@ __global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
     }
   }
 
-  if (p.idx) {
-    __syncthreads();  // every index of this CTA's pass is checked
-    bad = s_bad;
+  if constexpr (RL > 1) tap_stage_store<W, CV, NT>(tap_s, stage);
+  if (p.idx || RL > 1) {
+    __syncthreads();  // every index of this CTA's pass is checked; the staged taps are visible
+    if (p.idx) bad = s_bad;
   }
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     p.status[0] = bad ? CCONV_ERR_INDEX : CCONV_OK;
@@ -248,6 +378,7 @@ __global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
   }
   grid_launch_dependents();
   if (bad || !mine) return;
+  if constexpr (RL > 1) tap_stage_read<W, CV>(p, tap_s, cl, tw, tb);
 
   // ---- y and the shifted state (writes only after a clean verdict) -----------------------
 #pragma unroll
@@ -262,7 +393,7 @@ __global__ void __launch_bounds__(NT) cconv_update_kernel(const UpdArgs p) {
       yo[c] = f32_to_bf16(act_none ? z : silu_f(z));
     }
     uint16_t* st = p.state + (slot[r] * p.D + d0) * L;
-    uint16_t* yr = p.y + (i0 + r) * p.D + d0;
+    uint16_t* yr = p.y + row_of(r) * p.D + d0;
     if constexpr (RING) {
       if constexpr (VEC == 8)
         *reinterpret_cast<uint4*>(yr) = *reinterpret_cast<const uint4*>(yo);
@@ -395,29 +526,58 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
   const int off = L - (W - 1);
   const int mode = pos ? kUpdRing : (pad != 0 || act != CCONV_ACT_SILU) ? kUpdGeneral : kUpdPlain;
   const int64_t nvec = (D + vec - 1) / vec;
-  // Small batches on the vector path: 64-thread CTAs, with the fewest rows per thread (1, 2
-  // or 4) that keep the grid within one wave, as long as that grid stays within two waves.
-  // Measured at S=512 D=4096 W=4 in a CUDA graph (us per step, 64- against 256-thread
-  // CTAs): N=1 1.44 / 2.79, 16 1.89 / 3.11, 64 2.45 / 3.04, 128 3.29 / 4.64; from N=192 on
-  // the 256-thread CTAs win (256: 4.97 against 5.88).
+  // Small batches on the vector path: 64-thread CTAs (one row lane), when one or two rows
+  // per thread keep their grid within one wave; otherwise the 256-thread CTAs (8 row lanes
+  // sharing staged taps).  Measured in CUDA graphs at S=512 W=4, us per step, 64- against
+  // 256-thread CTAs: D=1024 N=64 1.95 / 2.17 and N=192 2.94 / 2.16; D=2048 N=64 2.03 / 2.22
+  // and N=128 2.67 / 2.22; D=4096 N=16 1.78 / 2.25 and N=64 2.46 / 2.18; D=8192 N=16
+  // 1.96 / 2.29 and N=64 3.24 / 2.79.
   int nt = kUpdThreads;
   int rows = 4;
   if (vec == 8) {
     const int64_t gx_small = (nvec + kUpdThreadsSmall - 1) / kUpdThreadsSmall;
-    int r = 1;
-    while (r < 4 && gx_small * ((N + r - 1) / r) > sms) r *= 2;
-    if (gx_small * ((N + r - 1) / r) <= 2 * static_cast<int64_t>(sms)) {
-      nt = kUpdThreadsSmall;
-      rows = r;
+    for (int r = 1; r <= 2; r *= 2) {
+      if (gx_small * ((N + r - 1) / r) <= sms) {
+        nt = kUpdThreadsSmall;
+        rows = r;
+        break;
+      }
     }
   }
-  const int64_t gx = (nvec + nt - 1) / nt;
+#ifdef CCONV_TILE_SWEEP
+  // CCONV_UPDATE_THREADS=256 or 64 picks the CTA size on the vector path.
+  static const int threads_override = [] {
+    const char* e = getenv("CCONV_UPDATE_THREADS");
+    const int v = e ? atoi(e) : 0;
+    return (v == kUpdThreads || v == kUpdThreadsSmall) ? v : 0;
+  }();
+  if (vec == 8 && threads_override == kUpdThreads && nt != kUpdThreads) {
+    nt = kUpdThreads;
+    rows = 4;
+  } else if (vec == 8 && threads_override == kUpdThreadsSmall && nt != kUpdThreadsSmall) {
+    const int64_t gx_small = (nvec + kUpdThreadsSmall - 1) / kUpdThreadsSmall;
+    int r = 1;
+    while (r < 4 && gx_small * ((N + r - 1) / r) > sms) r *= 2;
+    nt = kUpdThreadsSmall;
+    rows = r;
+  }
+#endif
+  // Channel vectors per CTA and row lanes (the kernels' own split, update_cv).
+  const int cv = (vec == 8 && nt == kUpdThreads) ? update_cv<8, kUpdThreads>() : nt;
+  const int rl = nt / cv;
+  const int64_t gx = (nvec + cv - 1) / cv;
   if (nt == kUpdThreads) {
-    // Rows per thread: 4 measured fastest for the decode workload (N=256, D=4096: 128 CTAs,
-    // 5.1 us per step in a CUDA graph against 8.0 us with one row): every CTA repeats the
-    // O(N) index check, so fewer, fuller CTAs cost less, and each thread keeps four rows'
-    // loads in flight.  Fewer rows only when four would leave more than half of the SMs idle.
-    while (rows > 1 && 2 * gx * ((N + rows - 1) / rows) < static_cast<int64_t>(sms)) rows /= 2;
+    // Rows per thread: 4 measured fastest for the decode workload (N=256, D=4096: 128 CTAs):
+    // every CTA repeats the O(N) index check, so fewer, fuller CTAs cost less, and each
+    // thread keeps four rows' loads in flight.  Fewer rows only when four would leave more
+    // than half of the SMs idle.
+    while (rows > 1 && 2 * gx * ((N + rl * rows - 1) / (rl * rows)) < static_cast<int64_t>(sms))
+      rows /= 2;
+    // A plain 4-row grid of more than one wave (one CTA per SM at its register count) runs
+    // as 2-row CTAs instead, two to an SM.  Measured at S=512 W=4, us per step, 4 against 2
+    // rows: D=4096 N=512 7.58 / 7.37, D=8192 N=256 7.43 / 6.96, D=8192 N=512 15.7 / 13.8.
+    if (rows == 4 && mode == kUpdPlain && !off && gx * ((N + rl * 4 - 1) / (rl * 4)) > sms)
+      rows = 2;
   }
 #ifdef CCONV_TILE_SWEEP
   // Sweep builds only: CCONV_UPDATE_ROWS = 1, 2, 4, 8 or 16 forces the rows per thread.
@@ -430,7 +590,22 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
 #endif
   if (nt == kUpdThreadsSmall && rows > 4) rows = 4;
   if ((off || mode != kUpdPlain) && rows != 4) rows = 1;  // general kernels: 1 and 4 rows
-  const int64_t gy = (N + rows - 1) / rows;
+  int64_t gy = (N + rl * rows - 1) / (rl * rows);
+  // Row lanes: the kernel splits the N rows evenly over gridDim.y groups, each of at most
+  // rl * rows rows as long as gy is at least the count above.  A grid short of the SM
+  // count gets more, smaller groups, up to one CTA per SM (D=4096 N=256: 9 groups of 28-29
+  // rows on 144 SMs instead of 8 of 32 on 128).
+  bool balance = true;
+#ifdef CCONV_TILE_SWEEP
+  // Sweep builds only: CCONV_UPDATE_BALANCE=0 keeps the smallest row-group count.
+  static const bool no_balance = [] {
+    const char* e = getenv("CCONV_UPDATE_BALANCE");
+    return e && atoi(e) == 0;
+  }();
+  balance = !no_balance;
+#endif
+  if (balance && rl > 1 && gx * gy < sms)
+    gy = std::max(gy, std::min(static_cast<int64_t>(sms) / gx, N));
   if (gx > 2147483647 || gy > 65535) return CCONV_ERR_SHAPE;
   UpdKernel kern = vec8 ? (nt == kUpdThreadsSmall
                                ? pick_update_kernel<8, kUpdThreadsSmall>(W, rows, off, mode)
@@ -454,8 +629,32 @@ static int update_impl(const void* x, int64_t N, int64_t D, int64_t ldx, void* s
   a.pad = pad ? 1 : 0;
   a.act = act;
   a.pos = pos;
+  a.gq = N / gy;
+  a.grem = N % gy;
 
-  const size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
+  size_t smem = state_indices ? static_cast<size_t>((S + 31) / 32) * 4 : 0;
+  if (rl > 1 && gx * gy <= sms) {
+    // One CTA per SM.  The step is bound by each SM's load/store rate, and a grid of at most
+    // one wave otherwise may be placed two CTAs to an SM (the 1- and 2-row kernels fit two)
+    // with other SMs idle.  Dynamic shared memory of just over half an SM's capacity keeps
+    // the CTAs apart.  Measured at S=512 W=4 (us per step, unpadded against padded):
+    // D=4096 N=128 3.85 / 2.85, D=8192 N=64 3.70 / 2.79, D=2048 N=256 3.43 / 2.87.
+    int per_sm = 0, reserved = 0;
+    rc = smem_per_sm_current_device(&per_sm, &reserved);
+    if (rc != CCONV_OK) return rc;
+    const size_t half = static_cast<size_t>(per_sm / 2 - reserved + 16);
+    if (half > smem) smem = half;
+  }
+#ifdef CCONV_TILE_SWEEP
+  // Sweep builds only: CCONV_UPDATE_SMEM_PAD_KB pads the dynamic shared memory (caps the
+  // CTAs that share an SM).
+  static const size_t pad_kb = [] {
+    const char* e = getenv("CCONV_UPDATE_SMEM_PAD_KB");
+    const int v = e ? atoi(e) : 0;
+    return static_cast<size_t>(v > 0 && v <= 200 ? v : 0);
+  }();
+  if (pad_kb * 1024 > smem) smem = pad_kb * 1024;
+#endif
   // Dynamic plus static shared memory above 48 KB needs the per-function opt-in.
   if (smem > 32 * 1024) {
     if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) != CCONV_OK)

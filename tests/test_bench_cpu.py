@@ -60,12 +60,21 @@ def test_profiled_fields_follow_the_kernel_sources(monkeypatch):
     # traffic and achieved occupancy come from captures of the kernels as they are now; once
     # a kernel source changes they must read as unmeasured (None), not as stale numbers
     name = "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>"
+    upd = "cconv_update_kernel<8, 4, 3, 4, 0, 256>"
+    current = {fam: bench.sources_sha16(files) for fam, files in bench.OCCUPANCY_SOURCES.items()}
     monkeypatch.setitem(bench.BWD_TRAFFIC, "sources_sha16", bench.sources_sha16())
-    monkeypatch.setitem(bench.ACHIEVED_OCCUPANCY, "sources_sha16", bench.all_sources_sha16())
+    monkeypatch.setitem(bench.ACHIEVED_OCCUPANCY, "sources_sha16", dict(current))
     assert bench.bwd_traffic() == bench.BWD_TRAFFIC["bytes_per_call"]
     assert bench.achieved_occupancy(name) == bench.ACHIEVED_OCCUPANCY["pct"][name]
+    assert bench.achieved_occupancy(upd) == bench.ACHIEVED_OCCUPANCY["pct"][upd]
     assert bench.achieved_occupancy("cconv_bwd_reduce1_kernel") is None  # not captured
+    assert bench.achieved_occupancy("some_other_kernel") is None
     monkeypatch.setitem(bench.BWD_TRAFFIC, "sources_sha16", "0" * 16)
-    monkeypatch.setitem(bench.ACHIEVED_OCCUPANCY, "sources_sha16", "0" * 16)
     assert bench.bwd_traffic() is None
+    # a change in one family's sources voids that family's figures only
+    monkeypatch.setitem(bench.ACHIEVED_OCCUPANCY, "sources_sha16", dict(current, update="0" * 16))
+    assert bench.achieved_occupancy(upd) is None
+    assert bench.achieved_occupancy(name) == bench.ACHIEVED_OCCUPANCY["pct"][name]
+    monkeypatch.setitem(bench.ACHIEVED_OCCUPANCY, "sources_sha16", dict(current, bwd="0" * 16))
     assert bench.achieved_occupancy(name) is None
+    assert bench.achieved_occupancy(upd) == bench.ACHIEVED_OCCUPANCY["pct"][upd]

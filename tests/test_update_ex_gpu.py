@@ -156,6 +156,18 @@ def _ring_steps(W, L, D, ldpad, pad, act, idx_rows, steps, seed, start):
     assert np.array_equal(bits(state_g), st_ref), f"ring W={W} L={L}: pool differs"
 
 
+@pytest.mark.parametrize("D,N,W,L_off,pad", [(808, 157, 4, 1, True), (4096, 200, 3, 0, False),
+                                              (2048, 300, 4, 1, False)])
+def test_row_lane_layouts_general(D, N, W, L_off, pad):
+    """The general kernels on the 256-thread CTAs: a partial channel block, row groups split
+    unevenly, padding rows mixed in."""
+    g = torch.Generator().manual_seed(D + N)
+    idx = torch.randperm(N + 40, generator=g)[:N]
+    if pad:
+        idx[::7] = -1
+    _steps(W, W - 1 + L_off, D, 0, pad, "silu", idx.tolist(), steps=2, seed=D + N)
+
+
 @pytest.mark.parametrize("W,L", [(4, 3), (4, 4), (3, 2), (3, 3), (2, 1), (2, 2), (1, 1)])
 @pytest.mark.parametrize("D,ldpad", [(4096, 0), (1000, 8), (1001, 0)])
 def test_circular_buffer(W, L, D, ldpad):

@@ -68,6 +68,40 @@ def test_widths_and_layouts(W, D, pad):
     assert np.array_equal(bits(state_g), st_ref)
 
 
+# Batches large enough for the 256-thread CTAs (32 channel vectors x 8 row lanes with staged
+# taps): a partial last channel block (D=808: 101 vectors), row groups split unevenly over a
+# grid sized to the SM count, 1-, 2- and 4-row kernels, bf16 and fp32 taps, no bias, and a
+# grid of more than one wave (D=8192 N=512).
+ROW_LANE_CASES = [
+    (808, 157, 4, torch.float32, True),
+    (808, 157, 3, torch.bfloat16, False),
+    (1024, 192, 1, torch.float32, True),
+    (2048, 300, 2, torch.bfloat16, True),
+    (4096, 128, 4, torch.float32, True),
+    (4096, 200, 4, torch.float32, False),
+    (8192, 512, 4, torch.float32, True),
+]
+
+
+@pytest.mark.parametrize("D,N,W,wdtype,bias", ROW_LANE_CASES,
+                         ids=[f"D{c[0]}-N{c[1]}-W{c[2]}-{str(c[3])[6:]}-b{int(c[4])}"
+                              for c in ROW_LANE_CASES])
+def test_row_lane_layouts(D, N, W, wdtype, bias):
+    S = N + 37
+    state, xr, idx, w, b = inputs.decode_inputs(S, N, D, W, bias, n_x=2, seed=D + N + W,
+                                                wdtype=wdtype)
+    state_g, xr_g, idx_g, wg = state.cuda(), xr.cuda(), idx.cuda(), w.cuda()
+    bg = None if b is None else b.cuda()
+    st_ref = bits(state)
+    for k in range(2):
+        st_ref = _step_and_check(xr_g[k], state_g, wg, bg, idx_g, st_ref, xr[k], idx, w, b,
+                                 f"D{D} N{N} W{W} step {k}")
+    assert np.array_equal(bits(state_g), st_ref)
+    # rows outside the index vector keep their state
+    untouched = np.setdiff1d(np.arange(S), idx.numpy())
+    assert np.array_equal(bits(state_g)[untouched], bits(state)[untouched])
+
+
 def test_null_indices_and_bf16_weights():
     S, N, D, W = 20, 16, 512, 4
     state, xr, _, w, b = inputs.decode_inputs(S, N, D, W, True, n_x=2, seed=21,
