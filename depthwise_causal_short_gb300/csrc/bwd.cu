@@ -245,7 +245,7 @@ __device__ __forceinline__ void bwd_boundary(int t, const TileCursor& c, SeqTrac
   }
   sq.next(t);
   if (hin_seq != sq.i) init_ring<VEC>(p.init, init_slot(p, sq.i), p.D, p.W, d0, active, hin);
-  ring_of<VEC>(hin, h);
+  ring_of<VEC>(hin, p.W, h);
 #pragma unroll
   for (int q = 0; q < P; ++q)
 #pragma unroll

@@ -192,7 +192,7 @@ __device__ __forceinline__ void fwd_boundary(int t, const TileCursor& c, SeqTrac
     store_final<VEC>(p.fin, sq.i, p.D, p.W, d0, h);
   sq.next(t);
   if (hin_seq != sq.i) init_ring<VEC>(p.init, seq_slot(p, sq.i), p.D, p.W, d0, active, hin);
-  ring_of<VEC>(hin, h);
+  ring_of<VEC>(hin, p.W, h);
   hin_seq = -1;
   if (sq.i + 1 < p.nseq) {
     init_ring<VEC>(p.init, seq_slot(p, sq.i + 1), p.D, p.W, d0, active, hin);

@@ -258,20 +258,51 @@ struct SeqTracker {
 };
 
 // Ring of the W-1 rows before a sequence, from its initial state (bf16 [.., D, W-1], entry
-// j = row ss - (W-1) + j), as this lane's bf16 pairs: hr[k-1][q] holds row ss - k for
-// channels (d0 + 2q, d0 + 2q + 1), zero for k > W - 1 or without a state (state == nullptr
-// or slot < 0).  The packed-sequence kernels fetch it one sequence ahead and keep it as bf16
-// (half the registers of fp32 pairs) until the sequence starts (ring_of).
+// j = row ss - (W-1) + j), zero for rows before the state (k > W - 1) or without a state
+// (state == nullptr or slot < 0).  The packed-sequence kernels fetch it one sequence ahead and
+// keep it as bf16 in 3 * VEC/2 words until the sequence starts; ring_of unpacks it there.
+// Nothing is done with the loaded words before then, so the loads do not hold up the warp
+// that issues them (packing them on arrival stalled it for a DRAM round trip at every
+// boundary: 1.4 us per backward call at 16 sequences, measured).
+//   W = 4 with 4 channels per lane: the words are the lane's 12 entries as they lie in
+//   memory (channel d0 + c's entries 0, 1, 2 at halves 3c, 3c + 1, 3c + 2), 24 bytes read as
+//   three 8-byte loads when they are 8-byte aligned.
+//   Otherwise: word hr[k-1][q] holds row ss - k for channels (d0 + 2q, d0 + 2q + 1).
 template <int VEC>
 __device__ __forceinline__ void init_ring(const uint16_t* state, int64_t slot, int64_t D, int W,
                                           int64_t d0, bool active, uint32_t (&hr)[3][VEC / 2]) {
   const int L = W - 1;
+  const bool have = state && slot >= 0 && active;
+  if constexpr (VEC == 4) {
+    if (L == 3) {
+      uint32_t* w = &hr[0][0];  // the 6 words in memory order
+      const uint16_t* s0 = have ? state + (slot * D + d0) * 3 : nullptr;
+      if (have && d0 + 4 <= D && (reinterpret_cast<uintptr_t>(s0) & 7u) == 0) {
+        const uint2* v = reinterpret_cast<const uint2*>(s0);
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          const uint2 t = v[u];
+          w[2 * u] = t.x;
+          w[2 * u + 1] = t.y;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 6; ++u) {
+          uint32_t lo = 0u, hi = 0u;
+          if (have && d0 + (2 * u) / 3 < D) lo = s0[2 * u];
+          if (have && d0 + (2 * u + 1) / 3 < D) hi = s0[2 * u + 1];
+          w[u] = lo | (hi << 16);
+        }
+      }
+      return;
+    }
+  }
 #pragma unroll
   for (int k = 1; k <= 3; ++k)
 #pragma unroll
     for (int q = 0; q < VEC / 2; ++q) {
       uint32_t lo = 0u, hi = 0u;
-      if (state && slot >= 0 && active && k <= L) {
+      if (have && k <= L) {
         const uint16_t* s0 = state + (slot * D + d0 + 2 * q) * L + (L - k);
         lo = s0[0];
         hi = s0[L];
@@ -280,9 +311,27 @@ __device__ __forceinline__ void init_ring(const uint16_t* state, int64_t slot, i
     }
 }
 
-// The fp32 ring of a sequence from its bf16 initial ring (exact).
+// The fp32 ring of a sequence from its bf16 initial ring (exact): h[j][q] = row ss - 1 - j,
+// channels (d0 + 2q, d0 + 2q + 1).
 template <int VEC>
-__device__ __forceinline__ void ring_of(const uint32_t (&hr)[3][VEC / 2], f2 (&h)[3][VEC / 2]) {
+__device__ __forceinline__ void ring_of(const uint32_t (&hr)[3][VEC / 2], int W,
+                                        f2 (&h)[3][VEC / 2]) {
+  if constexpr (VEC == 4) {
+    if (W == 4) {
+      // memory order: w0 = (c0e0, c0e1), w1 = (c0e2, c1e0), w2 = (c1e1, c1e2),
+      //               w3 = (c2e0, c2e1), w4 = (c2e2, c3e0), w5 = (c3e1, c3e2)
+      const uint32_t* w = &hr[0][0];
+      auto lo = [](uint32_t u) { return __uint_as_float(__byte_perm(u, 0u, 0x1044)); };
+      auto hi = [](uint32_t u) { return __uint_as_float(__byte_perm(u, 0u, 0x3244)); };
+      h[0][0] = f2_pack(lo(w[1]), hi(w[2]));  // entry 2 (row ss - 1)
+      h[0][1] = f2_pack(lo(w[4]), hi(w[5]));
+      h[1][0] = f2_pack(hi(w[0]), lo(w[2]));  // entry 1
+      h[1][1] = f2_pack(hi(w[3]), lo(w[5]));
+      h[2][0] = f2_pack(lo(w[0]), hi(w[1]));  // entry 0
+      h[2][1] = f2_pack(lo(w[3]), hi(w[4]));
+      return;
+    }
+  }
 #pragma unroll
   for (int j = 0; j < 3; ++j)
 #pragma unroll
