@@ -241,9 +241,10 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
 // host: launch with programmatic stream serialisation.  The kernel may be scheduled
 // before the previous kernel on the stream has finished (once that kernel's CTAs have all
 // triggered or exited); every cconv kernel executes griddepcontrol.wait before its first
-// global-memory access, so it still reads and writes only after the previous kernel has
-// completed and flushed.  Without a trigger in the previous kernel this is an ordinary
-// stream-ordered launch.
+// global-memory read or write, so it still reads and writes only after the previous kernel
+// has completed and flushed.  (The packed backward prefetches cu_seqlens into L2 before the
+// wait: a prefetch returns no data, and L2 is where device memory is coherent.)  Without a
+// trigger in the previous kernel this is an ordinary stream-ordered launch.
 // ------------------------------------------------------------------------------------
 // With CCONV_DEBUG set in the environment, failing CUDA calls are reported on stderr.
 cudaError_t report_cuda(const char* what, cudaError_t e);
