@@ -284,6 +284,52 @@ def test_backward_reads_initial_states_from_pool_slots(D):
         assert rel_err(f64(g), r) <= BWD_TOL, name
 
 
+def _offset_copy(t):
+    """t's values in a tensor that starts one element (2 bytes) into its buffer, so its data
+    pointer is not 8-byte aligned."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 8 != 0
+    return v
+
+
+@pytest.mark.parametrize("D", [1024, 4096])
+def test_unaligned_initial_states(D):
+    """The backward reads W = 4 initial rings as three 8-byte words per lane when the state is
+    8-byte aligned, and through 2-byte loads into the same layout otherwise.  A state that
+    starts 2 bytes into its buffer (dense, and a decode pool addressed through state indices)
+    must give the aligned call's results bit for bit, and the oracle's within tolerance.  The
+    forward, whose states must be 16-byte aligned, refuses it with CCONV_ERR_ALIGN."""
+    W, S = 4, 29
+    lens = [300, 1, 0, 2, 129, 777, 3]
+    x, dy, cu, w, b, pool, idx = _pool_case(lens, D, W, S, seed=D + 3)
+    xg, dyg, cug, wg, bg = (t.cuda() for t in (x, dy, cu, w, b))
+    dense = pool[idx.long()]
+    dense_g, pool_g = dense.cuda(), pool.cuda()
+    r0 = cc.cconv_bwd_varlen(xg, dyg, cug, wg, bg, initial_state=dense_g, want_dbias=True,
+                             want_dinit=True)
+    r1 = cc.cconv_bwd_varlen(xg, dyg, cug, wg, bg, initial_state=_offset_copy(dense_g),
+                             want_dbias=True, want_dinit=True)
+    status = torch.full((2,), 7, dtype=torch.int32, device="cuda")
+    r2 = cc.cconv_bwd_varlen(xg, dyg, cug, wg, bg, initial_state=_offset_copy(pool_g),
+                             state_indices=idx.cuda(), status=status, want_dbias=True,
+                             want_dinit=True)
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0]
+    as_bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+    for a, c, r in zip(r1, r2, r0):
+        assert torch.equal(as_bits(a), as_bits(r)) and torch.equal(as_bits(c), as_bits(r))
+    rdx, rdw, rdb, rdi = oracle.bwd_seq(f64(x), f64(dy), cu.numpy(), f64(w), f64(b), f64(dense),
+                                        "silu", want_dinit=True)
+    for name, g, r in (("dx", r1[0], rdx), ("dw", r1[1], rdw), ("dbias", r1[2], rdb),
+                       ("d_initial_state", r1[3], rdi)):
+        assert rel_err(f64(g), r) <= BWD_TOL, name
+    with pytest.raises(cc.CConvError) as e:
+        cc.cconv_fwd_varlen(xg, cug, wg, bg, initial_state=_offset_copy(dense_g))
+    assert e.value.status == -4
+
+
 @pytest.mark.parametrize("bad,mask", [([0, -1, 2], 1), ([0, 5, 2], 2), ([3, 1, 3], 4),
                                       ([-3, 9, 1], 3)])
 def test_backward_pool_indices_checked(bad, mask):
