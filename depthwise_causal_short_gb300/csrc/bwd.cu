@@ -577,11 +577,12 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
   // previous kernel on the stream may have written.
   int r0, r1;
   if constexpr (VL) {
-    // Equal cost per range.  A boundary costs fewer rows here than in the independent-
-    // pipeline form (whose 44 gave 75.0 / 89.3 us for 16 / 128 mixed sequences over 16384 x
-    // 4096 rows); measured: 16 rows 75.2 / 86.2, 24: 74.7 / 84.3, 32: 73.9 / 85.3, 64:
-    // 75.7 / 95.2 us.
-    constexpr int kBoundaryRows = 32;
+    // Equal cost per range, a sequence boundary counting as kBoundaryRows rows.  Measured over
+    // 16384 x 4096 rows with initial states, summed over ten length mixes of 8 to 128
+    // sequences: 12 rows 750.0, 16: 734.9, 20: 734.9, 32: 740.6 us (16 and 32 alike at 16
+    // sequences, 16 faster by 1.5 to 3.5 us at 64 and 128).  Before the initial rings stopped
+    // stalling the warps at each boundary, 32 had measured best.
+    constexpr int kBoundaryRows = 16;
     cost_split_range(p.cu, p.nseq, p.BT, kBoundaryRows, rg, p.wpc, lane, r0, r1);
   } else {
     r0 = static_cast<int>(static_cast<int64_t>(rg) * p.BT / p.wpc);
