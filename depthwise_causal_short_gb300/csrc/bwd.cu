@@ -697,8 +697,15 @@ __device__ __forceinline__ void bwd_cta_ls(const CUtensorMap* tmx, const CUtenso
 #pragma unroll
       for (int q = 0; q < P; ++q)
         f2_unpack(f2_mul(acc[j][q], f2_splat(0.5f)), v[2 * q], v[2 * q + 1]);
+      float* o = rec + warp * REC + j * CB + lane * VEC;
+      if constexpr (VEC == 4) {
+        // 16-byte aligned: every workspace is (the host checks it; the no-alloc array is
+        // 256-byte aligned), and each offset is a multiple of 4 floats.
+        *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+      } else {
 #pragma unroll
-      for (int q = 0; q < VEC; ++q) rec[warp * REC + j * CB + lane * VEC + q] = v[q];
+        for (int q = 0; q < VEC; ++q) o[q] = v[q];
+      }
     }
   }
 }
