@@ -4,7 +4,8 @@ Each case draws its shape and options from a fixed-seed generator, so a failure 
 reproducible case: batched forward / backward with random B, T, D tails, widths, bias,
 weight dtype and row strides; packed sequences with random length mixes (empty and short
 ones included), states, activation; decode updates with random pools, state lengths,
-padding rows and layouts, shifting or circular (random positions); several problems in one
+padding rows and layouts, shifting or circular (random positions), at small batches and at
+batches that take the 256-thread row-lane CTAs; several problems in one
 launch; and the same three backward calls at widths of 2048 channels and more, where they
 take the lockstep kernels (with ragged last strip groups and short ranges).  Sizes stay
 small enough for the fp64 oracle to finish in milliseconds.
@@ -206,6 +207,68 @@ def test_decode_ring(case):
     assert np.array_equal(bits(sg), st_ref), f"{what}: pool"
     live = (idx >= 0).numpy()
     assert rel_err(f64(y)[live], y_ref[live]) <= FWD_TOL, f"{what}: y"
+
+
+_ROW_LANE_THREADS: list[int] = []  # CTA size each test_decode_row_lanes case launched with
+
+
+# Batches large enough for the 256-thread decode CTAs (32 channel vectors x 8 row lanes,
+# staged taps, rows split evenly over a grid sized to the SM count, one CTA per SM): random
+# batch sizes and widths (partial last channel blocks included), plain, general and
+# circular-buffer modes, plain and bf16 taps, padding rows.
+@pytest.mark.parametrize("case", range(N_CASES // 2))
+def test_decode_row_lanes(case):
+    r = random.Random(9000 + case)
+    W = r.randint(1, 4)
+    ring = r.random() < 0.3
+    L = max(1, W - 1 + (r.random() < 0.4)) if ring else W - 1 + (r.random() < 0.3)
+    N = r.randint(60, 600)
+    S = N + r.randint(0, 90)
+    D = 8 * r.randint(8, 1024)
+    pad_rows = r.random() < 0.3
+    act = r.choice(["silu", None]) if (pad_rows or ring or L == W or r.random() < 0.3) else "silu"
+    wdtype = r.choice([torch.float32, torch.bfloat16])
+    g = torch.Generator().manual_seed(9000 + case)
+    state = torch.randn(S, D, L, generator=g).to(torch.bfloat16)
+    x = torch.randn(N, D, generator=g).to(torch.bfloat16)
+    w = (torch.rand(D, W, generator=g) - 0.5).to(wdtype)
+    b = (torch.rand(D, generator=g) - 0.5).to(wdtype) if r.random() < 0.5 else None
+    idx = torch.randperm(S, generator=g)[:N].to(torch.int32)
+    if pad_rows:
+        for i in range(N):
+            if r.random() < 0.2:
+                idx[i] = -1
+    pos = torch.tensor([r.randint(-20, 1000) for _ in range(N)], dtype=torch.int32)
+    dev = torch.device("cuda", 0)
+    sg = state.to(dev)
+    y = torch.zeros(N, D, dtype=torch.bfloat16, device=dev)
+    args = (x.to(dev), sg, w.to(dev), None if b is None else b.to(dev), idx.to(dev))
+    kw = dict(pad_rows=pad_rows, cache_seqlens=pos.to(dev) if ring else None, activation=act,
+              y=y)
+    ks = cc.describe(lambda: cc.cconv_update_ex(*args, **kw))  # records, launches nothing
+    _ROW_LANE_THREADS.append(ks[-1]["threads"])
+    _, status = cc.cconv_update_ex(*args, **kw)
+    torch.cuda.synchronize()
+    what = f"W={W} L={L} S={S} N={N} D={D} ring={ring} pad={pad_rows} act={act} w={wdtype}"
+    if ring:
+        rc, y_ref, st_ref = oracle.update_ring(bits(x), bits(state), idx.numpy(), pos.numpy(),
+                                               f64(w), f64(b), pad=pad_rows, activation=act)
+    else:
+        rc, y_ref, st_ref = oracle.update_ex(bits(x), bits(state), idx.numpy(), f64(w), f64(b),
+                                             pad=pad_rows, activation=act)
+    assert status.tolist() == [0 if rc == 0 else -8, rc], what
+    assert np.array_equal(bits(sg), st_ref), f"{what}: pool"
+    live = (idx >= 0).numpy()
+    assert rel_err(f64(y)[live], y_ref[live]) <= FWD_TOL, f"{what}: y"
+    assert not y[torch.from_numpy(~live).to(dev)].float().any(), f"{what}: padding y written"
+
+
+def test_decode_row_lanes_took_the_row_lane_kernels():
+    """Most of the cases above must have run on the 256-thread CTAs they are there for."""
+    if len(_ROW_LANE_THREADS) < N_CASES // 2:
+        pytest.skip("runs after the full set of test_decode_row_lanes cases")
+    share = sum(t == 256 for t in _ROW_LANE_THREADS) / len(_ROW_LANE_THREADS)
+    assert share >= 0.6, share
 
 
 # Widths from 2048 channels on take the lockstep backward kernels (a producer warp streams 8
