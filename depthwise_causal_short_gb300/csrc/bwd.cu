@@ -794,15 +794,15 @@ __global__ void __launch_bounds__(32 * kRedGroups)
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x >> 5;
   const int j = blockIdx.y;
-  const int64_t d = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  // D < 2^31, so the channel index fits 32 bits; the CTA's 32 channels share one strip.
+  const int d = static_cast<int>(blockIdx.x) * 32 + lane;
   float a = 0.f;
   if (d < D) {
-    const int64_t cb = d / cb_width;
-    const int c = static_cast<int>(d - cb * cb_width);
+    const int cb = static_cast<int>(blockIdx.x) / (cb_width / 32);
+    const int c = d - cb * cb_width;
     const int64_t rec = static_cast<int64_t>(kRec) * cb_width;
-    const int64_t sg = cb / sw;
-    const int64_t si = cb - sg * sw;
-    const float* base = ws + (sg * sw + si) * rec + static_cast<int64_t>(j) * cb_width + c;
+    // strip cb is record cb % sw of strip group cb / sw: offset (sg * sw + si) * rec = cb * rec
+    const float* base = ws + cb * rec + static_cast<int64_t>(j) * cb_width + c;
     const int64_t step = static_cast<int64_t>(n_sg) * sw * rec;  // next range group's CTA
     float a0 = 0.f, a1 = 0.f;
     int r = grp;
@@ -822,7 +822,7 @@ __global__ void __launch_bounds__(32 * kRedGroups)
   if (j < 4) {
     const int lag = j;
     if (lag < W) {
-      const int64_t o = d * W + (W - 1 - lag);
+      const int64_t o = static_cast<int64_t>(d) * W + (W - 1 - lag);
       if (wdt == CCONV_F32)
         static_cast<float*>(dw)[o] = t;
       else
@@ -859,15 +859,16 @@ __global__ void __launch_bounds__(32 * kRedGroups) cconv_bwd_reduce_kernel(const
   for (int u = 1; u < kMaxProblems; ++u)
     if (u < r.n && static_cast<int>(blockIdx.x) >= r.blk0[u]) k = u;
   const int64_t D = r.D[k];
-  const int64_t d = static_cast<int64_t>(blockIdx.x - r.blk0[k]) * 32 + lane;
+  const int blk = static_cast<int>(blockIdx.x) - r.blk0[k];  // block within problem k
+  const int d = blk * 32 + lane;                              // D < 2^31
   float a = 0.f;
   if (d < D) {
-    const int64_t cb = d / r.cb_width;
-    const int c = static_cast<int>(d - cb * r.cb_width);
+    const int cb = blk / (r.cb_width / 32);  // the CTA's 32 channels share one strip
+    const int c = d - cb * r.cb_width;
     const int64_t rec = static_cast<int64_t>(kRec) * r.cb_width;
-    const int64_t sg = r.sg0[k] + cb / r.sw;
-    const int64_t si = cb % r.sw;
-    const float* base = r.ws + (sg * r.sw + si) * rec + static_cast<int64_t>(j) * r.cb_width + c;
+    // strip cb is record cb % sw of strip group sg0 + cb / sw: offset (sg0 * sw + cb) * rec
+    const float* base = r.ws + (static_cast<int64_t>(r.sg0[k]) * r.sw + cb) * rec +
+                        static_cast<int64_t>(j) * r.cb_width + c;
     const int64_t step = static_cast<int64_t>(r.n_sg) * r.sw * rec;  // next range group's CTA
     float a0 = 0.f, a1 = 0.f;
     int q = grp;
@@ -888,7 +889,7 @@ __global__ void __launch_bounds__(32 * kRedGroups) cconv_bwd_reduce_kernel(const
   if (j < 4) {
     const int lag = j;
     if (lag < W) {
-      const int64_t o = d * W + (W - 1 - lag);
+      const int64_t o = static_cast<int64_t>(d) * W + (W - 1 - lag);
       if (r.wdt == CCONV_F32)
         static_cast<float*>(r.dw[k])[o] = t;
       else
