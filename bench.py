@@ -78,7 +78,7 @@ LAUNCHES_PER_STEP = 4                        # fwd, bwd stream, bwd reduce, upda
 # backward: stream kernel + reduction), averaged over back-to-back launches in one ncu
 # capture (profiles/, file named below), together with the hash of the kernel sources it
 # was taken on.  `traffic` is reported only while the sources still hash the same.
-BWD_TRAFFIC = {"bytes_per_call": 408_755_072, "sources_sha16": "075625ce2187a985",
+BWD_TRAFFIC = {"bytes_per_call": 408_681_728, "sources_sha16": "1c5b4950e9e17415",
                "profile": "profiles/cconv_bwd_traffic_b2_t8192_d4096.md"}
 TRAFFIC_SOURCES = ("csrc/bwd.cu", "csrc/strip.cuh", "csrc/common.cuh")
 
@@ -92,15 +92,15 @@ OCCUPANCY_SOURCES = {
     "update": ("csrc/update.cu", "csrc/common.cuh"),
 }
 ACHIEVED_OCCUPANCY = {
-    "sources_sha16": {"fwd": "7418f927c2fcbdd4", "bwd": "075625ce2187a985", "update": "ec15eacc1c4b0ba6"},
+    "sources_sha16": {"fwd": "7418f927c2fcbdd4", "bwd": "1c5b4950e9e17415", "update": "ec15eacc1c4b0ba6"},
     "pct": {
         "cconv_fwd_kernel<4, 8, 10, 8, 1, true, 0>": 14.21,
-        "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>": 13.97,
+        "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 0>": 13.92,
         "cconv_update_kernel<8, 4, 3, 4, 0, 256>": 11.55,
         "cconv_fwd_kernel<4, 8, 10, 8, 1, true, 1>": 13.77,
-        "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 1>": 13.78,
+        "cconv_bwd_ls_kernel<4, 12, 4, 8, 1, 1>": 13.72,
         "cconv_fwd_multi_kernel<4, 8, 10, 8, 1, true>": 14.00,
-        "cconv_bwd_ls_multi_kernel<4, 12, 4, 8>": 13.94,
+        "cconv_bwd_ls_multi_kernel<4, 12, 4, 8>": 14.00,
     },
     "profiles": ["profiles/cconv_fwd_bwd_update_kernels_b2_t8192_d4096.md",
                  "profiles/cconv_varlen_multi_bwd_kernels_b2_t8192_d4096.md"],
